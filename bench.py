@@ -1,0 +1,325 @@
+"""Benchmark: EF Top-k (0.1%) + int8 compression of a Llama-3-8B-shaped fp32
+gradient arena (291 tensors, 8,030,261,248 elements) on one GB300.
+
+One step = one gc_ef_topk_compress call over the whole arena: acc = g + e,
+per-tensor Top-k by |acc|, int8 stochastic rounding of the kept values,
+index/code payload, residual update.  Inputs (g, e: 64.2 GB) are resident in
+HBM and larger than L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded sample of the same workload.
+
+Multi-GPU: the compression of one worker's gradient does not shard (each
+data-parallel worker compresses its own gradient with its own residual), so
+N > 1 runs N independent replicas, one per GPU; value = all ranks' elements
+over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "EF Top-k compress gradient GB/s (elems/s) at 1 GB300; % of HBM roofline"
+UNIT = "GB/s"
+CFG = 5
+RHO = 0.001
+# kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan, two
+# sample levels and their selects, the streaming pass, three candidate radix
+# levels plus the full-pass level-1 histogram with their selects, count,
+# scan, write
+LAUNCHES_PER_STEP = 16
+# bytes the streaming pass must move per element: read g, read e, write e
+STREAM_BYTES_PER_ELEM = 12
+
+
+def workload_config(layout, k):
+    return {"workload": "llama3_8b_arena_ef_topk_0.1pct_int8", "tensors": layout.num_tensors,
+            "elements": layout.numel, "kept": int(k.sum()), "density": RHO, "ef": True, "int8": True,
+            "gradient": "student_t_nu3_x1e-3", "l2": "inputs (g + e, 64.2 GB) larger than L2; no flush",
+            "parallelism": "replicas"}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gc_topk.cu", "gc_common.cuh"):
+        with open(os.path.join(ROOT, "gradient_compression_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the streaming pass from the committed ncu summary,
+    scaled to this workload; None if missing or taken on different kernel source."""
+    p = os.path.join(ROOT, "profiles", "k_stream_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return float(d["bytes_per_element"])
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "util": float(parts[4]),
+                             "hw": parts[6], "hwt": parts[7], "swt": parts[8], "pcap": parts[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+def oracle_baseline(layout, k, tensors, it=0, seed=0):
+    """Times the oracle (single thread) on the given tensors; returns (GB/s, seconds, elements)."""
+    import oracle
+    oracle.lib()
+    n_tot, secs = 0, 0.0
+    off = layout.off
+    for t in tensors:
+        g = workloads.tensor_grad(CFG, layout, it, t, device="cpu").numpy()
+        e = np.zeros_like(g)
+        t0 = time.perf_counter()
+        oracle.ef_topk_tensor(g, e, int(k[t]), base=int(off[t]), int8=True, seed=seed, it=it)
+        secs += time.perf_counter() - t0
+        n_tot += g.size
+    return 4.0 * n_tot / secs / 1e9, secs, n_tot
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    layout = workloads.llama3_8b_layout()
+    k = workloads.k_per_tensor(layout.sizes, RHO)
+    sample_t = [1]                         # layer 0 q_proj: 16,777,216 elements
+    sample = "tensor 1 (layer-0 q_proj, 16,777,216 elements) per step"
+    for w in range(args.warmup):
+        oracle_baseline(layout, k, sample_t, it=w)
+    vals, secs_all = [], 0.0
+    for s in range(args.steps):
+        v, secs, n = oracle_baseline(layout, k, sample_t, it=args.warmup + s)
+        vals.append(v)
+        secs_all += secs
+    value = 4.0 * n * args.steps / secs_all / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs_all / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(layout, k),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import gradient_compression_gb300 as gc
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    layout = workloads.llama3_8b_layout()
+    k = workloads.k_per_tensor(layout.sizes, RHO)
+    N = layout.numel
+    flags = gc.GC_EF | gc.GC_INT8
+    L = gc.Layout(layout.off, k, device=dev)
+    g = workloads.make_grad(CFG, layout, 0, device=dev)
+    e = torch.zeros(N, dtype=torch.float32, device=dev)
+    comp = gc.TopkCompressor(L, flags, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(it, events=None):
+        if events is None:
+            gc.ef_topk_compress(L, g, e, comp.idx, comp.val, comp.q, comp.scale, 1234, it, flags, comp.workspace)
+        else:
+            gc.ef_topk_compress_profiled(L, g, e, comp.idx, comp.val, comp.q, comp.scale, 1234, it, flags,
+                                         comp.workspace, events)
+
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize()
+    diag = gc.get_device_status(comp.workspace)
+
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_begin.record(stream)
+    for s in range(args.steps):
+        step(args.warmup + s, ph[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_begin.elapsed_time(t_end)
+    stream_ms = [p[1].elapsed_time(p[2]) for p in ph]
+    phase = {"sample_ms": statistics.mean(p[0].elapsed_time(p[1]) for p in ph),
+             "stream_ms": statistics.mean(stream_ms),
+             "select_ms": statistics.mean(p[2].elapsed_time(p[3]) for p in ph),
+             "write_ms": statistics.mean(p[3].elapsed_time(p[4]) for p in ph)}
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * 4.0 * N / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    t_stream = statistics.mean(stream_ms) * 1e-3
+    achieved = STREAM_BYTES_PER_ELEM * N / t_stream / 1e9
+    bpe = profiled_traffic()
+    algo_step_bytes = 12 * N + 5 * int(k.sum()) + 4 * layout.num_tensors
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tensors = list(range(1, 10))        # layer 0: q, k, v, o, gate, up, down, two norms
+        v, secs, n = oracle_baseline(layout, k, tensors)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "layer 0 of the arena (9 tensors, %d elements), one iteration, %.1f s" % (n, secs)}
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(layout, k),
+            "elems_per_s": ws * N / (ms_per_step * 1e-3),
+            "hbm_roofline_frac_step": (algo_step_bytes / (ms_per_step * 1e-3) / 1e9) / peak,
+            "roofline": {"bound": "hbm", "kernel": "k_stream (acc = g + e, e write-back, candidate emission)",
+                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak,
+                         "traffic": None if bpe is None else bpe * N,
+                         "algorithmic_bytes": STREAM_BYTES_PER_ELEM * N},
+            "phases_ms": phase, "exact_tensors_warmup": int(diag.exact_tensors),
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
+    """Same metric through the public API with the gradient in pinned host memory:
+    per step H2D of g, the compression call, D2H of the payload (idx, codes, scales)."""
+    N = layout.numel
+    K = int(k.sum())
+    try:
+        g_host = torch.empty(N, dtype=torch.float32, pin_memory=True)
+    except RuntimeError as exc:
+        return {"value": None, "unit": UNIT, "error": "pinned host buffer: %s" % str(exc)[:120]}
+    g_host.copy_(g, non_blocking=False)
+    idx_h = torch.empty(K, dtype=torch.int32, pin_memory=True)
+    q_h = torch.empty(K, dtype=torch.int8, pin_memory=True)
+    sc_h = torch.empty(layout.num_tensors, dtype=torch.float32, pin_memory=True)
+    steps = max(2, min(args.steps, 5))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one(it):
+        g.copy_(g_host, non_blocking=True)
+        gc.ef_topk_compress(L, g, e, comp.idx, comp.val, comp.q, comp.scale, 99, it, flags, comp.workspace)
+        idx_h.copy_(comp.idx[:K], non_blocking=True)
+        q_h.copy_(comp.q[:K], non_blocking=True)
+        sc_h.copy_(comp.scale, non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    t0.record()
+    for s in range(steps):
+        one(1 + s)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": 4.0 * N / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 5 * K + 4 * layout.num_tensors}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

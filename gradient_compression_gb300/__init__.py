@@ -1,0 +1,254 @@
+"""Python binding of libgc (EF gradient compression on GB300).
+
+Argument marshalling only: every step of the compression path runs in the
+CUDA kernels of libgc.so, called through its C ABI (include/gc.h).  PyTorch
+provides device memory and the current stream.  There is no CPU fallback:
+if the library is not built, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgc.so")
+
+GC_OK, GC_ERR_INVALID_ARG, GC_ERR_LAYOUT, GC_ERR_WORKSPACE, GC_ERR_ALIGNMENT, GC_ERR_CUDA, GC_ERR_DEVICE = range(7)
+GC_EF, GC_INT8, GC_RANDK, GC_UNBIASED, GC_NO_MASK, GC_FORCE_EXACT = 0x1, 0x2, 0x4, 0x8, 0x10, 0x100
+GC_OP_TOPK, GC_OP_MOMENTUM, GC_OP_SIGN, GC_OP_QUANTIZE, GC_OP_DECOMPRESS = range(5)
+GC_Q_INT8, GC_Q_QSGD = 0, 1
+GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
+GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE = 0x1, 0x2, 0x4
+
+
+class gc_layout(C.Structure):
+    _fields_ = [("num_tensors", C.c_int32), ("off", C.c_void_p), ("k", C.c_void_p), ("koff", C.c_void_p)]
+
+
+class gc_diag(C.Structure):
+    _fields_ = [("error_bits", C.c_uint32), ("exact_tensors", C.c_uint32),
+                ("overflow_tensors", C.c_uint32), ("reserved", C.c_uint32)]
+
+
+class GCError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded libgc.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libgc.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                               "or python gradient_compression_gb300/build.py")
+        L = C.CDLL(LIB_PATH)
+        P, I32, I64, U32, U64, F, SZ = (C.c_void_p, C.c_int32, C.c_int64, C.c_uint32, C.c_uint64,
+                                        C.c_float, C.c_size_t)
+        LP = C.POINTER(gc_layout)
+        L.gc_workspace_size.argtypes = [LP, I32, U32, C.POINTER(SZ)]
+        L.gc_ef_topk_compress.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
+        L.gc_ef_topk_compress_profiled.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P, P, I32]
+        L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
+        L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
+        L.gc_quantize_stochastic.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, U64, P, SZ, P]
+        L.gc_sparse_decompress_accumulate.argtypes = [LP, LP, I32, P, P, P, P, P, P, SZ, P]
+        L.gc_dense_decompress_accumulate.argtypes = [LP, LP, I32, I32, I32, P, P, P, P, SZ, P]
+        L.gc_get_device_status.argtypes = [P, SZ, P, C.POINTER(gc_diag)]
+        L.gc_status_string.argtypes = [I32]
+        L.gc_status_string.restype = C.c_char_p
+        L.gc_version.restype = I32
+        for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled", "gc_ef_topk_compress_momentum",
+                     "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
+                     "gc_dense_decompress_accumulate", "gc_get_device_status"):
+            getattr(L, name).restype = I32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gc_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().gc_version())
+
+
+def _check(status: int, what: str) -> None:
+    if status != GC_OK:
+        raise GCError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Layout:
+    """A flat-arena layout: host arrays (validation, sizing) + device copies.
+
+    off[t]..off[t+1] are tensor t's elements; k (optional) kept entries per
+    tensor; koff their prefix sum.
+    """
+
+    def __init__(self, off, k=None, device="cuda"):
+        self.off = np.ascontiguousarray(off, dtype=np.int64)
+        self.T = int(self.off.size - 1)
+        if k is not None:
+            self.k = np.ascontiguousarray(k, dtype=np.int64)
+            self.koff = np.zeros(self.T + 1, np.int64)
+            self.koff[1:] = np.cumsum(self.k)
+        else:
+            self.k = self.koff = None
+        self.device = torch.device(device)
+        self._host = gc_layout(self.T, self.off.ctypes.data, None if self.k is None else self.k.ctypes.data,
+                               None if self.koff is None else self.koff.ctypes.data)
+        self._dev_off = self._dev_k = self._dev_koff = None
+        self._dev = None
+        if self.device.type == "cuda":
+            self._dev_off = torch.from_numpy(self.off).to(self.device)
+            if self.k is not None:
+                self._dev_k = torch.from_numpy(self.k).to(self.device)
+                self._dev_koff = torch.from_numpy(self.koff).to(self.device)
+            self._dev = gc_layout(self.T, _ptr(self._dev_off), _ptr(self._dev_k), _ptr(self._dev_koff))
+
+    @property
+    def numel(self) -> int:
+        return int(self.off[-1])
+
+    @property
+    def total_k(self) -> int:
+        return int(self.koff[-1]) if self.koff is not None else 0
+
+    @property
+    def words(self) -> int:
+        n = np.diff(self.off)
+        return int(((n + 31) // 32).sum())
+
+    def host(self):
+        return C.byref(self._host)
+
+    def dev(self):
+        if self._dev is None:
+            raise RuntimeError("layout has no device copy")
+        return C.byref(self._dev)
+
+
+def workspace_size(layout: Layout, op: int, flags: int = 0) -> int:
+    out = C.c_size_t(0)
+    _check(lib().gc_workspace_size(layout.host(), op, flags, C.byref(out)), "gc_workspace_size")
+    return int(out.value)
+
+
+def alloc_workspace(layout: Layout, op: int, flags: int = 0, device=None) -> torch.Tensor:
+    """A workspace tensor (uint8) of the size the operation needs."""
+    n = workspace_size(layout, op, flags)
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or layout.device)
+
+
+def ef_topk_compress(layout, g, e, idx, val, q, scale, seed, it, flags, workspace, stream=None):
+    _check(lib().gc_ef_topk_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx), _ptr(val),
+                                     _ptr(q), _ptr(scale), int(seed), int(it), int(flags), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "gc_ef_topk_compress")
+
+
+def ef_topk_compress_profiled(layout, g, e, idx, val, q, scale, seed, it, flags, workspace, events,
+                              stream=None):
+    """gc_ef_topk_compress recording `events` (torch.cuda.Event, up to 5) at its phase boundaries."""
+    arr = (C.c_void_p * len(events))(*[None if ev is None else ev.cuda_event for ev in events])
+    _check(lib().gc_ef_topk_compress_profiled(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx),
+                                              _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
+                                              _ptr(workspace), workspace.numel(), _stream(stream), arr,
+                                              len(events)), "gc_ef_topk_compress_profiled")
+
+
+def ef_topk_compress_momentum(layout, g, u, v, beta, idx, val, q, scale, seed, it, flags, workspace,
+                              stream=None):
+    _check(lib().gc_ef_topk_compress_momentum(layout.dev(), layout.host(), _ptr(g), _ptr(u), _ptr(v),
+                                              float(beta), _ptr(idx), _ptr(val), _ptr(q), _ptr(scale),
+                                              int(seed), int(it), int(flags), _ptr(workspace),
+                                              workspace.numel(), _stream(stream)),
+           "gc_ef_topk_compress_momentum")
+
+
+def sign_compress(layout, g, e, bits, mean_abs, workspace, stream=None):
+    _check(lib().gc_sign_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(bits), _ptr(mean_abs),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)), "gc_sign_compress")
+
+
+def quantize_stochastic(layout, g, e, codes, scale, mode, s_levels, seed, it, workspace, stream=None):
+    _check(lib().gc_quantize_stochastic(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(codes),
+                                        _ptr(scale), int(mode), int(s_levels), int(seed), int(it),
+                                        _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_quantize_stochastic")
+
+
+def _ptr_array(ts):
+    if ts is None:
+        return None
+    arr = (C.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+    return arr
+
+
+def sparse_decompress_accumulate(layout, idx_list, val_list, q_list, scale_list, out, workspace,
+                                 stream=None):
+    W = len(idx_list)
+    ip, vp, qp, sp = _ptr_array(idx_list), _ptr_array(val_list), _ptr_array(q_list), _ptr_array(scale_list)
+    _check(lib().gc_sparse_decompress_accumulate(layout.dev(), layout.host(), W, ip, vp, qp, sp, _ptr(out),
+                                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_sparse_decompress_accumulate")
+
+
+def dense_decompress_accumulate(layout, kind, s_levels, data_list, scale_list, out, workspace, stream=None):
+    W = len(data_list)
+    _check(lib().gc_dense_decompress_accumulate(layout.dev(), layout.host(), W, int(kind), int(s_levels),
+                                                _ptr_array(data_list), _ptr_array(scale_list), _ptr(out),
+                                                _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_dense_decompress_accumulate")
+
+
+def get_device_status(workspace, stream=None, raise_on_error=True) -> gc_diag:
+    d = gc_diag()
+    st = lib().gc_get_device_status(_ptr(workspace), workspace.numel(), _stream(stream), C.byref(d))
+    if st != GC_OK and (raise_on_error or st != GC_ERR_DEVICE):
+        raise GCError(st, f"gc_get_device_status (error bits 0x{d.error_bits:x})")
+    return d
+
+
+# ---------------------------------------------------------------------------- convenience
+
+class TopkCompressor:
+    """Owns the payload and workspace buffers of gc_ef_topk_compress for one layout."""
+
+    def __init__(self, layout: Layout, flags: int, device="cuda"):
+        self.layout, self.flags = layout, flags
+        K = layout.total_k
+        dev = torch.device(device)
+        self.idx = torch.empty(max(K, 1), dtype=torch.int32, device=dev)
+        int8 = bool(flags & GC_INT8)
+        self.val = None if int8 else torch.empty(max(K, 1), dtype=torch.float32, device=dev)
+        self.q = torch.empty(max(K, 1), dtype=torch.int8, device=dev) if int8 else None
+        self.scale = torch.empty(layout.T, dtype=torch.float32, device=dev) if int8 else None
+        self.workspace = alloc_workspace(layout, GC_OP_TOPK, flags, dev)
+
+    def __call__(self, g, e, seed, it, stream=None):
+        ef_topk_compress(self.layout, g, e, self.idx, self.val, self.q, self.scale, seed, it, self.flags,
+                         self.workspace, stream)
+        return self.idx, self.val, self.q, self.scale

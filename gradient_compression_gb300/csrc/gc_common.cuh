@@ -1,0 +1,221 @@
+// Device helpers shared by the libgc kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gc.h"
+
+namespace gc {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Work unit: one warp streams UNIT consecutive elements of one tensor.
+constexpr int UNIT_SHIFT = 12;
+constexpr int64_t UNIT = int64_t(1) << UNIT_SHIFT;
+// Unit block: UB_UNITS consecutive units of one tensor, one CTA of the
+// selection kernels (thread per unit on the candidate path).
+constexpr int UB_UNITS = 256;
+// Radix digits of the 32-bit selection key: 11 + 11 + 10 bits.
+constexpr int NBINS = 2048;
+// Per-warp candidate staging capacity in shared memory (entries per unit).
+constexpr int WCAP = 512;
+// Tensors at most this long are sampled completely when the candidate
+// threshold is estimated.
+constexpr int64_t SMALL_N = 65536;
+// Expected number of Top-k members in a tensor's sample.
+constexpr int64_t SAMPLE_HITS = 128;
+constexpr int RUN = 16;  // sampled elements per contiguous run
+
+// Tensor state flags.
+constexpr uint32_t TS_NOEMIT = 1u;    // k_t == 0: nothing is selected
+constexpr uint32_t TS_DENSE = 2u;     // select with full passes over the tensor
+constexpr uint32_t TS_OVERFLOW = 4u;  // candidate staging overflowed
+constexpr uint32_t TS_TEST_DONE = 8u; // threshold estimate fixed early (no second sample level)
+
+// Diagnostic words at the head of every workspace.
+constexpr int DIAG_ERR = 0, DIAG_EXACT = 1, DIAG_OVF = 2, DIAG_ABORT = 3;
+constexpr size_t DIAG_BYTES = 256;
+
+struct alignas(16) TensorState {
+  uint32_t t_est;       // candidate threshold on the selection key
+  uint32_t flags;       // TS_*
+  uint32_t prefix;      // radix digits fixed so far
+  uint32_t rank;        // 1-based rank still sought inside the current bucket
+  uint32_t maxkey;      // largest key seen (int8 scale)
+  uint32_t cand_count;  // candidates reserved by the streaming pass
+  uint32_t thr;         // exact key of the k-th element
+  uint32_t r_eq;        // how many elements with key == thr are kept (lowest indices)
+  uint32_t sample_j;    // rank sought in the sample
+  uint32_t pad[7];
+};
+static_assert(sizeof(TensorState) == 64, "TensorState is 64 bytes");
+
+// ---------------------------------------------------------------- sizing
+// Candidate capacity of a tensor, identical on host and device.
+__host__ __device__ inline int64_t cand_capacity(int64_t n, int64_t k) {
+  if (k <= 0) return 0;
+  if (n <= SMALL_N) return n;
+  int64_t c = 2 * k + 4096;
+  return c < n ? c : n;
+}
+
+__host__ __device__ inline int64_t units_of(int64_t n) { return (n + UNIT - 1) >> UNIT_SHIFT; }
+__host__ __device__ inline int64_t ublocks_of(int64_t n) {
+  return (units_of(n) + UB_UNITS - 1) / UB_UNITS;
+}
+
+// Sample plan of a tensor: `runs` runs of RUN consecutive elements spaced
+// `stride` apart (all of the tensor when it is small).  m = sampled count.
+__host__ __device__ inline void sample_plan(int64_t n, int64_t k, int64_t* runs, int64_t* stride,
+                                            int64_t* m) {
+  if (n <= SMALL_N || k <= 0) {
+    *stride = RUN;
+    *runs = (n + RUN - 1) / RUN;
+    *m = n;
+    return;
+  }
+  int64_t want = (SAMPLE_HITS * n + k - 1) / k;  // ceil(SAMPLE_HITS / rho)
+  int64_t r = (want + RUN - 1) / RUN;
+  int64_t rmax = n / RUN;
+  if (r > rmax) r = rmax;
+  if (r < 1) r = 1;
+  *runs = r;
+  *stride = n / r;
+  *m = r * RUN;
+}
+
+// ---------------------------------------------------------------- keys
+// Top-k key: the fp32 bit pattern shifted left by one, which drops the sign
+// bit; for finite values it orders by |x| and maps +0 and -0 together.
+__device__ __forceinline__ uint32_t mag_key(float x) { return __float_as_uint(x) << 1; }
+__device__ __forceinline__ float key_magnitude(uint32_t key) { return __uint_as_float(key >> 1); }
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The four words of the block holding arena elements 4b .. 4b+3.
+__device__ __forceinline__ uint4 philox_block(uint64_t seed, uint64_t iter, uint64_t b,
+                                              uint32_t purpose) {
+  return philox4x32_10(make_uint4((uint32_t)b, (uint32_t)(b >> 32), (uint32_t)iter, purpose),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t uint4_word(uint4 w, int j) {
+  return j == 0 ? w.x : (j == 1 ? w.y : (j == 2 ? w.z : w.w));
+}
+
+__device__ __forceinline__ uint32_t philox_word(uint64_t seed, uint64_t iter, uint64_t i,
+                                                uint32_t purpose) {
+  return uint4_word(philox_block(seed, iter, i >> 2, purpose), (int)(i & 3));
+}
+
+constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
+
+// ---------------------------------------------------------------- rounding
+// ceil(f * 2^32) for fp32 0 <= f < 1, exactly, from f's bits.
+__device__ __forceinline__ uint64_t ceil_frac_2p32(float f) {
+  const uint32_t b = __float_as_uint(f);
+  if (b == 0u) return 0ull;
+  const int ex = (int)((b >> 23) & 0xFFu);
+  uint64_t mant = b & 0x7FFFFFu;
+  int sh;  // f = mant * 2^sh
+  if (ex == 0) {
+    sh = -149;
+  } else {
+    mant |= 0x800000u;
+    sh = ex - 150;
+  }
+  const int s2 = sh + 32;  // f * 2^32 = mant * 2^s2, s2 <= 8 because f < 1
+  if (s2 >= 0) return mant << s2;
+  const int rs = -s2;
+  if (rs >= 40) return 1ull;  // 0 < f * 2^32 < 1
+  return (mant + ((1ull << rs) - 1ull)) >> rs;
+}
+
+// Stochastic rounding of x >= 0: floor(x) + 1 iff r * 2^-32 < frac(x).
+__device__ __forceinline__ int stochastic_round(float x, uint32_t r) {
+  const float f = floorf(x);
+  const float frac = __fsub_rn(x, f);  // exact
+  return (int)f + (((uint64_t)r < ceil_frac_2p32(frac)) ? 1 : 0);
+}
+
+// int8 code of x for scale s (s == 0 gives 0).
+__device__ __forceinline__ int int8_code(float x, float s, uint32_t r) {
+  if (s == 0.0f) return 0;
+  int m = stochastic_round(__fdiv_rn(fabsf(x), s), r);
+  m = m > 127 ? 127 : m;
+  return signbit(x) ? -m : m;
+}
+
+// ---------------------------------------------------------------- lookup
+// Largest t in [0, T) with offs[t] <= x (offs[0] <= x < offs[T]).
+__device__ __forceinline__ int find_segment(const int64_t* __restrict__ offs, int T, int64_t x) {
+  int lo = 0, hi = T;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(offs + mid) <= x)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- warp scans
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+// Exclusive prefix and total over the warp of small per-lane counts (0..7).
+__device__ __forceinline__ void warp_count_scan(unsigned c, unsigned lane, unsigned* pre,
+                                                unsigned* tot) {
+  const unsigned b0 = __ballot_sync(FULL, c & 1u);
+  const unsigned b1 = __ballot_sync(FULL, c & 2u);
+  const unsigned b2 = __ballot_sync(FULL, c & 4u);
+  const unsigned lt = (1u << lane) - 1u;
+  *pre = __popc(b0 & lt) + 2u * __popc(b1 & lt) + 4u * __popc(b2 & lt);
+  *tot = __popc(b0) + 2u * __popc(b1) + 4u * __popc(b2);
+}
+
+// Exclusive prefix and total of arbitrary per-lane unsigned values.
+__device__ __forceinline__ unsigned warp_excl_scan(unsigned v, unsigned lane, unsigned* tot) {
+  unsigned x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned y = __shfl_up_sync(FULL, x, d);
+    if (lane >= (unsigned)d) x += y;
+  }
+  *tot = __shfl_sync(FULL, x, 31);
+  return x - v;
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = max(v, __shfl_xor_sync(FULL, v, d));
+  return v;
+}
+
+// Shared-memory histogram add, aggregated over lanes that hit the same bin.
+__device__ __forceinline__ void smem_hist_add(uint32_t* hist, uint32_t bin, bool pred) {
+  const unsigned active = __ballot_sync(FULL, pred);
+  if (pred) {
+    const unsigned peers = __match_any_sync(active, bin);
+    if ((int)lane_id() == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+  }
+}
+
+// Streaming (evict-first) 16-byte accesses.
+__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
+
+}  // namespace gc

@@ -1,0 +1,615 @@
+// Dense compressors and receivers (sm_103a): 1-bit sign with EF, int8 and
+// QSGD stochastic quantization, and their decoders.
+//
+// Method: mbrenndoerfer.com "Gradient Compression", 1-bit SGD
+// (Q(g) = sign(g) ||g||_1 / d, one scalar per layer) and QSGD
+// (Q_s(g) = ||g|| sgn(g) xi(g, s), stochastic rounding); inferensys.com
+// genomic glossary "Gradient Compression", 8-bit quantization and
+// stochastic rounding.
+//
+// Each compressor is two streaming passes over the arena (the per-tensor
+// scale must be known before any code or residual can be written):
+//   pass 1: acc = g (+ e, written back), per-unit partial of sum|acc| or
+//           sum acc^2 (fp32 Neumaier per lane, fp64 across lanes), or the
+//           per-tensor max key (int8)
+//   reduce: per tensor, unit partials summed in a fixed order in fp64
+//   pass 2: bits / codes and the EF residual
+#include <cmath>
+#include <cstring>
+
+#include "gc_common.cuh"
+#include "gc_host.h"
+
+namespace gc {
+
+enum { DOP_SIGN = 0, DOP_INT8 = 1, DOP_QSGD = 2 };
+
+struct DenseArgs {
+  int T;
+  int op;
+  int ef;
+  int s_levels;
+  const int64_t* off;
+  const float* g;
+  float* e;
+  uint32_t* bits;
+  int8_t* codes;
+  float* scale;  // mean_abs (sign), max/127 (int8), norm (QSGD)
+  uint64_t seed, iter;
+  uint32_t* diag;
+  uint32_t* maxkey;   // [T]
+  int64_t* units_off; // [T+1]
+  int64_t* woff;      // [T+1]
+  double* upart;      // [U]
+  int64_t U, W, N;
+};
+
+__device__ __forceinline__ bool aborted(const DenseArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
+
+__global__ void __launch_bounds__(1024) k_dplan(DenseArgs A) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  int64_t carry_u = 0, carry_w = 0;
+  for (int base = 0; base < A.T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    int64_t nu = 0, nw = 0;
+    if (t < A.T) {
+      const int64_t n = A.off[t + 1] - A.off[t];
+      if (n < 1 || n > INT64_C(2147483647)) s_bad = 1;
+      nu = units_of(n);
+      nw = (n + 31) >> 5;
+    }
+    // two block scans (same helper shape as the Top-k planner)
+    for (int which = 0; which < 2; ++which) {
+      const int64_t v = which == 0 ? nu : nw;
+      const unsigned lane = lane_id(), w = threadIdx.x >> 5, nwp = blockDim.x >> 5;
+      int64_t x = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(FULL, x, d);
+        if (lane >= (unsigned)d) x += y;
+      }
+      if (lane == 31) s_warp[w] = x;
+      __syncthreads();
+      if (w == 0) {
+        int64_t z = lane < nwp ? s_warp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int64_t y = __shfl_up_sync(FULL, z, d);
+          if (lane >= (unsigned)d) z += y;
+        }
+        if (lane < nwp) s_warp[lane] = z;
+      }
+      __syncthreads();
+      const int64_t excl = (w == 0 ? 0 : s_warp[w - 1]) + x - v;
+      const int64_t tot = s_warp[nwp - 1];
+      __syncthreads();
+      if (which == 0) {
+        if (t < A.T) A.units_off[t] = carry_u + excl;
+        carry_u += tot;
+      } else {
+        if (t < A.T) A.woff[t] = carry_w + excl;
+        carry_w += tot;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    A.units_off[A.T] = carry_u;
+    A.woff[A.T] = carry_w;
+    if (s_bad || carry_u != A.U || carry_w != A.W || A.off[0] != 0 || A.off[A.T] != A.N) {
+      A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
+      A.diag[DIAG_ABORT] = 1u;
+    }
+  }
+}
+
+struct Neumaier {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = __fadd_rn(s, x);
+    if (fabsf(s) >= fabsf(x))
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
+    else
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
+    s = t;
+  }
+};
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+  return v;
+}
+
+constexpr int DTHREADS = 256;
+constexpr int DWARPS = DTHREADS / 32;
+
+struct UnitRef {
+  int t;
+  int64_t base, lstart;
+  int len;
+};
+
+__device__ __forceinline__ UnitRef unit_ref(const DenseArgs& A, int64_t u) {
+  UnitRef r;
+  r.t = find_segment(A.units_off, A.T, u);
+  r.base = A.off[r.t];
+  const int64_t n = A.off[r.t + 1] - r.base;
+  r.lstart = (u - A.units_off[r.t]) << UNIT_SHIFT;
+  r.len = (int)min((int64_t)UNIT, n - r.lstart);
+  return r;
+}
+
+// Pass 1: acc (+ EF write-back) and the per-unit reduction input.
+template <int OP, bool EF>
+__global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
+  for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
+    const UnitRef r = unit_ref(A, u);
+    const int64_t g0 = r.base + r.lstart;
+    Neumaier acc_sum;
+    uint32_t mx = 0u;
+    auto take = [&](float x) {
+      if (OP == DOP_SIGN) acc_sum.add(fabsf(x));
+      else if (OP == DOP_QSGD) acc_sum.add(__fmul_rn(x, x));
+      else mx = max(mx, mag_key(x));
+    };
+    if ((g0 & 3) == 0) {
+      const int nv = r.len >> 2;
+      const float4* g4 = reinterpret_cast<const float4*>(A.g + g0);
+      float4* e4 = reinterpret_cast<float4*>(A.e + g0);
+      for (int v0 = 0; v0 < nv; v0 += 128) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int vi = v0 + 32 * j + (int)lane;
+          if (vi < nv) {
+            x[j] = ld_stream(g4 + vi);
+            if (EF) y[j] = ld_stream(e4 + vi);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int vi = v0 + 32 * j + (int)lane;
+          if (vi < nv) {
+            float4 a = x[j];
+            if (EF) {
+              a.x = __fadd_rn(a.x, y[j].x);
+              a.y = __fadd_rn(a.y, y[j].y);
+              a.z = __fadd_rn(a.z, y[j].z);
+              a.w = __fadd_rn(a.w, y[j].w);
+              st_stream(e4 + vi, a);
+            }
+            take(a.x); take(a.y); take(a.z); take(a.w);
+          }
+        }
+      }
+      const int rem = r.len & 3;
+      if ((int)lane < rem) {
+        const int64_t gi = g0 + 4 * nv + lane;
+        float a = A.g[gi];
+        if (EF) {
+          a = __fadd_rn(a, A.e[gi]);
+          A.e[gi] = a;
+        }
+        take(a);
+      }
+    } else {
+      for (int i = (int)lane; i < r.len; i += 32) {
+        const int64_t gi = g0 + i;
+        float a = A.g[gi];
+        if (EF) {
+          a = __fadd_rn(a, A.e[gi]);
+          A.e[gi] = a;
+        }
+        take(a);
+      }
+    }
+    if (OP == DOP_INT8) {
+      mx = warp_max_u32(mx);
+      if (lane == 0) atomicMax(A.maxkey + r.t, mx);
+    } else {
+      const double part = warp_sum_f64((double)acc_sum.s + (double)acc_sum.c);
+      if (lane == 0) A.upart[u] = part;
+    }
+  }
+}
+
+// Per-tensor scale from the unit partials (fixed order, so deterministic).
+__global__ void __launch_bounds__(256) k_dreduce(DenseArgs A) {
+  __shared__ double s_part[256];
+  if (aborted(A)) return;
+  const int t = blockIdx.x;
+  const int64_t n = A.off[t + 1] - A.off[t];
+  if (A.op == DOP_INT8) {
+    if (threadIdx.x == 0) A.scale[t] = __fdiv_rn(key_magnitude(A.maxkey[t]), 127.0f);
+    return;
+  }
+  double s = 0.0;
+  for (int64_t u = A.units_off[t] + threadIdx.x; u < A.units_off[t + 1]; u += blockDim.x) s += A.upart[u];
+  s_part[threadIdx.x] = s;
+  __syncthreads();
+  for (int h = 128; h > 0; h >>= 1) {
+    if ((int)threadIdx.x < h) s_part[threadIdx.x] += s_part[threadIdx.x + h];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double tot = s_part[0];
+    A.scale[t] = (A.op == DOP_SIGN) ? __double2float_rn(tot / (double)n) : __double2float_rn(sqrt(tot));
+  }
+}
+
+// Code of x for the dense quantizers; *dec receives the decoded value.
+template <int OP>
+__device__ __forceinline__ int dense_code(float x, float sc, int s_levels, uint32_t r, float* dec) {
+  if (OP == DOP_INT8) {
+    const int c = int8_code(x, sc, r);
+    *dec = __fmul_rn((float)c, sc);
+    return c;
+  }
+  int level = 0;
+  if (sc != 0.0f) {
+    float y = __fdiv_rn(__fmul_rn(fabsf(x), (float)s_levels), sc);
+    y = fminf(y, (float)s_levels + 1.0f);
+    level = min(s_levels, stochastic_round(y, r));
+  }
+  const float mag = __fdiv_rn(__fmul_rn((float)level, sc), (float)s_levels);
+  const bool neg = signbit(x);
+  *dec = neg ? -mag : mag;
+  return neg ? -level : level;
+}
+
+// Pass 2 of the sign compressor: bits and residual.
+template <bool EF>
+__global__ void __launch_bounds__(DTHREADS) k_sign2(DenseArgs A) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
+  const float* src = EF ? A.e : A.g;
+  for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
+    const UnitRef r = unit_ref(A, u);
+    const int64_t g0 = r.base + r.lstart;
+    const float mu = A.scale[r.t];
+    uint32_t* wbase = A.bits + A.woff[r.t] + (r.lstart >> 5);
+    const int nwords = (r.len + 31) >> 5;
+    if ((g0 & 3) == 0) {
+      // 32 lanes x 4 elements = 4 words per step; 8 steps fill one word per lane
+      const int nslots = (r.len + 3) >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src + g0);
+      float4* e4 = reinterpret_cast<float4*>(A.e + g0);
+      for (int v0 = 0; v0 < nslots; v0 += 256) {
+        uint32_t myword = 0u;
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const int vi = v0 + 32 * st + (int)lane;
+          unsigned nib = 0u;
+          if (vi < nslots) {
+            const int li = vi * 4;
+            if (li + 4 <= r.len) {
+              float4 a = ld_stream(s4 + vi);
+              nib = (signbit(a.x) ? 0u : 1u) | (signbit(a.y) ? 0u : 2u) | (signbit(a.z) ? 0u : 4u) |
+                    (signbit(a.w) ? 0u : 8u);
+              if (EF) {
+                a.x = __fsub_rn(a.x, signbit(a.x) ? -mu : mu);
+                a.y = __fsub_rn(a.y, signbit(a.y) ? -mu : mu);
+                a.z = __fsub_rn(a.z, signbit(a.z) ? -mu : mu);
+                a.w = __fsub_rn(a.w, signbit(a.w) ? -mu : mu);
+                st_stream(e4 + vi, a);
+              }
+            } else {
+              for (int j = 0; li + j < r.len; ++j) {
+                const int64_t gi = g0 + li + j;
+                const float a = src[gi];
+                if (!signbit(a)) nib |= 1u << j;
+                if (EF) A.e[gi] = __fsub_rn(a, signbit(a) ? -mu : mu);
+              }
+            }
+          }
+          uint32_t w = nib << (4 * (lane & 7));
+          w |= __shfl_xor_sync(FULL, w, 1);
+          w |= __shfl_xor_sync(FULL, w, 2);
+          w |= __shfl_xor_sync(FULL, w, 4);
+          const uint32_t mine = __shfl_sync(FULL, w, 8 * (lane & 3));
+          if ((int)(lane >> 2) == st) myword = mine;
+        }
+        const int wi = (v0 >> 3) + (int)lane;  // 8 slots per word
+        if (wi < nwords) wbase[wi] = myword;
+      }
+    } else {
+      for (int i0 = 0; i0 < r.len; i0 += 32) {
+        const int i = i0 + (int)lane;
+        const bool valid = i < r.len;
+        float a = 0.0f;
+        if (valid) a = src[g0 + i];
+        const unsigned w = __ballot_sync(FULL, valid && !signbit(a));
+        if (valid && EF) A.e[g0 + i] = __fsub_rn(a, signbit(a) ? -mu : mu);
+        if (lane == 0) wbase[i0 >> 5] = w;
+      }
+    }
+  }
+}
+
+// Pass 2 of the int8 / QSGD quantizers: codes and residual.
+template <int OP, bool EF>
+__global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
+  const float* src = EF ? A.e : A.g;
+  const uint32_t purpose = (OP == DOP_INT8) ? PURPOSE_INT8 : PURPOSE_QSGD;
+  for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
+    const UnitRef r = unit_ref(A, u);
+    const int64_t g0 = r.base + r.lstart;
+    const float sc = A.scale[r.t];
+    if ((g0 & 3) == 0) {
+      const int nv = r.len >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src + g0);
+      float4* e4 = reinterpret_cast<float4*>(A.e + g0);
+      char4* c4 = reinterpret_cast<char4*>(A.codes + g0);
+      for (int v0 = 0; v0 < nv; v0 += 128) {
+        float4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int vi = v0 + 32 * j + (int)lane;
+          if (vi < nv) x[j] = ld_stream(s4 + vi);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int vi = v0 + 32 * j + (int)lane;
+          if (vi < nv) {
+            const uint4 rw = philox_block(A.seed, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, purpose);
+            float4 d;
+            char4 c;
+            c.x = (signed char)dense_code<OP>(x[j].x, sc, A.s_levels, rw.x, &d.x);
+            c.y = (signed char)dense_code<OP>(x[j].y, sc, A.s_levels, rw.y, &d.y);
+            c.z = (signed char)dense_code<OP>(x[j].z, sc, A.s_levels, rw.z, &d.z);
+            c.w = (signed char)dense_code<OP>(x[j].w, sc, A.s_levels, rw.w, &d.w);
+            __stcs(reinterpret_cast<int*>(c4 + vi), *reinterpret_cast<int*>(&c));
+            if (EF) {
+              float4 res;
+              res.x = __fsub_rn(x[j].x, d.x);
+              res.y = __fsub_rn(x[j].y, d.y);
+              res.z = __fsub_rn(x[j].z, d.z);
+              res.w = __fsub_rn(x[j].w, d.w);
+              st_stream(e4 + vi, res);
+            }
+          }
+        }
+      }
+      const int rem = r.len & 3;
+      if ((int)lane < rem) {
+        const int64_t gi = g0 + 4 * nv + lane;
+        const float x = src[gi];
+        float d;
+        A.codes[gi] = (int8_t)dense_code<OP>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        if (EF) A.e[gi] = __fsub_rn(x, d);
+      }
+    } else {
+      for (int i = (int)lane; i < r.len; i += 32) {
+        const int64_t gi = g0 + i;
+        const float x = src[gi];
+        float d;
+        A.codes[gi] = (int8_t)dense_code<OP>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        if (EF) A.e[gi] = __fsub_rn(x, d);
+      }
+    }
+  }
+}
+
+// Receiver: out += decode(payload) for one worker.
+template <int KIND>
+__global__ void __launch_bounds__(DTHREADS) k_ddecode(DenseArgs A, const void* data, const float* scl,
+                                                      float* out) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
+  for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
+    const UnitRef r = unit_ref(A, u);
+    const int64_t g0 = r.base + r.lstart;
+    const float sc = scl[r.t];
+    for (int i = (int)lane; i < r.len; i += 32) {
+      const int64_t gi = g0 + i;
+      float d;
+      if (KIND == GC_DENSE_SIGN) {
+        const uint32_t* bits = static_cast<const uint32_t*>(data) + A.woff[r.t] + (r.lstart >> 5);
+        d = ((bits[i >> 5] >> (i & 31)) & 1u) ? sc : -sc;
+      } else {
+        const int c = static_cast<const int8_t*>(data)[gi];
+        if (KIND == GC_DENSE_INT8) {
+          d = __fmul_rn((float)c, sc);
+        } else {
+          const int level = c < 0 ? -c : c;
+          const float mag = __fdiv_rn(__fmul_rn((float)level, sc), (float)A.s_levels);
+          d = c < 0 ? -mag : mag;
+        }
+      }
+      out[gi] = __fadd_rn(out[gi], d);
+    }
+  }
+}
+
+// ============================================================================ host
+
+struct DenseTotals {
+  int64_t U = 0, W = 0, N = 0;
+};
+
+static DenseTotals dense_totals(const gc_layout* h) {
+  DenseTotals z;
+  for (int t = 0; t < h->num_tensors; ++t) {
+    const int64_t n = h->off[t + 1] - h->off[t];
+    z.U += units_of(n);
+    z.W += (n + 31) >> 5;
+  }
+  z.N = h->off[h->num_tensors];
+  return z;
+}
+
+struct DenseCarve {
+  size_t o_max, zero_bytes, o_units, o_woff, o_part, total;
+};
+
+static DenseCarve carve_dense(int T, const DenseTotals& z) {
+  DenseCarve c;
+  size_t p = DIAG_BYTES;
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes, 256);
+    return at;
+  };
+  c.o_max = take(4 * (size_t)T);
+  c.zero_bytes = p;
+  c.o_units = take(8 * (size_t)(T + 1));
+  c.o_woff = take(8 * (size_t)(T + 1));
+  c.o_part = take(8 * (size_t)z.U);
+  c.total = p;
+  return c;
+}
+
+size_t dense_workspace_bytes(const gc_layout* h) {
+  return carve_dense(h->num_tensors, dense_totals(h)).total;
+}
+
+template <class K>
+static int dense_grid(K kernel, int64_t units) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, DTHREADS, 0);
+  if (per_sm < 1) per_sm = 1;
+  int64_t want = (units + DWARPS - 1) / DWARPS;
+  int64_t grid = (int64_t)sms * per_sm;
+  if (grid > want) grid = want;
+  if (grid < 1) grid = 1;
+  return (int)grid;
+}
+
+static gc_status dense_setup(const gc_layout* dev, const gc_layout* host, void* ws, size_t ws_bytes,
+                             cudaStream_t s, DenseArgs* A) {
+  gc_status st = validate_layout(host, false);
+  if (st != GC_OK) return st;
+  if (!dev || !dev->off || dev->num_tensors != host->num_tensors) return GC_ERR_INVALID_ARG;
+  const DenseTotals z = dense_totals(host);
+  const DenseCarve c = carve_dense(host->num_tensors, z);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  memset(A, 0, sizeof *A);
+  A->T = host->num_tensors;
+  A->off = dev->off;
+  A->diag = reinterpret_cast<uint32_t*>(w);
+  A->maxkey = reinterpret_cast<uint32_t*>(w + c.o_max);
+  A->units_off = reinterpret_cast<int64_t*>(w + c.o_units);
+  A->woff = reinterpret_cast<int64_t*>(w + c.o_woff);
+  A->upart = reinterpret_cast<double*>(w + c.o_part);
+  A->U = z.U;
+  A->W = z.W;
+  A->N = z.N;
+  if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
+  k_dplan<<<1, 1024, 0, s>>>(*A);
+  return GC_OK;
+}
+
+template <int OP, bool EF>
+static void launch_quant(const DenseArgs& A, cudaStream_t s) {
+  k_dense1<OP, EF><<<dense_grid(k_dense1<OP, EF>, A.U), DTHREADS, 0, s>>>(A);
+  k_dreduce<<<A.T, 256, 0, s>>>(A);
+  if (OP == DOP_SIGN)
+    k_sign2<EF><<<dense_grid(k_sign2<EF>, A.U), DTHREADS, 0, s>>>(A);
+  else
+    k_quant2<OP, EF><<<dense_grid(k_quant2<OP, EF>, A.U), DTHREADS, 0, s>>>(A);
+}
+
+}  // namespace gc
+
+using namespace gc;
+
+extern "C" gc_status gc_sign_compress(const gc_layout* dev, const gc_layout* host, const float* g,
+                                      float* e, uint32_t* bits, float* mean_abs, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  if (!g || !bits || !mean_abs) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || (e && !aligned16(e))) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DenseArgs A;
+  gc_status st = dense_setup(dev, host, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.op = DOP_SIGN;
+  A.ef = e ? 1 : 0;
+  A.g = g;
+  A.e = e;
+  A.bits = bits;
+  A.scale = mean_abs;
+  if (e)
+    launch_quant<DOP_SIGN, true>(A, s);
+  else
+    launch_quant<DOP_SIGN, false>(A, s);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layout* host,
+                                            const float* g, float* e, int8_t* codes, float* scale,
+                                            int32_t mode, int32_t s_levels, uint64_t seed,
+                                            uint64_t iter, void* workspace, size_t ws_bytes,
+                                            void* stream) {
+  if (!g || !codes || !scale) return GC_ERR_INVALID_ARG;
+  if (mode != GC_Q_INT8 && mode != GC_Q_QSGD) return GC_ERR_INVALID_ARG;
+  if (mode == GC_Q_QSGD && (s_levels < 1 || s_levels > 127)) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || (e && !aligned16(e)) || ((uintptr_t)codes & 3u)) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DenseArgs A;
+  gc_status st = dense_setup(dev, host, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.op = (mode == GC_Q_INT8) ? DOP_INT8 : DOP_QSGD;
+  A.ef = e ? 1 : 0;
+  A.s_levels = s_levels;
+  A.g = g;
+  A.e = e;
+  A.codes = codes;
+  A.scale = scale;
+  A.seed = seed;
+  A.iter = iter;
+  if (mode == GC_Q_INT8) {
+    if (e) launch_quant<DOP_INT8, true>(A, s);
+    else launch_quant<DOP_INT8, false>(A, s);
+  } else {
+    if (e) launch_quant<DOP_QSGD, true>(A, s);
+    else launch_quant<DOP_QSGD, false>(A, s);
+  }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const gc_layout* host,
+                                                    int32_t W, int32_t kind, int32_t s_levels,
+                                                    const void* const* data,
+                                                    const float* const* scale, float* out,
+                                                    void* workspace, size_t ws_bytes,
+                                                    void* stream) {
+  if (W < 0 || !out || (W > 0 && (!data || !scale))) return GC_ERR_INVALID_ARG;
+  if (kind != GC_DENSE_SIGN && kind != GC_DENSE_INT8 && kind != GC_DENSE_QSGD) return GC_ERR_INVALID_ARG;
+  if (kind == GC_DENSE_QSGD && (s_levels < 1 || s_levels > 127)) return GC_ERR_INVALID_ARG;
+  if (!aligned16(out)) return GC_ERR_ALIGNMENT;
+  for (int w = 0; w < W; ++w)
+    if (!data[w] || !scale[w]) return GC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DenseArgs A;
+  gc_status st = dense_setup(dev, host, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.s_levels = s_levels;
+  for (int w = 0; w < W; ++w) {
+    if (kind == GC_DENSE_SIGN)
+      k_ddecode<GC_DENSE_SIGN><<<dense_grid(k_ddecode<GC_DENSE_SIGN>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+    else if (kind == GC_DENSE_INT8)
+      k_ddecode<GC_DENSE_INT8><<<dense_grid(k_ddecode<GC_DENSE_INT8>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+    else
+      k_ddecode<GC_DENSE_QSGD><<<dense_grid(k_ddecode<GC_DENSE_QSGD>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+  }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}

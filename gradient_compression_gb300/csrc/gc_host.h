@@ -1,0 +1,37 @@
+// Host-side helpers of libgc: argument validation and workspace sizing.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gc.h"
+
+namespace gc {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0u; }
+
+// Checks a host layout: T >= 1, off[0] = 0, 1 <= n_t < 2^31; with
+// `sparse`, also 0 <= k_t <= n_t and koff = prefix sum of k.
+inline gc_status validate_layout(const gc_layout* h, bool sparse) {
+  if (!h || h->num_tensors < 1 || !h->off) return GC_ERR_INVALID_ARG;
+  if (sparse && (!h->k || !h->koff)) return GC_ERR_INVALID_ARG;
+  if (h->off[0] != 0) return GC_ERR_LAYOUT;
+  if (sparse && h->koff[0] != 0) return GC_ERR_LAYOUT;
+  for (int t = 0; t < h->num_tensors; ++t) {
+    const int64_t n = h->off[t + 1] - h->off[t];
+    if (n < 1 || n > INT64_C(2147483647)) return GC_ERR_LAYOUT;
+    if (sparse) {
+      const int64_t k = h->k[t];
+      if (k < 0 || k > n) return GC_ERR_LAYOUT;
+      if (h->koff[t + 1] - h->koff[t] != k) return GC_ERR_LAYOUT;
+    }
+  }
+  return GC_OK;
+}
+
+// Defined by the operation files.
+size_t topk_workspace_bytes(const gc_layout* h, bool sampled);
+size_t dense_workspace_bytes(const gc_layout* h);
+
+}  // namespace gc

@@ -1,0 +1,1135 @@
+// EF Top-k / random-k / momentum-corrected Top-k compression (sm_103a).
+//
+// Method: mbrenndoerfer.com "Gradient Compression", Top-K Sparsification
+// (g^ = TopK(g + e), e = (g + e) - g^, fp32 value + int32 index payload);
+// inferensys.com zh glossary (Random-k; Top-k + 8-bit); inferensys.com
+// "Gradient Sparsification" (per-layer selection, momentum correction and
+// factor masking).
+//
+// Pipeline for one call (all tensors of the arena at once, stream-ordered):
+//   plan       per-tensor prefix tables (units, unit blocks, candidate and
+//              sample regions) from the device layout
+//   sample1/2  a strided sample of acc per tensor -> a threshold estimate
+//              t_est well below the k-th magnitude (Top-k, momentum only;
+//              random-k keys are uniform, so t_est is set analytically)
+//   stream     THE pass over HBM: acc = g + e (or the momentum update),
+//              write-back of e (u, v), and emission of every element whose
+//              key >= t_est into an index-ordered per-unit candidate chunk,
+//              plus the level-1 histogram of candidate keys
+//   select     exact radix select (11 + 11 + 10 bits) of the k-th key over
+//              the candidates; a tensor whose candidates are insufficient
+//              (fewer than k, or overflow) is selected by full passes over
+//              its acc instead (same result)
+//   count/scan/write  index-ordered compaction of the kept set into the
+//              payload, int8 stochastic rounding, and the residual scatter
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "gc_common.cuh"
+#include "gc_host.h"
+
+namespace gc {
+
+enum { MODE_TOPK = 0, MODE_RANDK = 1, MODE_MOM = 2 };
+enum { PH_S1 = 0, PH_S2 = 1, PH_C1 = 2, PH_C1D = 3, PH_C2 = 4, PH_C3 = 5 };
+
+struct TopkArgs {
+  int T;
+  int mode;
+  uint32_t flags;
+  int int8;
+  int ef;
+  int unbiased;
+  int masking;
+  float beta;
+  const int64_t* off;
+  const int64_t* kk;
+  const int64_t* koff;
+  const float* g;
+  float* e;
+  float* u;
+  float* v;
+  int32_t* idx;
+  float* val;
+  int8_t* q;
+  float* scale;
+  uint64_t seed, iter;
+  // workspace
+  uint32_t* diag;
+  TensorState* ts;
+  uint32_t* hist;
+  int64_t* units_off;
+  int64_t* ublk_off;
+  int64_t* cand_off;
+  int64_t* soff;
+  uint2* chunk;
+  uint32_t* ugt;
+  uint32_t* ueq;
+  uint32_t* bgt;
+  uint32_t* beq;
+  uint32_t* ckey;
+  int32_t* cidx;
+  float* cval;
+  uint32_t* skey;
+  int64_t U, UB, C, S, N, K;
+};
+
+// ============================================================================ plan
+
+__device__ int64_t block_excl_scan_i64(int64_t v, int64_t* s_warp, int64_t* total) {
+  const unsigned lane = lane_id(), w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t y = __shfl_up_sync(FULL, x, d);
+    if (lane >= (unsigned)d) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int64_t z = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t y = __shfl_up_sync(FULL, z, d);
+      if (lane >= (unsigned)d) z += y;
+    }
+    if (lane < nw) s_warp[lane] = z;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int64_t before = (w == 0 ? 0 : s_warp[w - 1]);
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0;
+  const bool sampled = (A.mode != MODE_RANDK);
+  for (int base = 0; base < A.T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    int64_t nu = 0, nb = 0, nc = 0, ns = 0;
+    if (t < A.T) {
+      const int64_t n = A.off[t + 1] - A.off[t];
+      const int64_t k = A.kk[t];
+      if (n < 1 || n > INT64_C(2147483647) || k < 0 || k > n || A.koff[t + 1] - A.koff[t] != k) s_bad = 1;
+      nu = units_of(n);
+      nb = ublocks_of(n);
+      nc = cand_capacity(n, k);
+      if (sampled && k > 0) {
+        int64_t runs, stride, m;
+        sample_plan(n, k, &runs, &stride, &m);
+        ns = m;
+      }
+      TensorState st;
+      memset(&st, 0, sizeof st);
+      if (k <= 0) st.flags = TS_NOEMIT;
+      if (A.mode == MODE_RANDK && k > 0) {
+        // keys ~kappa, kappa uniform on 32-bit words: emit kappa < tau with
+        // tau chosen so that about k + 4 sqrt(k) + 16 elements qualify
+        const double want = (double)k + 4.0 * sqrt((double)k) + 16.0;
+        const double tau = floor(want * 4294967296.0 / (double)n);
+        st.t_est = (tau >= 4294967296.0) ? 0u : ~((uint32_t)tau - 1u);
+      }
+      if (k >= n) st.t_est = 0u;
+      A.ts[t] = st;
+      if (A.int8 && k <= 0) A.scale[t] = 0.0f;
+    }
+    int64_t tot;
+    int64_t eu = block_excl_scan_i64(nu, s_warp, &tot);
+    if (t < A.T) A.units_off[t] = carry_u + eu;
+    carry_u += tot;
+    int64_t eb = block_excl_scan_i64(nb, s_warp, &tot);
+    if (t < A.T) A.ublk_off[t] = carry_b + eb;
+    carry_b += tot;
+    int64_t ec = block_excl_scan_i64(nc, s_warp, &tot);
+    if (t < A.T) A.cand_off[t] = carry_c + ec;
+    carry_c += tot;
+    int64_t es = block_excl_scan_i64(ns, s_warp, &tot);
+    if (t < A.T) A.soff[t] = carry_s + es;
+    carry_s += tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    A.units_off[A.T] = carry_u;
+    A.ublk_off[A.T] = carry_b;
+    A.cand_off[A.T] = carry_c;
+    A.soff[A.T] = carry_s;
+    if (s_bad || carry_u != A.U || carry_b != A.UB || carry_c != A.C || carry_s != A.S ||
+        A.off[0] != 0 || A.off[A.T] != A.N || A.koff[0] != 0 || A.koff[A.T] != A.K) {
+      A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
+      A.diag[DIAG_ABORT] = 1u;
+    }
+  }
+}
+
+// ============================================================================ acc of one element
+
+// acc of element gi computed from the inputs (used by the sampler; the
+// streaming pass computes the same expression).
+template <int MODE>
+__device__ __forceinline__ float acc_from_inputs(const TopkArgs& A, int64_t gi) {
+  if (MODE == MODE_MOM) {
+    const float un = __fadd_rn(__fmul_rn(A.beta, A.u[gi]), A.g[gi]);
+    return __fadd_rn(A.v[gi], un);
+  }
+  return A.ef ? __fadd_rn(A.g[gi], A.e[gi]) : A.g[gi];
+}
+
+// After the streaming pass: the kept value source and the selection key.
+template <int MODE>
+__device__ __forceinline__ const float* value_source(const TopkArgs& A) {
+  if (MODE == MODE_MOM) return A.v;
+  return A.ef ? A.e : A.g;
+}
+
+template <int MODE>
+__device__ __forceinline__ uint32_t key_of(const TopkArgs& A, float value, int64_t gi) {
+  if (MODE == MODE_RANDK) return ~philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_RANDK);
+  return mag_key(value);
+}
+
+__device__ __forceinline__ bool aborted(const TopkArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
+
+// ============================================================================ sampling
+
+constexpr int SX = 16;  // CTAs per tensor in the sampling and candidate-histogram kernels
+
+template <int MODE>
+__global__ void __launch_bounds__(256) k_sample1(TopkArgs A) {
+  __shared__ uint32_t sh[NBINS];
+  const int t = blockIdx.x;
+  if (aborted(A)) return;
+  const TensorState* st = A.ts + t;
+  if (st->flags & TS_NOEMIT) return;
+  const int64_t base = A.off[t], n = A.off[t + 1] - base;
+  if (A.kk[t] >= n) return;  // t_est = 0 already
+  int64_t runs, stride, m;
+  sample_plan(n, A.kk[t], &runs, &stride, &m);
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  const int half = threadIdx.x >> 4, l16 = threadIdx.x & 15;  // 16 runs per CTA step
+  uint32_t* sk = A.skey + A.soff[t];
+  for (int64_t r0 = (int64_t)blockIdx.y * 16; r0 < runs; r0 += (int64_t)gridDim.y * 16) {
+    const int64_t r = r0 + half;
+    const int64_t li = r * stride + l16;
+    const bool valid = (r < runs) && (li < n);
+    uint32_t key = 0;
+    if (valid) {
+      key = mag_key(acc_from_inputs<MODE>(A, base + li));
+      sk[r * RUN + l16] = key;
+    }
+    smem_hist_add(sh, key >> 21, valid);
+  }
+  __syncthreads();
+  uint32_t* row = A.hist + (size_t)t * NBINS;
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
+    if (sh[i]) atomicAdd(row + i, sh[i]);
+}
+
+__global__ void __launch_bounds__(256) k_sample2(TopkArgs A) {
+  __shared__ uint32_t sh[NBINS];
+  const int t = blockIdx.x;
+  if (aborted(A)) return;
+  const TensorState st = A.ts[t];
+  if (st.flags & (TS_NOEMIT | TS_TEST_DONE)) return;
+  const int64_t n = A.off[t + 1] - A.off[t];
+  if (A.kk[t] >= n) return;
+  int64_t runs, stride, m;
+  sample_plan(n, A.kk[t], &runs, &stride, &m);
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  const uint32_t* sk = A.skey + A.soff[t];
+  // small tensors store their sample at the element's own index
+  const int64_t len = (n <= SMALL_N) ? n : m;
+  for (int64_t i0 = (int64_t)blockIdx.y * blockDim.x; i0 < len; i0 += (int64_t)gridDim.y * blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
+    const bool valid = i < len;
+    const uint32_t key = valid ? sk[i] : 0u;
+    const bool hit = valid && ((key >> 21) == st.prefix);
+    smem_hist_add(sh, (key >> 10) & 0x7FFu, hit);
+  }
+  __syncthreads();
+  uint32_t* row = A.hist + (size_t)t * NBINS;
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
+    if (sh[i]) atomicAdd(row + i, sh[i]);
+}
+
+// ============================================================================ select
+
+__device__ void block_scan_u32(uint32_t v, uint32_t* s_warp, uint32_t* excl, uint32_t* total) {
+  const unsigned lane = lane_id(), w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned tw;
+  const unsigned e = warp_excl_scan(v, lane, &tw);
+  if (lane == 0) s_warp[w] = tw;
+  __syncthreads();
+  if (w == 0) {
+    unsigned z = lane < nw ? s_warp[lane] : 0u, tz;
+    const unsigned ez = warp_excl_scan(z, lane, &tz);
+    if (lane < nw) s_warp[lane] = ez;
+    if (lane == 0) s_warp[31] = tz;
+  }
+  __syncthreads();
+  *excl = s_warp[w] + e;
+  *total = s_warp[31];
+  __syncthreads();
+}
+
+// One radix level of the k-th key search for every tensor (one CTA each).
+__global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
+  __shared__ uint32_t s_warp[32];
+  __shared__ uint32_t s_res[3];
+  const int t = blockIdx.x;
+  if (aborted(A)) return;
+  TensorState* st = A.ts + t;
+  const uint32_t flags = st->flags;
+  if (flags & TS_NOEMIT) return;
+  const int64_t n = A.off[t + 1] - A.off[t];
+  const int64_t k = A.kk[t];
+  uint32_t* row = A.hist + (size_t)t * NBINS;
+  uint32_t rank = st->rank;
+
+  if (phase == PH_S1 || phase == PH_S2) {
+    if (k >= n) return;
+    if (phase == PH_S2 && (flags & TS_TEST_DONE)) return;
+    if (phase == PH_S1) {
+      int64_t runs, stride, m;
+      sample_plan(n, k, &runs, &stride, &m);
+      int64_t j;
+      if (m >= n) {
+        j = k;
+      } else {
+        const double lam = (double)k * (double)m / (double)n;
+        j = (int64_t)ceil(lam + 4.0 * sqrt(lam) + 4.0);
+      }
+      if (j > m) {
+        if (threadIdx.x == 0) {
+          st->t_est = 0u;
+          st->flags = flags | TS_TEST_DONE;
+        }
+        for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+        return;
+      }
+      rank = (uint32_t)j;
+    }
+  } else if (phase == PH_C1) {
+    const int64_t cap = A.cand_off[t + 1] - A.cand_off[t];
+    const int64_t cnt = st->cand_count;
+    const bool dense = (flags & TS_OVERFLOW) || cnt > cap || cnt < k || (A.flags & GC_FORCE_EXACT);
+    if (dense) {
+      for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+      if (threadIdx.x == 0) {
+        st->flags = flags | TS_DENSE;
+        st->maxkey = 0u;
+        st->prefix = 0u;
+        st->rank = (uint32_t)k;
+        atomicAdd(A.diag + DIAG_EXACT, 1u);
+        if ((flags & TS_OVERFLOW) || cnt > cap) atomicAdd(A.diag + DIAG_OVF, 1u);
+      }
+      return;
+    }
+    rank = (uint32_t)k;
+  } else if (phase == PH_C1D) {
+    if (!(flags & TS_DENSE)) return;
+    rank = (uint32_t)k;
+  }
+
+  // Thread i owns bins 2047-8i down to 2040-8i (keys in descending order).
+  uint32_t h[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = row[NBINS - 1 - 8 * threadIdx.x - j];
+    sum += h[j];
+  }
+  uint32_t pre, total;
+  block_scan_u32(sum, s_warp, &pre, &total);
+  if (threadIdx.x == 0) s_res[0] = 0xFFFFFFFFu;
+  __syncthreads();
+  const uint32_t r0 = rank - 1u;
+  if (rank >= 1u && rank <= total && r0 >= pre && r0 < pre + sum) {
+    uint32_t acc = pre;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 < acc + h[j]) {
+        s_res[0] = NBINS - 1 - 8 * threadIdx.x - j;
+        s_res[1] = acc;
+        break;
+      }
+      acc += h[j];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = s_res[0];
+  if (b == 0xFFFFFFFFu) {
+    atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+    st->flags = flags | TS_NOEMIT;  // never write a wrong payload
+    return;
+  }
+  const uint32_t above = s_res[1];
+  rank -= above;
+  switch (phase) {
+    case PH_S1:
+      st->prefix = b;
+      st->rank = rank;
+      break;
+    case PH_S2:
+      st->t_est = (st->prefix << 21) | (b << 10);
+      st->prefix = 0u;
+      st->rank = 0u;
+      break;
+    case PH_C1:
+    case PH_C1D:
+      st->prefix = b;
+      st->rank = rank;
+      break;
+    case PH_C2:
+      st->prefix = (st->prefix << 11) | b;
+      st->rank = rank;
+      break;
+    case PH_C3: {
+      st->thr = (st->prefix << 10) | b;
+      st->r_eq = rank;
+      st->rank = rank;
+      if (A.int8) A.scale[t] = __fdiv_rn(key_magnitude(st->maxkey), 127.0f);
+      break;
+    }
+  }
+}
+
+// ============================================================================ streaming pass
+
+// Appends this lane's flagged entries (bit j of m -> entry j) to the warp's
+// shared-memory chunk, in (lane, j) order, i.e. index order.
+__device__ __forceinline__ void warp_append(float* sval, uint32_t* skey, uint16_t* spos, int& cnt,
+                                            bool& ovf, unsigned m, const uint32_t* key,
+                                            const float* val, int pos0, unsigned lane) {
+  unsigned pre, tot;
+  warp_count_scan(__popc(m), lane, &pre, &tot);
+  if (ovf || cnt + (int)tot > WCAP) {
+    ovf = true;
+    return;
+  }
+  int o = cnt + (int)pre;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if ((m >> j) & 1u) {
+      sval[o] = val[j];
+      skey[o] = key[j];
+      spos[o] = (uint16_t)(pos0 + j);
+      ++o;
+    }
+  }
+  cnt += (int)tot;
+}
+
+template <int MODE, bool EF, bool LOADG>
+__device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t gi, float* value,
+                                              uint32_t* key) {
+  float x = 0.0f;
+  if (MODE == MODE_MOM) {
+    const float un = __fadd_rn(__fmul_rn(A.beta, A.u[gi]), A.g[gi]);
+    x = __fadd_rn(A.v[gi], un);
+    A.u[gi] = un;
+    A.v[gi] = x;
+  } else if (LOADG) {
+    x = A.g[gi];
+    if (EF) {
+      x = __fadd_rn(x, A.e[gi]);
+      A.e[gi] = x;
+    }
+  }
+  *value = x;
+  *key = (MODE == MODE_RANDK) ? ~philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_RANDK)
+                              : mag_key(x);
+}
+
+constexpr int STREAM_THREADS = 256;
+constexpr int STREAM_WARPS = STREAM_THREADS / 32;
+constexpr int STREAM_UNROLL = 4;
+constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
+
+template <int MODE, bool EF, bool LOADG>
+__global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const unsigned lane = lane_id();
+  float* sval = reinterpret_cast<float*>(smem) + warp * WCAP;
+  uint32_t* skey = reinterpret_cast<uint32_t*>(smem + (size_t)STREAM_WARPS * WCAP * 4) + warp * WCAP;
+  uint16_t* spos = reinterpret_cast<uint16_t*>(smem + (size_t)STREAM_WARPS * WCAP * 8) + warp * WCAP;
+  if (aborted(A)) return;
+  const int64_t nwarps = (int64_t)gridDim.x * STREAM_WARPS;
+  for (int64_t u = (int64_t)blockIdx.x * STREAM_WARPS + warp; u < A.U; u += nwarps) {
+    const int t = find_segment(A.units_off, A.T, u);
+    const int64_t base = A.off[t];
+    const int64_t n = A.off[t + 1] - base;
+    const int64_t lstart = (u - A.units_off[t]) << UNIT_SHIFT;
+    const int len = (int)min((int64_t)UNIT, n - lstart);
+    const int64_t g0 = base + lstart;
+    const bool emit = !(A.ts[t].flags & TS_NOEMIT);
+    const uint32_t test = A.ts[t].t_est;
+    int cnt = 0;
+    bool ovf = false;
+    if ((g0 & 3) == 0) {
+      const int nv = len >> 2;
+      const float4* g4 = reinterpret_cast<const float4*>(A.g + g0);
+      float4* e4 = reinterpret_cast<float4*>(A.e + g0);
+      float4* u4 = reinterpret_cast<float4*>(A.u + g0);
+      float4* v4 = reinterpret_cast<float4*>(A.v + g0);
+      for (int v0 = 0; v0 < nv; v0 += 32 * STREAM_UNROLL) {
+        float4 x[STREAM_UNROLL], y[STREAM_UNROLL], z[STREAM_UNROLL];
+#pragma unroll
+        for (int j = 0; j < STREAM_UNROLL; ++j) {
+          const int vi = v0 + j * 32 + (int)lane;
+          if (vi < nv) {
+            if (LOADG || MODE == MODE_MOM) x[j] = ld_stream(g4 + vi);
+            if (MODE == MODE_MOM) {
+              y[j] = ld_stream(u4 + vi);
+              z[j] = ld_stream(v4 + vi);
+            } else if (EF) {
+              y[j] = ld_stream(e4 + vi);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < STREAM_UNROLL; ++j) {
+          const int vi = v0 + j * 32 + (int)lane;
+          const bool valid = vi < nv;
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t kk[4];
+          if (valid) {
+            if (MODE == MODE_MOM) {
+              float4 un, vn;
+              un.x = __fadd_rn(__fmul_rn(A.beta, y[j].x), x[j].x);
+              un.y = __fadd_rn(__fmul_rn(A.beta, y[j].y), x[j].y);
+              un.z = __fadd_rn(__fmul_rn(A.beta, y[j].z), x[j].z);
+              un.w = __fadd_rn(__fmul_rn(A.beta, y[j].w), x[j].w);
+              vn.x = __fadd_rn(z[j].x, un.x);
+              vn.y = __fadd_rn(z[j].y, un.y);
+              vn.z = __fadd_rn(z[j].z, un.z);
+              vn.w = __fadd_rn(z[j].w, un.w);
+              st_stream(u4 + vi, un);
+              st_stream(v4 + vi, vn);
+              a[0] = vn.x; a[1] = vn.y; a[2] = vn.z; a[3] = vn.w;
+            } else if (LOADG) {
+              float4 s = x[j];
+              if (EF) {
+                s.x = __fadd_rn(s.x, y[j].x);
+                s.y = __fadd_rn(s.y, y[j].y);
+                s.z = __fadd_rn(s.z, y[j].z);
+                s.w = __fadd_rn(s.w, y[j].w);
+                st_stream(e4 + vi, s);
+              }
+              a[0] = s.x; a[1] = s.y; a[2] = s.z; a[3] = s.w;
+            }
+          }
+          unsigned m = 0u;
+          if (MODE == MODE_RANDK) {
+            const uint4 w = philox_block(A.seed, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, PURPOSE_RANDK);
+            kk[0] = ~w.x; kk[1] = ~w.y; kk[2] = ~w.z; kk[3] = ~w.w;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) kk[c] = mag_key(a[c]);
+          }
+          if (valid && emit) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) m |= (kk[c] >= test ? 1u : 0u) << c;
+          }
+          if (__any_sync(FULL, m != 0u))
+            warp_append(sval, skey, spos, cnt, ovf, m, kk, a, vi * 4, lane);
+        }
+      }
+      const int rem = len & 3;
+      if (rem) {
+        const int li = nv * 4 + (int)lane;
+        const bool valid = (int)lane < rem;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t kk[4] = {0u, 0u, 0u, 0u};
+        if (valid) stream_scalar<MODE, EF, LOADG>(A, g0 + li, &a[0], &kk[0]);
+        const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
+        if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
+      }
+    } else {
+      for (int i0 = 0; i0 < len; i0 += 32) {
+        const int li = i0 + (int)lane;
+        const bool valid = li < len;
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t kk[4] = {0u, 0u, 0u, 0u};
+        if (valid) stream_scalar<MODE, EF, LOADG>(A, g0 + li, &a[0], &kk[0]);
+        const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
+        if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
+      }
+    }
+    // flush the unit's candidates as one chunk
+    __syncwarp();
+    uint2 ch = make_uint2(0u, 0u);
+    if (emit && cnt > 0 && !ovf) {
+      uint32_t start = 0u;
+      if (lane == 0) start = atomicAdd(&A.ts[t].cand_count, (uint32_t)cnt);
+      start = __shfl_sync(FULL, start, 0);
+      const int64_t cap = A.cand_off[t + 1] - A.cand_off[t];
+      if ((int64_t)start + cnt > cap) {
+        ovf = true;
+      } else {
+        const int64_t cb = A.cand_off[t] + start;
+        uint32_t mx = 0u;
+        uint32_t* row = A.hist + (size_t)t * NBINS;
+        for (int j = (int)lane; j < cnt; j += 32) {
+          const uint32_t key = skey[j];
+          A.ckey[cb + j] = key;
+          A.cidx[cb + j] = (int32_t)(lstart + spos[j]);
+          A.cval[cb + j] = sval[j];
+          atomicAdd(row + (key >> 21), 1u);
+          mx = max(mx, key);
+        }
+        mx = warp_max_u32(mx);
+        if (lane == 0) atomicMax(&A.ts[t].maxkey, mx);
+        ch = make_uint2(start, (uint32_t)cnt);
+      }
+    }
+    if (lane == 0) {
+      if (emit && ovf) atomicOr(&A.ts[t].flags, TS_OVERFLOW);
+      A.chunk[u] = ch;
+    }
+    __syncwarp();
+  }
+}
+
+// ============================================================================ unit-block kernels
+
+struct UnitBlock {
+  int t;
+  int64_t u0;
+  int nu;
+  int64_t base, n;
+};
+
+__device__ __forceinline__ UnitBlock unit_block(const TopkArgs& A) {
+  UnitBlock r;
+  r.t = find_segment(A.ublk_off, A.T, (int64_t)blockIdx.x);
+  r.u0 = A.units_off[r.t] + ((int64_t)blockIdx.x - A.ublk_off[r.t]) * UB_UNITS;
+  const int64_t u1 = min(r.u0 + UB_UNITS, A.units_off[r.t + 1]);
+  r.nu = (int)(u1 - r.u0);
+  r.base = A.off[r.t];
+  r.n = A.off[r.t + 1] - r.base;
+  return r;
+}
+
+// Histogram level `level` (1, 2, 3) of the keys matching the tensor's
+// prefix.  Level 1 runs only for tensors selected by full passes (the
+// candidate level-1 histogram comes from the streaming pass).
+template <int MODE>
+__global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
+  __shared__ uint32_t sh[NBINS];
+  __shared__ uint32_t s_max;
+  if (aborted(A)) return;
+  const UnitBlock ub = unit_block(A);
+  const TensorState st = A.ts[ub.t];
+  if (st.flags & TS_NOEMIT) return;
+  const bool dense = (st.flags & TS_DENSE) != 0u;
+  if (level == 1 && !dense) return;
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  if (threadIdx.x == 0) s_max = 0u;
+  __syncthreads();
+  const int shift_prev = (level == 2) ? 21 : 10;
+  const uint32_t mask = (level == 3) ? 0x3FFu : 0x7FFu;
+  const int shift = (level == 1) ? 21 : ((level == 2) ? 10 : 0);
+  if (dense) {
+    const unsigned lane = lane_id();
+    const float* src = value_source<MODE>(A);
+    uint32_t mx = 0u;
+    for (int ui = threadIdx.x >> 5; ui < ub.nu; ui += blockDim.x >> 5) {
+      const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
+      const int len = (int)min((int64_t)UNIT, ub.n - lstart);
+      for (int i0 = 0; i0 < len; i0 += 32) {
+        const int64_t li = lstart + i0 + lane;
+        const bool valid = i0 + (int)lane < len;
+        uint32_t key = 0u;
+        if (valid) {
+          const int64_t gi = ub.base + li;
+          const float x = (MODE == MODE_RANDK) ? 0.0f : src[gi];
+          key = key_of<MODE>(A, x, gi);
+        }
+        const bool hit = valid && (level == 1 || (key >> shift_prev) == st.prefix);
+        if (valid) mx = max(mx, key);
+        smem_hist_add(sh, (key >> shift) & mask, hit);
+      }
+    }
+    if (level == 1) {
+      mx = warp_max_u32(mx);
+      if (lane == 0) atomicMax(&s_max, mx);
+    }
+  } else if (threadIdx.x < ub.nu) {
+    const uint2 ch = A.chunk[ub.u0 + threadIdx.x];
+    const int64_t cb = A.cand_off[ub.t] + ch.x;
+    for (uint32_t j = 0; j < ch.y; ++j) {
+      const uint32_t key = A.ckey[cb + j];
+      if ((key >> shift_prev) == st.prefix) atomicAdd(sh + ((key >> shift) & mask), 1u);
+    }
+  }
+  __syncthreads();
+  uint32_t* row = A.hist + (size_t)ub.t * NBINS;
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
+    if (sh[i]) atomicAdd(row + i, sh[i]);
+  if (level == 1 && threadIdx.x == 0) atomicMax(&A.ts[ub.t].maxkey, s_max);
+}
+
+// Per-unit counts of keys above / equal to the k-th key, and their sums
+// per unit block.
+template <int MODE>
+__global__ void __launch_bounds__(256) k_count(TopkArgs A) {
+  __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
+  __shared__ uint32_t s_warp[32];
+  if (aborted(A)) return;
+  const UnitBlock ub = unit_block(A);
+  const TensorState st = A.ts[ub.t];
+  const int tid = threadIdx.x;
+  s_gt[tid] = 0u;
+  s_eq[tid] = 0u;
+  __syncthreads();
+  if (!(st.flags & TS_NOEMIT)) {
+    if (st.flags & TS_DENSE) {
+      const unsigned lane = lane_id();
+      const float* src = value_source<MODE>(A);
+      for (int ui = tid >> 5; ui < ub.nu; ui += blockDim.x >> 5) {
+        const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
+        const int len = (int)min((int64_t)UNIT, ub.n - lstart);
+        uint32_t gt = 0u, eq = 0u;
+        for (int i0 = 0; i0 < len; i0 += 32) {
+          const bool valid = i0 + (int)lane < len;
+          uint32_t key = 0u;
+          if (valid) {
+            const int64_t gi = ub.base + lstart + i0 + lane;
+            key = key_of<MODE>(A, (MODE == MODE_RANDK) ? 0.0f : src[gi], gi);
+          }
+          gt += __popc(__ballot_sync(FULL, valid && key > st.thr));
+          eq += __popc(__ballot_sync(FULL, valid && key == st.thr));
+        }
+        if (lane == 0) {
+          s_gt[ui] = gt;
+          s_eq[ui] = eq;
+        }
+      }
+    } else if (tid < ub.nu) {
+      const uint2 ch = A.chunk[ub.u0 + tid];
+      const int64_t cb = A.cand_off[ub.t] + ch.x;
+      uint32_t gt = 0u, eq = 0u;
+      for (uint32_t j = 0; j < ch.y; ++j) {
+        const uint32_t key = A.ckey[cb + j];
+        gt += key > st.thr;
+        eq += key == st.thr;
+      }
+      s_gt[tid] = gt;
+      s_eq[tid] = eq;
+    }
+  }
+  __syncthreads();
+  const uint32_t gt = s_gt[tid], eq = s_eq[tid];
+  if (tid < ub.nu) {
+    A.ugt[ub.u0 + tid] = gt;
+    A.ueq[ub.u0 + tid] = eq;
+  }
+  uint32_t pre, tg, te;
+  block_scan_u32(gt, s_warp, &pre, &tg);
+  block_scan_u32(eq, s_warp, &pre, &te);
+  if (tid == 0) {
+    A.bgt[blockIdx.x] = tg;
+    A.beq[blockIdx.x] = te;
+  }
+}
+
+// Exclusive scan of the unit-block sums of each tensor (one CTA each).
+__global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
+  __shared__ uint32_t s_warp[32];
+  if (aborted(A)) return;
+  const int t = blockIdx.x;
+  const int64_t b0 = A.ublk_off[t], b1 = A.ublk_off[t + 1];
+  uint32_t carry_g = 0u, carry_e = 0u;
+  for (int64_t c = b0; c < b1; c += blockDim.x) {
+    const int64_t b = c + threadIdx.x;
+    const uint32_t g = b < b1 ? A.bgt[b] : 0u;
+    const uint32_t e = b < b1 ? A.beq[b] : 0u;
+    uint32_t pg, tg, pe, te;
+    block_scan_u32(g, s_warp, &pg, &tg);
+    block_scan_u32(e, s_warp, &pe, &te);
+    if (b < b1) {
+      A.bgt[b] = carry_g + pg;
+      A.beq[b] = carry_e + pe;
+    }
+    carry_g += tg;
+    carry_e += te;
+  }
+}
+
+// Writes one kept element: payload slot `pos` (absolute), residual.
+template <int MODE>
+__device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base, int64_t n,
+                                          int64_t li, float x, int64_t pos, float s) {
+  if (pos >= A.koff[t + 1]) {  // only reachable if the selection were inconsistent
+    atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+    return;
+  }
+  const int64_t gi = base + li;
+  A.idx[pos] = (int32_t)li;
+  if (MODE == MODE_RANDK) {
+    if (A.unbiased) {
+      const float c = __double2float_rn((double)n / (double)A.kk[t]);
+      A.val[pos] = __fmul_rn(A.g[gi], c);
+    } else {
+      A.val[pos] = x;
+      if (A.ef) A.e[gi] = 0.0f;
+    }
+    return;
+  }
+  float* res = (MODE == MODE_MOM) ? A.v : (A.ef ? A.e : nullptr);
+  if (A.int8) {
+    const int c = int8_code(x, s, philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_INT8));
+    const float d = __fmul_rn((float)c, s);
+    A.q[pos] = (int8_t)c;
+    if (A.val) A.val[pos] = d;
+    if (res) res[gi] = __fsub_rn(x, d);
+  } else {
+    A.val[pos] = x;
+    if (res) res[gi] = 0.0f;
+  }
+  if (MODE == MODE_MOM && A.masking) A.u[gi] = 0.0f;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) k_write(TopkArgs A) {
+  __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
+  __shared__ uint32_t s_warp[32];
+  if (aborted(A)) return;
+  const UnitBlock ub = unit_block(A);
+  const TensorState st = A.ts[ub.t];
+  if (st.flags & TS_NOEMIT) return;
+  const int tid = threadIdx.x;
+  const uint32_t gt = tid < ub.nu ? A.ugt[ub.u0 + tid] : 0u;
+  const uint32_t eq = tid < ub.nu ? A.ueq[ub.u0 + tid] : 0u;
+  uint32_t pg, pe, tg, te;
+  block_scan_u32(gt, s_warp, &pg, &tg);
+  block_scan_u32(eq, s_warp, &pe, &te);
+  s_gt[tid] = A.bgt[blockIdx.x] + pg;
+  s_eq[tid] = A.beq[blockIdx.x] + pe;
+  __syncthreads();
+  const int64_t kbase = A.koff[ub.t];
+  const float s = A.int8 ? A.scale[ub.t] : 0.0f;
+  const uint32_t thr = st.thr, r_eq = st.r_eq;
+  if (st.flags & TS_DENSE) {
+    const unsigned lane = lane_id();
+    const unsigned lt = (1u << lane) - 1u;
+    const float* src = value_source<MODE>(A);
+    for (int ui = tid >> 5; ui < ub.nu; ui += blockDim.x >> 5) {
+      const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
+      const int len = (int)min((int64_t)UNIT, ub.n - lstart);
+      const uint32_t eqb = s_eq[ui];
+      int64_t selpos = (int64_t)s_gt[ui] + min(eqb, r_eq);
+      uint32_t eqrun = 0u;
+      for (int i0 = 0; i0 < len; i0 += 32) {
+        const int64_t li = lstart + i0 + lane;
+        const bool valid = i0 + (int)lane < len;
+        float x = 0.0f;
+        uint32_t key = 0u;
+        if (valid) {
+          const int64_t gi = ub.base + li;
+          x = (MODE == MODE_RANDK && A.unbiased) ? 0.0f : src[gi];
+          key = key_of<MODE>(A, x, gi);
+        }
+        const bool isgt = valid && key > thr, iseq = valid && key == thr;
+        const unsigned eqm = __ballot_sync(FULL, iseq);
+        const bool sel = isgt || (iseq && eqb + eqrun + __popc(eqm & lt) < r_eq);
+        const unsigned selm = __ballot_sync(FULL, sel);
+        if (sel) emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + selpos + __popc(selm & lt), s);
+        selpos += __popc(selm);
+        eqrun += __popc(eqm);
+      }
+    }
+  } else if (tid < ub.nu) {
+    const uint2 ch = A.chunk[ub.u0 + tid];
+    const int64_t cb = A.cand_off[ub.t] + ch.x;
+    const uint32_t eqb = s_eq[tid];
+    int64_t selpos = (int64_t)s_gt[tid] + min(eqb, r_eq);
+    uint32_t eqrun = 0u;
+    for (uint32_t j = 0; j < ch.y; ++j) {
+      const uint32_t key = A.ckey[cb + j];
+      const bool iseq = key == thr;
+      const bool sel = key > thr || (iseq && eqb + eqrun < r_eq);
+      eqrun += iseq;
+      if (sel) {
+        emit_kept<MODE>(A, ub.t, ub.base, ub.n, A.cidx[cb + j], A.cval[cb + j], kbase + selpos, s);
+        ++selpos;
+      }
+    }
+  }
+}
+
+// ============================================================================ host side
+
+struct TopkLayoutTotals {
+  int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0;
+};
+
+static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
+  TopkLayoutTotals r;
+  for (int t = 0; t < h->num_tensors; ++t) {
+    const int64_t n = h->off[t + 1] - h->off[t];
+    const int64_t k = h->k[t];
+    r.U += units_of(n);
+    r.UB += ublocks_of(n);
+    r.C += cand_capacity(n, k);
+    if (sampled && k > 0) {
+      int64_t runs, stride, m;
+      sample_plan(n, k, &runs, &stride, &m);
+      r.S += m;
+    }
+    r.K += k;
+  }
+  r.N = h->off[h->num_tensors];
+  return r;
+}
+
+struct TopkCarve {
+  size_t zero_bytes = 0, total = 0;
+  size_t o_ts, o_hist, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
+      o_cidx, o_cval, o_skey;
+};
+
+static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
+  TopkCarve c;
+  size_t p = DIAG_BYTES;
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes, 256);
+    return at;
+  };
+  c.o_ts = take(sizeof(TensorState) * (size_t)T);
+  c.o_hist = take((size_t)T * NBINS * 4);
+  c.zero_bytes = p;
+  c.o_units = take(8 * (size_t)(T + 1));
+  c.o_ublk = take(8 * (size_t)(T + 1));
+  c.o_cand = take(8 * (size_t)(T + 1));
+  c.o_soff = take(8 * (size_t)(T + 1));
+  c.o_chunk = take(8 * (size_t)z.U);
+  c.o_ugt = take(4 * (size_t)z.U);
+  c.o_ueq = take(4 * (size_t)z.U);
+  c.o_bgt = take(4 * (size_t)z.UB);
+  c.o_beq = take(4 * (size_t)z.UB);
+  c.o_ckey = take(4 * (size_t)z.C);
+  c.o_cidx = take(4 * (size_t)z.C);
+  c.o_cval = take(4 * (size_t)z.C);
+  c.o_skey = take(4 * (size_t)z.S);
+  c.total = p;
+  return c;
+}
+
+size_t topk_workspace_bytes(const gc_layout* h, bool sampled) {
+  return carve_topk(h->num_tensors, totals_of(h, sampled)).total;
+}
+
+template <class K>
+static int stream_grid(K kernel, int64_t units) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, STREAM_THREADS, STREAM_SMEM);
+  if (per_sm < 1) per_sm = 1;
+  int64_t want = (units + STREAM_WARPS - 1) / STREAM_WARPS;
+  int64_t grid = (int64_t)sms * per_sm;
+  if (grid > want) grid = want;
+  if (grid < 1) grid = 1;
+  return (int)grid;
+}
+
+template <int MODE, bool EF, bool LOADG>
+static void launch_stream(const TopkArgs& A, cudaStream_t s) {
+  auto kern = k_stream<MODE, EF, LOADG>;
+  k_stream<MODE, EF, LOADG><<<stream_grid(kern, A.U), STREAM_THREADS, STREAM_SMEM, s>>>(A);
+}
+
+struct PhaseEvents {
+  void* const* ev = nullptr;
+  int n = 0;
+  void mark(int i, cudaStream_t s) const {
+    if (i < n && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+  }
+};
+
+template <int MODE>
+static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
+  const int T = A.T;
+  k_plan<<<1, 1024, 0, s>>>(A);
+  if (MODE != MODE_RANDK) {
+    k_sample1<MODE><<<dim3(T, SX), 256, 0, s>>>(A);
+    k_select<<<T, 256, 0, s>>>(A, PH_S1);
+    k_sample2<<<dim3(T, SX), 256, 0, s>>>(A);
+    k_select<<<T, 256, 0, s>>>(A, PH_S2);
+  }
+  pe.mark(1, s);
+  if (MODE == MODE_MOM) {
+    launch_stream<MODE_MOM, false, true>(A, s);
+  } else if (MODE == MODE_TOPK) {
+    if (A.ef)
+      launch_stream<MODE_TOPK, true, true>(A, s);
+    else
+      launch_stream<MODE_TOPK, false, true>(A, s);
+  } else {
+    if (A.unbiased)
+      launch_stream<MODE_RANDK, false, false>(A, s);
+    else if (A.ef)
+      launch_stream<MODE_RANDK, true, true>(A, s);
+    else
+      launch_stream<MODE_RANDK, false, true>(A, s);
+  }
+  pe.mark(2, s);
+  const unsigned UBg = (unsigned)A.UB;
+  k_select<<<T, 256, 0, s>>>(A, PH_C1);
+  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 1);
+  k_select<<<T, 256, 0, s>>>(A, PH_C1D);
+  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 2);
+  k_select<<<T, 256, 0, s>>>(A, PH_C2);
+  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 3);
+  k_select<<<T, 256, 0, s>>>(A, PH_C3);
+  pe.mark(3, s);
+  k_count<MODE><<<UBg, 256, 0, s>>>(A);
+  k_scan<<<T, 256, 0, s>>>(A);
+  k_write<MODE><<<UBg, 256, 0, s>>>(A);
+  pe.mark(4, s);
+}
+
+static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host, const float* g,
+                          float* e, float* u, float* v, float beta, int32_t* idx, float* val,
+                          int8_t* q, float* scale, uint64_t seed, uint64_t iter, uint32_t flags,
+                          void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe) {
+  gc_status st = validate_layout(host, true);
+  if (st != GC_OK) return st;
+  if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
+    return GC_ERR_INVALID_ARG;
+  const bool int8 = (flags & GC_INT8) != 0u;
+  if (!g || !idx) return GC_ERR_INVALID_ARG;
+  if (int8 && (!q || !scale)) return GC_ERR_INVALID_ARG;
+  if (!int8 && !val) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || (e && !aligned16(e)) || (u && !aligned16(u)) || (v && !aligned16(v)))
+    return GC_ERR_ALIGNMENT;
+  const TopkLayoutTotals z = totals_of(host, mode != MODE_RANDK);
+  const TopkCarve c = carve_topk(host->num_tensors, z);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
+  if (z.K == 0 && z.N == 0) return GC_OK;
+
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  TopkArgs A;
+  memset(&A, 0, sizeof A);
+  A.T = host->num_tensors;
+  A.mode = mode;
+  A.flags = flags;
+  A.int8 = int8 ? 1 : 0;
+  A.ef = (mode == MODE_MOM) ? 0 : ((flags & GC_EF) ? 1 : 0);
+  A.unbiased = (flags & GC_UNBIASED) ? 1 : 0;
+  A.masking = (flags & GC_NO_MASK) ? 0 : 1;
+  A.beta = beta;
+  A.off = dev->off;
+  A.kk = dev->k;
+  A.koff = dev->koff;
+  A.g = g;
+  A.e = e;
+  A.u = u;
+  A.v = v;
+  A.idx = idx;
+  A.val = val;
+  A.q = q;
+  A.scale = scale;
+  A.seed = seed;
+  A.iter = iter;
+  A.diag = reinterpret_cast<uint32_t*>(w);
+  A.ts = reinterpret_cast<TensorState*>(w + c.o_ts);
+  A.hist = reinterpret_cast<uint32_t*>(w + c.o_hist);
+  A.units_off = reinterpret_cast<int64_t*>(w + c.o_units);
+  A.ublk_off = reinterpret_cast<int64_t*>(w + c.o_ublk);
+  A.cand_off = reinterpret_cast<int64_t*>(w + c.o_cand);
+  A.soff = reinterpret_cast<int64_t*>(w + c.o_soff);
+  A.chunk = reinterpret_cast<uint2*>(w + c.o_chunk);
+  A.ugt = reinterpret_cast<uint32_t*>(w + c.o_ugt);
+  A.ueq = reinterpret_cast<uint32_t*>(w + c.o_ueq);
+  A.bgt = reinterpret_cast<uint32_t*>(w + c.o_bgt);
+  A.beq = reinterpret_cast<uint32_t*>(w + c.o_beq);
+  A.ckey = reinterpret_cast<uint32_t*>(w + c.o_ckey);
+  A.cidx = reinterpret_cast<int32_t*>(w + c.o_cidx);
+  A.cval = reinterpret_cast<float*>(w + c.o_cval);
+  A.skey = reinterpret_cast<uint32_t*>(w + c.o_skey);
+  A.U = z.U;
+  A.UB = z.UB;
+  A.C = z.C;
+  A.S = z.S;
+  A.N = z.N;
+  A.K = z.K;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pe.mark(0, s);
+  if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
+  if (mode == MODE_TOPK)
+    launch_pipeline<MODE_TOPK>(A, s, pe);
+  else if (mode == MODE_RANDK)
+    launch_pipeline<MODE_RANDK>(A, s, pe);
+  else
+    launch_pipeline<MODE_MOM>(A, s, pe);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+}  // namespace gc
+
+using namespace gc;
+
+static gc_status topk_entry(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
+                            int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
+                            uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
+                            void* stream, const PhaseEvents& pe) {
+  const uint32_t known = GC_EF | GC_INT8 | GC_RANDK | GC_UNBIASED | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  const bool randk = (flags & GC_RANDK) != 0u;
+  if (randk && (flags & GC_INT8)) return GC_ERR_INVALID_ARG;
+  if ((flags & GC_UNBIASED) && (!randk || (flags & GC_EF))) return GC_ERR_INVALID_ARG;
+  if ((flags & GC_EF) && !e) return GC_ERR_INVALID_ARG;
+  return run_topk(randk ? MODE_RANDK : MODE_TOPK, dev, host, g, (flags & GC_EF) ? e : nullptr,
+                  nullptr, nullptr, 0.0f, idx, val, q, scale, seed, iter, flags, workspace,
+                  ws_bytes, stream, pe);
+}
+
+extern "C" gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host,
+                                         const float* g, float* e, int32_t* idx, float* val,
+                                         int8_t* q, float* scale, uint64_t seed, uint64_t iter,
+                                         uint32_t flags, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+  return topk_entry(dev, host, g, e, idx, val, q, scale, seed, iter, flags, workspace, ws_bytes,
+                    stream, PhaseEvents{});
+}
+
+extern "C" gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc_layout* host,
+                                                  const float* g, float* e, int32_t* idx,
+                                                  float* val, int8_t* q, float* scale,
+                                                  uint64_t seed, uint64_t iter, uint32_t flags,
+                                                  void* workspace, size_t ws_bytes, void* stream,
+                                                  void* const* events, int32_t n_events) {
+  if (n_events < 0 || n_events > 5 || (n_events > 0 && !events)) return GC_ERR_INVALID_ARG;
+  PhaseEvents pe;
+  pe.ev = events;
+  pe.n = n_events;
+  return topk_entry(dev, host, g, e, idx, val, q, scale, seed, iter, flags, workspace, ws_bytes,
+                    stream, pe);
+}
+
+extern "C" gc_status gc_ef_topk_compress_momentum(const gc_layout* dev, const gc_layout* host,
+                                                  const float* g, float* u, float* v, float beta,
+                                                  int32_t* idx, float* val, int8_t* q,
+                                                  float* scale, uint64_t seed, uint64_t iter,
+                                                  uint32_t flags, void* workspace,
+                                                  size_t ws_bytes, void* stream) {
+  const uint32_t known = GC_INT8 | GC_NO_MASK | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if (!u || !v) return GC_ERR_INVALID_ARG;
+  return run_topk(MODE_MOM, dev, host, g, nullptr, u, v, beta, idx, val, q, scale, seed, iter,
+                  flags, workspace, ws_bytes, stream, PhaseEvents{});
+}

@@ -1,0 +1,239 @@
+/*
+ * gc.h -- C ABI of the GB300 error-feedback gradient-compression library
+ * (libgc.so, hand-written sm_103a CUDA).
+ *
+ * The method (page titles and sections it follows):
+ *  - mbrenndoerfer.com "Gradient Compression", Top-K Sparsification:
+ *      g^_t = TopK(g_t + e_{t-1}),   e_t = (g_t + e_{t-1}) - g^_t,
+ *    with a sparse wire format of one fp32 value plus one int32 index per
+ *    kept entry; 1-bit SGD, Q(g) = sign(g) * ||g||_1 / d with a per-layer
+ *    scalar; QSGD, Q_s(g) = ||g|| * sgn(g) * xi(g, s) with stochastic
+ *    rounding; the union of per-worker sparse vectors on the receiver.
+ *  - inferensys.com "Gradient Compression" (zh glossary): Random-k with a
+ *    per-iteration random mask; the Top-k + 8-bit pipeline; all-gather of
+ *    sparse indices and values.
+ *  - inferensys.com "Gradient Compression" (genomic glossary) and
+ *    "Gradient Sparsification": per-layer selection, 8-bit quantization,
+ *    stochastic rounding, DGC momentum correction and momentum factor masking.
+ *
+ * Data model.  A gradient is a flat fp32 "arena"; tensor t (a layer)
+ * occupies elements [off[t], off[t+1]) and is compressed independently.
+ * n_t = off[t+1] - off[t] must satisfy 1 <= n_t <= 2^31 - 1.  Sparse
+ * payloads list, per tensor, k_t entries in ascending TENSOR-LOCAL int32
+ * index order, tensor t's entries at [koff[t], koff[t+1]) with koff the
+ * prefix sum of k.  Sign bits are packed LSB-first, 32 per uint32 word, each
+ * tensor starting on a new word (word offset = sum of ceil(n_t'/32) over
+ * t' < t), pad bits zero.
+ *
+ * Order of selection.  Top-k keeps the k_t elements of largest |x|; equal
+ * magnitudes (and +0 / -0) go to the lower index.  Random-k keeps the k_t
+ * smallest Philox keys, ties to the lower index.
+ *
+ * Random numbers.  Philox4x32-10 (Salmon et al., SC'11).  Element i of the
+ * arena, call (seed, iter) and purpose p (1 int8 rounding, 2 QSGD, 3
+ * random-k) uses word (i mod 4) of the block with counter
+ * (lo32(i/4), hi32(i/4), lo32(iter), p) and key (lo32(seed), hi32(seed)).
+ * Stochastic rounding rounds |x| up iff r * 2^-32 < frac(|x|).
+ *
+ * Arithmetic.  IEEE fp32, round to nearest even, one rounding per written
+ * operation (no fused multiply-add, no flush to zero).  Results are
+ * bit-identical from run to run; per-tensor norms are reduced in a fixed
+ * order.
+ *
+ * Conventions for every entry point.
+ *  - Pointers named "device" point to device memory owned by the caller;
+ *    the library never allocates, frees or retains them.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and return; nothing synchronises except
+ *    gc_get_device_status.
+ *  - A layout is passed twice: `dev` (its arrays in device memory, read by
+ *    the kernels) and `host` (the same values in host memory, used for
+ *    validation and launch sizing).  They must hold identical values; a
+ *    mismatch in the totals is detected on the device and reported by
+ *    gc_get_device_status as GC_DIAG_LAYOUT_MISMATCH, and all kernels of
+ *    that call then do nothing.
+ *  - `workspace` is caller-owned device scratch of at least
+ *    gc_workspace_size() bytes for that operation and layout, 256-byte
+ *    aligned.  It may be reused between calls but not shared by calls that
+ *    run concurrently.
+ *  - Buffers must not alias each other, except where stated.
+ *  - g, e, u, v, out must be 16-byte aligned.
+ *  - Argument errors are returned before anything is enqueued.  No C++
+ *    exception crosses this interface.
+ */
+#ifndef GC_H_
+#define GC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gc_status {
+  GC_OK = 0,
+  GC_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad flag or mode */
+  GC_ERR_LAYOUT = 2,      /* off not starting at 0 / not increasing, n_t >= 2^31, k_t > n_t,
+                             koff not the prefix sum of k */
+  GC_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than gc_workspace_size */
+  GC_ERR_ALIGNMENT = 4,   /* a data pointer is not 16-byte aligned */
+  GC_ERR_CUDA = 5,        /* a CUDA launch or copy failed (cudaGetLastError) */
+  GC_ERR_DEVICE = 6       /* gc_get_device_status found an error word set on the device */
+} gc_status;
+
+/* Flags of the sparse compressors. */
+#define GC_EF 0x1u          /* error feedback: acc = g + e, residual written back to e */
+#define GC_INT8 0x2u        /* Top-k only: kept values sent as int8 codes + one fp32 scale per tensor */
+#define GC_RANDK 0x4u       /* random-k selection instead of Top-k */
+#define GC_UNBIASED 0x8u    /* random-k only, without GC_EF: send g * (n/k), no residual */
+#define GC_NO_MASK 0x10u    /* momentum only: keep u on the selected set (no factor masking) */
+#define GC_FORCE_EXACT 0x100u /* select with full passes over the tensor instead of the
+                                 sampled candidate threshold (same results; for testing) */
+
+/* Operations, for gc_workspace_size. */
+typedef enum gc_op {
+  GC_OP_TOPK = 0,       /* gc_ef_topk_compress (Top-k and random-k) */
+  GC_OP_MOMENTUM = 1,   /* gc_ef_topk_compress_momentum */
+  GC_OP_SIGN = 2,       /* gc_sign_compress */
+  GC_OP_QUANTIZE = 3,   /* gc_quantize_stochastic */
+  GC_OP_DECOMPRESS = 4  /* gc_sparse_decompress_accumulate, gc_dense_decompress_accumulate */
+} gc_op;
+
+/* Dense quantizer modes. */
+#define GC_Q_INT8 0 /* s = max|acc| / 127, code = sgn * min(127, SR(|acc| / s)) */
+#define GC_Q_QSGD 1 /* N = ||acc||_2, code = sgn * min(s, SR(|acc| * s / N)) */
+
+/* Dense payload kinds for gc_dense_decompress_accumulate. */
+#define GC_DENSE_SIGN 0
+#define GC_DENSE_INT8 1
+#define GC_DENSE_QSGD 2
+
+typedef struct gc_layout {
+  int32_t num_tensors;  /* T >= 1 */
+  const int64_t* off;   /* [T+1] element offsets, off[0] = 0, strictly increasing */
+  const int64_t* k;     /* [T] kept entries per tensor, 0 <= k_t <= n_t; may be NULL for dense ops */
+  const int64_t* koff;  /* [T+1] prefix sum of k; may be NULL for dense ops */
+} gc_layout;
+
+/* Diagnostics of the last call that used a workspace. */
+typedef struct gc_diag {
+  uint32_t error_bits;       /* GC_DIAG_* bits */
+  uint32_t exact_tensors;    /* tensors selected by full passes (fallback or GC_FORCE_EXACT) */
+  uint32_t overflow_tensors; /* tensors whose candidate list overflowed (then selected exactly) */
+  uint32_t reserved;
+} gc_diag;
+
+#define GC_DIAG_LAYOUT_MISMATCH 0x1u /* dev and host layouts disagree; the call did nothing */
+#define GC_DIAG_SELECT 0x2u          /* internal selection inconsistency (should never be set) */
+#define GC_DIAG_INDEX_RANGE 0x4u     /* decompress met a payload index >= n_t; entry skipped */
+
+/* Bytes of workspace that operation `op` needs for layout `host` and
+ * `flags`.  *bytes is set on GC_OK. */
+gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32_t flags, size_t* bytes);
+
+/* EF Top-k (or random-k) compression of a whole arena (mbrenndoerfer.com
+ * "Gradient Compression", Top-K Sparsification equations; inferensys.com
+ * zh glossary, Random-k and Top-k + 8-bit).
+ *   acc = g + e        (GC_EF; without it acc = g and e may be NULL)
+ *   S_t = the k_t kept elements of tensor t (Top-k by |acc|, or random-k)
+ *   payload: idx[koff[t] + j] = local index of the j-th kept element
+ *            (ascending); val = acc there, or with GC_INT8 q = int8 code,
+ *            scale[t] = max|acc_t| / 127, and val (optional) = q * scale[t];
+ *            GC_RANDK|GC_UNBIASED: val = g * (float)(n_t / k_t), no EF
+ *   residual (GC_EF): e = acc off S, +0 on S, or acc - q * scale with GC_INT8.
+ * g: device fp32[N] (read only).  e: device fp32[N] in/out.  idx: device
+ * int32[sum k].  val: device fp32[sum k] (required without GC_INT8,
+ * optional with it).  q: device int8[sum k] and scale: device fp32[T],
+ * both required iff GC_INT8.  seed, iter: Philox key and counter words.
+ * GC_INT8 cannot be combined with GC_RANDK. */
+gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
+                              int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
+                              uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* gc_ef_topk_compress with timing hooks: `events` is a host array of
+ * `n_events` (0..5) cudaEvent_t handles created by the caller, recorded on
+ * `stream` at the phase boundaries of the call: [0] start, [1] before the
+ * streaming pass over g and e, [2] after it, [3] after the k-th key search,
+ * [4] after the payload write.  NULL entries are skipped.  Results are
+ * identical to gc_ef_topk_compress. */
+gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc_layout* host, const float* g,
+                                       float* e, int32_t* idx, float* val, int8_t* q, float* scale,
+                                       uint64_t seed, uint64_t iter, uint32_t flags,
+                                       void* workspace, size_t ws_bytes, void* stream,
+                                       void* const* events, int32_t n_events);
+
+/* DGC momentum correction + Top-k (inferensys.com "Gradient Sparsification",
+ * momentum correction and momentum factor masking; genomic glossary, DGC):
+ *   u = beta * u + g;  v = v + u;  S = Top-k of |v|;  payload v[S] (or int8);
+ *   v[S] = +0 (int8: v - q * scale);  u[S] = +0 unless GC_NO_MASK.
+ * u, v: device fp32[N] in/out.  Other arguments as gc_ef_topk_compress
+ * (GC_EF, GC_RANDK, GC_UNBIASED are not accepted here). */
+gc_status gc_ef_topk_compress_momentum(const gc_layout* dev, const gc_layout* host, const float* g,
+                                       float* u, float* v, float beta, int32_t* idx, float* val,
+                                       int8_t* q, float* scale, uint64_t seed, uint64_t iter,
+                                       uint32_t flags, void* workspace, size_t ws_bytes,
+                                       void* stream);
+
+/* 1-bit sign compression with EF (mbrenndoerfer.com "Gradient Compression",
+ * 1-bit SGD equation, per-layer scalar):
+ *   acc = g + e (e may be NULL: no EF);  mean_abs[t] = (float)(sum|acc_t| / n_t);
+ *   bit = 1 iff acc has a clear sign bit;  e = acc - (bit ? mean_abs : -mean_abs).
+ * bits: device uint32[sum ceil(n_t/32)].  mean_abs: device fp32[T].  The
+ * sum is reduced in a fixed order (relative error below 1e-6). */
+gc_status gc_sign_compress(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
+                           uint32_t* bits, float* mean_abs, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* Dense stochastic quantization (genomic glossary: 8-bit quantization,
+ * stochastic rounding, QSGD; mbrenndoerfer.com QSGD equation):
+ *   mode GC_Q_INT8: scale[t] = max|acc_t| / 127, code = sgn * min(127, SR(|acc| / scale))
+ *   mode GC_Q_QSGD: scale[t] = (float)||acc_t||_2, code = sgn * min(s, SR((|acc| * s) / N)),
+ *                   decoded value sgn * ((|code| * N) / s);  1 <= s_levels <= 127.
+ *   acc = g + e with EF (e != NULL), and then e = acc - decoded value.
+ * codes: device int8[N].  scale: device fp32[T]. */
+gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layout* host, const float* g,
+                                 float* e, int8_t* codes, float* scale, int32_t mode,
+                                 int32_t s_levels, uint64_t seed, uint64_t iter, void* workspace,
+                                 size_t ws_bytes, void* stream);
+
+/* Receiver of W workers' sparse payloads (mbrenndoerfer.com: the union of
+ * different sparse vectors; zh glossary: all-gather of indices and values):
+ *   for w = 0..W-1 in order: out[off[t] + idx_w[j]] += value_w[j],
+ *   value = val_w[j], or q_w[j] * scale_w[t] when val is NULL.
+ * idx, val, q, scale: HOST arrays of W device pointers (val NULL, or q and
+ * scale NULL).  Indices within one worker's tensor must be distinct; an
+ * index >= n_t is skipped and flagged (GC_DIAG_INDEX_RANGE).  out: device
+ * fp32[N], caller-initialised, accumulated into; it must not alias a payload. */
+gc_status gc_sparse_decompress_accumulate(const gc_layout* dev, const gc_layout* host, int32_t W,
+                                          const int32_t* const* idx, const float* const* val,
+                                          const int8_t* const* q, const float* const* scale,
+                                          float* out, void* workspace, size_t ws_bytes,
+                                          void* stream);
+
+/* Receiver of W workers' dense payloads, out += decode(payload_w) in order
+ * w = 0..W-1.  kind GC_DENSE_SIGN: data = uint32 bits (word layout above),
+ * decode = bit ? scale[t] : -scale[t].  GC_DENSE_INT8: data = int8 codes,
+ * decode = code * scale[t].  GC_DENSE_QSGD: decode = sgn * ((|code| * N) / s).
+ * data, scale: HOST arrays of W device pointers. */
+gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const gc_layout* host, int32_t W,
+                                         int32_t kind, int32_t s_levels, const void* const* data,
+                                         const float* const* scale, float* out, void* workspace,
+                                         size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then reads the diagnostics that the last call using
+ * `workspace` left there.  Returns GC_ERR_DEVICE if an error bit is set. */
+gc_status gc_get_device_status(const void* workspace, size_t ws_bytes, void* stream, gc_diag* out);
+
+/* Static description of a status code. */
+const char* gc_status_string(gc_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t gc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_H_ */

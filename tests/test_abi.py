@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports what include/gc.h declares, and rejects
+bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gc():
+    from gradient_compression_gb300 import build
+    build.build()
+    import gradient_compression_gb300 as gcmod
+    gcmod.lib()
+    return gcmod
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(gc):
+    names = _declared_functions()
+    assert len(names) >= 10
+    L = C.CDLL(gc.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(gc):
+    assert gc.status_string(gc.GC_OK) == "ok"
+    assert "workspace" in gc.status_string(gc.GC_ERR_WORKSPACE)
+    assert gc.version() >= 100
+
+
+def _host_layout(gc, sizes, k=None):
+    off = np.zeros(len(sizes) + 1, np.int64)
+    off[1:] = np.cumsum(sizes)
+    return gc.Layout(off, k, device="cpu")
+
+
+def test_workspace_size_scales_with_layout(gc):
+    small = _host_layout(gc, [1000, 5000], [10, 50])
+    big = _host_layout(gc, [10_000_000, 5000], [10_000, 50])
+    s1 = gc.workspace_size(small, gc.GC_OP_TOPK, gc.GC_EF)
+    s2 = gc.workspace_size(big, gc.GC_OP_TOPK, gc.GC_EF)
+    assert 0 < s1 < s2
+    assert gc.workspace_size(big, gc.GC_OP_SIGN) > 0
+    assert gc.workspace_size(big, gc.GC_OP_DECOMPRESS) > 0
+    # random-k needs no sample buffer
+    assert gc.workspace_size(big, gc.GC_OP_TOPK, gc.GC_RANDK) < s2
+
+
+def test_layout_validation(gc):
+    out = C.c_size_t()
+    bad_k = _host_layout(gc, [10, 20], [11, 1])           # k > n
+    assert gc.lib().gc_workspace_size(bad_k.host(), gc.GC_OP_TOPK, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    lay = _host_layout(gc, [10, 20], [1, 1])
+    lay.off[1] = 10; lay.off[2] = 10                         # empty tensor
+    assert gc.lib().gc_workspace_size(lay.host(), gc.GC_OP_TOPK, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    huge = _host_layout(gc, [2 ** 31], [1])                  # n >= 2^31
+    assert gc.lib().gc_workspace_size(huge.host(), gc.GC_OP_TOPK, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    assert gc.lib().gc_workspace_size(lay.host(), 99, 0, C.byref(out)) == gc.GC_ERR_INVALID_ARG
+
+
+def test_argument_errors_return_before_any_launch(gc):
+    lay = _host_layout(gc, [100], [5])
+    L = gc.lib()
+    P = C.c_void_p
+    # flags that do not combine, or unknown bits
+    for flags in (gc.GC_RANDK | gc.GC_INT8, gc.GC_UNBIASED, gc.GC_RANDK | gc.GC_UNBIASED | gc.GC_EF, 1 << 20):
+        st = L.gc_ef_topk_compress(lay.host(), lay.host(), P(16), P(16), P(16), P(16), P(16), P(16),
+                                   0, 0, flags, P(256), 1 << 20, None)
+        assert st == gc.GC_ERR_INVALID_ARG, flags
+    # misaligned gradient pointer
+    st = L.gc_ef_topk_compress(lay.host(), lay.host(), P(18), P(16), P(16), P(16), None, None,
+                               0, 0, gc.GC_EF, P(256), 1 << 20, None)
+    assert st == gc.GC_ERR_ALIGNMENT
+    # workspace too small / misaligned
+    st = L.gc_ef_topk_compress(lay.host(), lay.host(), P(16), P(16), P(16), P(16), None, None,
+                               0, 0, gc.GC_EF, P(256), 8, None)
+    assert st == gc.GC_ERR_WORKSPACE
+    st = L.gc_ef_topk_compress(lay.host(), lay.host(), P(16), P(16), P(16), P(16), None, None,
+                               0, 0, gc.GC_EF, P(260), 1 << 30, None)
+    assert st == gc.GC_ERR_WORKSPACE
+    # missing payload buffers
+    st = L.gc_ef_topk_compress(lay.host(), lay.host(), P(16), P(16), P(16), None, None, None,
+                               0, 0, gc.GC_EF, P(256), 1 << 30, None)
+    assert st == gc.GC_ERR_INVALID_ARG
+    st = L.gc_quantize_stochastic(lay.host(), lay.host(), P(16), None, P(16), P(16), 1, 0, 0, 0,
+                                  P(256), 1 << 30, None)
+    assert st == gc.GC_ERR_INVALID_ARG                       # QSGD needs s >= 1
+    st = L.gc_dense_decompress_accumulate(lay.host(), lay.host(), 1, 7, 16, None, None, P(16),
+                                          P(256), 1 << 30, None)
+    assert st == gc.GC_ERR_INVALID_ARG

@@ -1,0 +1,407 @@
+"""GPU parity: every libgc entry point, called through the C ABI, against the
+oracle on the same seeded inputs.
+
+Bit-exact for indices, selected values, residuals, int8/QSGD codes, sign
+bits, max-abs scales and scatter-add sums.  Norm-type scales (sign mean-|acc|,
+QSGD L2 norm) are reduced in a different order on the two sides and must
+agree within 1e-6 relative; the oracle is then re-run with the GPU's scale
+and everything downstream of the scale must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+F32 = np.float32
+REL_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def gc(cuda_device):
+    from gradient_compression_gb300 import build
+    build.build()
+    import gradient_compression_gb300 as gcmod
+    return gcmod
+
+
+def _layout(gc, sizes, k=None, rho=None):
+    if k is None:
+        k = workloads.k_per_tensor(sizes, rho)
+    return gc.Layout(workloads.prefix(sizes), np.asarray(k, np.int64), device="cuda")
+
+
+def _bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def _grad(n, seed, kind="t3"):
+    gen = torch.Generator().manual_seed(seed)
+    if kind == "t3":
+        x = torch.distributions.StudentT(3.0).sample((n,)) * 1e-3
+    elif kind == "ties":
+        x = torch.randint(-2, 3, (n,), generator=gen).float() * 1e-3
+    elif kind == "zeros":
+        x = torch.zeros(n)
+        x[::3] = -0.0
+    else:
+        raise ValueError(kind)
+    return x.float()
+
+
+def _topk_check(gc, L, g_h, e_h, flags, seed, it, ws=None, expect_exact=None):
+    """Runs one GPU call and the oracle; asserts bit-exact payload and residual."""
+    dev = L.device
+    K = L.total_k
+    int8 = bool(flags & gc.GC_INT8)
+    g = torch.from_numpy(g_h).to(dev)
+    e = torch.from_numpy(e_h).to(dev) if e_h is not None else None
+    idx = torch.full((max(K, 1),), -1, dtype=torch.int32, device=dev)
+    val = torch.empty(max(K, 1), dtype=torch.float32, device=dev)
+    q = torch.zeros(max(K, 1), dtype=torch.int8, device=dev) if int8 else None
+    sc = torch.zeros(L.T, dtype=torch.float32, device=dev) if int8 else None
+    if ws is None:
+        ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    gc.ef_topk_compress(L, g, e, idx, val, q, sc, seed, it, flags, ws)
+    diag = gc.get_device_status(ws)
+    assert diag.error_bits == 0
+    if expect_exact is not None:
+        assert diag.exact_tensors == expect_exact, (diag.exact_tensors, expect_exact)
+    gi, gv = idx.cpu().numpy()[:K], val.cpu().numpy()[:K]
+    e_ref = e_h.copy() if e_h is not None else None
+    randk = bool(flags & gc.GC_RANDK)
+    for t in range(L.T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+        et = e_ref[a:b] if e_ref is not None else None
+        if randk:
+            ri, rv = oracle.randk_tensor(g_h[a:b], et, int(L.k[t]), base=a, seed=seed, it=it,
+                                         unbiased=bool(flags & gc.GC_UNBIASED))
+            rq = rs = None
+        else:
+            ri, rv, rq, rs = oracle.ef_topk_tensor(g_h[a:b], et, int(L.k[t]), base=a, int8=int8,
+                                                   seed=seed, it=it)
+        assert np.array_equal(gi[ka:kb], ri), f"tensor {t}: indices differ"
+        if int8:
+            assert np.array_equal(q.cpu().numpy()[ka:kb], rq), f"tensor {t}: codes differ"
+            assert _bits(sc.cpu().numpy()[t:t + 1])[0] == _bits(np.asarray([rs], F32))[0], f"tensor {t}: scale"
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"tensor {t}: dequantized values differ"
+        else:
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"tensor {t}: values differ"
+    if e is not None:
+        assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), "residual differs"
+    return e_ref, diag
+
+
+# ----------------------------------------------------------------------------- EF Top-k
+
+LAYOUTS = {
+    "single_1": [1],
+    "tiny_ragged": [3, 5, 7, 1, 2],
+    "misaligned": [4097, 1, 33, 100_003, 6],
+    "many_small": [64] * 40 + [513, 4096, 4095],
+    "medium": [300_000, 70_001, 12_345],
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYOUTS))
+@pytest.mark.parametrize("flags_name", ["ef", "ef_int8", "noef", "ef_exact", "ef_int8_exact"])
+def test_topk_layouts(gc, name, flags_name):
+    sizes = LAYOUTS[name]
+    flags = {"ef": gc.GC_EF, "ef_int8": gc.GC_EF | gc.GC_INT8, "noef": 0,
+             "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT,
+             "ef_int8_exact": gc.GC_EF | gc.GC_INT8 | gc.GC_FORCE_EXACT}[flags_name]
+    rng = np.random.default_rng(len(sizes))
+    k = [int(min(n, max(0, int(rng.integers(0, 3)) if n < 8 else int(np.ceil(0.01 * n))))) for n in sizes]
+    if len(sizes) > 2:
+        k[0] = sizes[0]               # k = n
+        k[-1] = 0                     # k = 0
+    L = _layout(gc, sizes, k=k)
+    n = L.numel
+    g = _grad(n, 3).numpy()
+    e = (np.random.default_rng(4).standard_normal(n) * 1e-4).astype(F32) if flags & gc.GC_EF else None
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    for it in range(3):
+        g = _grad(n, 10 + it).numpy()
+        e, _ = _topk_check(gc, L, g, e, flags, seed=5, it=it, ws=ws)
+
+
+@pytest.mark.parametrize("kind", ["ties", "zeros"])
+@pytest.mark.parametrize("exact", [False, True])
+def test_topk_ties(gc, kind, exact):
+    sizes = [10_000, 4096, 333, 70_000]
+    L = _layout(gc, sizes, k=[37, 4096, 1, 700])
+    n = L.numel
+    flags = gc.GC_EF | (gc.GC_FORCE_EXACT if exact else 0)
+    e = np.zeros(n, F32)
+    if kind == "zeros":
+        e[::5] = -0.0
+    g = _grad(n, 1, kind).numpy()
+    _topk_check(gc, L, g, e, flags, seed=1, it=0)
+
+
+def test_topk_flat_2p20_ten_iterations(gc):
+    """One flat fp32 gradient of 2^20 elements at 0.1% (k = 1049), EF, 10 fresh gradients."""
+    lay = workloads.flat_layout(1 << 20)
+    L = _layout(gc, lay.sizes, rho=0.001)
+    assert L.total_k == 1049
+    e = np.zeros(L.numel, F32)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    for it in range(10):
+        g = workloads.make_grad(1, lay, it).numpy()
+        e, d = _topk_check(gc, L, g, e, gc.GC_EF, seed=0, it=it, ws=ws, expect_exact=0)
+
+
+def test_topk_resnet50_and_randk(gc):
+    lay = workloads.resnet50_layout()
+    L = _layout(gc, lay.sizes, rho=0.01)
+    assert L.total_k == 255_658
+    e = np.zeros(L.numel, F32)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    for it in range(3):
+        g = workloads.make_grad(2, lay, it).numpy()
+        e, d = _topk_check(gc, L, g, e, gc.GC_EF, seed=2, it=it, ws=ws)
+        assert d.exact_tensors <= 3      # only degenerate tensors may need full passes
+    e = np.zeros(L.numel, F32)
+    for it in range(2):
+        g = workloads.make_grad(2, lay, 100 + it).numpy()
+        e, _ = _topk_check(gc, L, g, e, gc.GC_EF | gc.GC_RANDK, seed=3, it=it)
+
+
+@pytest.mark.parametrize("flags_name", ["ef", "plain", "unbiased", "ef_exact"])
+def test_randk_layouts(gc, flags_name):
+    flags = {"ef": gc.GC_EF | gc.GC_RANDK, "plain": gc.GC_RANDK, "unbiased": gc.GC_RANDK | gc.GC_UNBIASED,
+             "ef_exact": gc.GC_EF | gc.GC_RANDK | gc.GC_FORCE_EXACT}[flags_name]
+    sizes = [4097, 1, 33, 100_003, 6, 64, 250_000]
+    L = _layout(gc, sizes, k=[41, 1, 33, 1000, 0, 3, 2500])
+    n = L.numel
+    e = np.zeros(n, F32) if flags & gc.GC_EF else None
+    for it in range(2):
+        g = _grad(n, 20 + it).numpy()
+        e, _ = _topk_check(gc, L, g, e, flags, seed=9, it=it)
+
+
+# ----------------------------------------------------------------------------- momentum
+
+def _momentum_check(gc, L, beta, flags, iters, seed=4, gen=None):
+    dev = L.device
+    n, K = L.numel, L.total_k
+    int8 = bool(flags & gc.GC_INT8)
+    u_h = np.zeros(n, F32)
+    v_h = np.zeros(n, F32)
+    u, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    idx = torch.empty(max(K, 1), dtype=torch.int32, device=dev)
+    val = torch.empty(max(K, 1), dtype=torch.float32, device=dev)
+    q = torch.empty(max(K, 1), dtype=torch.int8, device=dev) if int8 else None
+    sc = torch.empty(L.T, dtype=torch.float32, device=dev) if int8 else None
+    ws = gc.alloc_workspace(L, gc.GC_OP_MOMENTUM, flags)
+    for it in range(iters):
+        g_h = gen(it) if gen else _grad(n, 40 + it).numpy()
+        gc.ef_topk_compress_momentum(L, torch.from_numpy(g_h).to(dev), u, v, beta, idx, val, q, sc, seed, it,
+                                     flags, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gi, gv = idx.cpu().numpy()[:K], val.cpu().numpy()[:K]
+        for t in range(L.T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            ri, rv, rq, rs = oracle.momentum_topk_tensor(g_h[a:b], u_h[a:b], v_h[a:b], int(L.k[t]), beta,
+                                                         masking=not (flags & gc.GC_NO_MASK), base=a,
+                                                         int8=int8, seed=seed, it=it)
+            assert np.array_equal(gi[ka:kb], ri), f"it {it} tensor {t}: indices"
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"it {it} tensor {t}: values"
+            if int8:
+                assert np.array_equal(q.cpu().numpy()[ka:kb], rq)
+                assert sc.cpu().numpy()[t] == rs
+        assert np.array_equal(_bits(u.cpu().numpy()), _bits(u_h)), f"it {it}: u"
+        assert np.array_equal(_bits(v.cpu().numpy()), _bits(v_h)), f"it {it}: v"
+
+
+@pytest.mark.parametrize("flags_name", ["mask", "nomask", "int8", "exact"])
+def test_momentum_layouts(gc, flags_name):
+    flags = {"mask": 0, "nomask": gc.GC_NO_MASK, "int8": gc.GC_INT8, "exact": gc.GC_FORCE_EXACT}[flags_name]
+    sizes = [4097, 1, 33, 100_003, 64, 70_000]
+    L = _layout(gc, sizes, rho=0.005)
+    _momentum_check(gc, L, 0.9, flags, iters=3)
+
+
+# ----------------------------------------------------------------------------- sign / quantize
+
+def _sign_check(gc, L, g_h, e_h):
+    dev = L.device
+    g = torch.from_numpy(g_h).to(dev)
+    e = torch.from_numpy(e_h).to(dev) if e_h is not None else None
+    bits = torch.zeros(L.words, dtype=torch.int32, device=dev)
+    mu = torch.zeros(L.T, dtype=torch.float32, device=dev)
+    ws = gc.alloc_workspace(L, gc.GC_OP_SIGN)
+    gc.sign_compress(L, g, e, bits, mu, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    gb, gm = bits.cpu().numpy().view(np.uint32), mu.cpu().numpy()
+    ge = e.cpu().numpy() if e is not None else None
+    n = np.diff(L.off)
+    woff = workloads.prefix((n + 31) // 32)
+    e_ref = e_h.copy() if e_h is not None else None
+    for t in range(L.T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        et = e_ref[a:b] if e_ref is not None else None
+        _, mu_ref = oracle.sign_tensor(g_h[a:b], None if et is None else et.copy())
+        assert abs(float(gm[t]) - mu_ref) <= REL_TOL * abs(mu_ref), f"tensor {t}: mean |acc|"
+        rb, _ = oracle.sign_tensor(g_h[a:b], et, mu_given=float(gm[t]))
+        assert np.array_equal(gb[woff[t]:woff[t + 1]], rb), f"tensor {t}: sign bits"
+    if ge is not None:
+        assert np.array_equal(_bits(ge), _bits(e_ref)), "residual"
+    return e_ref
+
+
+@pytest.mark.parametrize("ef", [True, False])
+def test_sign_layouts(gc, ef):
+    sizes = [4097, 1, 33, 100_003, 6, 64, 31, 32, 250_000]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n = L.numel
+    e = np.zeros(n, F32) if ef else None
+    for it in range(3):
+        g = _grad(n, 60 + it).numpy()
+        g[::17] = -0.0
+        e = _sign_check(gc, L, g, e)
+
+
+def _quant_check(gc, L, g_h, e_h, mode, s, seed, it):
+    dev = L.device
+    g = torch.from_numpy(g_h).to(dev)
+    e = torch.from_numpy(e_h).to(dev) if e_h is not None else None
+    codes = torch.zeros(L.numel, dtype=torch.int8, device=dev)
+    sc = torch.zeros(L.T, dtype=torch.float32, device=dev)
+    ws = gc.alloc_workspace(L, gc.GC_OP_QUANTIZE)
+    gc.quantize_stochastic(L, g, e, codes, sc, gc.GC_Q_INT8 if mode == "int8" else gc.GC_Q_QSGD, s, seed, it, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    gcodes, gsc = codes.cpu().numpy(), sc.cpu().numpy()
+    e_ref = e_h.copy() if e_h is not None else None
+    for t in range(L.T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        et = e_ref[a:b] if e_ref is not None else None
+        _, ref_sc = oracle.quantize_tensor(g_h[a:b], None if et is None else et.copy(), mode, s, base=a,
+                                           seed=seed, it=it)
+        if mode == "int8":
+            assert gsc[t] == F32(ref_sc), f"tensor {t}: int8 scale must be exact"
+        else:
+            assert abs(float(gsc[t]) - ref_sc) <= REL_TOL * abs(ref_sc), f"tensor {t}: norm"
+        rc, _ = oracle.quantize_tensor(g_h[a:b], et, mode, s, base=a, seed=seed, it=it,
+                                       scale_given=float(gsc[t]))
+        assert np.array_equal(gcodes[a:b], rc), f"tensor {t}: codes"
+    if e is not None:
+        assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), "residual"
+    return e_ref
+
+
+@pytest.mark.parametrize("mode,s", [("int8", 0), ("qsgd", 16), ("qsgd", 1), ("qsgd", 127)])
+@pytest.mark.parametrize("ef", [False, True])
+def test_quantize_layouts(gc, mode, s, ef):
+    sizes = [4097, 1, 33, 100_003, 6, 64, 250_000]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n = L.numel
+    e = (np.random.default_rng(1).standard_normal(n) * 1e-5).astype(F32) if ef else None
+    for it in range(2):
+        g = _grad(n, 80 + it).numpy()
+        g[5] = 0.0
+        e = _quant_check(gc, L, g, e, mode, s, seed=11, it=it)
+
+
+def test_quantize_zero_tensor(gc):
+    L = _layout(gc, [100, 37], k=[0, 0])
+    for mode, s in (("int8", 0), ("qsgd", 16)):
+        _quant_check(gc, L, np.zeros(137, F32), None, mode, s, seed=0, it=0)
+
+
+# ----------------------------------------------------------------------------- receivers
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_sparse_decompress(gc, int8):
+    sizes = [4097, 1, 33, 100_003, 6, 64, 250_000]
+    k = [41, 1, 33, 1000, 0, 3, 2500]
+    lay = workloads.Layout("t", sizes)
+    L = _layout(gc, sizes, k=k)
+    W = 5
+    kk = np.asarray(k, np.int64)
+    payloads = [workloads.make_sparse_payload(lay, kk, w, device="cpu", cfg=0, int8=int8) for w in range(W)]
+    base = _grad(L.numel, 7).numpy()
+    out = torch.from_numpy(base).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    idx = [p[0].cuda() for p in payloads]
+    if int8:
+        gc.sparse_decompress_accumulate(L, idx, None, [p[2].cuda() for p in payloads],
+                                        [p[3].cuda() for p in payloads], out, ws)
+    else:
+        gc.sparse_decompress_accumulate(L, idx, [p[1].cuda() for p in payloads], None, None, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    ref = base.copy()
+    if int8:
+        oracle.sparse_accumulate(L.off, L.koff, [p[0].numpy() for p in payloads], None,
+                                 [p[2].numpy() for p in payloads], [p[3].numpy() for p in payloads], ref)
+    else:
+        oracle.sparse_accumulate(L.off, L.koff, [p[0].numpy() for p in payloads],
+                                 [p[1].numpy() for p in payloads], None, None, ref)
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))
+
+
+def test_sparse_decompress_flags_bad_index(gc):
+    L = _layout(gc, [10, 20], k=[1, 1])
+    out = torch.zeros(30, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    idx = torch.tensor([3, 25], dtype=torch.int32, device="cuda")        # 25 >= n_1 = 20
+    val = torch.tensor([1.0, 2.0], device="cuda")
+    gc.sparse_decompress_accumulate(L, [idx], [val], None, None, out, ws)
+    d = gc.get_device_status(ws, raise_on_error=False)
+    assert d.error_bits & gc.GC_DIAG_INDEX_RANGE
+    o = out.cpu().numpy()
+    assert o[3] == 1.0 and o.sum() == 1.0
+
+
+@pytest.mark.parametrize("kind", ["sign", "int8", "qsgd"])
+def test_dense_decompress(gc, kind):
+    sizes = [4097, 1, 33, 100_003, 6, 64, 31]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n, W, s = L.numel, 3, 16
+    rng = np.random.default_rng(2)
+    base = _grad(n, 8).numpy()
+    out = torch.from_numpy(base).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    datas, scales = [], []
+    for w in range(W):
+        if kind == "sign":
+            datas.append(rng.integers(0, 2 ** 32, L.words, dtype=np.uint64).astype(np.uint32))
+        elif kind == "int8":
+            datas.append(rng.integers(-127, 128, n).astype(np.int8))
+        else:
+            datas.append(rng.integers(-s, s + 1, n).astype(np.int8))
+        scales.append(rng.uniform(1e-4, 1e-2, L.T).astype(F32))
+    kd = {"sign": gc.GC_DENSE_SIGN, "int8": gc.GC_DENSE_INT8, "qsgd": gc.GC_DENSE_QSGD}[kind]
+    dd = [torch.from_numpy(d.view(np.int32) if kind == "sign" else d).cuda() for d in datas]
+    gc.dense_decompress_accumulate(L, kd, s, dd, [torch.from_numpy(x).cuda() for x in scales], out, ws)
+    ref = base.copy()
+    woff = workloads.prefix((np.diff(L.off) + 31) // 32)
+    for w in range(W):
+        for t in range(L.T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            if kind == "sign":
+                oracle.sign_decode_accumulate(datas[w][woff[t]:woff[t + 1]], scales[w][t], ref[a:b])
+            else:
+                oracle.codes_decode_accumulate(datas[w][a:b], scales[w][t], kind, ref[a:b], s)
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))
+
+
+def test_layout_mismatch_is_reported_not_run(gc):
+    sizes = [1000, 2000]
+    L = _layout(gc, sizes, k=[10, 20])
+    bad = _layout(gc, [1000, 3000], k=[10, 20])          # device copy disagrees with the host mirror
+    L._dev_off.copy_(bad._dev_off)
+    g = torch.zeros(3000, device="cuda")
+    e = torch.zeros(3000, device="cuda")
+    idx = torch.full((30,), -7, dtype=torch.int32, device="cuda")
+    val = torch.zeros(30, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    gc.ef_topk_compress(L, g, e, idx, val, None, None, 0, 0, gc.GC_EF, ws)
+    d = gc.get_device_status(ws, raise_on_error=False)
+    assert d.error_bits & gc.GC_DIAG_LAYOUT_MISMATCH
+    assert (idx.cpu() == -7).all()

@@ -219,6 +219,24 @@ def make_grad(cfg: int, layout: Layout, it: int, device="cpu", worker: int = 0,
     return out
 
 
+def tensor_grad(cfg: int, layout: Layout, it: int, t: int, device="cpu", worker: int = 0) -> torch.Tensor:
+    """Tensor t of the seeded gradient of iteration `it`, alone (same recipe as make_grad)."""
+    n = layout.sizes[t]
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    gen = _gen(out.device, cfg, it, t, worker)
+    if cfg in (1, 5):
+        fill_student_t(out, 3.0, 1e-3, gen)
+    elif cfg == 2:
+        fill_laplace(out, float(resnet_scales(layout)[t]), gen)
+    elif cfg == 3:
+        fill_student_t(out, 2.5, 1e-3, gen)
+    elif cfg == 4:
+        fill_mixture(out, gen)
+    else:
+        raise ValueError(cfg)
+    return out
+
+
 def make_sparse_payload(layout: Layout, k: np.ndarray, worker: int, device="cpu", cfg: int = 5,
                         int8: bool = False):
     """A seeded sparse payload for one simulated worker.
