@@ -35,8 +35,14 @@ import workloads  # noqa: E402
 
 METRIC = "EF Top-k compress gradient GB/s (elems/s) at 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
-CFG = 5
-RHO = 0.001
+# workload name -> (generator config id, density, int8, oracle-baseline tensors, reference-arm tensor)
+WORKLOADS = {
+    "llama3_8b": (5, 0.001, True, list(range(1, 10)), 1),
+    "bert_large": (3, 0.001, True, list(range(0, 3)), 0),
+    "resnet50": (2, 0.01, False, list(range(0, 161)), 160),
+    "flat_2p20": (1, 0.001, False, [0], 0),
+}
+CFG, RHO, INT8 = 5, 0.001, True
 # kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan, two
 # sample levels and their selects, the streaming pass, three candidate radix
 # levels plus the full-pass level-1 histogram with their selects, count,
@@ -46,10 +52,17 @@ LAUNCHES_PER_STEP = 16
 STREAM_BYTES_PER_ELEM = 12
 
 
+GRADIENT = {1: "student_t_nu3_x1e-3", 2: "laplace_loguniform_scale", 3: "student_t_nu2.5_x1e-3",
+            5: "student_t_nu3_x1e-3"}
+
+
 def workload_config(layout, k):
-    return {"workload": "llama3_8b_arena_ef_topk_0.1pct_int8", "tensors": layout.num_tensors,
-            "elements": layout.numel, "kept": int(k.sum()), "density": RHO, "ef": True, "int8": True,
-            "gradient": "student_t_nu3_x1e-3", "l2": "inputs (g + e, 64.2 GB) larger than L2; no flush",
+    big = 8 * layout.numel > 129e6
+    return {"workload": "%s_arena_ef_topk_%gpct%s" % (layout.name, 100 * RHO, "_int8" if INT8 else ""),
+            "tensors": layout.num_tensors, "elements": layout.numel, "kept": int(k.sum()), "density": RHO,
+            "ef": True, "int8": INT8, "gradient": GRADIENT[CFG],
+            "l2": ("inputs (g + e, %.1f GB) larger than L2; no flush" % (8 * layout.numel / 1e9)) if big
+            else "inputs fit in L2 (not flushed): latency-bound case",
             "parallelism": "replicas"}
 
 
@@ -146,7 +159,7 @@ def oracle_baseline(layout, k, tensors, it=0, seed=0):
         g = workloads.tensor_grad(CFG, layout, it, t, device="cpu").numpy()
         e = np.zeros_like(g)
         t0 = time.perf_counter()
-        oracle.ef_topk_tensor(g, e, int(k[t]), base=int(off[t]), int8=True, seed=seed, it=it)
+        oracle.ef_topk_tensor(g, e, int(k[t]), base=int(off[t]), int8=INT8, seed=seed, it=it)
         secs += time.perf_counter() - t0
         n_tot += g.size
     return 4.0 * n_tot / secs / 1e9, secs, n_tot
@@ -156,10 +169,10 @@ def run_reference(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return
-    layout = workloads.llama3_8b_layout()
+    layout = workloads.LAYOUTS[CFG]()
     k = workloads.k_per_tensor(layout.sizes, RHO)
-    sample_t = [1]                         # layer 0 q_proj: 16,777,216 elements
-    sample = "tensor 1 (layer-0 q_proj, 16,777,216 elements) per step"
+    sample_t = [WORKLOADS[args.workload][4]]
+    sample = "tensor %d (%d elements) of the arena per step" % (sample_t[0], layout.sizes[sample_t[0]])
     for w in range(args.warmup):
         oracle_baseline(layout, k, sample_t, it=w)
     vals, secs_all = [], 0.0
@@ -186,10 +199,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    layout = workloads.llama3_8b_layout()
+    layout = workloads.LAYOUTS[CFG]()
     k = workloads.k_per_tensor(layout.sizes, RHO)
     N = layout.numel
-    flags = gc.GC_EF | gc.GC_INT8
+    flags = gc.GC_EF | (gc.GC_INT8 if INT8 else 0)
     L = gc.Layout(layout.off, k, device=dev)
     g = workloads.make_grad(CFG, layout, 0, device=dev)
     e = torch.zeros(N, dtype=torch.float32, device=dev)
@@ -239,7 +252,7 @@ def run_ours(args):
     t_stream = statistics.mean(stream_ms) * 1e-3
     achieved = STREAM_BYTES_PER_ELEM * N / t_stream / 1e9
     bpe = profiled_traffic()
-    algo_step_bytes = 12 * N + 5 * int(k.sum()) + 4 * layout.num_tensors
+    algo_step_bytes = 12 * N + (5 * int(k.sum()) + 4 * layout.num_tensors if INT8 else 8 * int(k.sum()))
 
     e2e = None
     if not args.no_e2e:
@@ -247,10 +260,11 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tensors = list(range(1, 10))        # layer 0: q, k, v, o, gate, up, down, two norms
+        tensors = WORKLOADS[args.workload][3]
         v, secs, n = oracle_baseline(layout, k, tensors)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "layer 0 of the arena (9 tensors, %d elements), one iteration, %.1f s" % (n, secs)}
+               "sample": "tensors %d..%d of the arena (%d elements), one iteration, %.1f s"
+               % (tensors[0], tensors[-1], n, secs)}
 
     if rank != 0:
         return
@@ -280,7 +294,7 @@ def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
         return {"value": None, "unit": UNIT, "error": "pinned host buffer: %s" % str(exc)[:120]}
     g_host.copy_(g, non_blocking=False)
     idx_h = torch.empty(K, dtype=torch.int32, pin_memory=True)
-    q_h = torch.empty(K, dtype=torch.int8, pin_memory=True)
+    q_h = torch.empty(K, dtype=torch.int8 if INT8 else torch.float32, pin_memory=True)
     sc_h = torch.empty(layout.num_tensors, dtype=torch.float32, pin_memory=True)
     steps = max(2, min(args.steps, 5))
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -289,8 +303,11 @@ def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
         g.copy_(g_host, non_blocking=True)
         gc.ef_topk_compress(L, g, e, comp.idx, comp.val, comp.q, comp.scale, 99, it, flags, comp.workspace)
         idx_h.copy_(comp.idx[:K], non_blocking=True)
-        q_h.copy_(comp.q[:K], non_blocking=True)
-        sc_h.copy_(comp.scale, non_blocking=True)
+        if INT8:
+            q_h.copy_(comp.q[:K], non_blocking=True)
+            sc_h.copy_(comp.scale, non_blocking=True)
+        else:
+            q_h.copy_(comp.val[:K], non_blocking=True)
 
     one(0)
     torch.cuda.synchronize()
@@ -301,7 +318,8 @@ def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     return {"value": 4.0 * N / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms, "steps": steps,
-            "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 5 * K + 4 * layout.num_tensors}
+            "h2d_bytes_per_step": 4 * N,
+            "d2h_bytes_per_step": (5 * K + 4 * layout.num_tensors) if INT8 else 8 * K}
 
 
 def main():
@@ -310,11 +328,15 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3_8b",
+                    help="the measured workload is llama3_8b; the others are smaller cases for profiling")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    global CFG, RHO, INT8
+    CFG, RHO, INT8 = WORKLOADS[args.workload][:3]
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -172,6 +172,9 @@ def ef_topk_compress(layout, g, e, idx, val, q, scale, seed, it, flags, workspac
 def ef_topk_compress_profiled(layout, g, e, idx, val, q, scale, seed, it, flags, workspace, events,
                               stream=None):
     """gc_ef_topk_compress recording `events` (torch.cuda.Event, up to 5) at its phase boundaries."""
+    for ev in events:
+        if ev is not None and not ev.cuda_event:
+            ev.record()          # torch creates its CUDA event lazily, on the first record
     arr = (C.c_void_p * len(events))(*[None if ev is None else ev.cuda_event for ev in events])
     _check(lib().gc_ef_topk_compress_profiled(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx),
                                               _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
