@@ -22,6 +22,7 @@ GC_OP_TOPK, GC_OP_MOMENTUM, GC_OP_SIGN, GC_OP_QUANTIZE, GC_OP_DECOMPRESS = range
 GC_Q_INT8, GC_Q_QSGD = 0, 1
 GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
 GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE = 0x1, 0x2, 0x4
+GC_NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 
 
 class gc_layout(C.Structure):
@@ -56,6 +57,7 @@ def lib() -> C.CDLL:
         L.gc_workspace_size.argtypes = [LP, I32, U32, C.POINTER(SZ)]
         L.gc_ef_topk_compress.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_topk_compress_profiled.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P, P, I32]
+        L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
         L.gc_quantize_stochastic.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, U64, P, SZ, P]
@@ -65,7 +67,8 @@ def lib() -> C.CDLL:
         L.gc_status_string.argtypes = [I32]
         L.gc_status_string.restype = C.c_char_p
         L.gc_version.restype = I32
-        for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled", "gc_ef_topk_compress_momentum",
+        for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
+                     "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
             getattr(L, name).restype = I32
@@ -167,6 +170,18 @@ def ef_topk_compress(layout, g, e, idx, val, q, scale, seed, it, flags, workspac
     _check(lib().gc_ef_topk_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx), _ptr(val),
                                      _ptr(q), _ptr(scale), int(seed), int(it), int(flags), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "gc_ef_topk_compress")
+
+
+def ef_topk_compress_noalloc(layout, g, e, idx, val, q, scale, seed, it, flags, stream=None):
+    """gc_ef_topk_compress with the library's built-in scratch instead of a workspace.
+
+    For callers that cannot allocate device memory where they compress; the
+    layout's workspace must fit in GC_NOALLOC_MAX_WORKSPACE_BYTES, and calls
+    must not overlap on the GPU (they share that scratch).
+    """
+    _check(lib().gc_ef_topk_compress_noalloc(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx),
+                                             _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
+                                             _stream(stream)), "gc_ef_topk_compress_noalloc")
 
 
 def ef_topk_compress_profiled(layout, g, e, idx, val, q, scale, seed, it, flags, workspace, events,

@@ -164,6 +164,28 @@ gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc_layout* ho
                                        void* workspace, size_t ws_bytes, void* stream,
                                        void* const* events, int32_t n_events);
 
+/* Size of the scratch array built into libgc for gc_ef_topk_compress_noalloc. */
+#define GC_NOALLOC_MAX_WORKSPACE_BYTES (32u << 20)
+
+/* gc_ef_topk_compress without a caller-provided workspace.  The pages have
+ * no counterpart: this is a library convenience.  It serves callers that
+ * cannot allocate device memory at the point where they compress (their
+ * memory manager owns the GPU's memory, or a cudaMalloc there would stall the
+ * device).  Inputs, outputs and results are those of gc_ef_topk_compress; the
+ * scratch is one array of GC_NOALLOC_MAX_WORKSPACE_BYTES inside the library,
+ * held on every GPU that loads it until the process exits.
+ *  - Layouts whose gc_workspace_size(GC_OP_TOPK, flags) exceeds that size are
+ *    rejected with GC_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture on the device.
+ *  - All calls share the array: calls that overlap on the GPU (other streams,
+ *    other threads) race on it and must be serialized by the caller.
+ *  - It allocates and frees nothing. */
+gc_status gc_ef_topk_compress_noalloc(const gc_layout* dev, const gc_layout* host, const float* g,
+                                      float* e, int32_t* idx, float* val, int8_t* q, float* scale,
+                                      uint64_t seed, uint64_t iter, uint32_t flags, void* stream);
+
 /* DGC momentum correction + Top-k (inferensys.com "Gradient Sparsification",
  * momentum correction and momentum factor masking; genomic glossary, DGC):
  *   u = beta * u + g;  v = v + u;  S = Top-k of |v|;  payload v[S] (or int8);
