@@ -57,6 +57,8 @@ def lib() -> C.CDLL:
         L.gc_workspace_size.argtypes = [LP, I32, U32, C.POINTER(SZ)]
         L.gc_ef_topk_compress.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_topk_compress_profiled.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P, P, I32]
+        L.gc_ef_topk_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
+        L.gc_ef_residual_materialize.argtypes = [LP, LP, P, P, P]
         L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
@@ -68,7 +70,8 @@ def lib() -> C.CDLL:
         L.gc_status_string.restype = C.c_char_p
         L.gc_version.restype = I32
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
-                     "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_momentum",
+                     "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
+                     "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
             getattr(L, name).restype = I32
@@ -170,6 +173,26 @@ def ef_topk_compress(layout, g, e, idx, val, q, scale, seed, it, flags, workspac
     _check(lib().gc_ef_topk_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx), _ptr(val),
                                      _ptr(q), _ptr(scale), int(seed), int(it), int(flags), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "gc_ef_topk_compress")
+
+
+RESIDUAL_DESC_BYTES = 32
+
+
+def alloc_residual_desc(layout: Layout, device=None) -> torch.Tensor:
+    """Zeroed gc_residual_desc[T] for gc_ef_topk_compress_lazy (no pending selection)."""
+    return torch.zeros(layout.T * RESIDUAL_DESC_BYTES, dtype=torch.uint8, device=device or layout.device)
+
+
+def ef_topk_compress_lazy(layout, g, e, rd, idx, val, q, scale, seed, it, flags, workspace, stream=None):
+    _check(lib().gc_ef_topk_compress_lazy(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(rd), _ptr(idx),
+                                          _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
+                                          _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_ef_topk_compress_lazy")
+
+
+def ef_residual_materialize(layout, e, rd, stream=None):
+    _check(lib().gc_ef_residual_materialize(layout.dev(), layout.host(), _ptr(e), _ptr(rd), _stream(stream)),
+           "gc_ef_residual_materialize")
 
 
 def ef_topk_compress_noalloc(layout, g, e, idx, val, q, scale, seed, it, flags, stream=None):

@@ -25,13 +25,12 @@ constexpr int WCAP = 512;
 constexpr int64_t SMALL_N = 65536;
 // Expected number of Top-k members in a tensor's sample.
 constexpr int64_t SAMPLE_HITS = 128;
-constexpr int RUN = 16;  // sampled elements per contiguous run
+constexpr int RUN = 128;  // sampled elements per contiguous run (one warp, one float4 per lane)
 
 // Tensor state flags.
 constexpr uint32_t TS_NOEMIT = 1u;    // k_t == 0: nothing is selected
 constexpr uint32_t TS_DENSE = 2u;     // select with full passes over the tensor
 constexpr uint32_t TS_OVERFLOW = 4u;  // candidate staging overflowed
-constexpr uint32_t TS_TEST_DONE = 8u; // threshold estimate fixed early (no second sample level)
 
 // Diagnostic words at the head of every workspace.
 constexpr int DIAG_ERR = 0, DIAG_EXACT = 1, DIAG_OVF = 2, DIAG_ABORT = 3;
@@ -46,8 +45,7 @@ struct alignas(16) TensorState {
   uint32_t cand_count;  // candidates reserved by the streaming pass
   uint32_t thr;         // exact key of the k-th element
   uint32_t r_eq;        // how many elements with key == thr are kept (lowest indices)
-  uint32_t sample_j;    // rank sought in the sample
-  uint32_t pad[7];
+  uint32_t pad[8];
 };
 static_assert(sizeof(TensorState) == 64, "TensorState is 64 bytes");
 
@@ -81,8 +79,19 @@ __host__ __device__ inline void sample_plan(int64_t n, int64_t k, int64_t* runs,
   if (r > rmax) r = rmax;
   if (r < 1) r = 1;
   *runs = r;
-  *stride = n / r;
+  *stride = (n / r) & ~int64_t(3);  // keeps float4 alignment of every run; still >= RUN
   *m = r * RUN;
+}
+
+// Element offset of sample run r inside its stride window: a hashed jitter
+// (multiple of 4, run stays inside the window) so that runs of a tensor do
+// not sit at a power-of-two spacing, which would map them all onto the same
+// DRAM channels.  Zero when the tensor is sampled completely.
+__host__ __device__ inline int64_t sample_run_start(int64_t r, int64_t stride) {
+  const int64_t slack = (stride - RUN) >> 2;
+  if (slack <= 0) return r * stride;
+  const uint32_t h = (uint32_t)r * 2654435761u;
+  return r * stride + 4 * (int64_t)(h % (uint32_t)(slack + 1));
 }
 
 // ---------------------------------------------------------------- keys
@@ -154,7 +163,9 @@ __device__ __forceinline__ int stochastic_round(float x, uint32_t r) {
 // int8 code of x for scale s (s == 0 gives 0).
 __device__ __forceinline__ int int8_code(float x, float s, uint32_t r) {
   if (s == 0.0f) return 0;
-  int m = stochastic_round(__fdiv_rn(fabsf(x), s), r);
+  // |x| <= max|acc| keeps |x| / s near 127; the clamp (which cannot change
+  // min(127, .)) only guards the float -> int conversion
+  int m = stochastic_round(fminf(__fdiv_rn(fabsf(x), s), 128.0f), r);
   m = m > 127 ? 127 : m;
   return signbit(x) ? -m : m;
 }

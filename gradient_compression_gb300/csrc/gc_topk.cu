@@ -32,7 +32,7 @@
 namespace gc {
 
 enum { MODE_TOPK = 0, MODE_RANDK = 1, MODE_MOM = 2 };
-enum { PH_S1 = 0, PH_S2 = 1, PH_C1 = 2, PH_C1D = 3, PH_C2 = 4, PH_C3 = 5 };
+enum { PH_C1 = 0, PH_C1D = 1, PH_C2 = 2, PH_C3 = 3 };
 
 struct TopkArgs {
   int T;
@@ -55,6 +55,7 @@ struct TopkArgs {
   int8_t* q;
   float* scale;
   uint64_t seed, iter;
+  gc_residual_desc* rd;  // pending-residual descriptors (lazy mode), else null
   // workspace
   uint32_t* diag;
   TensorState* ts;
@@ -169,15 +170,39 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
 
 // ============================================================================ acc of one element
 
-// acc of element gi computed from the inputs (used by the sampler; the
-// streaming pass computes the same expression).
+// Lazy mode.  An element whose stored value x is the acc of the call
+// described by d was kept by that call iff its key is above the k-th key, or
+// equal to it at an index up to the last kept tie.
+__device__ __forceinline__ bool lazy_kept(float x, int64_t li, const gc_residual_desc& d) {
+  const uint32_t key = mag_key(x);
+  return (d.flags & 1u) && (key > d.thr || (key == d.thr && li <= (int64_t)d.last_tie));
+}
+
+// Residual of a kept element: +0, or acc - q*s with the int8 code redrawn
+// from that call's Philox words (equal to what the eager update writes).
+// Not inlined, so that the rare redraw stays out of the streaming loop.
+__device__ __noinline__ float lazy_kept_residual(float x, int64_t gi, gc_residual_desc d) {
+  if (!(d.flags & 2u)) return 0.0f;
+  const int c = int8_code(x, d.scale, philox_word(d.seed, d.iter, (uint64_t)gi, PURPOSE_INT8));
+  return __fsub_rn(x, __fmul_rn((float)c, d.scale));
+}
+
+// Exact EF residual of an element stored in pending form.
+__device__ __forceinline__ float lazy_fix(float x, int64_t li, int64_t gi, const gc_residual_desc& d) {
+  return lazy_kept(x, li, d) ? lazy_kept_residual(x, gi, d) : x;
+}
+
+// acc of element gi (local index li of tensor t) computed from the inputs
+// (used by the sampler; the streaming pass computes the same expression).
 template <int MODE>
-__device__ __forceinline__ float acc_from_inputs(const TopkArgs& A, int64_t gi) {
+__device__ __forceinline__ float acc_from_inputs(const TopkArgs& A, int t, int64_t li, int64_t gi) {
   if (MODE == MODE_MOM) {
     const float un = __fadd_rn(__fmul_rn(A.beta, A.u[gi]), A.g[gi]);
     return __fadd_rn(A.v[gi], un);
   }
-  return A.ef ? __fadd_rn(A.g[gi], A.e[gi]) : A.g[gi];
+  if (!A.ef) return A.g[gi];
+  const float r = A.rd ? lazy_fix(A.e[gi], li, gi, A.rd[t]) : A.e[gi];
+  return __fadd_rn(A.g[gi], r);
 }
 
 // After the streaming pass: the kept value source and the selection key.
@@ -197,66 +222,45 @@ __device__ __forceinline__ bool aborted(const TopkArgs& A) { return A.diag[DIAG_
 
 // ============================================================================ sampling
 
-constexpr int SX = 16;  // CTAs per tensor in the sampling and candidate-histogram kernels
-
+// Four consecutive acc values (elements li .. li+3 of tensor t, arena base
+// `base`), read with one 16-byte load per input when aligned and complete.
 template <int MODE>
-__global__ void __launch_bounds__(256) k_sample1(TopkArgs A) {
-  __shared__ uint32_t sh[NBINS];
-  const int t = blockIdx.x;
-  if (aborted(A)) return;
-  const TensorState* st = A.ts + t;
-  if (st->flags & TS_NOEMIT) return;
-  const int64_t base = A.off[t], n = A.off[t + 1] - base;
-  if (A.kk[t] >= n) return;  // t_est = 0 already
-  int64_t runs, stride, m;
-  sample_plan(n, A.kk[t], &runs, &stride, &m);
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  __syncthreads();
-  const int half = threadIdx.x >> 4, l16 = threadIdx.x & 15;  // 16 runs per CTA step
-  uint32_t* sk = A.skey + A.soff[t];
-  for (int64_t r0 = (int64_t)blockIdx.y * 16; r0 < runs; r0 += (int64_t)gridDim.y * 16) {
-    const int64_t r = r0 + half;
-    const int64_t li = r * stride + l16;
-    const bool valid = (r < runs) && (li < n);
-    uint32_t key = 0;
-    if (valid) {
-      key = mag_key(acc_from_inputs<MODE>(A, base + li));
-      sk[r * RUN + l16] = key;
+__device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64_t base, int64_t n,
+                                                 int64_t li, bool vec, float a[4], bool ok[4]) {
+  const int64_t gi = base + li;
+  if (vec && li + 4 <= n) {
+    const float4 g4 = ld_stream(reinterpret_cast<const float4*>(A.g + gi));
+    if (MODE == MODE_MOM) {
+      const float4 u4 = ld_stream(reinterpret_cast<const float4*>(A.u + gi));
+      const float4 v4 = ld_stream(reinterpret_cast<const float4*>(A.v + gi));
+      a[0] = __fadd_rn(v4.x, __fadd_rn(__fmul_rn(A.beta, u4.x), g4.x));
+      a[1] = __fadd_rn(v4.y, __fadd_rn(__fmul_rn(A.beta, u4.y), g4.y));
+      a[2] = __fadd_rn(v4.z, __fadd_rn(__fmul_rn(A.beta, u4.z), g4.z));
+      a[3] = __fadd_rn(v4.w, __fadd_rn(__fmul_rn(A.beta, u4.w), g4.w));
+    } else if (A.ef) {
+      float4 e4 = ld_stream(reinterpret_cast<const float4*>(A.e + gi));
+      if (A.rd) {
+        const gc_residual_desc d = A.rd[t];
+        e4.x = lazy_fix(e4.x, li + 0, gi + 0, d);
+        e4.y = lazy_fix(e4.y, li + 1, gi + 1, d);
+        e4.z = lazy_fix(e4.z, li + 2, gi + 2, d);
+        e4.w = lazy_fix(e4.w, li + 3, gi + 3, d);
+      }
+      a[0] = __fadd_rn(g4.x, e4.x);
+      a[1] = __fadd_rn(g4.y, e4.y);
+      a[2] = __fadd_rn(g4.z, e4.z);
+      a[3] = __fadd_rn(g4.w, e4.w);
+    } else {
+      a[0] = g4.x; a[1] = g4.y; a[2] = g4.z; a[3] = g4.w;
     }
-    smem_hist_add(sh, key >> 21, valid);
+    ok[0] = ok[1] = ok[2] = ok[3] = true;
+    return;
   }
-  __syncthreads();
-  uint32_t* row = A.hist + (size_t)t * NBINS;
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
-    if (sh[i]) atomicAdd(row + i, sh[i]);
-}
-
-__global__ void __launch_bounds__(256) k_sample2(TopkArgs A) {
-  __shared__ uint32_t sh[NBINS];
-  const int t = blockIdx.x;
-  if (aborted(A)) return;
-  const TensorState st = A.ts[t];
-  if (st.flags & (TS_NOEMIT | TS_TEST_DONE)) return;
-  const int64_t n = A.off[t + 1] - A.off[t];
-  if (A.kk[t] >= n) return;
-  int64_t runs, stride, m;
-  sample_plan(n, A.kk[t], &runs, &stride, &m);
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  __syncthreads();
-  const uint32_t* sk = A.skey + A.soff[t];
-  // small tensors store their sample at the element's own index
-  const int64_t len = (n <= SMALL_N) ? n : m;
-  for (int64_t i0 = (int64_t)blockIdx.y * blockDim.x; i0 < len; i0 += (int64_t)gridDim.y * blockDim.x) {
-    const int64_t i = i0 + threadIdx.x;
-    const bool valid = i < len;
-    const uint32_t key = valid ? sk[i] : 0u;
-    const bool hit = valid && ((key >> 21) == st.prefix);
-    smem_hist_add(sh, (key >> 10) & 0x7FFu, hit);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    ok[j] = li + j < n;
+    a[j] = ok[j] ? acc_from_inputs<MODE>(A, t, li + j, gi + j) : 0.0f;
   }
-  __syncthreads();
-  uint32_t* row = A.hist + (size_t)t * NBINS;
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
-    if (sh[i]) atomicAdd(row + i, sh[i]);
 }
 
 // ============================================================================ select
@@ -271,52 +275,174 @@ __device__ void block_scan_u32(uint32_t v, uint32_t* s_warp, uint32_t* excl, uin
     unsigned z = lane < nw ? s_warp[lane] : 0u, tz;
     const unsigned ez = warp_excl_scan(z, lane, &tz);
     if (lane < nw) s_warp[lane] = ez;
-    if (lane == 0) s_warp[31] = tz;
+    if (lane == 0) s_warp[32] = tz;
   }
   __syncthreads();
   *excl = s_warp[w] + e;
-  *total = s_warp[31];
+  *total = s_warp[32];
   __syncthreads();
+}
+
+// Finds the bucket holding the rank-th largest key of a 2048-bin histogram
+// (bins in key order; `row` in global or shared memory).  Returns the bin and
+// the number of keys in the bins above it, or 0xFFFFFFFF when the histogram
+// holds fewer than `rank` keys.  Called by all 256 threads of the block.
+__device__ uint32_t find_bucket(const uint32_t* row, uint32_t rank, uint32_t* above,
+                                uint32_t* s_warp, uint32_t* s_res) {
+  // thread i owns `per` bins from 2047 - per*i downwards (keys in descending
+  // order); blockDim.x is 256, 512 or 1024
+  const int per = NBINS / (int)blockDim.x;
+  uint32_t h[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = j < per ? row[NBINS - 1 - per * threadIdx.x - j] : 0u;
+    sum += h[j];
+  }
+  uint32_t pre, total;
+  block_scan_u32(sum, s_warp, &pre, &total);
+  if (threadIdx.x == 0) s_res[0] = 0xFFFFFFFFu;
+  __syncthreads();
+  const uint32_t r0 = rank - 1u;
+  if (rank >= 1u && rank <= total && r0 >= pre && r0 < pre + sum) {
+    uint32_t acc = pre;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < per && r0 < acc + h[j]) {
+        s_res[0] = NBINS - 1 - per * threadIdx.x - j;
+        s_res[1] = acc;
+        break;
+      }
+      acc += h[j];
+    }
+  }
+  __syncthreads();
+  const uint32_t b = s_res[0];
+  *above = s_res[1];
+  __syncthreads();
+  return b;
+}
+
+// Threshold estimate t_est from a strided sample of acc, one CTA of 1024
+// threads per tensor.  The sample is runs of RUN = 128 consecutive elements
+// (one warp, 16 bytes per lane per input) spaced `stride` apart; small
+// tensors are sampled completely.  Level 1: shared-memory histogram of the
+// sample keys' top 11 bits -> the bucket of the j-th largest sample key.
+// Level 2: the next 11 bits of the sample keys in that bucket (re-read from
+// the sample key buffer) -> t_est = the lower edge of that level-2 bucket,
+// which is <= the j-th largest sample key.
+template <int MODE>
+__global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
+  __shared__ uint32_t s_warp[33];
+  __shared__ uint32_t s_res[2];
+  __shared__ uint32_t sh[NBINS];
+  const int t = blockIdx.x;
+  if (aborted(A)) return;
+  TensorState* st = A.ts + t;
+  if (st->flags & TS_NOEMIT) return;
+  const int64_t base = A.off[t], n = A.off[t + 1] - base;
+  const int64_t k = A.kk[t];
+  if (k >= n) return;  // t_est = 0 already
+  int64_t runs, stride, m;
+  sample_plan(n, k, &runs, &stride, &m);
+  int64_t j;
+  if (m >= n) {
+    j = k;
+  } else {
+    const double lam = (double)k * (double)m / (double)n;
+    j = (int64_t)ceil(lam + 4.0 * sqrt(lam) + 4.0);
+  }
+  if (j > m) {
+    if (threadIdx.x == 0) st->t_est = 0u;
+    return;
+  }
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  const unsigned lane = lane_id();
+  const bool vec = (base & 3) == 0;
+  uint32_t* sk = A.skey + A.soff[t];
+  const int64_t nwarp = blockDim.x >> 5;
+  for (int64_t r0 = threadIdx.x >> 5; r0 < runs; r0 += 2 * nwarp) {
+    float a[2][4];
+    bool ok[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t r = r0 + h * nwarp;
+      if (r < runs) {
+        acc4_from_inputs<MODE>(A, t, base, n, sample_run_start(r, stride) + 4 * lane, vec, a[h], ok[h]);
+      } else {
+        ok[h][0] = ok[h][1] = ok[h][2] = ok[h][3] = false;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t r = r0 + h * nwarp;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t key = mag_key(a[h][c]);
+        if (ok[h][c]) {
+          sk[r * RUN + 4 * lane + c] = key;
+          atomicAdd(sh + (key >> 21), 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t above;
+  const uint32_t b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  if (b1 == 0xFFFFFFFFu) {
+    if (threadIdx.x == 0) {
+      atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+      st->t_est = 0u;
+    }
+    return;
+  }
+  const uint32_t rank2 = (uint32_t)j - above;
+  constexpr int U8 = 8;
+  for (int64_t i0 = 0; i0 < m; i0 += (int64_t)blockDim.x * U8) {
+    uint32_t kk[U8];
+#pragma unroll
+    for (int u = 0; u < U8; ++u) {
+      const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
+      kk[u] = i < m ? __ldcg(sk + i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U8; ++u) {
+      const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
+      smem_hist_add(sh, (kk[u] >> 10) & 0x7FFu, i < m && (kk[u] >> 21) == b1);
+    }
+  }
+  __syncthreads();
+  uint32_t above2;
+  const uint32_t b2 = find_bucket(sh, rank2, &above2, s_warp, s_res);
+  if (threadIdx.x == 0) {
+    if (b2 == 0xFFFFFFFFu) {
+      atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+      st->t_est = b1 << 21;
+    } else {
+      st->t_est = (b1 << 21) | (b2 << 10);
+    }
+  }
 }
 
 // One radix level of the k-th key search for every tensor (one CTA each).
 __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
-  __shared__ uint32_t s_warp[32];
+  __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[3];
   const int t = blockIdx.x;
   if (aborted(A)) return;
   TensorState* st = A.ts + t;
   const uint32_t flags = st->flags;
-  if (flags & TS_NOEMIT) return;
-  const int64_t n = A.off[t + 1] - A.off[t];
+  if (flags & TS_NOEMIT) {
+    if (phase == PH_C1 && A.rd && threadIdx.x == 0) A.rd[t] = gc_residual_desc{0u, 0u, 0, 0.0f, 0ull, 0ull};
+    return;
+  }
   const int64_t k = A.kk[t];
   uint32_t* row = A.hist + (size_t)t * NBINS;
   uint32_t rank = st->rank;
 
-  if (phase == PH_S1 || phase == PH_S2) {
-    if (k >= n) return;
-    if (phase == PH_S2 && (flags & TS_TEST_DONE)) return;
-    if (phase == PH_S1) {
-      int64_t runs, stride, m;
-      sample_plan(n, k, &runs, &stride, &m);
-      int64_t j;
-      if (m >= n) {
-        j = k;
-      } else {
-        const double lam = (double)k * (double)m / (double)n;
-        j = (int64_t)ceil(lam + 4.0 * sqrt(lam) + 4.0);
-      }
-      if (j > m) {
-        if (threadIdx.x == 0) {
-          st->t_est = 0u;
-          st->flags = flags | TS_TEST_DONE;
-        }
-        for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
-        return;
-      }
-      rank = (uint32_t)j;
-    }
-  } else if (phase == PH_C1) {
+  if (phase == PH_C1) {
     const int64_t cap = A.cand_off[t + 1] - A.cand_off[t];
     const int64_t cnt = st->cand_count;
     const bool dense = (flags & TS_OVERFLOW) || cnt > cap || cnt < k || (A.flags & GC_FORCE_EXACT);
@@ -338,51 +464,17 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
     rank = (uint32_t)k;
   }
 
-  // Thread i owns bins 2047-8i down to 2040-8i (keys in descending order).
-  uint32_t h[8], sum = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    h[j] = row[NBINS - 1 - 8 * threadIdx.x - j];
-    sum += h[j];
-  }
-  uint32_t pre, total;
-  block_scan_u32(sum, s_warp, &pre, &total);
-  if (threadIdx.x == 0) s_res[0] = 0xFFFFFFFFu;
-  __syncthreads();
-  const uint32_t r0 = rank - 1u;
-  if (rank >= 1u && rank <= total && r0 >= pre && r0 < pre + sum) {
-    uint32_t acc = pre;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (r0 < acc + h[j]) {
-        s_res[0] = NBINS - 1 - 8 * threadIdx.x - j;
-        s_res[1] = acc;
-        break;
-      }
-      acc += h[j];
-    }
-  }
-  __syncthreads();
+  uint32_t above;
+  const uint32_t b = find_bucket(row, rank, &above, s_warp, s_res);
   for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
   if (threadIdx.x != 0) return;
-  const uint32_t b = s_res[0];
   if (b == 0xFFFFFFFFu) {
     atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
     st->flags = flags | TS_NOEMIT;  // never write a wrong payload
     return;
   }
-  const uint32_t above = s_res[1];
   rank -= above;
   switch (phase) {
-    case PH_S1:
-      st->prefix = b;
-      st->rank = rank;
-      break;
-    case PH_S2:
-      st->t_est = (st->prefix << 21) | (b << 10);
-      st->prefix = 0u;
-      st->rank = 0u;
-      break;
     case PH_C1:
     case PH_C1D:
       st->prefix = b;
@@ -396,7 +488,13 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
       st->thr = (st->prefix << 10) | b;
       st->r_eq = rank;
       st->rank = rank;
-      if (A.int8) A.scale[t] = __fdiv_rn(key_magnitude(st->maxkey), 127.0f);
+      float sc = 0.0f;
+      if (A.int8) {
+        sc = __fdiv_rn(key_magnitude(st->maxkey), 127.0f);
+        A.scale[t] = sc;
+      }
+      // last_tie is filled in by the payload write
+      if (A.rd) A.rd[t] = gc_residual_desc{1u | (A.int8 ? 2u : 0u), st->thr, -1, sc, A.seed, A.iter};
       break;
     }
   }
@@ -428,8 +526,9 @@ __device__ __forceinline__ void warp_append(float* sval, uint32_t* skey, uint16_
   cnt += (int)tot;
 }
 
-template <int MODE, bool EF, bool LOADG>
-__device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t gi, float* value,
+template <int MODE, bool EF, bool LOADG, bool LAZY>
+__device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t li, int64_t gi,
+                                              const gc_residual_desc& d, float* value,
                                               uint32_t* key) {
   float x = 0.0f;
   if (MODE == MODE_MOM) {
@@ -440,7 +539,7 @@ __device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t gi, flo
   } else if (LOADG) {
     x = A.g[gi];
     if (EF) {
-      x = __fadd_rn(x, A.e[gi]);
+      x = __fadd_rn(x, LAZY ? lazy_fix(A.e[gi], li, gi, d) : A.e[gi]);
       A.e[gi] = x;
     }
   }
@@ -454,8 +553,8 @@ constexpr int STREAM_WARPS = STREAM_THREADS / 32;
 constexpr int STREAM_UNROLL = 4;
 constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
 
-template <int MODE, bool EF, bool LOADG>
-__global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
+template <int MODE, bool EF, bool LOADG, bool LAZY>
+__global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_stream(TopkArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
@@ -473,6 +572,8 @@ __global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
     const int64_t g0 = base + lstart;
     const bool emit = !(A.ts[t].flags & TS_NOEMIT);
     const uint32_t test = A.ts[t].t_est;
+    gc_residual_desc d;
+    if (LAZY) d = A.rd[t];
     int cnt = 0;
     bool ovf = false;
     if ((g0 & 3) == 0) {
@@ -519,6 +620,18 @@ __global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
             } else if (LOADG) {
               float4 s = x[j];
               if (EF) {
+                if (LAZY) {
+                  const int64_t li0 = lstart + 4 * vi;
+                  const bool k0 = lazy_kept(y[j].x, li0 + 0, d), k1 = lazy_kept(y[j].y, li0 + 1, d);
+                  const bool k2 = lazy_kept(y[j].z, li0 + 2, d), k3 = lazy_kept(y[j].w, li0 + 3, d);
+                  if (k0 | k1 | k2 | k3) {
+                    const int64_t gq = g0 + 4 * vi;
+                    if (k0) y[j].x = lazy_kept_residual(y[j].x, gq + 0, d);
+                    if (k1) y[j].y = lazy_kept_residual(y[j].y, gq + 1, d);
+                    if (k2) y[j].z = lazy_kept_residual(y[j].z, gq + 2, d);
+                    if (k3) y[j].w = lazy_kept_residual(y[j].w, gq + 3, d);
+                  }
+                }
                 s.x = __fadd_rn(s.x, y[j].x);
                 s.y = __fadd_rn(s.y, y[j].y);
                 s.z = __fadd_rn(s.z, y[j].z);
@@ -550,7 +663,7 @@ __global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
         const bool valid = (int)lane < rem;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t kk[4] = {0u, 0u, 0u, 0u};
-        if (valid) stream_scalar<MODE, EF, LOADG>(A, g0 + li, &a[0], &kk[0]);
+        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, &a[0], &kk[0]);
         const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
         if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
       }
@@ -560,7 +673,7 @@ __global__ void __launch_bounds__(STREAM_THREADS) k_stream(TopkArgs A) {
         const bool valid = li < len;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t kk[4] = {0u, 0u, 0u, 0u};
-        if (valid) stream_scalar<MODE, EF, LOADG>(A, g0 + li, &a[0], &kk[0]);
+        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, &a[0], &kk[0]);
         const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
         if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
       }
@@ -664,12 +777,26 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
       mx = warp_max_u32(mx);
       if (lane == 0) atomicMax(&s_max, mx);
     }
-  } else if (threadIdx.x < ub.nu) {
-    const uint2 ch = A.chunk[ub.u0 + threadIdx.x];
-    const int64_t cb = A.cand_off[ub.t] + ch.x;
-    for (uint32_t j = 0; j < ch.y; ++j) {
-      const uint32_t key = A.ckey[cb + j];
-      if ((key >> shift_prev) == st.prefix) atomicAdd(sh + ((key >> shift) & mask), 1u);
+  } else {
+    // this CTA's slice of the tensor's candidate keys (order is irrelevant here)
+    const int64_t nb = A.ublk_off[ub.t + 1] - A.ublk_off[ub.t];
+    const int64_t bi = (int64_t)blockIdx.x - A.ublk_off[ub.t];
+    const int64_t cnt = st.cand_count;
+    const int64_t lo = cnt * bi / nb, hi = cnt * (bi + 1) / nb;
+    const uint32_t* ck = A.ckey + A.cand_off[ub.t];
+    constexpr int U8 = 8;
+    for (int64_t i0 = lo; i0 < hi; i0 += (int64_t)blockDim.x * U8) {
+      uint32_t kk[U8];
+#pragma unroll
+      for (int u = 0; u < U8; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
+        kk[u] = i < hi ? __ldcs(ck + i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U8; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
+        if (i < hi && (kk[u] >> shift_prev) == st.prefix) atomicAdd(sh + ((kk[u] >> shift) & mask), 1u);
+      }
     }
   }
   __syncthreads();
@@ -684,7 +811,7 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
 template <int MODE>
 __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
-  __shared__ uint32_t s_warp[32];
+  __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
   const UnitBlock ub = unit_block(A);
   const TensorState st = A.ts[ub.t];
@@ -717,12 +844,18 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
       }
     } else if (tid < ub.nu) {
       const uint2 ch = A.chunk[ub.u0 + tid];
-      const int64_t cb = A.cand_off[ub.t] + ch.x;
+      const uint32_t* ck = A.ckey + A.cand_off[ub.t] + ch.x;
       uint32_t gt = 0u, eq = 0u;
-      for (uint32_t j = 0; j < ch.y; ++j) {
-        const uint32_t key = A.ckey[cb + j];
-        gt += key > st.thr;
-        eq += key == st.thr;
+      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
+        uint32_t kk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ch.y ? __ldcs(ck + j0 + u) : 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool v = j0 + u < ch.y;
+          gt += v && kk[u] > st.thr;
+          eq += v && kk[u] == st.thr;
+        }
       }
       s_gt[tid] = gt;
       s_eq[tid] = eq;
@@ -745,7 +878,7 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
 
 // Exclusive scan of the unit-block sums of each tensor (one CTA each).
 __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
-  __shared__ uint32_t s_warp[32];
+  __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
   const int t = blockIdx.x;
   const int64_t b0 = A.ublk_off[t], b1 = A.ublk_off[t + 1];
@@ -769,7 +902,8 @@ __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
 // Writes one kept element: payload slot `pos` (absolute), residual.
 template <int MODE>
 __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base, int64_t n,
-                                          int64_t li, float x, int64_t pos, float s) {
+                                          int64_t li, float x, int64_t pos, float s, bool last_tie) {
+  if (A.rd && last_tie) A.rd[t].last_tie = (int32_t)li;
   if (pos >= A.koff[t + 1]) {  // only reachable if the selection were inconsistent
     atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
     return;
@@ -786,7 +920,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
     }
     return;
   }
-  float* res = (MODE == MODE_MOM) ? A.v : (A.ef ? A.e : nullptr);
+  float* res = (MODE == MODE_MOM) ? A.v : ((A.ef && !A.rd) ? A.e : nullptr);
   if (A.int8) {
     const int c = int8_code(x, s, philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_INT8));
     const float d = __fmul_rn((float)c, s);
@@ -803,7 +937,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
 template <int MODE>
 __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
-  __shared__ uint32_t s_warp[32];
+  __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
   const UnitBlock ub = unit_block(A);
   const TensorState st = A.ts[ub.t];
@@ -844,7 +978,9 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
         const unsigned eqm = __ballot_sync(FULL, iseq);
         const bool sel = isgt || (iseq && eqb + eqrun + __popc(eqm & lt) < r_eq);
         const unsigned selm = __ballot_sync(FULL, sel);
-        if (sel) emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + selpos + __popc(selm & lt), s);
+        if (sel)
+          emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + selpos + __popc(selm & lt), s,
+                          iseq && eqb + eqrun + __popc(eqm & lt) + 1u == r_eq);
         selpos += __popc(selm);
         eqrun += __popc(eqm);
       }
@@ -855,14 +991,28 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
     const uint32_t eqb = s_eq[tid];
     int64_t selpos = (int64_t)s_gt[tid] + min(eqb, r_eq);
     uint32_t eqrun = 0u;
-    for (uint32_t j = 0; j < ch.y; ++j) {
-      const uint32_t key = A.ckey[cb + j];
-      const bool iseq = key == thr;
-      const bool sel = key > thr || (iseq && eqb + eqrun < r_eq);
-      eqrun += iseq;
-      if (sel) {
-        emit_kept<MODE>(A, ub.t, ub.base, ub.n, A.cidx[cb + j], A.cval[cb + j], kbase + selpos, s);
-        ++selpos;
+    for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
+      uint32_t kk[8];
+      int32_t ci[8];
+      float cv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool v = j0 + u < ch.y;
+        kk[u] = v ? __ldcs(A.ckey + cb + j0 + u) : 0u;
+        ci[u] = v ? __ldcs(A.cidx + cb + j0 + u) : 0;
+        cv[u] = v ? __ldcs(A.cval + cb + j0 + u) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= ch.y) break;
+        const bool iseq = kk[u] == thr;
+        const bool sel = kk[u] > thr || (iseq && eqb + eqrun < r_eq);
+        const bool last = iseq && eqb + eqrun + 1u == r_eq;
+        eqrun += iseq;
+        if (sel) {
+          emit_kept<MODE>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
+          ++selpos;
+        }
       }
     }
   }
@@ -945,17 +1095,31 @@ static int stream_grid(K kernel, int64_t units) {
   return (int)grid;
 }
 
-template <int MODE, bool EF, bool LOADG>
+template <int MODE, bool EF, bool LOADG, bool LAZY = false>
 static void launch_stream(const TopkArgs& A, cudaStream_t s) {
-  auto kern = k_stream<MODE, EF, LOADG>;
-  k_stream<MODE, EF, LOADG><<<stream_grid(kern, A.U), STREAM_THREADS, STREAM_SMEM, s>>>(A);
+  auto kern = k_stream<MODE, EF, LOADG, LAZY>;
+  k_stream<MODE, EF, LOADG, LAZY><<<stream_grid(kern, A.U), STREAM_THREADS, STREAM_SMEM, s>>>(A);
 }
 
+// Optional CUDA events recorded on the call's stream.  With n <= 5 they
+// mark the phases (start, before the streaming pass, after it, after the
+// k-th key search, after the payload write); with n > 5, event 0 marks the
+// start and event j the end of the j-th enqueued operation.
 struct PhaseEvents {
   void* const* ev = nullptr;
   int n = 0;
-  void mark(int i, cudaStream_t s) const {
+  mutable int ops = 0;
+  void record(int i, cudaStream_t s) const {
     if (i < n && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+  }
+  void start(cudaStream_t s) const { record(0, s); }
+  // after each enqueued operation; `phase` > 0 if it ends that phase
+  void done(int phase, cudaStream_t s) const {
+    ++ops;
+    if (n > 5)
+      record(ops, s);
+    else if (phase > 0)
+      record(phase, s);
   }
 };
 
@@ -963,17 +1127,17 @@ template <int MODE>
 static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
   const int T = A.T;
   k_plan<<<1, 1024, 0, s>>>(A);
+  pe.done(MODE == MODE_RANDK ? 1 : 0, s);
   if (MODE != MODE_RANDK) {
-    k_sample1<MODE><<<dim3(T, SX), 256, 0, s>>>(A);
-    k_select<<<T, 256, 0, s>>>(A, PH_S1);
-    k_sample2<<<dim3(T, SX), 256, 0, s>>>(A);
-    k_select<<<T, 256, 0, s>>>(A, PH_S2);
+    k_sample<MODE><<<T, 1024, 0, s>>>(A);
+    pe.done(1, s);
   }
-  pe.mark(1, s);
   if (MODE == MODE_MOM) {
     launch_stream<MODE_MOM, false, true>(A, s);
   } else if (MODE == MODE_TOPK) {
-    if (A.ef)
+    if (A.ef && A.rd)
+      launch_stream<MODE_TOPK, true, true, true>(A, s);
+    else if (A.ef)
       launch_stream<MODE_TOPK, true, true>(A, s);
     else
       launch_stream<MODE_TOPK, false, true>(A, s);
@@ -985,26 +1149,35 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
     else
       launch_stream<MODE_RANDK, false, true>(A, s);
   }
-  pe.mark(2, s);
+  pe.done(2, s);
   const unsigned UBg = (unsigned)A.UB;
   k_select<<<T, 256, 0, s>>>(A, PH_C1);
+  pe.done(0, s);
   k_hist<MODE><<<UBg, 256, 0, s>>>(A, 1);
+  pe.done(0, s);
   k_select<<<T, 256, 0, s>>>(A, PH_C1D);
+  pe.done(0, s);
   k_hist<MODE><<<UBg, 256, 0, s>>>(A, 2);
+  pe.done(0, s);
   k_select<<<T, 256, 0, s>>>(A, PH_C2);
+  pe.done(0, s);
   k_hist<MODE><<<UBg, 256, 0, s>>>(A, 3);
+  pe.done(0, s);
   k_select<<<T, 256, 0, s>>>(A, PH_C3);
-  pe.mark(3, s);
+  pe.done(3, s);
   k_count<MODE><<<UBg, 256, 0, s>>>(A);
+  pe.done(0, s);
   k_scan<<<T, 256, 0, s>>>(A);
+  pe.done(0, s);
   k_write<MODE><<<UBg, 256, 0, s>>>(A);
-  pe.mark(4, s);
+  pe.done(4, s);
 }
 
 static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host, const float* g,
                           float* e, float* u, float* v, float beta, int32_t* idx, float* val,
                           int8_t* q, float* scale, uint64_t seed, uint64_t iter, uint32_t flags,
-                          void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe) {
+                          void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe,
+                          gc_residual_desc* rd = nullptr) {
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
@@ -1044,6 +1217,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.scale = scale;
   A.seed = seed;
   A.iter = iter;
+  A.rd = rd;
   A.diag = reinterpret_cast<uint32_t*>(w);
   A.ts = reinterpret_cast<TensorState*>(w + c.o_ts);
   A.hist = reinterpret_cast<uint32_t*>(w + c.o_hist);
@@ -1068,8 +1242,9 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.K = z.K;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  pe.mark(0, s);
+  pe.start(s);
   if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
+  pe.done(0, s);
   if (mode == MODE_TOPK)
     launch_pipeline<MODE_TOPK>(A, s, pe);
   else if (mode == MODE_RANDK)
@@ -1113,7 +1288,7 @@ extern "C" gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc
                                                   uint64_t seed, uint64_t iter, uint32_t flags,
                                                   void* workspace, size_t ws_bytes, void* stream,
                                                   void* const* events, int32_t n_events) {
-  if (n_events < 0 || n_events > 5 || (n_events > 0 && !events)) return GC_ERR_INVALID_ARG;
+  if (n_events < 0 || n_events > 32 || (n_events > 0 && !events)) return GC_ERR_INVALID_ARG;
   PhaseEvents pe;
   pe.ev = events;
   pe.n = n_events;
@@ -1132,4 +1307,50 @@ extern "C" gc_status gc_ef_topk_compress_momentum(const gc_layout* dev, const gc
   if (!u || !v) return GC_ERR_INVALID_ARG;
   return run_topk(MODE_MOM, dev, host, g, nullptr, u, v, beta, idx, val, q, scale, seed, iter,
                   flags, workspace, ws_bytes, stream, PhaseEvents{});
+}
+
+extern "C" gc_status gc_ef_topk_compress_lazy(const gc_layout* dev, const gc_layout* host,
+                                              const float* g, float* e, gc_residual_desc* rd,
+                                              int32_t* idx, float* val, int8_t* q, float* scale,
+                                              uint64_t seed, uint64_t iter, uint32_t flags,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if (!e || !rd) return GC_ERR_INVALID_ARG;
+  return run_topk(MODE_TOPK, dev, host, g, e, nullptr, nullptr, 0.0f, idx, val, q, scale, seed,
+                  iter, flags | GC_EF, workspace, ws_bytes, stream, PhaseEvents{}, rd);
+}
+
+namespace gc {
+
+// e <- exact residual for every tensor with a pending selection.
+__global__ void __launch_bounds__(256) k_materialize(const int64_t* off, int T, float* e,
+                                                     const gc_residual_desc* rd) {
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const gc_residual_desc d = rd[t];
+    if (!(d.flags & 1u)) continue;
+    const int64_t base = off[t], n = off[t + 1] - base;
+    for (int64_t li = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; li < n;
+         li += (int64_t)gridDim.x * blockDim.x)
+      e[base + li] = lazy_fix(e[base + li], li, base + li, d);
+  }
+}
+
+__global__ void k_clear_desc(gc_residual_desc* rd, int T) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x)
+    rd[t] = gc_residual_desc{0u, 0u, 0, 0.0f, 0ull, 0ull};
+}
+
+}  // namespace gc
+
+extern "C" gc_status gc_ef_residual_materialize(const gc_layout* dev, const gc_layout* host, float* e,
+                                                gc_residual_desc* rd, void* stream) {
+  const gc_status st = validate_layout(host, false);
+  if (st != GC_OK) return st;
+  if (!dev || !dev->off || dev->num_tensors != host->num_tensors || !e || !rd) return GC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = host->num_tensors;
+  k_materialize<<<dim3(256, (unsigned)std::min(T, 65535)), 256, 0, s>>>(dev->off, T, e, rd);
+  k_clear_desc<<<(T + 255) / 256, 256, 0, s>>>(rd, T);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

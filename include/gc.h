@@ -88,6 +88,7 @@ typedef enum gc_status {
 #define GC_RANDK 0x4u       /* random-k selection instead of Top-k */
 #define GC_UNBIASED 0x8u    /* random-k only, without GC_EF: send g * (n/k), no residual */
 #define GC_NO_MASK 0x10u    /* momentum only: keep u on the selected set (no factor masking) */
+#define GC_LAZY 0x20u       /* set by gc_ef_topk_compress_lazy; not accepted elsewhere */
 #define GC_FORCE_EXACT 0x100u /* select with full passes over the tensor instead of the
                                  sampled candidate threshold (same results; for testing) */
 
@@ -153,16 +154,56 @@ gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const
                               void* stream);
 
 /* gc_ef_topk_compress with timing hooks: `events` is a host array of
- * `n_events` (0..5) cudaEvent_t handles created by the caller, recorded on
- * `stream` at the phase boundaries of the call: [0] start, [1] before the
- * streaming pass over g and e, [2] after it, [3] after the k-th key search,
- * [4] after the payload write.  NULL entries are skipped.  Results are
- * identical to gc_ef_topk_compress. */
+ * `n_events` (0..32) cudaEvent_t handles created by the caller, recorded on
+ * `stream`.  With n_events <= 5 they mark the phases of the call: [0] start,
+ * [1] before the streaming pass over g and e, [2] after it, [3] after the
+ * k-th key search, [4] after the payload write.  With n_events > 5, [0] marks
+ * the start and [j] the end of the j-th operation the call enqueues (for
+ * per-kernel timing).  NULL entries are skipped.  Results are identical to
+ * gc_ef_topk_compress. */
 gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc_layout* host, const float* g,
                                        float* e, int32_t* idx, float* val, int8_t* q, float* scale,
                                        uint64_t seed, uint64_t iter, uint32_t flags,
                                        void* workspace, size_t ws_bytes, void* stream,
                                        void* const* events, int32_t n_events);
+
+/* Residual of one tensor kept in pending form by gc_ef_topk_compress_lazy
+ * (device memory, caller-owned; all-zero = no pending selection). */
+typedef struct gc_residual_desc {
+  uint32_t flags;    /* bit 0: a selection is pending; bit 1: it was int8-quantized */
+  uint32_t thr;      /* selection key of the k-th kept element: (bits(acc) << 1) */
+  int32_t last_tie;  /* largest kept local index among elements whose key == thr */
+  float scale;       /* int8 scale of that call */
+  uint64_t seed;     /* Philox key of that call */
+  uint64_t iter;     /* Philox counter word of that call */
+} gc_residual_desc;
+
+/* EF Top-k (+ int8) with the residual update deferred ("lazy" residual).
+ * The pages' residual e_t = (g_t + e_{t-1}) - g^_t is not scattered into e
+ * at the kept positions; instead e keeps acc everywhere and rd[t] records
+ * which elements were kept (every element whose key exceeds thr, plus those
+ * equal to thr up to last_tie) and, for int8, how their codes were drawn.
+ * The next call's streaming pass recomputes the exact residual of each
+ * element from (e, rd) in registers before adding g, which saves the k
+ * random read-modify-writes of the eager update.  Payloads are bit-identical
+ * to gc_ef_topk_compress(GC_EF | flags), and gc_ef_residual_materialize turns
+ * (e, rd) into the plain residual (for checkpoints or switching to the eager
+ * entry point).
+ *   e:  device fp32[N], pending residual in/out (a plain residual when rd is
+ *       all zero, e.g. before the first call).
+ *   rd: device gc_residual_desc[T], in/out.
+ * flags: GC_INT8 and GC_FORCE_EXACT are accepted; GC_EF is implied; the
+ * layout must not change between calls sharing (e, rd). */
+gc_status gc_ef_topk_compress_lazy(const gc_layout* dev, const gc_layout* host, const float* g,
+                                   float* e, gc_residual_desc* rd, int32_t* idx, float* val,
+                                   int8_t* q, float* scale, uint64_t seed, uint64_t iter,
+                                   uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
+
+/* Applies the pending residual of gc_ef_topk_compress_lazy: e <- the exact
+ * EF residual, rd <- all zero.  One pass over the tensors with a pending
+ * selection; no workspace. */
+gc_status gc_ef_residual_materialize(const gc_layout* dev, const gc_layout* host, float* e,
+                                     gc_residual_desc* rd, void* stream);
 
 /* Size of the scratch array built into libgc for gc_ef_topk_compress_noalloc. */
 #define GC_NOALLOC_MAX_WORKSPACE_BYTES (32u << 20)

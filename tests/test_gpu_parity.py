@@ -41,7 +41,8 @@ def _bits(a):
 def _grad(n, seed, kind="t3"):
     gen = torch.Generator().manual_seed(seed)
     if kind == "t3":
-        x = torch.distributions.StudentT(3.0).sample((n,)) * 1e-3
+        x = torch.empty(n)
+        workloads.fill_student_t(x, 3.0, 1e-3, gen)
     elif kind == "ties":
         x = torch.randint(-2, 3, (n,), generator=gen).float() * 1e-3
     elif kind == "zeros":
@@ -405,3 +406,53 @@ def test_layout_mismatch_is_reported_not_run(gc):
     d = gc.get_device_status(ws, raise_on_error=False)
     assert d.error_bits & gc.GC_DIAG_LAYOUT_MISMATCH
     assert (idx.cpu() == -7).all()
+
+
+# ----------------------------------------------------------------------------- lazy residual
+
+@pytest.mark.parametrize("name", ["misaligned", "many_small", "medium", "flat"])
+@pytest.mark.parametrize("flags_name", ["ef", "ef_int8", "ef_int8_exact"])
+def test_topk_lazy_residual(gc, name, flags_name):
+    """Payloads of gc_ef_topk_compress_lazy equal the oracle's at every step, and
+    materializing a copy of (e, rd) gives the oracle's residual at every step."""
+    sizes = [1 << 20] if name == "flat" else LAYOUTS[name]
+    flags = {"ef": 0, "ef_int8": gc.GC_INT8, "ef_int8_exact": gc.GC_INT8 | gc.GC_FORCE_EXACT}[flags_name]
+    k = workloads.k_per_tensor(sizes, 0.01)
+    if len(sizes) > 2:
+        k[0] = sizes[0]
+        k[-1] = 0
+    L = _layout(gc, sizes, k=k)
+    n, K = L.numel, L.total_k
+    int8 = bool(flags & gc.GC_INT8)
+    e_ref = (np.random.default_rng(4).standard_normal(n) * 1e-4).astype(F32)
+    e = torch.from_numpy(e_ref).cuda()
+    rd = gc.alloc_residual_desc(L)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF | flags)
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    val = torch.empty(K, dtype=torch.float32, device="cuda")
+    q = torch.empty(K, dtype=torch.int8, device="cuda") if int8 else None
+    sc = torch.empty(L.T, dtype=torch.float32, device="cuda") if int8 else None
+    for it in range(4):
+        g_h = _grad(n, 200 + it).numpy()
+        gc.ef_topk_compress_lazy(L, torch.from_numpy(g_h).cuda(), e, rd, idx, val, q, sc, 3, it, flags, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+        for t in range(L.T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            ri, rv, rq, rs = oracle.ef_topk_tensor(g_h[a:b], e_ref[a:b], int(L.k[t]), base=a, int8=int8,
+                                                   seed=3, it=it)
+            assert np.array_equal(gi[ka:kb], ri), f"it {it} tensor {t}: indices"
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"it {it} tensor {t}: values"
+            if int8:
+                assert np.array_equal(q.cpu().numpy()[ka:kb], rq), f"it {it} tensor {t}: codes"
+                assert sc.cpu().numpy()[t] == rs
+        e_copy, rd_copy = e.clone(), rd.clone()
+        gc.ef_residual_materialize(L, e_copy, rd_copy)
+        assert np.array_equal(_bits(e_copy.cpu().numpy()), _bits(e_ref)), f"it {it}: materialized residual"
+        assert int(rd_copy.sum()) == 0
+    # switching back to the eager entry point after materializing continues the same sequence
+    gc.ef_residual_materialize(L, e, rd)
+    g_h = _grad(n, 300).numpy()
+    assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref))
+    _topk_check(gc, L, g_h, e_ref, gc.GC_EF | flags, seed=3, it=9)
