@@ -360,6 +360,121 @@ def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
             "h2d": "g read in place from pinned host memory by the kernels (NVLink-C2C)"}
 
 
+# ---------------------------------------------------------------------------- other rows
+
+OPS = {
+    # op: (generator config, layout, density, what, algorithmic bytes per element, per kept, per tensor)
+    "randk": (2, "resnet50", 0.01, "random-k (Philox keys) with EF", 12, 8, 0),
+    "momentum": (4, "gpt2_medium", 0.005, "DGC momentum correction + Top-k, beta 0.9, factor masking", 20, 8, 0),
+    "sign": (4, "gpt2_medium", None, "1-bit sign + EF, mean-|acc| scale per tensor", 12.125, 0, 4),
+    "sign_lazy": (4, "gpt2_medium", None, "1-bit sign + EF, one pass (residual applied by the next call)",
+                  12.125, 0, 4),
+    "qsgd": (4, "gpt2_medium", None, "QSGD s = 16 (Philox stochastic rounding), no EF", 5, 0, 4),
+    "decompress": (5, "llama3_8b", 0.001, "scatter-add of W = 8 workers' sparse fp32 payloads", 0, 0, 0),
+}
+
+
+def run_op(args):
+    """Measures one of the other compression rows on its own workload (one JSON line)."""
+    import gradient_compression_gb300 as gc
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    cfg, lname, rho, what, b_elem, b_kept, b_tensor = OPS[args.op]
+    layout = workloads.LAYOUTS[cfg]()
+    N, T = layout.numel, layout.num_tensors
+    k = workloads.k_per_tensor(layout.sizes, rho) if rho else np.zeros(T, np.int64)
+    L = gc.Layout(layout.off, k, device=dev)
+    K = int(k.sum())
+    grads = [workloads.make_grad(cfg, layout, i, device=dev) for i in range(2)] if args.op != "decompress" else []
+    extra = {}
+    if args.op in ("randk", "momentum"):
+        flags = (gc.GC_EF | gc.GC_RANDK) if args.op == "randk" else 0
+        op = gc.GC_OP_TOPK if args.op == "randk" else gc.GC_OP_MOMENTUM
+        ws = gc.alloc_workspace(L, op, flags)
+        idx = torch.empty(K, dtype=torch.int32, device=dev)
+        val = torch.empty(K, dtype=torch.float32, device=dev)
+        a = torch.zeros(N, device=dev)
+        b = torch.zeros(N, device=dev) if args.op == "momentum" else None
+
+        def step(it):
+            if args.op == "randk":
+                gc.ef_topk_compress(L, grads[it % 2], a, idx, val, None, None, 5, it, flags, ws)
+            else:
+                gc.ef_topk_compress_momentum(L, grads[it % 2], a, b, 0.9, idx, val, None, None, 5, it, 0, ws)
+        algo = b_elem * N + b_kept * K
+    elif args.op in ("sign", "sign_lazy", "qsgd"):
+        ws = gc.alloc_workspace(L, gc.GC_OP_QUANTIZE if args.op == "qsgd" else gc.GC_OP_SIGN)
+        sc = torch.empty(T, device=dev)
+        if args.op == "sign_lazy":
+            e = torch.zeros(N, device=dev)
+            bits = torch.empty(L.words, dtype=torch.int32, device=dev)
+            mus = [torch.empty(T, device=dev) for _ in range(2)]
+
+            def step(it):
+                gc.sign_compress_lazy(L, grads[it % 2], e, None if it == 0 else mus[(it - 1) % 2], bits,
+                                      mus[it % 2], ws)
+        elif args.op == "sign":
+            e = torch.zeros(N, device=dev)
+            bits = torch.empty(L.words, dtype=torch.int32, device=dev)
+
+            def step(it):
+                gc.sign_compress(L, grads[it % 2], e, bits, sc, ws)
+        else:
+            codes = torch.empty(N, dtype=torch.int8, device=dev)
+
+            def step(it):
+                gc.quantize_stochastic(L, grads[it % 2], None, codes, sc, gc.GC_Q_QSGD, 16, 5, it, ws)
+        algo = b_elem * N + b_tensor * T
+    else:
+        W = 8
+        pays = [workloads.make_sparse_payload(layout, k, w, device=dev, cfg=cfg) for w in range(W)]
+        out = torch.zeros(N, device=dev)
+        ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+        idxs, vals = [p[0] for p in pays], [p[1] for p in pays]
+        # touched elements: the union of the workers' index sets (counted once)
+        touched = 0
+        for t in range(T):
+            a0, b0 = int(L.koff[t]), int(L.koff[t + 1])
+            if b0 > a0:
+                touched += int(torch.unique(torch.cat([ix[a0:b0] for ix in idxs])).numel())
+
+        def step(it):
+            gc.sparse_decompress_accumulate(L, idxs, vals, None, None, out, ws)
+        algo = 8 * touched + 8 * K * W
+        extra = {"workers": W, "touched_elements": touched, "payload_entries": K * W,
+                 "sector_bound_bytes": 64 * K * W + 8 * K * W}
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(0)
+    time.sleep(0.3)
+    t0.record()
+    for s_ in range(args.steps):
+        step(args.warmup + s_)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    peak, peak_kind = measured_peaks()
+    achieved = algo / (ms * 1e-3) / 1e9
+    if args.op == "decompress":
+        value, unit, metric = K * W / (ms * 1e-3) / 1e9, "G entries/s", "sparse decompress/scatter-add throughput"
+    else:
+        value, unit, metric = 4.0 * N / (ms * 1e-3) / 1e9, UNIT, "%s compress gradient GB/s" % args.op
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s_%s" % (lname, args.op), "what": what, "tensors": T, "elements": N,
+                       "kept": K, "density": rho},
+            "roofline": {"bound": "hbm", "kernel": "whole call", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "algorithmic_bytes": algo}, "clocks": clocks}
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -368,6 +483,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3_8b",
                     help="the measured workload is llama3_8b; the others are smaller cases for profiling")
+    ap.add_argument("--op", choices=("topk",) + tuple(OPS), default="topk",
+                    help="topk is the measured headline; the others measure the remaining compression rows")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -377,6 +494,8 @@ def main():
     CFG, RHO, INT8 = WORKLOADS[args.workload][:3]
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "topk":
+        run_op(args)
     else:
         run_ours(args)
 

@@ -59,6 +59,8 @@ def lib() -> C.CDLL:
         L.gc_ef_topk_compress_profiled.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P, SZ, P, P, I32]
         L.gc_ef_topk_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_residual_materialize.argtypes = [LP, LP, P, P, P]
+        L.gc_sign_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, SZ, P]
+        L.gc_sign_residual_materialize.argtypes = [LP, LP, P, P, P]
         L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
@@ -71,6 +73,7 @@ def lib() -> C.CDLL:
         L.gc_version.restype = I32
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
                      "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
+                     "gc_sign_compress_lazy", "gc_sign_residual_materialize",
                      "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
@@ -232,6 +235,17 @@ def ef_topk_compress_momentum(layout, g, u, v, beta, idx, val, q, scale, seed, i
 def sign_compress(layout, g, e, bits, mean_abs, workspace, stream=None):
     _check(lib().gc_sign_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(bits), _ptr(mean_abs),
                                   _ptr(workspace), workspace.numel(), _stream(stream)), "gc_sign_compress")
+
+
+def sign_compress_lazy(layout, g, e, prev_mean_abs, bits, mean_abs, workspace, stream=None):
+    _check(lib().gc_sign_compress_lazy(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(prev_mean_abs),
+                                       _ptr(bits), _ptr(mean_abs), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "gc_sign_compress_lazy")
+
+
+def sign_residual_materialize(layout, e, mean_abs, stream=None):
+    _check(lib().gc_sign_residual_materialize(layout.dev(), layout.host(), _ptr(e), _ptr(mean_abs),
+                                              _stream(stream)), "gc_sign_residual_materialize")
 
 
 def quantize_stochastic(layout, g, e, codes, scale, mode, s_levels, seed, it, workspace, stream=None):

@@ -133,31 +133,17 @@ __device__ __forceinline__ uint32_t philox_word(uint64_t seed, uint64_t iter, ui
 constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
 // ---------------------------------------------------------------- rounding
-// ceil(f * 2^32) for fp32 0 <= f < 1, exactly, from f's bits.
-__device__ __forceinline__ uint64_t ceil_frac_2p32(float f) {
-  const uint32_t b = __float_as_uint(f);
-  if (b == 0u) return 0ull;
-  const int ex = (int)((b >> 23) & 0xFFu);
-  uint64_t mant = b & 0x7FFFFFu;
-  int sh;  // f = mant * 2^sh
-  if (ex == 0) {
-    sh = -149;
-  } else {
-    mant |= 0x800000u;
-    sh = ex - 150;
-  }
-  const int s2 = sh + 32;  // f * 2^32 = mant * 2^s2, s2 <= 8 because f < 1
-  if (s2 >= 0) return mant << s2;
-  const int rs = -s2;
-  if (rs >= 40) return 1ull;  // 0 < f * 2^32 < 1
-  return (mant + ((1ull << rs) - 1ull)) >> rs;
-}
-
-// Stochastic rounding of x >= 0: floor(x) + 1 iff r * 2^-32 < frac(x).
+// Stochastic rounding of x >= 0: floor(x) + 1 iff r * 2^-32 < frac(x),
+// decided exactly in fp32/integer arithmetic: F = frac * 2^32 is exact (a
+// power-of-two scaling of an fp32 value below 1), so r < F holds iff
+// r < floor(F), or r == floor(F) and F is not an integer.
 __device__ __forceinline__ int stochastic_round(float x, uint32_t r) {
   const float f = floorf(x);
   const float frac = __fsub_rn(x, f);  // exact
-  return (int)f + (((uint64_t)r < ceil_frac_2p32(frac)) ? 1 : 0);
+  const float F = __fmul_rn(frac, 4294967296.0f);
+  const uint32_t u = __float2uint_rz(F);  // floor(F), F < 2^32
+  const bool up = r < u || (r == u && truncf(F) != F);
+  return (int)f + (up ? 1 : 0);
 }
 
 // int8 code of x for scale s (s == 0 gives 0).

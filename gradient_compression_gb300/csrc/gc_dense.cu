@@ -245,12 +245,13 @@ __global__ void __launch_bounds__(256) k_dreduce(DenseArgs A) {
   }
 }
 
-// Code of x for the dense quantizers; *dec receives the decoded value.
-template <int OP>
+// Code of x for the dense quantizers; with DEC, *dec receives the decoded
+// value (needed only for the EF residual).
+template <int OP, bool DEC>
 __device__ __forceinline__ int dense_code(float x, float sc, int s_levels, uint32_t r, float* dec) {
   if (OP == DOP_INT8) {
     const int c = int8_code(x, sc, r);
-    *dec = __fmul_rn((float)c, sc);
+    if (DEC) *dec = __fmul_rn((float)c, sc);
     return c;
   }
   int level = 0;
@@ -259,9 +260,11 @@ __device__ __forceinline__ int dense_code(float x, float sc, int s_levels, uint3
     y = fminf(y, (float)s_levels + 1.0f);
     level = min(s_levels, stochastic_round(y, r));
   }
-  const float mag = __fdiv_rn(__fmul_rn((float)level, sc), (float)s_levels);
   const bool neg = signbit(x);
-  *dec = neg ? -mag : mag;
+  if (DEC) {
+    const float mag = __fdiv_rn(__fmul_rn((float)level, sc), (float)s_levels);
+    *dec = neg ? -mag : mag;
+  }
   return neg ? -level : level;
 }
 
@@ -336,6 +339,108 @@ __global__ void __launch_bounds__(DTHREADS) k_sign2(DenseArgs A) {
   }
 }
 
+// Single-pass sign compression with the residual kept pending.  The sign
+// bits depend only on acc, not on the scale, so bits, e and the scale's
+// partial sums come out of one pass; the residual e = acc - (bit ? mu : -mu)
+// is left to the next call (which receives this call's mu as `prev_mu` and
+// applies it in registers before adding g) or to gc_sign_residual_materialize.
+// With PREV, e holds the previous call's acc.
+template <bool PREV>
+__global__ void __launch_bounds__(DTHREADS) k_sign_lazy(DenseArgs A, const float* prev_mu) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5;
+  const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
+  for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
+    const UnitRef r = unit_ref(A, u);
+    const int64_t g0 = r.base + r.lstart;
+    const float mp = PREV ? prev_mu[r.t] : 0.0f;
+    uint32_t* wbase = A.bits + A.woff[r.t] + (r.lstart >> 5);
+    const int nwords = (r.len + 31) >> 5;
+    Neumaier sum;
+    auto acc_of = [&](float gv, float ev) {
+      if (PREV) ev = __fsub_rn(ev, signbit(ev) ? -mp : mp);
+      return __fadd_rn(gv, ev);
+    };
+    if ((g0 & 3) == 0) {
+      const int nslots = (r.len + 3) >> 2;
+      const float4* g4 = reinterpret_cast<const float4*>(A.g + g0);
+      float4* e4 = reinterpret_cast<float4*>(A.e + g0);
+      for (int v0 = 0; v0 < nslots; v0 += 256) {
+        uint32_t myword = 0u;
+#pragma unroll 2
+        for (int st = 0; st < 8; ++st) {
+          const int vi = v0 + 32 * st + (int)lane;
+          unsigned nib = 0u;
+          if (vi < nslots) {
+            const int li = vi * 4;
+            if (li + 4 <= r.len) {
+              const float4 gv = ld_stream(g4 + vi);
+              const float4 ev = ld_stream(e4 + vi);
+              float4 a;
+              a.x = acc_of(gv.x, ev.x);
+              a.y = acc_of(gv.y, ev.y);
+              a.z = acc_of(gv.z, ev.z);
+              a.w = acc_of(gv.w, ev.w);
+              st_stream(e4 + vi, a);
+              nib = (signbit(a.x) ? 0u : 1u) | (signbit(a.y) ? 0u : 2u) | (signbit(a.z) ? 0u : 4u) |
+                    (signbit(a.w) ? 0u : 8u);
+              sum.add(fabsf(a.x));
+              sum.add(fabsf(a.y));
+              sum.add(fabsf(a.z));
+              sum.add(fabsf(a.w));
+            } else {
+              for (int j = 0; li + j < r.len; ++j) {
+                const int64_t gi = g0 + li + j;
+                const float a = acc_of(A.g[gi], A.e[gi]);
+                A.e[gi] = a;
+                if (!signbit(a)) nib |= 1u << j;
+                sum.add(fabsf(a));
+              }
+            }
+          }
+          uint32_t w = nib << (4 * (lane & 7));
+          w |= __shfl_xor_sync(FULL, w, 1);
+          w |= __shfl_xor_sync(FULL, w, 2);
+          w |= __shfl_xor_sync(FULL, w, 4);
+          const uint32_t mine = __shfl_sync(FULL, w, 8 * (lane & 3));
+          if ((int)(lane >> 2) == st) myword = mine;
+        }
+        const int wi = (v0 >> 3) + (int)lane;
+        if (wi < nwords) wbase[wi] = myword;
+      }
+    } else {
+      for (int i0 = 0; i0 < r.len; i0 += 32) {
+        const int i = i0 + (int)lane;
+        const bool valid = i < r.len;
+        float a = 0.0f;
+        if (valid) {
+          a = acc_of(A.g[g0 + i], A.e[g0 + i]);
+          A.e[g0 + i] = a;
+          sum.add(fabsf(a));
+        }
+        const unsigned w = __ballot_sync(FULL, valid && !signbit(a));
+        if (lane == 0) wbase[i0 >> 5] = w;
+      }
+    }
+    const double part = warp_sum_f64((double)sum.s + (double)sum.c);
+    if (lane == 0) A.upart[u] = part;
+  }
+}
+
+// e <- acc - (bit ? mu : -mu) per tensor (pending sign residual made explicit).
+__global__ void __launch_bounds__(256) k_sign_materialize(const int64_t* off, int T, float* e,
+                                                          const float* mu) {
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const float m = mu[t];
+    const int64_t base = off[t], n = off[t + 1] - base;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+      const float a = e[base + i];
+      e[base + i] = __fsub_rn(a, signbit(a) ? -m : m);
+    }
+  }
+}
+
 // Pass 2 of the int8 / QSGD quantizers: codes and residual.
 template <int OP, bool EF>
 __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
@@ -368,10 +473,10 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
             const uint4 rw = philox_block(A.seed, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, purpose);
             float4 d;
             char4 c;
-            c.x = (signed char)dense_code<OP>(x[j].x, sc, A.s_levels, rw.x, &d.x);
-            c.y = (signed char)dense_code<OP>(x[j].y, sc, A.s_levels, rw.y, &d.y);
-            c.z = (signed char)dense_code<OP>(x[j].z, sc, A.s_levels, rw.z, &d.z);
-            c.w = (signed char)dense_code<OP>(x[j].w, sc, A.s_levels, rw.w, &d.w);
+            c.x = (signed char)dense_code<OP, EF>(x[j].x, sc, A.s_levels, rw.x, &d.x);
+            c.y = (signed char)dense_code<OP, EF>(x[j].y, sc, A.s_levels, rw.y, &d.y);
+            c.z = (signed char)dense_code<OP, EF>(x[j].z, sc, A.s_levels, rw.z, &d.z);
+            c.w = (signed char)dense_code<OP, EF>(x[j].w, sc, A.s_levels, rw.w, &d.w);
             __stcs(reinterpret_cast<int*>(c4 + vi), *reinterpret_cast<int*>(&c));
             if (EF) {
               float4 res;
@@ -389,7 +494,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + 4 * nv + lane;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     } else {
@@ -397,7 +502,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + i;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     }
@@ -611,5 +716,40 @@ extern "C" gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const 
     else
       k_ddecode<GC_DENSE_QSGD><<<dense_grid(k_ddecode<GC_DENSE_QSGD>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
   }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_sign_compress_lazy(const gc_layout* dev, const gc_layout* host,
+                                           const float* g, float* e, const float* prev_mean_abs,
+                                           uint32_t* bits, float* mean_abs, void* workspace,
+                                           size_t ws_bytes, void* stream) {
+  if (!g || !e || !bits || !mean_abs) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(e)) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DenseArgs A;
+  gc_status st = dense_setup(dev, host, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.op = DOP_SIGN;
+  A.ef = 1;
+  A.g = g;
+  A.e = e;
+  A.bits = bits;
+  A.scale = mean_abs;
+  if (prev_mean_abs)
+    k_sign_lazy<true><<<dense_grid(k_sign_lazy<true>, A.U), DTHREADS, 0, s>>>(A, prev_mean_abs);
+  else
+    k_sign_lazy<false><<<dense_grid(k_sign_lazy<false>, A.U), DTHREADS, 0, s>>>(A, nullptr);
+  k_dreduce<<<A.T, 256, 0, s>>>(A);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_sign_residual_materialize(const gc_layout* dev, const gc_layout* host,
+                                                  float* e, const float* mean_abs, void* stream) {
+  const gc_status st = validate_layout(host, false);
+  if (st != GC_OK) return st;
+  if (!dev || !dev->off || dev->num_tensors != host->num_tensors || !e || !mean_abs) return GC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = host->num_tensors;
+  k_sign_materialize<<<dim3(256, (unsigned)(T < 65535 ? T : 65535)), 256, 0, s>>>(dev->off, T, e, mean_abs);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

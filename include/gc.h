@@ -249,6 +249,24 @@ gc_status gc_sign_compress(const gc_layout* dev, const gc_layout* host, const fl
                            uint32_t* bits, float* mean_abs, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/* Single-pass sign compression with the residual kept pending.  The bits
+ * and mean_abs are those of gc_sign_compress with EF; e is left holding acc,
+ * and the residual e = acc - (bit ? mean_abs : -mean_abs) is applied by the
+ * next call (pass this call's mean_abs as its prev_mean_abs) in registers
+ * before g is added, or by gc_sign_residual_materialize.  One pass over g
+ * and e instead of two.
+ *   e: device fp32[N]: on entry a plain residual (prev_mean_abs == NULL) or
+ *      the previous call's acc; on exit this call's acc.
+ *   prev_mean_abs: device fp32[T] of the previous call, or NULL. */
+gc_status gc_sign_compress_lazy(const gc_layout* dev, const gc_layout* host, const float* g,
+                                float* e, const float* prev_mean_abs, uint32_t* bits,
+                                float* mean_abs, void* workspace, size_t ws_bytes, void* stream);
+
+/* e <- e - (signbit(e) ? -mean_abs[t] : mean_abs[t]): turns the pending form
+ * left by gc_sign_compress_lazy into the plain EF residual. */
+gc_status gc_sign_residual_materialize(const gc_layout* dev, const gc_layout* host, float* e,
+                                       const float* mean_abs, void* stream);
+
 /* Dense stochastic quantization (genomic glossary: 8-bit quantization,
  * stochastic rounding, QSGD; mbrenndoerfer.com QSGD equation):
  *   mode GC_Q_INT8: scale[t] = max|acc_t| / 127, code = sgn * min(127, SR(|acc| / scale))

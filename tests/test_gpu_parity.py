@@ -456,3 +456,35 @@ def test_topk_lazy_residual(gc, name, flags_name):
     g_h = _grad(n, 300).numpy()
     assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref))
     _topk_check(gc, L, g_h, e_ref, gc.GC_EF | flags, seed=3, it=9)
+
+
+@pytest.mark.parametrize("name", ["misaligned_sign", "many_small", "medium"])
+def test_sign_lazy_residual(gc, name):
+    """Single-pass sign compression: bits and mean |acc| as the oracle's at every
+    step, and the materialized pending residual equals the oracle's residual."""
+    sizes = {"misaligned_sign": [4097, 1, 33, 100_003, 6, 64, 31, 32, 250_000]}.get(name) or LAYOUTS[name]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n = L.numel
+    woff = workloads.prefix((np.diff(L.off) + 31) // 32)
+    e_ref = (np.random.default_rng(6).standard_normal(n) * 1e-4).astype(F32)
+    e = torch.from_numpy(e_ref).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_SIGN)
+    bits = torch.empty(L.words, dtype=torch.int32, device="cuda")
+    mu = torch.empty(L.T, dtype=torch.float32, device="cuda")
+    prev = None
+    for it in range(3):
+        g_h = _grad(n, 400 + it).numpy()
+        g_h[::13] = -0.0
+        gc.sign_compress_lazy(L, torch.from_numpy(g_h).cuda(), e, prev, bits, mu, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gb, gm = bits.cpu().numpy().view(np.uint32), mu.cpu().numpy()
+        for t in range(L.T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            _, mu_ref = oracle.sign_tensor(g_h[a:b], e_ref[a:b].copy())
+            assert abs(float(gm[t]) - mu_ref) <= REL_TOL * abs(mu_ref), f"it {it} tensor {t}: mean |acc|"
+            rb, _ = oracle.sign_tensor(g_h[a:b], e_ref[a:b], mu_given=float(gm[t]))
+            assert np.array_equal(gb[woff[t]:woff[t + 1]], rb), f"it {it} tensor {t}: bits"
+        e_copy = e.clone()
+        gc.sign_residual_materialize(L, e_copy, mu)
+        assert np.array_equal(_bits(e_copy.cpu().numpy()), _bits(e_ref)), f"it {it}: residual"
+        prev = mu.clone()
