@@ -134,16 +134,14 @@ constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
 // ---------------------------------------------------------------- rounding
 // Stochastic rounding of x >= 0: floor(x) + 1 iff r * 2^-32 < frac(x),
-// decided exactly in fp32/integer arithmetic: F = frac * 2^32 is exact (a
-// power-of-two scaling of an fp32 value below 1), so r < F holds iff
-// r < floor(F), or r == floor(F) and F is not an integer.
+// decided exactly: F = frac * 2^32 is exact (a power-of-two scaling of an
+// fp32 value below 1), and for an integer r, r < F iff r < ceil(F); since
+// frac <= 1 - 2^-24, ceil(F) <= 2^32 - 256 converts to uint32 exactly.
 __device__ __forceinline__ int stochastic_round(float x, uint32_t r) {
   const float f = floorf(x);
   const float frac = __fsub_rn(x, f);  // exact
-  const float F = __fmul_rn(frac, 4294967296.0f);
-  const uint32_t u = __float2uint_rz(F);  // floor(F), F < 2^32
-  const bool up = r < u || (r == u && truncf(F) != F);
-  return (int)f + (up ? 1 : 0);
+  const uint32_t c = __float2uint_rz(ceilf(__fmul_rn(frac, 4294967296.0f)));
+  return (int)f + (r < c ? 1 : 0);
 }
 
 // int8 code of x for scale s (s == 0 gives 0).

@@ -1,0 +1,187 @@
+"""Parity at the benchmark sizes, through the C ABI, in the launch
+configuration bench.py times.
+
+- BERT-large (335,141,888 elements): EF Top-k 0.1% + int8, two iterations,
+  every tensor against the oracle.
+- GPT-2-medium (354,823,168 elements): sign + EF, QSGD s = 16 and momentum
+  correction Top-k 0.5%, every tensor against the oracle.
+- Llama-3-8B (8,030,261,248 elements, 64 GB of g + e): EF Top-k 0.1% + int8,
+  two iterations; sampled tensors (the smallest, a k/v projection, a q
+  projection, an MLP matrix and the 525M-element embedding) bit-exact against
+  the oracle, and for the whole arena the properties that hold at any size:
+  payload index order and range, code range, and the EF identity
+  e' = acc off the kept set, e' = acc - q * s on it.  Then the receiver with
+  W = 8 workers' payloads, sampled tensors against the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+F32 = np.float32
+
+
+@pytest.fixture(scope="module")
+def gc(cuda_device):
+    from gradient_compression_gb300 import build
+    build.build()
+    import gradient_compression_gb300 as gcmod
+    return gcmod
+
+
+def _bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def _check_topk_tensor(L, t, g_h, e_h, gi, gq, gsc, ge, seed, it, int8=True):
+    """One tensor's GPU payload (gi, gq, gsc) and residual (ge) against the oracle."""
+    a = int(L.off[t])
+    e_ref = e_h.copy()
+    ri, rv, rq, rs = oracle.ef_topk_tensor(g_h, e_ref, int(L.k[t]), base=a, int8=int8, seed=seed, it=it)
+    assert np.array_equal(gi, ri), f"tensor {t}: indices"
+    if int8:
+        assert np.array_equal(gq, rq), f"tensor {t}: codes"
+        assert _bits(np.asarray([gsc], F32))[0] == _bits(np.asarray([rs], F32))[0], f"tensor {t}: scale"
+    assert np.array_equal(_bits(ge), _bits(e_ref)), f"tensor {t}: residual"
+    return e_ref
+
+
+def test_bert_large_topk_int8_full(gc):
+    lay = workloads.bert_large_layout()
+    k = workloads.k_per_tensor(lay.sizes, 0.001)
+    L = gc.Layout(lay.off, k, device="cuda")
+    flags = gc.GC_EF | gc.GC_INT8
+    comp = gc.TopkCompressor(L, flags)
+    e = torch.zeros(L.numel, device="cuda")
+    e_ref = np.zeros(L.numel, F32)
+    for it in range(2):
+        g = workloads.make_grad(3, lay, it, device="cuda")
+        comp(g, e, seed=3, it=it)
+        assert gc.get_device_status(comp.workspace).error_bits == 0
+        g_h = g.cpu().numpy()
+        ri, _, rq, rs = oracle.ef_topk_layout(L.off, L.k, g_h, e_ref, int8=True, seed=3, it=it)
+        assert np.array_equal(comp.idx.cpu().numpy()[:L.total_k], ri)
+        assert np.array_equal(comp.q.cpu().numpy()[:L.total_k], rq)
+        assert np.array_equal(_bits(comp.scale.cpu().numpy()), _bits(rs))
+        assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref))
+
+
+def test_gpt2_medium_dense_and_momentum_full(gc):
+    lay = workloads.gpt2_medium_layout()
+    T, N = lay.num_tensors, lay.numel
+    L = gc.Layout(lay.off, workloads.k_per_tensor(lay.sizes, 0.005), device="cuda")
+    off = L.off
+    woff = workloads.prefix((np.diff(off) + 31) // 32)
+    g = workloads.make_grad(4, lay, 0, device="cuda")
+    g_h = g.cpu().numpy()
+    # sign + EF (e starts at zero)
+    e = torch.zeros(N, device="cuda")
+    bits = torch.empty(L.words, dtype=torch.int32, device="cuda")
+    mu = torch.empty(T, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_SIGN)
+    gc.sign_compress(L, g, e, bits, mu, ws)
+    gb, gm, ge = bits.cpu().numpy().view(np.uint32), mu.cpu().numpy(), e.cpu().numpy()
+    for t in range(T):
+        a, b = int(off[t]), int(off[t + 1])
+        _, mref = oracle.sign_tensor(g_h[a:b], np.zeros(b - a, F32))
+        assert abs(float(gm[t]) - mref) <= 1e-6 * mref, f"sign tensor {t}: mean |acc|"
+        et = np.zeros(b - a, F32)
+        rb, _ = oracle.sign_tensor(g_h[a:b], et, mu_given=float(gm[t]))
+        assert np.array_equal(gb[woff[t]:woff[t + 1]], rb), f"sign tensor {t}: bits"
+        assert np.array_equal(_bits(ge[a:b]), _bits(et)), f"sign tensor {t}: residual"
+    # QSGD s = 16, no EF
+    codes = torch.empty(N, dtype=torch.int8, device="cuda")
+    norm = torch.empty(T, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_QUANTIZE)
+    gc.quantize_stochastic(L, g, None, codes, norm, gc.GC_Q_QSGD, 16, 11, 0, ws)
+    gcod, gn = codes.cpu().numpy(), norm.cpu().numpy()
+    for t in range(T):
+        a, b = int(off[t]), int(off[t + 1])
+        _, nref = oracle.quantize_tensor(g_h[a:b], None, "qsgd", 16, base=a, seed=11, it=0)
+        assert abs(float(gn[t]) - nref) <= 1e-6 * nref, f"qsgd tensor {t}: norm"
+        rc, _ = oracle.quantize_tensor(g_h[a:b], None, "qsgd", 16, base=a, seed=11, it=0,
+                                       scale_given=float(gn[t]))
+        assert np.array_equal(gcod[a:b], rc), f"qsgd tensor {t}: codes"
+    # momentum correction Top-k 0.5%, beta 0.9, two iterations
+    u = torch.zeros(N, device="cuda")
+    v = torch.zeros(N, device="cuda")
+    u_h, v_h = np.zeros(N, F32), np.zeros(N, F32)
+    K = L.total_k
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    val = torch.empty(K, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_MOMENTUM)
+    for it in range(2):
+        if it:
+            g = workloads.make_grad(4, lay, it, device="cuda")
+            g_h = g.cpu().numpy()
+        gc.ef_topk_compress_momentum(L, g, u, v, 0.9, idx, val, None, None, 4, it, 0, ws)
+        gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+        for t in range(T):
+            a, b = int(off[t]), int(off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            ri, rv, _, _ = oracle.momentum_topk_tensor(g_h[a:b], u_h[a:b], v_h[a:b], int(L.k[t]), 0.9,
+                                                       base=a, seed=4, it=it)
+            assert np.array_equal(gi[ka:kb], ri) and np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"momentum t {t}"
+        assert np.array_equal(_bits(u.cpu().numpy()), _bits(u_h))
+        assert np.array_equal(_bits(v.cpu().numpy()), _bits(v_h))
+
+
+def test_llama3_8b_topk_int8_and_decompress_full(gc):
+    lay = workloads.llama3_8b_layout()
+    k = workloads.k_per_tensor(lay.sizes, 0.001)
+    L = gc.Layout(lay.off, k, device="cuda")
+    T, N, K = lay.num_tensors, lay.numel, L.total_k
+    flags = gc.GC_EF | gc.GC_INT8
+    comp = gc.TopkCompressor(L, flags)
+    sizes = np.diff(L.off)
+    sample = [int(np.argmin(sizes)), 2, 1, 5, 0]          # norm, k_proj, q_proj, gate_proj, embedding
+    e = torch.zeros(N, device="cuda")
+    e_prev = {t: np.zeros(int(sizes[t]), F32) for t in sample}
+    g = torch.empty(N, device="cuda")
+    for it in range(2):
+        workloads.make_grad(5, lay, it, device="cuda", out=g)
+        acc = g + e                                         # fp32 RNE add (torch), for the properties
+        comp(g, e, seed=5, it=it)
+        d = gc.get_device_status(comp.workspace)
+        assert d.error_bits == 0 and d.exact_tensors == 0
+        idx_all, q_all, sc_all = comp.idx[:K], comp.q[:K], comp.scale
+        # properties over the whole arena
+        owner = torch.repeat_interleave(torch.arange(T, device="cuda"), torch.from_numpy(k).cuda())
+        base = torch.from_numpy(L.off[:-1]).cuda()[owner]
+        assert int(idx_all.min()) >= 0 and bool((idx_all.long() < torch.from_numpy(sizes).cuda()[owner]).all())
+        same = owner[1:] == owner[:-1]
+        assert bool((idx_all[1:][same] > idx_all[:-1][same]).all()), "indices ascending within each tensor"
+        assert int(q_all.abs().max()) <= 127
+        gidx = base + idx_all.long()
+        expect = acc.clone()
+        expect[gidx] = acc[gidx] - q_all.float() * sc_all[owner]
+        assert torch.equal(e.view(torch.int32), expect.view(torch.int32)), "EF identity over the arena"
+        del expect, acc
+        # sampled tensors against the oracle
+        for t in sample:
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            e_prev[t] = _check_topk_tensor(L, t, g[a:b].cpu().numpy(), e_prev[t], comp.idx[ka:kb].cpu().numpy(),
+                                           comp.q[ka:kb].cpu().numpy(), float(comp.scale[t]),
+                                           e[a:b].cpu().numpy(), 5, it)
+    del e, g
+    torch.cuda.empty_cache()
+    # receiver: W = 8 workers' seeded fp32 payloads into one dense arena
+    W = 8
+    pays = [workloads.make_sparse_payload(lay, k, w, device="cuda", cfg=5) for w in range(W)]
+    out = torch.zeros(N, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    gc.sparse_decompress_accumulate(L, [p[0] for p in pays], [p[1] for p in pays], None, None, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    for t in sample:
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+        ref = np.zeros(b - a, F32)
+        oracle.sparse_accumulate(np.asarray([0, b - a]), np.asarray([0, kb - ka]),
+                                 [p[0][ka:kb].cpu().numpy() for p in pays], [p[1][ka:kb].cpu().numpy() for p in pays],
+                                 None, None, ref)
+        assert np.array_equal(_bits(out[a:b].cpu().numpy()), _bits(ref)), f"decompress tensor {t}"
