@@ -66,6 +66,21 @@ def workload_config(layout, k):
             "parallelism": "replicas"}
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (replicas run independently; the job ends with the last)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gradient_gbs(elements_per_rank: int, world_size: int, ms_per_step: float) -> float:
+    """Whole-job gradient GB/s: every rank compresses its own arena of fp32 elements."""
+    return world_size * 4.0 * elements_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_info():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -246,12 +261,9 @@ def run_ours(args):
              "stream_ms": statistics.mean(stream_ms),
              "select_ms": statistics.mean(p[2].elapsed_time(p[3]) for p in ph),
              "write_ms": statistics.mean(p[3].elapsed_time(p[4]) for p in ph)}
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = ws * 4.0 * N / (ms_per_step * 1e-3) / 1e9
+    value = job_gradient_gbs(N, ws, ms_per_step)
     peak, peak_kind = measured_peaks()
     t_stream = statistics.mean(stream_ms) * 1e-3
     achieved = STREAM_BYTES_PER_ELEM * N / t_stream / 1e9

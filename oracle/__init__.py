@@ -11,7 +11,7 @@ import ctypes as C
 
 import numpy as np
 
-from .build import build
+from . import build as _build_mod
 
 _lib = None
 
@@ -19,7 +19,7 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
+        _lib = C.CDLL(_build_mod.build())
         _declare(_lib)
     return _lib
 

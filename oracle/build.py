@@ -12,13 +12,19 @@ SRC = os.path.join(HERE, "oracle.cpp")
 LIB = os.path.join(HERE, "liboracle.so")
 
 
+FLAGS = ["-std=c++17", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra"]
+
+
+def compile_oracle(src: str, out: str) -> str:
+    subprocess.check_call(["g++", *FLAGS, "-o", out, src])
+    return out
+
+
 def build(force: bool = False) -> str:
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
-           "-Wall", "-Wextra", "-o", tmp, SRC]
-    subprocess.check_call(cmd)
+    compile_oracle(SRC, tmp)
     os.replace(tmp, LIB)
     return LIB
 
