@@ -21,7 +21,7 @@ GC_EF, GC_INT8, GC_RANDK, GC_UNBIASED, GC_NO_MASK, GC_FORCE_EXACT = 0x1, 0x2, 0x
 GC_OP_TOPK, GC_OP_MOMENTUM, GC_OP_SIGN, GC_OP_QUANTIZE, GC_OP_DECOMPRESS = range(5)
 GC_Q_INT8, GC_Q_QSGD = 0, 1
 GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
-GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE = 0x1, 0x2, 0x4
+GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE, GC_DIAG_BAD_THRESHOLD = 0x1, 0x2, 0x4, 0x8
 GC_NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 
 
@@ -61,6 +61,9 @@ def lib() -> C.CDLL:
         L.gc_ef_residual_materialize.argtypes = [LP, LP, P, P, P]
         L.gc_sign_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, SZ, P]
         L.gc_sign_residual_materialize.argtypes = [LP, LP, P, P, P]
+        L.gc_ef_threshold_compress.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
+        L.gc_warmup_density.argtypes = [I64, I64, C.c_double, C.c_double, I32, I32]
+        L.gc_warmup_density.restype = C.c_double
         L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
@@ -73,7 +76,7 @@ def lib() -> C.CDLL:
         L.gc_version.restype = I32
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
                      "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
-                     "gc_sign_compress_lazy", "gc_sign_residual_materialize",
+                     "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
                      "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
@@ -196,6 +199,21 @@ def ef_topk_compress_lazy(layout, g, e, rd, idx, val, q, scale, seed, it, flags,
 def ef_residual_materialize(layout, e, rd, stream=None):
     _check(lib().gc_ef_residual_materialize(layout.dev(), layout.host(), _ptr(e), _ptr(rd), _stream(stream)),
            "gc_ef_residual_materialize")
+
+
+def ef_threshold_compress(layout, g, e, tau, count, idx, val, q, scale, seed, it, flags, workspace, stream=None):
+    _check(lib().gc_ef_threshold_compress(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(tau), _ptr(count),
+                                          _ptr(idx), _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it),
+                                          int(flags), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_ef_threshold_compress")
+
+
+WARMUP_KINDS = {"linear": 0, "exponential": 1, "step": 2}
+
+
+def warmup_density(step, warmup_steps, rho_start, rho_final, kind="exponential", stages=4):
+    return float(lib().gc_warmup_density(int(step), int(warmup_steps), float(rho_start), float(rho_final),
+                                         WARMUP_KINDS[kind], int(stages)))
 
 
 def ef_topk_compress_noalloc(layout, g, e, idx, val, q, scale, seed, it, flags, stream=None):

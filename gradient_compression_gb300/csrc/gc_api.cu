@@ -1,6 +1,8 @@
 // libgc entry points that are not tied to one operation.
 #include <cuda_runtime.h>
 
+#include <cmath>
+
 #include "gc_common.cuh"
 #include "gc_host.h"
 
@@ -65,3 +67,13 @@ extern "C" const char* gc_status_string(gc_status s) {
 }
 
 extern "C" int32_t gc_version(void) { return 100; }
+
+extern "C" double gc_warmup_density(int64_t step, int64_t warmup_steps, double rho_start,
+                                    double rho_final, int32_t kind, int32_t stages) {
+  if (warmup_steps <= 0 || step >= warmup_steps) return rho_final;
+  if (step < 0) step = 0;
+  double f = (double)step / (double)warmup_steps;
+  if (kind == 2 && stages > 0) f = floor(f * stages) / stages;
+  if (kind == 0) return rho_start + (rho_final - rho_start) * f;
+  return rho_start * pow(rho_final / rho_start, f);
+}

@@ -45,7 +45,8 @@ struct alignas(16) TensorState {
   uint32_t cand_count;  // candidates reserved by the streaming pass
   uint32_t thr;         // exact key of the k-th element
   uint32_t r_eq;        // how many elements with key == thr are kept (lowest indices)
-  uint32_t pad[8];
+  uint32_t keff;        // elements kept (k_t, or fewer under a threshold)
+  uint32_t pad[7];
 };
 static_assert(sizeof(TensorState) == 64, "TensorState is 64 bytes");
 

@@ -56,6 +56,9 @@ struct TopkArgs {
   float* scale;
   uint64_t seed, iter;
   gc_residual_desc* rd;  // pending-residual descriptors (lazy mode), else null
+  const float* tau;      // per-tensor magnitude thresholds (threshold mode), else null
+  int64_t* count_out;    // per-tensor kept counts (threshold mode)
+  int sampled;           // threshold estimated by sampling (Top-k and momentum)
   // workspace
   uint32_t* diag;
   TensorState* ts;
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0;
-  const bool sampled = (A.mode != MODE_RANDK);
+  const bool sampled = A.sampled != 0;
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
     int64_t nu = 0, nb = 0, nc = 0, ns = 0;
@@ -137,7 +140,18 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
         st.t_est = (tau >= 4294967296.0) ? 0u : ~((uint32_t)tau - 1u);
       }
       if (k >= n) st.t_est = 0u;
+      if (A.tau && k > 0) {
+        const float tau = A.tau[t];
+        if (tau >= 0.0f) {
+          st.t_est = mag_key(tau);  // |acc| >= tau  <=>  key(acc) >= key(tau)
+        } else {                    // NaN or negative: reported, nothing kept
+          st.flags = TS_NOEMIT;
+          atomicOr(A.diag + DIAG_ERR, GC_DIAG_BAD_THRESHOLD);
+        }
+      }
+      st.keff = (uint32_t)k;
       A.ts[t] = st;
+      if (A.count_out && (st.flags & TS_NOEMIT)) A.count_out[t] = 0;
       if (A.int8 && k <= 0) A.scale[t] = 0.0f;
     }
     int64_t tot;
@@ -445,23 +459,42 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
   if (phase == PH_C1) {
     const int64_t cap = A.cand_off[t + 1] - A.cand_off[t];
     const int64_t cnt = st->cand_count;
-    const bool dense = (flags & TS_OVERFLOW) || cnt > cap || cnt < k || (A.flags & GC_FORCE_EXACT);
+    const bool ovf = (flags & TS_OVERFLOW) || cnt > cap;
+    int64_t kt = A.kk[t];
+    if (A.tau) {
+      // threshold mode: every candidate passes |acc| >= tau; keep at most k_t
+      // of them.  An overflowing candidate list has more than k_t entries.
+      if (!ovf && cnt < kt) kt = cnt;
+      if (threadIdx.x == 0) {
+        st->keff = (uint32_t)kt;
+        A.count_out[t] = kt;
+        if (kt == 0) {
+          st->flags = flags | TS_NOEMIT;
+          if (A.int8) A.scale[t] = 0.0f;
+        }
+      }
+      if (kt == 0) {
+        for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+        return;
+      }
+    }
+    const bool dense = ovf || cnt < kt || (A.flags & GC_FORCE_EXACT);
     if (dense) {
       for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
       if (threadIdx.x == 0) {
         st->flags = flags | TS_DENSE;
         st->maxkey = 0u;
         st->prefix = 0u;
-        st->rank = (uint32_t)k;
+        st->rank = (uint32_t)kt;
         atomicAdd(A.diag + DIAG_EXACT, 1u);
         if ((flags & TS_OVERFLOW) || cnt > cap) atomicAdd(A.diag + DIAG_OVF, 1u);
       }
       return;
     }
-    rank = (uint32_t)k;
+    rank = (uint32_t)kt;
   } else if (phase == PH_C1D) {
     if (!(flags & TS_DENSE)) return;
-    rank = (uint32_t)k;
+    rank = st->keff;
   }
 
   uint32_t above;
@@ -1127,8 +1160,8 @@ template <int MODE>
 static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
   const int T = A.T;
   k_plan<<<1, 1024, 0, s>>>(A);
-  pe.done(MODE == MODE_RANDK ? 1 : 0, s);
-  if (MODE != MODE_RANDK) {
+  pe.done(A.sampled ? 0 : 1, s);
+  if (A.sampled) {
     k_sample<MODE><<<T, 1024, 0, s>>>(A);
     pe.done(1, s);
   }
@@ -1177,7 +1210,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
                           float* e, float* u, float* v, float beta, int32_t* idx, float* val,
                           int8_t* q, float* scale, uint64_t seed, uint64_t iter, uint32_t flags,
                           void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe,
-                          gc_residual_desc* rd = nullptr) {
+                          gc_residual_desc* rd = nullptr, const float* tau = nullptr,
+                          int64_t* count_out = nullptr) {
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
@@ -1188,7 +1222,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   if (!int8 && !val) return GC_ERR_INVALID_ARG;
   if (!aligned16(g) || (e && !aligned16(e)) || (u && !aligned16(u)) || (v && !aligned16(v)))
     return GC_ERR_ALIGNMENT;
-  const TopkLayoutTotals z = totals_of(host, mode != MODE_RANDK);
+  const bool sampled = mode != MODE_RANDK && !tau;
+  const TopkLayoutTotals z = totals_of(host, sampled);
   const TopkCarve c = carve_topk(host->num_tensors, z);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
   if (z.K == 0 && z.N == 0) return GC_OK;
@@ -1218,6 +1253,9 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.seed = seed;
   A.iter = iter;
   A.rd = rd;
+  A.tau = tau;
+  A.count_out = count_out;
+  A.sampled = sampled ? 1 : 0;
   A.diag = reinterpret_cast<uint32_t*>(w);
   A.ts = reinterpret_cast<TensorState*>(w + c.o_ts);
   A.hist = reinterpret_cast<uint32_t*>(w + c.o_hist);
@@ -1353,4 +1391,19 @@ extern "C" gc_status gc_ef_residual_materialize(const gc_layout* dev, const gc_l
   k_materialize<<<dim3(256, (unsigned)std::min(T, 65535)), 256, 0, s>>>(dev->off, T, e, rd);
   k_clear_desc<<<(T + 255) / 256, 256, 0, s>>>(rd, T);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_ef_threshold_compress(const gc_layout* dev, const gc_layout* host,
+                                              const float* g, float* e, const float* tau,
+                                              int64_t* count, int32_t* idx, float* val, int8_t* q,
+                                              float* scale, uint64_t seed, uint64_t iter,
+                                              uint32_t flags, void* workspace, size_t ws_bytes,
+                                              void* stream) {
+  const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if (!tau || !count) return GC_ERR_INVALID_ARG;
+  if ((flags & GC_EF) && !e) return GC_ERR_INVALID_ARG;
+  return run_topk(MODE_TOPK, dev, host, g, (flags & GC_EF) ? e : nullptr, nullptr, nullptr, 0.0f,
+                  idx, val, q, scale, seed, iter, flags, workspace, ws_bytes, stream, PhaseEvents{},
+                  nullptr, tau, count);
 }

@@ -128,6 +128,7 @@ typedef struct gc_diag {
 #define GC_DIAG_LAYOUT_MISMATCH 0x1u /* dev and host layouts disagree; the call did nothing */
 #define GC_DIAG_SELECT 0x2u          /* internal selection inconsistency (should never be set) */
 #define GC_DIAG_INDEX_RANGE 0x4u     /* decompress met a payload index >= n_t; entry skipped */
+#define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold was negative or NaN; that tensor kept nothing */
 
 /* Bytes of workspace that operation `op` needs for layout `host` and
  * `flags`.  *bytes is set on GC_OK. */
@@ -152,6 +153,36 @@ gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const
                               int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                               uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
                               void* stream);
+
+/* Threshold sparsification with EF (genomic glossary "Gradient
+ * Compression": gradients below a fixed or adaptive magnitude threshold are
+ * dropped; "Gradient Sparsification": the threshold adapts to each
+ * iteration's distribution).  Tensor t keeps every element with
+ * |acc| >= tau[t], at most k_t of them (the largest, in the Top-k order);
+ * payload, int8 option and residual as gc_ef_topk_compress.
+ *   tau:   device fp32[T], >= 0 (the caller adapts it between calls if it
+ *          wants an adaptive threshold); a negative or NaN entry keeps
+ *          nothing and sets GC_DIAG_BAD_THRESHOLD.
+ *   count: device int64[T] out: entries kept; tensor t's payload is
+ *          [koff[t], koff[t] + count[t]) of the k_t slots, the rest untouched.
+ * flags: GC_EF, GC_INT8, GC_FORCE_EXACT.  Workspace: gc_workspace_size(
+ * GC_OP_TOPK, flags) is sufficient. */
+gc_status gc_ef_threshold_compress(const gc_layout* dev, const gc_layout* host, const float* g,
+                                   float* e, const float* tau, int64_t* count, int32_t* idx,
+                                   float* val, int8_t* q, float* scale, uint64_t seed,
+                                   uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
+                                   void* stream);
+
+/* Density (fraction of elements kept) of a warm-up schedule ("Gradient
+ * Sparsification", warm-up: sparsity introduced gradually over the first
+ * iterations by a linear, exponential or step schedule): from rho_start at
+ * step 0 to rho_final at step >= warmup_steps.
+ *   kind 0 linear: rho_start + (rho_final - rho_start) * f
+ *   kind 1 exponential: rho_start * (rho_final / rho_start)^f
+ *   kind 2 step: kind 1 evaluated at f rounded down to a multiple of 1/stages
+ * with f = step / warmup_steps.  Host only; k_t = min(n_t, ceil(density * n_t)). */
+double gc_warmup_density(int64_t step, int64_t warmup_steps, double rho_start, double rho_final,
+                         int32_t kind, int32_t stages);
 
 /* gc_ef_topk_compress with timing hooks: `events` is a host array of
  * `n_events` (0..32) cudaEvent_t handles created by the caller, recorded on

@@ -35,6 +35,7 @@ def _declare(L):
     L.oracle_stochastic_round.restype = C.c_double
     L.oracle_select.argtypes = [_I64, _I64, _P, _I32, _I32, _P]
     L.oracle_ef_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
+    L.oracle_threshold_tensor.argtypes = [_I64, _I64, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32]
     L.oracle_randk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
     L.oracle_momentum_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _F, _I32, _P, _P, _P, _P,
                                               _U64, _U64, _I32, _I32]
@@ -42,8 +43,10 @@ def _declare(L):
     L.oracle_quantize_tensor.argtypes = [_I64, _U64, _P, _P, _P, _P, _I32, _I32, _U64, _U64, _P]
     L.oracle_sparse_accumulate.argtypes = [_I32, _P, _P, _I32, _P, _P, _P, _P, _P]
     L.oracle_sign_decode_accumulate.argtypes = [_I64, _P, _F, _P]
+    L.oracle_warmup_density.argtypes = [_I64, _I64, C.c_double, C.c_double, _I32, _I32]
+    L.oracle_warmup_density.restype = C.c_double
     L.oracle_codes_decode_accumulate.argtypes = [_I64, _P, _F, _I32, _I32, _P]
-    for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor",
+    for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor", "oracle_threshold_tensor",
                  "oracle_momentum_topk_tensor", "oracle_sign_tensor", "oracle_quantize_tensor",
                  "oracle_sparse_accumulate", "oracle_sign_decode_accumulate",
                  "oracle_codes_decode_accumulate"):
@@ -104,6 +107,27 @@ def ef_topk_tensor(g, e, k, base=0, int8=False, seed=0, it=0, method=1):
     _check(lib().oracle_ef_topk_tensor(n, k, base, _p(g), _p(e), _p(idx), _p(val), _p(q), _p(sc),
                                        seed, it, int(int8), method), "ef_topk")
     return idx, val, q, (float(sc[0]) if int8 else None)
+
+
+def threshold_tensor(g, e, kmax, tau, base=0, int8=False, seed=0, it=0):
+    """Returns (idx, val, q, scale, count); idx/val/q hold `count` entries."""
+    g = _c(g, np.float32); n = g.size
+    if e is not None:
+        assert e.dtype == np.float32 and e.flags.c_contiguous and e.size == n
+    idx = np.zeros(kmax, np.int32); val = np.zeros(kmax, np.float32)
+    q = np.zeros(kmax, np.int8) if int8 else None
+    sc = np.zeros(1, np.float32) if int8 else None
+    cnt = np.zeros(1, np.int64)
+    _check(lib().oracle_threshold_tensor(n, kmax, float(tau), base, _p(g), _p(e), _p(idx), _p(val), _p(q), _p(sc),
+                                         _p(cnt), seed, it, int(int8)), "threshold")
+    c = int(cnt[0])
+    return idx[:c], val[:c], (q[:c] if int8 else None), (float(sc[0]) if int8 else None), c
+
+
+def warmup_density(step, warmup_steps, rho_start, rho_final, kind):
+    """Density of the warm-up schedule (see oracle_warmup_density)."""
+    return lib().oracle_warmup_density(int(step), int(warmup_steps), float(rho_start), float(rho_final),
+                                       {"linear": 0, "exponential": 1, "step": 2}[kind], 4)
 
 
 def randk_tensor(g, e, k, base=0, seed=0, it=0, unbiased=False, method=1):

@@ -239,6 +239,46 @@ int oracle_ef_topk_tensor(int64_t n, int64_t k, uint64_t base, const float* g, f
   return 0;
 }
 
+// ------------------------------------------------------------------ threshold
+// Threshold sparsification ([P3] "Threshold-based": gradients below a fixed
+// or adaptive magnitude threshold are dropped; [P5] the threshold is
+// dynamic): S = {i : |acc_i| >= tau}; if more than kmax elements pass, only
+// the kmax largest are kept (Top-kmax, same order as Top-k).  Payload and
+// residual as in EF Top-k.  Returns the number kept in *count.
+int oracle_threshold_tensor(int64_t n, int64_t kmax, float tau, uint64_t base, const float* g,
+                            float* e, int32_t* idx, float* val, int8_t* q, float* scale,
+                            int64_t* count, uint64_t seed, uint64_t iter, int32_t use_int8) {
+  if (n < 0 || kmax < 0 || kmax > n || !(tau >= 0.0f)) return 1;
+  int64_t passing = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const float acc = e ? g[i] + e[i] : g[i];
+    if (std::fabs(acc) >= tau) ++passing;
+  }
+  const int64_t k = passing < kmax ? passing : kmax;
+  *count = k;
+  // the kept set is then exactly the Top-k of acc with this k
+  return oracle_ef_topk_tensor(n, k, base, g, e, idx, val, q, scale, seed, iter, use_int8, 1);
+}
+
+// Warm-up schedule ([P5] warm-up: sparsification introduced gradually, the
+// ratio rising by a predefined linear, exponential or step schedule over the
+// first iterations; [P3] DGC warm-up training).  Density (fraction kept) at
+// `step` of a warm-up of `warmup_steps`, from rho_start to rho_final:
+//   kind 0 linear:      rho_start + (rho_final - rho_start) * f
+//   kind 1 exponential: rho_start * (rho_final / rho_start)^f   (geometric)
+//   kind 2 step:        the exponential value at the start of the current
+//                       one of `stages` equal stages, f = floor(f*stages)/stages
+// with f = step / warmup_steps; rho_final from step >= warmup_steps on.
+double oracle_warmup_density(int64_t step, int64_t warmup_steps, double rho_start, double rho_final,
+                             int32_t kind, int32_t stages) {
+  if (warmup_steps <= 0 || step >= warmup_steps) return rho_final;
+  if (step < 0) step = 0;
+  double f = (double)step / (double)warmup_steps;
+  if (kind == 2) f = std::floor(f * stages) / stages;
+  if (kind == 0) return rho_start + (rho_final - rho_start) * f;
+  return rho_start * std::pow(rho_final / rho_start, f);
+}
+
 // ------------------------------------------------------------------ random-k
 // [P1] Random-k: a per-iteration random mask picks exactly k of the n
 // elements.  The mask is the k smallest Philox keys (purpose 3), a uniform

@@ -99,3 +99,12 @@ def test_argument_errors_return_before_any_launch(gc):
     st = L.gc_dense_decompress_accumulate(lay.host(), lay.host(), 1, 7, 16, None, None, P(16),
                                           P(256), 1 << 30, None)
     assert st == gc.GC_ERR_INVALID_ARG
+
+
+def test_warmup_density_matches_oracle(gc):
+    import oracle
+    for kind in ("linear", "exponential", "step"):
+        for step in (-3, 0, 1, 5, 9, 10, 11, 100):
+            a = gc.warmup_density(step, 10, 0.25, 0.001, kind, 4)
+            b = oracle.warmup_density(step, 10, 0.25, 0.001, kind)
+            assert a == pytest.approx(b, rel=1e-15, abs=0)

@@ -488,3 +488,63 @@ def test_sign_lazy_residual(gc, name):
         gc.sign_residual_materialize(L, e_copy, mu)
         assert np.array_equal(_bits(e_copy.cpu().numpy()), _bits(e_ref)), f"it {it}: residual"
         prev = mu.clone()
+
+
+# ----------------------------------------------------------------------------- threshold
+
+@pytest.mark.parametrize("flags_name", ["ef", "ef_int8", "noef", "ef_exact"])
+def test_threshold_layouts(gc, flags_name):
+    flags = {"ef": gc.GC_EF, "ef_int8": gc.GC_EF | gc.GC_INT8, "noef": 0,
+             "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT}[flags_name]
+    sizes = [4097, 1, 33, 100_003, 6, 70_000, 300_000]
+    kmax = [60, 1, 33, 500, 3, 2000, 3000]
+    L = _layout(gc, sizes, k=kmax)
+    n, K, T = L.numel, L.total_k, L.T
+    int8 = bool(flags & gc.GC_INT8)
+    # thresholds: some tensors pass fewer than k_t, some more, tau = 0 and tau = inf
+    tau_h = np.asarray([2e-3, 0.0, np.inf, 2e-2, 0.0, 3e-3, 1e-2], F32)
+    tau = torch.from_numpy(tau_h).cuda()
+    e_ref = (np.random.default_rng(9).standard_normal(n) * 1e-4).astype(F32) if flags & gc.GC_EF else None
+    e = torch.from_numpy(e_ref).cuda() if e_ref is not None else None
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    cnt = torch.full((T,), -1, dtype=torch.int64, device="cuda")
+    idx = torch.full((K,), -1, dtype=torch.int32, device="cuda")
+    val = torch.zeros(K, device="cuda")
+    q = torch.zeros(K, dtype=torch.int8, device="cuda") if int8 else None
+    sc = torch.zeros(T, device="cuda") if int8 else None
+    counts_seen = set()
+    for it in range(2):
+        g_h = _grad(n, 500 + it).numpy()
+        gc.ef_threshold_compress(L, torch.from_numpy(g_h).cuda(), e, tau, cnt, idx, val, q, sc, 7, it, flags, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gcnt, gi, gv = cnt.cpu().numpy(), idx.cpu().numpy(), val.cpu().numpy()
+        for t in range(T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka = int(L.koff[t])
+            et = e_ref[a:b] if e_ref is not None else None
+            ri, rv, rq, rs, c = oracle.threshold_tensor(g_h[a:b], et, int(kmax[t]), float(tau_h[t]), base=a,
+                                                        int8=int8, seed=7, it=it)
+            assert gcnt[t] == c, f"it {it} tensor {t}: count {gcnt[t]} vs {c}"
+            counts_seen.add((t, c < kmax[t]))
+            assert np.array_equal(gi[ka:ka + c], ri), f"it {it} tensor {t}: indices"
+            if int8:
+                assert np.array_equal(q.cpu().numpy()[ka:ka + c], rq)
+                assert sc.cpu().numpy()[t] == (rs if c else 0.0)
+            assert np.array_equal(_bits(gv[ka:ka + c]), _bits(rv)), f"it {it} tensor {t}: values"
+        if e is not None:
+            assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref))
+    assert {c for _, c in counts_seen} == {True, False}     # both regimes exercised
+
+
+def test_threshold_rejects_negative_tau(gc):
+    L = _layout(gc, [100, 200], k=[5, 5])
+    tau = torch.tensor([-1.0, 1e-3], device="cuda")
+    cnt = torch.full((2,), -1, dtype=torch.int64, device="cuda")
+    idx = torch.zeros(10, dtype=torch.int32, device="cuda")
+    val = torch.zeros(10, device="cuda")
+    g = torch.from_numpy(_grad(300, 1).numpy()).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, 0)
+    gc.ef_threshold_compress(L, g, None, tau, cnt, idx, val, None, None, 0, 0, 0, ws)
+    d = gc.get_device_status(ws, raise_on_error=False)
+    assert d.error_bits & gc.GC_DIAG_BAD_THRESHOLD
+    assert int(cnt[0]) == 0

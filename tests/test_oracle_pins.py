@@ -474,3 +474,40 @@ def test_single_worker_decompress_restores_acc():
     out = np.zeros(layout.numel, F32)
     oracle.sparse_accumulate(off, workloads.prefix(k), [idx], [val], None, None, out)
     assert np.all(out + e == g + e0)
+
+
+# ----------------------------------------------------------------------------- threshold / warm-up
+
+def test_threshold_keeps_mask_then_caps_at_topk():
+    rng = np.random.default_rng(21)
+    for n in (1, 7, 100, 4097):
+        g = (rng.standard_t(3, n) * 1e-3).astype(F32)
+        e0 = (rng.standard_normal(n) * 1e-4).astype(F32)
+        acc = g + e0
+        for tau in (0.0, 1e-3, 3e-3, np.inf):
+            mask_idx = np.nonzero(np.abs(acc) >= F32(tau))[0]
+            for kmax in sorted({0, 1, n // 3, n}):
+                e = e0.copy()
+                idx, val, _, _, cnt = oracle.threshold_tensor(g, e, kmax, tau)
+                if mask_idx.size <= kmax:
+                    assert cnt == mask_idx.size and np.array_equal(idx, mask_idx)
+                else:
+                    assert cnt == kmax and idx.tolist() == _brute_topk(acc, kmax)
+                sent = np.zeros(n, F32); sent[idx] = val
+                assert np.all(sent + e == acc)
+
+
+def test_warmup_schedule_closed_forms():
+    a, b, W = 0.25, 0.001, 10
+    for kind in ("linear", "exponential", "step"):
+        assert oracle.warmup_density(0, W, a, b, kind) == a
+        assert oracle.warmup_density(W, W, a, b, kind) == b
+        assert oracle.warmup_density(10 * W, W, a, b, kind) == b
+        seq = [oracle.warmup_density(s, W, a, b, kind) for s in range(W + 1)]
+        assert all(x >= y for x, y in zip(seq, seq[1:]))      # sparsity only rises
+    assert oracle.warmup_density(5, W, a, b, "linear") == pytest.approx((a + b) / 2)
+    assert oracle.warmup_density(5, W, a, b, "exponential") == pytest.approx(math.sqrt(a * b))
+    # 4 stages: constant within a stage, geometric from stage to stage
+    st = [oracle.warmup_density(s, 8, a, b, "step") for s in range(8)]
+    assert st[0] == st[1] == a and st[2] == st[3] and st[6] == st[7]
+    assert st[2] == pytest.approx(a * (b / a) ** 0.25) and st[6] == pytest.approx(a * (b / a) ** 0.75)
