@@ -383,6 +383,8 @@ OPS = {
                   12.125, 0, 4),
     "qsgd": (4, "gpt2_medium", None, "QSGD s = 16 (Philox stochastic rounding), no EF", 5, 0, 4),
     "decompress": (5, "llama3_8b", 0.001, "scatter-add of W = 8 workers' sparse fp32 payloads", 0, 0, 0),
+    "threshold": (3, "bert_large", 0.002, "threshold |acc| >= 1e-2 with EF, capped at 0.2% per tensor", 12, 8, 0),
+    "clip": (3, "bert_large", 0.001, "DGC local clipping (max norm = half of ||g_t||) + EF Top-k 0.1%", 16, 8, 0),
 }
 
 
@@ -415,6 +417,27 @@ def run_op(args):
             else:
                 gc.ef_topk_compress_momentum(L, grads[it % 2], a, b, 0.9, idx, val, None, None, 5, it, 0, ws)
         algo = b_elem * N + b_kept * K
+    elif args.op in ("threshold", "clip"):
+        ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+        idx = torch.empty(K, dtype=torch.int32, device=dev)
+        val = torch.empty(K, dtype=torch.float32, device=dev)
+        e = torch.zeros(N, device=dev)
+        cnt = torch.zeros(T, dtype=torch.int64, device=dev)
+        norm = torch.empty(T, device=dev)
+        tau = torch.full((T,), 1e-2, device=dev)
+        cap = torch.stack([0.5 * torch.linalg.vector_norm(grads[0][int(L.off[t]):int(L.off[t + 1])])
+                           for t in range(T)]).float()
+
+        def step(it):
+            if args.op == "threshold":
+                gc.ef_threshold_compress(L, grads[it % 2], e, tau, cnt, idx, val, None, None, 5, it, gc.GC_EF, ws)
+            else:
+                gc.ef_topk_compress_clipped(L, grads[it % 2], e, cap, norm, idx, val, None, None, 5, it, gc.GC_EF, ws)
+        step(0)
+        torch.cuda.synchronize()
+        kept = int(cnt.sum()) if args.op == "threshold" else K
+        algo = b_elem * N + b_kept * kept
+        extra = {"kept_per_step": kept}
     elif args.op in ("sign", "sign_lazy", "qsgd"):
         ws = gc.alloc_workspace(L, gc.GC_OP_QUANTIZE if args.op == "qsgd" else gc.GC_OP_SIGN)
         sc = torch.empty(T, device=dev)

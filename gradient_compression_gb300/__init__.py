@@ -61,6 +61,7 @@ def lib() -> C.CDLL:
         L.gc_ef_residual_materialize.argtypes = [LP, LP, P, P, P]
         L.gc_sign_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, SZ, P]
         L.gc_sign_residual_materialize.argtypes = [LP, LP, P, P, P]
+        L.gc_ef_topk_compress_clipped.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_threshold_compress.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_warmup_density.argtypes = [I64, I64, C.c_double, C.c_double, I32, I32]
         L.gc_warmup_density.restype = C.c_double
@@ -77,6 +78,7 @@ def lib() -> C.CDLL:
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
                      "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
                      "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
+                     "gc_ef_topk_compress_clipped",
                      "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
@@ -199,6 +201,14 @@ def ef_topk_compress_lazy(layout, g, e, rd, idx, val, q, scale, seed, it, flags,
 def ef_residual_materialize(layout, e, rd, stream=None):
     _check(lib().gc_ef_residual_materialize(layout.dev(), layout.host(), _ptr(e), _ptr(rd), _stream(stream)),
            "gc_ef_residual_materialize")
+
+
+def ef_topk_compress_clipped(layout, g, e, max_norm, norm, idx, val, q, scale, seed, it, flags, workspace,
+                             stream=None):
+    _check(lib().gc_ef_topk_compress_clipped(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(max_norm),
+                                             _ptr(norm), _ptr(idx), _ptr(val), _ptr(q), _ptr(scale), int(seed),
+                                             int(it), int(flags), _ptr(workspace), workspace.numel(),
+                                             _stream(stream)), "gc_ef_topk_compress_clipped")
 
 
 def ef_threshold_compress(layout, g, e, tau, count, idx, val, q, scale, seed, it, flags, workspace, stream=None):

@@ -46,7 +46,9 @@ struct alignas(16) TensorState {
   uint32_t thr;         // exact key of the k-th element
   uint32_t r_eq;        // how many elements with key == thr are kept (lowest indices)
   uint32_t keff;        // elements kept (k_t, or fewer under a threshold)
-  uint32_t pad[7];
+  float gmul;           // multiplier applied to g (local clipping), else 1
+  uint32_t cnt_tau;     // elements with |acc| >= tau (threshold mode, full-pass path)
+  uint32_t pad[5];
 };
 static_assert(sizeof(TensorState) == 64, "TensorState is 64 bytes");
 

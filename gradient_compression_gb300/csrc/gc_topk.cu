@@ -59,6 +59,9 @@ struct TopkArgs {
   const float* tau;      // per-tensor magnitude thresholds (threshold mode), else null
   int64_t* count_out;    // per-tensor kept counts (threshold mode)
   int sampled;           // threshold estimated by sampling (Top-k and momentum)
+  const float* clip;     // per-tensor maximum L2 norm of g (local clipping), else null
+  float* norm_out;       // per-tensor ||g||_2 (local clipping)
+  double* upart;         // per-unit partial sums of g^2 (local clipping)
   // workspace
   uint32_t* diag;
   TensorState* ts;
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
         }
       }
       st.keff = (uint32_t)k;
+      st.gmul = 1.0f;
       A.ts[t] = st;
       if (A.count_out && (st.flags & TS_NOEMIT)) A.count_out[t] = 0;
       if (A.int8 && k <= 0) A.scale[t] = 0.0f;
@@ -214,9 +218,10 @@ __device__ __forceinline__ float acc_from_inputs(const TopkArgs& A, int t, int64
     const float un = __fadd_rn(__fmul_rn(A.beta, A.u[gi]), A.g[gi]);
     return __fadd_rn(A.v[gi], un);
   }
-  if (!A.ef) return A.g[gi];
+  const float gv = __fmul_rn(A.ts[t].gmul, A.g[gi]);
+  if (!A.ef) return gv;
   const float r = A.rd ? lazy_fix(A.e[gi], li, gi, A.rd[t]) : A.e[gi];
-  return __fadd_rn(A.g[gi], r);
+  return __fadd_rn(gv, r);
 }
 
 // After the streaming pass: the kept value source and the selection key.
@@ -243,7 +248,14 @@ __device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64
                                                  int64_t li, bool vec, float a[4], bool ok[4]) {
   const int64_t gi = base + li;
   if (vec && li + 4 <= n) {
-    const float4 g4 = ld_stream(reinterpret_cast<const float4*>(A.g + gi));
+    float4 g4 = ld_stream(reinterpret_cast<const float4*>(A.g + gi));
+    if (MODE != MODE_MOM) {
+      const float c = A.ts[t].gmul;
+      g4.x = __fmul_rn(c, g4.x);
+      g4.y = __fmul_rn(c, g4.y);
+      g4.z = __fmul_rn(c, g4.z);
+      g4.w = __fmul_rn(c, g4.w);
+    }
     if (MODE == MODE_MOM) {
       const float4 u4 = ld_stream(reinterpret_cast<const float4*>(A.u + gi));
       const float4 v4 = ld_stream(reinterpret_cast<const float4*>(A.v + gi));
@@ -274,6 +286,86 @@ __device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64
   for (int j = 0; j < 4; ++j) {
     ok[j] = li + j < n;
     a[j] = ok[j] ? acc_from_inputs<MODE>(A, t, li + j, gi + j) : 0.0f;
+  }
+}
+
+// ============================================================================ local clipping
+
+struct Neumaier32 {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = __fadd_rn(s, x);
+    if (fabsf(s) >= fabsf(x))
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
+    else
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
+    s = t;
+  }
+};
+
+// Per-unit partial sums of g^2 (fp32 Neumaier per lane, fp64 across lanes).
+__global__ void __launch_bounds__(256) k_gnorm(TopkArgs A) {
+  if (aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < A.U; u += nwarps) {
+    const int t = find_segment(A.units_off, A.T, u);
+    const int64_t base = A.off[t], n = A.off[t + 1] - base;
+    const int64_t lstart = (u - A.units_off[t]) << UNIT_SHIFT;
+    const int len = (int)min((int64_t)UNIT, n - lstart);
+    const int64_t g0 = base + lstart;
+    Neumaier32 acc;
+    if ((g0 & 3) == 0) {
+      const int nv = len >> 2;
+      const float4* g4 = reinterpret_cast<const float4*>(A.g + g0);
+      for (int vi = (int)lane; vi < nv; vi += 32) {
+        const float4 x = ld_stream(g4 + vi);
+        acc.add(__fmul_rn(x.x, x.x));
+        acc.add(__fmul_rn(x.y, x.y));
+        acc.add(__fmul_rn(x.z, x.z));
+        acc.add(__fmul_rn(x.w, x.w));
+      }
+      if ((int)lane < (len & 3)) {
+        const float x = A.g[g0 + 4 * nv + lane];
+        acc.add(__fmul_rn(x, x));
+      }
+    } else {
+      for (int i = (int)lane; i < len; i += 32) {
+        const float x = A.g[g0 + i];
+        acc.add(__fmul_rn(x, x));
+      }
+    }
+    double part = (double)acc.s + (double)acc.c;
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) part += __shfl_xor_sync(FULL, part, dd);
+    if (lane == 0) A.upart[u] = part;
+  }
+}
+
+// Per tensor: N = ||g_t||_2 (fixed-order fp64 sum of the unit partials) and
+// the clipping multiplier c = C / N when N > C, else 1.
+__global__ void __launch_bounds__(256) k_gscale(TopkArgs A) {
+  __shared__ double s_part[256];
+  if (aborted(A)) return;
+  const int t = blockIdx.x;
+  double v = 0.0;
+  for (int64_t u = A.units_off[t] + threadIdx.x; u < A.units_off[t + 1]; u += blockDim.x) v += A.upart[u];
+  s_part[threadIdx.x] = v;
+  __syncthreads();
+  for (int h = 128; h > 0; h >>= 1) {
+    if ((int)threadIdx.x < h) s_part[threadIdx.x] += s_part[threadIdx.x + h];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float N = __double2float_rn(sqrt(s_part[0]));
+    const float C = A.clip[t];
+    float c = 1.0f;
+    if (!(C >= 0.0f))
+      atomicOr(A.diag + DIAG_ERR, GC_DIAG_BAD_THRESHOLD);
+    else if (N > C)
+      c = __fdiv_rn(C, N);
+    A.norm_out[t] = N;
+    A.ts[t].gmul = c;
   }
 }
 
@@ -355,7 +447,9 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
   if (st->flags & TS_NOEMIT) return;
   const int64_t base = A.off[t], n = A.off[t + 1] - base;
   const int64_t k = A.kk[t];
-  if (k >= n) return;  // t_est = 0 already
+  if (k >= n) return;  // t_est set by the planner
+  // threshold mode: never below the threshold's own key
+  const uint32_t floor_key = A.tau ? mag_key(A.tau[t]) : 0u;
   int64_t runs, stride, m;
   sample_plan(n, k, &runs, &stride, &m);
   int64_t j;
@@ -366,7 +460,7 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
     j = (int64_t)ceil(lam + 4.0 * sqrt(lam) + 4.0);
   }
   if (j > m) {
-    if (threadIdx.x == 0) st->t_est = 0u;
+    if (threadIdx.x == 0) st->t_est = floor_key;
     return;
   }
   for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
@@ -408,7 +502,7 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
   if (b1 == 0xFFFFFFFFu) {
     if (threadIdx.x == 0) {
       atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
-      st->t_est = 0u;
+      st->t_est = floor_key;
     }
     return;
   }
@@ -433,9 +527,9 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
   if (threadIdx.x == 0) {
     if (b2 == 0xFFFFFFFFu) {
       atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
-      st->t_est = b1 << 21;
+      st->t_est = max(b1 << 21, floor_key);
     } else {
-      st->t_est = (b1 << 21) | (b2 << 10);
+      st->t_est = max((b1 << 21) | (b2 << 10), floor_key);
     }
   }
 }
@@ -461,24 +555,36 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
     const int64_t cnt = st->cand_count;
     const bool ovf = (flags & TS_OVERFLOW) || cnt > cap;
     int64_t kt = A.kk[t];
+    bool force_dense = false;
     if (A.tau) {
-      // threshold mode: every candidate passes |acc| >= tau; keep at most k_t
-      // of them.  An overflowing candidate list has more than k_t entries.
-      if (!ovf && cnt < kt) kt = cnt;
-      if (threadIdx.x == 0) {
-        st->keff = (uint32_t)kt;
-        A.count_out[t] = kt;
+      // threshold mode: candidates are the elements with key >= t_est >= key(tau).
+      // Enough of them (>= k_t): keep the k_t largest.  Fewer, and t_est is
+      // key(tau) itself: keep them all.  Fewer otherwise (or overflow): the
+      // full-pass path counts |acc| >= tau exactly and decides there.
+      const uint32_t tkey = mag_key(A.tau[t]);
+      if (!ovf && cnt < kt) {
+        if (st->t_est == tkey)
+          kt = cnt;
+        else
+          force_dense = true;
+      }
+      if (!force_dense && !ovf) {
+        if (threadIdx.x == 0) {
+          st->keff = (uint32_t)kt;
+          A.count_out[t] = kt;
+          if (kt == 0) {
+            st->flags = flags | TS_NOEMIT;
+            if (A.int8) A.scale[t] = 0.0f;
+            if (A.rd) A.rd[t] = gc_residual_desc{0u, 0u, 0, 0.0f, 0ull, 0ull};
+          }
+        }
         if (kt == 0) {
-          st->flags = flags | TS_NOEMIT;
-          if (A.int8) A.scale[t] = 0.0f;
+          for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+          return;
         }
       }
-      if (kt == 0) {
-        for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
-        return;
-      }
     }
-    const bool dense = ovf || cnt < kt || (A.flags & GC_FORCE_EXACT);
+    const bool dense = ovf || force_dense || cnt < kt || (A.flags & GC_FORCE_EXACT);
     if (dense) {
       for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
       if (threadIdx.x == 0) {
@@ -494,7 +600,24 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
     rank = (uint32_t)kt;
   } else if (phase == PH_C1D) {
     if (!(flags & TS_DENSE)) return;
-    rank = st->keff;
+    if (A.tau) {
+      const uint32_t kt = min(st->cnt_tau, (uint32_t)A.kk[t]);
+      if (threadIdx.x == 0) {
+        st->keff = kt;
+        A.count_out[t] = kt;
+        if (kt == 0) {
+          st->flags = flags | TS_NOEMIT;
+          if (A.int8) A.scale[t] = 0.0f;
+        }
+      }
+      if (kt == 0) {
+        for (int i = threadIdx.x; i < NBINS; i += blockDim.x) row[i] = 0u;
+        return;
+      }
+      rank = kt;
+    } else {
+      rank = st->keff;
+    }
   }
 
   uint32_t above;
@@ -561,7 +684,7 @@ __device__ __forceinline__ void warp_append(float* sval, uint32_t* skey, uint16_
 
 template <int MODE, bool EF, bool LOADG, bool LAZY>
 __device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t li, int64_t gi,
-                                              const gc_residual_desc& d, float* value,
+                                              const gc_residual_desc& d, float gmul, float* value,
                                               uint32_t* key) {
   float x = 0.0f;
   if (MODE == MODE_MOM) {
@@ -570,7 +693,7 @@ __device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t li, int
     A.u[gi] = un;
     A.v[gi] = x;
   } else if (LOADG) {
-    x = A.g[gi];
+    x = __fmul_rn(gmul, A.g[gi]);
     if (EF) {
       x = __fadd_rn(x, LAZY ? lazy_fix(A.e[gi], li, gi, d) : A.e[gi]);
       A.e[gi] = x;
@@ -607,6 +730,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_s
     const uint32_t test = A.ts[t].t_est;
     gc_residual_desc d;
     if (LAZY) d = A.rd[t];
+    const float gmul = A.ts[t].gmul;
     int cnt = 0;
     bool ovf = false;
     if ((g0 & 3) == 0) {
@@ -652,6 +776,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_s
               a[0] = vn.x; a[1] = vn.y; a[2] = vn.z; a[3] = vn.w;
             } else if (LOADG) {
               float4 s = x[j];
+              s.x = __fmul_rn(gmul, s.x);
+              s.y = __fmul_rn(gmul, s.y);
+              s.z = __fmul_rn(gmul, s.z);
+              s.w = __fmul_rn(gmul, s.w);
               if (EF) {
                 if (LAZY) {
                   const int64_t li0 = lstart + 4 * vi;
@@ -696,7 +824,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_s
         const bool valid = (int)lane < rem;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t kk[4] = {0u, 0u, 0u, 0u};
-        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, &a[0], &kk[0]);
+        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, gmul, &a[0], &kk[0]);
         const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
         if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
       }
@@ -706,7 +834,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_s
         const bool valid = li < len;
         float a[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t kk[4] = {0u, 0u, 0u, 0u};
-        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, &a[0], &kk[0]);
+        if (valid) stream_scalar<MODE, EF, LOADG, LAZY>(A, lstart + li, g0 + li, d, gmul, &a[0], &kk[0]);
         const unsigned m = (valid && emit && kk[0] >= test) ? 1u : 0u;
         if (__any_sync(FULL, m != 0u)) warp_append(sval, skey, spos, cnt, ovf, m, kk, a, li, lane);
       }
@@ -772,7 +900,7 @@ __device__ __forceinline__ UnitBlock unit_block(const TopkArgs& A) {
 template <int MODE>
 __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
   __shared__ uint32_t sh[NBINS];
-  __shared__ uint32_t s_max;
+  __shared__ uint32_t s_max, s_tau;
   if (aborted(A)) return;
   const UnitBlock ub = unit_block(A);
   const TensorState st = A.ts[ub.t];
@@ -780,8 +908,14 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
   const bool dense = (st.flags & TS_DENSE) != 0u;
   if (level == 1 && !dense) return;
   for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  if (threadIdx.x == 0) s_max = 0u;
+  if (threadIdx.x == 0) {
+    s_max = 0u;
+    s_tau = 0u;
+  }
   __syncthreads();
+  // threshold mode, full-pass level 1: also count |acc| >= tau exactly
+  const bool count_tau = level == 1 && A.tau != nullptr;
+  const uint32_t tkey = count_tau ? mag_key(A.tau[ub.t]) : 0u;
   const int shift_prev = (level == 2) ? 21 : 10;
   const uint32_t mask = (level == 3) ? 0x3FFu : 0x7FFu;
   const int shift = (level == 1) ? 21 : ((level == 2) ? 10 : 0);
@@ -803,6 +937,10 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
         }
         const bool hit = valid && (level == 1 || (key >> shift_prev) == st.prefix);
         if (valid) mx = max(mx, key);
+        if (count_tau) {
+          const unsigned c = __popc(__ballot_sync(FULL, valid && key >= tkey));
+          if (lane == 0 && c) atomicAdd(&s_tau, c);
+        }
         smem_hist_add(sh, (key >> shift) & mask, hit);
       }
     }
@@ -836,7 +974,10 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
   uint32_t* row = A.hist + (size_t)ub.t * NBINS;
   for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
     if (sh[i]) atomicAdd(row + i, sh[i]);
-  if (level == 1 && threadIdx.x == 0) atomicMax(&A.ts[ub.t].maxkey, s_max);
+  if (level == 1 && threadIdx.x == 0) {
+    atomicMax(&A.ts[ub.t].maxkey, s_max);
+    if (count_tau && s_tau) atomicAdd(&A.ts[ub.t].cnt_tau, s_tau);
+  }
 }
 
 // Per-unit counts of keys above / equal to the k-th key, and their sums
@@ -1079,7 +1220,7 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
 struct TopkCarve {
   size_t zero_bytes = 0, total = 0;
   size_t o_ts, o_hist, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
-      o_cidx, o_cval, o_skey;
+      o_cidx, o_cval, o_skey, o_upart;
 };
 
 static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
@@ -1106,6 +1247,7 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   c.o_cidx = take(4 * (size_t)z.C);
   c.o_cval = take(4 * (size_t)z.C);
   c.o_skey = take(4 * (size_t)z.S);
+  c.o_upart = take(8 * (size_t)z.U);
   c.total = p;
   return c;
 }
@@ -1160,6 +1302,10 @@ template <int MODE>
 static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
   const int T = A.T;
   k_plan<<<1, 1024, 0, s>>>(A);
+  if (A.clip) {
+    k_gnorm<<<stream_grid(k_gnorm, A.U), 256, 0, s>>>(A);
+    k_gscale<<<T, 256, 0, s>>>(A);
+  }
   pe.done(A.sampled ? 0 : 1, s);
   if (A.sampled) {
     k_sample<MODE><<<T, 1024, 0, s>>>(A);
@@ -1211,7 +1357,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
                           int8_t* q, float* scale, uint64_t seed, uint64_t iter, uint32_t flags,
                           void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe,
                           gc_residual_desc* rd = nullptr, const float* tau = nullptr,
-                          int64_t* count_out = nullptr) {
+                          int64_t* count_out = nullptr, const float* clip = nullptr,
+                          float* norm_out = nullptr) {
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
@@ -1222,7 +1369,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   if (!int8 && !val) return GC_ERR_INVALID_ARG;
   if (!aligned16(g) || (e && !aligned16(e)) || (u && !aligned16(u)) || (v && !aligned16(v)))
     return GC_ERR_ALIGNMENT;
-  const bool sampled = mode != MODE_RANDK && !tau;
+  const bool sampled = mode != MODE_RANDK;
   const TopkLayoutTotals z = totals_of(host, sampled);
   const TopkCarve c = carve_topk(host->num_tensors, z);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
@@ -1272,6 +1419,9 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.cidx = reinterpret_cast<int32_t*>(w + c.o_cidx);
   A.cval = reinterpret_cast<float*>(w + c.o_cval);
   A.skey = reinterpret_cast<uint32_t*>(w + c.o_skey);
+  A.upart = reinterpret_cast<double*>(w + c.o_upart);
+  A.clip = clip;
+  A.norm_out = norm_out;
   A.U = z.U;
   A.UB = z.UB;
   A.C = z.C;
@@ -1406,4 +1556,18 @@ extern "C" gc_status gc_ef_threshold_compress(const gc_layout* dev, const gc_lay
   return run_topk(MODE_TOPK, dev, host, g, (flags & GC_EF) ? e : nullptr, nullptr, nullptr, 0.0f,
                   idx, val, q, scale, seed, iter, flags, workspace, ws_bytes, stream, PhaseEvents{},
                   nullptr, tau, count);
+}
+
+extern "C" gc_status gc_ef_topk_compress_clipped(const gc_layout* dev, const gc_layout* host,
+                                                 const float* g, float* e, const float* max_norm,
+                                                 float* norm, int32_t* idx, float* val, int8_t* q,
+                                                 float* scale, uint64_t seed, uint64_t iter,
+                                                 uint32_t flags, void* workspace, size_t ws_bytes,
+                                                 void* stream) {
+  const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if (!(flags & GC_EF) || !e || !max_norm || !norm) return GC_ERR_INVALID_ARG;
+  return run_topk(MODE_TOPK, dev, host, g, e, nullptr, nullptr, 0.0f, idx, val, q, scale, seed, iter,
+                  flags, workspace, ws_bytes, stream, PhaseEvents{}, nullptr, nullptr, nullptr,
+                  max_norm, norm);
 }

@@ -128,7 +128,7 @@ typedef struct gc_diag {
 #define GC_DIAG_LAYOUT_MISMATCH 0x1u /* dev and host layouts disagree; the call did nothing */
 #define GC_DIAG_SELECT 0x2u          /* internal selection inconsistency (should never be set) */
 #define GC_DIAG_INDEX_RANGE 0x4u     /* decompress met a payload index >= n_t; entry skipped */
-#define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold was negative or NaN; that tensor kept nothing */
+#define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold or clipping norm was negative or NaN */
 
 /* Bytes of workspace that operation `op` needs for layout `host` and
  * `flags`.  *bytes is set on GC_OK. */
@@ -153,6 +153,23 @@ gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const
                               int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                               uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
                               void* stream);
+
+/* EF Top-k with DGC local gradient clipping (genomic glossary "Gradient
+ * Compression", DGC: local gradient clipping normalizes the gradient's
+ * magnitude before compression; zh glossary: clipping before quantization
+ * controls the range).  Per tensor: N = ||g_t||_2 (fp64 sum in a fixed
+ * order), g' = (C / N) * g when N > C (C / N rounded to fp32), else g; then
+ * gc_ef_topk_compress(GC_EF | flags) on g'.
+ *   max_norm: device fp32[T], C >= 0 (negative or NaN: no clipping, and
+ *             GC_DIAG_BAD_THRESHOLD is set).
+ *   norm:     device fp32[T] out: N (within 1e-6 relative of an fp64 sum).
+ * flags: GC_EF (required), GC_INT8, GC_FORCE_EXACT.  Reads g twice (norm,
+ * then the streaming pass). */
+gc_status gc_ef_topk_compress_clipped(const gc_layout* dev, const gc_layout* host, const float* g,
+                                      float* e, const float* max_norm, float* norm, int32_t* idx,
+                                      float* val, int8_t* q, float* scale, uint64_t seed,
+                                      uint64_t iter, uint32_t flags, void* workspace,
+                                      size_t ws_bytes, void* stream);
 
 /* Threshold sparsification with EF (genomic glossary "Gradient
  * Compression": gradients below a fixed or adaptive magnitude threshold are

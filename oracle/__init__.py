@@ -35,6 +35,7 @@ def _declare(L):
     L.oracle_stochastic_round.restype = C.c_double
     L.oracle_select.argtypes = [_I64, _I64, _P, _I32, _I32, _P]
     L.oracle_ef_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
+    L.oracle_clip_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _F, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32]
     L.oracle_threshold_tensor.argtypes = [_I64, _I64, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32]
     L.oracle_randk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
     L.oracle_momentum_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _F, _I32, _P, _P, _P, _P,
@@ -46,7 +47,7 @@ def _declare(L):
     L.oracle_warmup_density.argtypes = [_I64, _I64, C.c_double, C.c_double, _I32, _I32]
     L.oracle_warmup_density.restype = C.c_double
     L.oracle_codes_decode_accumulate.argtypes = [_I64, _P, _F, _I32, _I32, _P]
-    for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor", "oracle_threshold_tensor",
+    for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor", "oracle_threshold_tensor", "oracle_clip_topk_tensor",
                  "oracle_momentum_topk_tensor", "oracle_sign_tensor", "oracle_quantize_tensor",
                  "oracle_sparse_accumulate", "oracle_sign_decode_accumulate",
                  "oracle_codes_decode_accumulate"):
@@ -107,6 +108,21 @@ def ef_topk_tensor(g, e, k, base=0, int8=False, seed=0, it=0, method=1):
     _check(lib().oracle_ef_topk_tensor(n, k, base, _p(g), _p(e), _p(idx), _p(val), _p(q), _p(sc),
                                        seed, it, int(int8), method), "ef_topk")
     return idx, val, q, (float(sc[0]) if int8 else None)
+
+
+def clip_topk_tensor(g, e, k, max_norm, base=0, int8=False, seed=0, it=0, norm_given=None):
+    """Returns (idx, val, q, scale, norm computed)."""
+    g = _c(g, np.float32); n = g.size
+    if e is not None:
+        assert e.dtype == np.float32 and e.flags.c_contiguous and e.size == n
+    idx = np.zeros(k, np.int32); val = np.zeros(k, np.float32)
+    q = np.zeros(k, np.int8) if int8 else None
+    sc = np.zeros(1, np.float32) if int8 else None
+    nout = np.zeros(1, np.float32)
+    ng = None if norm_given is None else np.asarray([norm_given], np.float32)
+    _check(lib().oracle_clip_topk_tensor(n, k, base, _p(g), _p(e), float(max_norm), _p(ng), _p(nout), _p(idx),
+                                         _p(val), _p(q), _p(sc), seed, it, int(int8)), "clip_topk")
+    return idx, val, q, (float(sc[0]) if int8 else None), float(nout[0])
 
 
 def threshold_tensor(g, e, kmax, tau, base=0, int8=False, seed=0, it=0):

@@ -239,6 +239,32 @@ int oracle_ef_topk_tensor(int64_t n, int64_t k, uint64_t base, const float* g, f
   return 0;
 }
 
+// ------------------------------------------------------------------ clipping
+// DGC local gradient clipping ([P3] DGC bullets: local gradient clipping
+// normalizes the gradient magnitude before compression; [P1] gradient
+// clipping is applied before quantization to control range), per tensor:
+//   N = (float)sqrt(sum g^2)  (fp64 sum in index order)
+//   g' = (N > C) ? (C / N) * g : g     (C / N rounded to fp32 first)
+// then EF Top-k of g' (with int8 if requested).  norm_given != NULL
+// replaces the computed N (to compare against a norm reduced elsewhere).
+int oracle_clip_topk_tensor(int64_t n, int64_t k, uint64_t base, const float* g, float* e,
+                            float max_norm, const float* norm_given, float* norm_out, int32_t* idx,
+                            float* val, int8_t* q, float* scale, uint64_t seed, uint64_t iter,
+                            int32_t use_int8) {
+  if (n < 0 || k < 0 || k > n || !(max_norm >= 0.0f)) return 1;
+  double ss = 0.0;
+  for (int64_t i = 0; i < n; ++i) ss += (double)g[i] * (double)g[i];
+  float N = (float)std::sqrt(ss);
+  if (norm_out) *norm_out = N;
+  if (norm_given) N = *norm_given;
+  std::vector<float> gc(g, g + n);
+  if (N > max_norm) {
+    const float c = max_norm / N;
+    for (int64_t i = 0; i < n; ++i) gc[i] = c * g[i];
+  }
+  return oracle_ef_topk_tensor(n, k, base, gc.data(), e, idx, val, q, scale, seed, iter, use_int8, 1);
+}
+
 // ------------------------------------------------------------------ threshold
 // Threshold sparsification ([P3] "Threshold-based": gradients below a fixed
 // or adaptive magnitude threshold are dropped; [P5] the threshold is

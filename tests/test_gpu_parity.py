@@ -496,13 +496,13 @@ def test_sign_lazy_residual(gc, name):
 def test_threshold_layouts(gc, flags_name):
     flags = {"ef": gc.GC_EF, "ef_int8": gc.GC_EF | gc.GC_INT8, "noef": 0,
              "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT}[flags_name]
-    sizes = [4097, 1, 33, 100_003, 6, 70_000, 300_000]
-    kmax = [60, 1, 33, 500, 3, 2000, 3000]
+    sizes = [4097, 1, 33, 100_003, 6, 70_000, 300_000, 500_000]
+    kmax = [60, 1, 33, 500, 3, 2000, 3000, 500]
     L = _layout(gc, sizes, k=kmax)
     n, K, T = L.numel, L.total_k, L.T
     int8 = bool(flags & gc.GC_INT8)
     # thresholds: some tensors pass fewer than k_t, some more, tau = 0 and tau = inf
-    tau_h = np.asarray([2e-3, 0.0, np.inf, 2e-2, 0.0, 3e-3, 1e-2], F32)
+    tau_h = np.asarray([2e-3, 0.0, np.inf, 2e-2, 0.0, 3e-3, 1e-2, 1e-3], F32)   # last: ~40% pass, cap 0.1%
     tau = torch.from_numpy(tau_h).cuda()
     e_ref = (np.random.default_rng(9).standard_normal(n) * 1e-4).astype(F32) if flags & gc.GC_EF else None
     e = torch.from_numpy(e_ref).cuda() if e_ref is not None else None
@@ -548,3 +548,44 @@ def test_threshold_rejects_negative_tau(gc):
     d = gc.get_device_status(ws, raise_on_error=False)
     assert d.error_bits & gc.GC_DIAG_BAD_THRESHOLD
     assert int(cnt[0]) == 0
+
+
+# ----------------------------------------------------------------------------- local clipping
+
+@pytest.mark.parametrize("flags_name", ["ef", "ef_int8", "ef_exact"])
+def test_clipped_topk_layouts(gc, flags_name):
+    flags = {"ef": gc.GC_EF, "ef_int8": gc.GC_EF | gc.GC_INT8, "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT}[flags_name]
+    sizes = [4097, 1, 33, 100_003, 6, 70_000, 300_000]
+    L = _layout(gc, sizes, rho=0.01)
+    n, K, T = L.numel, L.total_k, L.T
+    int8 = bool(flags & gc.GC_INT8)
+    e_ref = (np.random.default_rng(10).standard_normal(n) * 1e-4).astype(F32)
+    e = torch.from_numpy(e_ref).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    val = torch.empty(K, device="cuda")
+    q = torch.empty(K, dtype=torch.int8, device="cuda") if int8 else None
+    sc = torch.empty(T, device="cuda") if int8 else None
+    norm = torch.empty(T, device="cuda")
+    for it in range(2):
+        g_h = _grad(n, 600 + it).numpy()
+        gn = [float(np.linalg.norm(g_h[int(L.off[t]):int(L.off[t + 1])].astype(np.float64))) for t in range(T)]
+        # clip some tensors hard, some mildly, one to zero, leave others alone
+        cap = np.asarray([0.5 * gn[0], 10 * gn[1], 0.0, 0.9 * gn[3], np.inf, 0.1 * gn[5], 2 * gn[6]], F32)
+        gc.ef_topk_compress_clipped(L, torch.from_numpy(g_h).cuda(), e, torch.from_numpy(cap).cuda(), norm,
+                                    idx, val, q, sc, 8, it, flags, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gi, gv, gno = idx.cpu().numpy(), val.cpu().numpy(), norm.cpu().numpy()
+        for t in range(T):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            _, _, _, _, nref = oracle.clip_topk_tensor(g_h[a:b], e_ref[a:b].copy(), int(L.k[t]), float(cap[t]),
+                                                       base=a, int8=int8, seed=8, it=it)
+            assert abs(float(gno[t]) - nref) <= 1e-6 * nref, f"it {it} tensor {t}: norm"
+            ri, rv, rq, rs, _ = oracle.clip_topk_tensor(g_h[a:b], e_ref[a:b], int(L.k[t]), float(cap[t]), base=a,
+                                                        int8=int8, seed=8, it=it, norm_given=float(gno[t]))
+            assert np.array_equal(gi[ka:kb], ri), f"it {it} tensor {t}: indices"
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"it {it} tensor {t}: values"
+            if int8:
+                assert np.array_equal(q.cpu().numpy()[ka:kb], rq) and sc.cpu().numpy()[t] == rs
+        assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), f"it {it}: residual"

@@ -33,6 +33,8 @@ MUTANTS = {
     "philox_key_not_bumped": ("    k0 += W0;\n    k1 += W1;", "    k1 += W1;", ["test_philox_matches_triton_interpreter"]),
     "decompress_tensor_offset_lost": ("out[off[t] + i] = out[off[t] + i] + v;", "out[i] = out[i] + v;",
                                       ["test_sparse_accumulate_matches_numpy_add_at"]),
+    "clip_ratio_inverted": ("const float c = max_norm / N;", "const float c = N / max_norm;",
+                            ["test_clipping_scales_to_max_norm_and_leaves_small_tensors"]),
     "randk_largest_keys": ("if (key[a] != key[b]) return key[a] < key[b];", "if (key[a] != key[b]) return key[a] > key[b];",
                            ["test_randk_selection_is_k_smallest_keys"]),
 }

@@ -511,3 +511,27 @@ def test_warmup_schedule_closed_forms():
     st = [oracle.warmup_density(s, 8, a, b, "step") for s in range(8)]
     assert st[0] == st[1] == a and st[2] == st[3] and st[6] == st[7]
     assert st[2] == pytest.approx(a * (b / a) ** 0.25) and st[6] == pytest.approx(a * (b / a) ** 0.75)
+
+
+def test_clipping_scales_to_max_norm_and_leaves_small_tensors():
+    rng = np.random.default_rng(23)
+    g = (rng.standard_normal(5000) * 1e-2).astype(F32)
+    gnorm = np.linalg.norm(g.astype(np.float64))
+    # C above the norm: identical to plain EF Top-k
+    e1, e2 = np.zeros(5000, F32), np.zeros(5000, F32)
+    i1, v1, _, _, N = oracle.clip_topk_tensor(g, e1, 50, 10 * gnorm)
+    i2, v2, _, _ = oracle.ef_topk_tensor(g, e2, 50)
+    assert abs(N - gnorm) <= 1e-6 * gnorm
+    assert np.array_equal(i1, i2) and np.array_equal(v1, v2) and np.array_equal(e1, e2)
+    # C below the norm: the clipped gradient has norm C (to rounding) and the
+    # kept values are the clipped ones
+    C = F32(0.25 * gnorm)
+    e = np.zeros(5000, F32)
+    idx, val, _, _, N = oracle.clip_topk_tensor(g, e, 5000, C)   # k = n: everything is sent
+    c = C / F32(N)
+    assert np.array_equal(val, g * c)
+    assert abs(np.linalg.norm(val.astype(np.float64)) - C) <= 1e-6 * C
+    # C = 0 sends zeros and leaves the residual at e
+    e = np.full(5000, 1e-5, F32)
+    idx, val, _, _, _ = oracle.clip_topk_tensor(g, e, 10, 0.0)
+    assert np.all(np.abs(val) == F32(1e-5))
