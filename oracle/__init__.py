@@ -36,6 +36,8 @@ def _declare(L):
     L.oracle_select.argtypes = [_I64, _I64, _P, _I32, _I32, _P]
     L.oracle_ef_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
     L.oracle_clip_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _F, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32]
+    L.oracle_powersgd_tensor.argtypes = [_I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.oracle_powersgd_decode_accumulate.argtypes = [_I64, _I64, _I32, _P, _P, _P]
     L.oracle_threshold_tensor.argtypes = [_I64, _I64, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _U64, _U64, _I32]
     L.oracle_randk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _U64, _U64, _I32, _I32]
     L.oracle_momentum_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _F, _I32, _P, _P, _P, _P,
@@ -48,6 +50,7 @@ def _declare(L):
     L.oracle_warmup_density.restype = C.c_double
     L.oracle_codes_decode_accumulate.argtypes = [_I64, _P, _F, _I32, _I32, _P]
     for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor", "oracle_threshold_tensor", "oracle_clip_topk_tensor",
+                 "oracle_powersgd_tensor", "oracle_powersgd_decode_accumulate",
                  "oracle_momentum_topk_tensor", "oracle_sign_tensor", "oracle_quantize_tensor",
                  "oracle_sparse_accumulate", "oracle_sign_decode_accumulate",
                  "oracle_codes_decode_accumulate"):
@@ -123,6 +126,30 @@ def clip_topk_tensor(g, e, k, max_norm, base=0, int8=False, seed=0, it=0, norm_g
     _check(lib().oracle_clip_topk_tensor(n, k, base, _p(g), _p(e), float(max_norm), _p(ng), _p(nout), _p(idx),
                                          _p(val), _p(q), _p(sc), seed, it, int(int8)), "clip_topk")
     return idx, val, q, (float(sc[0]) if int8 else None), float(nout[0])
+
+
+def powersgd_tensor(g, e, q, r, p_raw_given=None, p_given=None, q_given=None):
+    """One PowerSGD step on an m x n matrix.  g, e: (m, n) fp32 (e updated in
+    place); q: (n, r) fp32 warm start, updated in place.  Returns (p, p_raw)."""
+    g = _c(g, np.float32)
+    m, n = g.shape
+    assert e.dtype == np.float32 and e.flags.c_contiguous and e.shape == (m, n)
+    assert q.dtype == np.float32 and q.flags.c_contiguous and q.shape == (n, r)
+    p = np.zeros((m, r), np.float32); p_raw = np.zeros((m, r), np.float32)
+    pr = None if p_raw_given is None else _c(p_raw_given, np.float32)
+    pg = None if p_given is None else _c(p_given, np.float32)
+    qg = None if q_given is None else _c(q_given, np.float32)
+    _check(lib().oracle_powersgd_tensor(m, n, r, _p(g), _p(e), _p(q), _p(p), _p(p_raw), _p(pr), _p(pg), _p(qg)),
+           "powersgd")
+    return p, p_raw
+
+
+def powersgd_decode_accumulate(p, q, out):
+    m, r = p.shape
+    n = q.shape[0]
+    _check(lib().oracle_powersgd_decode_accumulate(m, n, r, _p(_c(p, np.float32)), _p(_c(q, np.float32)), _p(out)),
+           "powersgd_decode")
+    return out
 
 
 def threshold_tensor(g, e, kmax, tau, base=0, int8=False, seed=0, it=0):

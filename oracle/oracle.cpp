@@ -469,6 +469,83 @@ int oracle_quantize_tensor(int64_t n, uint64_t base, const float* g, float* e, i
   return 0;
 }
 
+// ------------------------------------------------------------------ PowerSGD
+// PowerSGD with error feedback ([P4] PowerSGD section: G ~ P Q^T with
+// P (m x r), Q (n x r), found by power iteration that alternates between
+// updating P and Q, with error feedback on the residual G - P Q^T; [P2]
+// rank-4 PowerSGD; [P3] low-rank compression).  One power-iteration step per
+// call, warm-started from the previous call's Q (row-major n x r):
+//   M = G + E                                         (fp32)
+//   P = M Q            P_ik = (float) sum_j M_ij Q_jk (fp64 sum, j ascending)
+//   orthonormalize P's columns (modified Gram-Schmidt), k = 0..r-1:
+//     for j < k: d = (float) sum_i P_ij P_ik (fp64);  P_ik = P_ik - d * P_ij
+//     nrm = (float) sqrt(sum_i P_ik^2) (fp64);  if nrm > 0: P_ik = P_ik / nrm
+//   Q = M^T P          Q_jk = (float) sum_i M_ij P_ik (fp64 sum, i ascending)
+//   E = M - P Q^T      with s_ij = 0; s_ij = s_ij + P_ik * Q_jk for k = 0..r-1 (fp32)
+// G, E are row-major m x n; P is row-major m x r.  p_raw_out receives P
+// before orthonormalization.  p_raw_given, p_given, q_given replace the
+// computed P (before / after orthonormalization) and Q: used to compare
+// each later step against values reduced elsewhere.
+namespace {
+double dot_rows(int64_t len, const float* a, int64_t sa, const float* b, int64_t sb) {
+  double s = 0.0;
+  for (int64_t i = 0; i < len; ++i) s += (double)a[i * sa] * (double)b[i * sb];
+  return s;
+}
+}  // namespace
+
+int oracle_powersgd_tensor(int64_t m, int64_t n, int32_t r, const float* g, float* e, float* q,
+                           float* p, float* p_raw_out, const float* p_raw_given,
+                           const float* p_given, const float* q_given) {
+  if (m < 1 || n < 1 || r < 1 || r > 8) return 1;
+  std::vector<float> M(m * n);
+  for (int64_t x = 0; x < m * n; ++x) M[x] = g[x] + e[x];
+  // P = M Q
+  for (int64_t i = 0; i < m; ++i)
+    for (int32_t k = 0; k < r; ++k) p[i * r + k] = (float)dot_rows(n, &M[i * n], 1, q + k, r);
+  if (p_raw_out)
+    for (int64_t x = 0; x < m * r; ++x) p_raw_out[x] = p[x];
+  if (p_raw_given)
+    for (int64_t x = 0; x < m * r; ++x) p[x] = p_raw_given[x];
+  // modified Gram-Schmidt
+  for (int32_t k = 0; k < r; ++k) {
+    for (int32_t j = 0; j < k; ++j) {
+      const float d = (float)dot_rows(m, p + j, r, p + k, r);
+      for (int64_t i = 0; i < m; ++i) p[i * r + k] = p[i * r + k] - d * p[i * r + j];
+    }
+    const float nrm = (float)std::sqrt(dot_rows(m, p + k, r, p + k, r));
+    if (nrm > 0.0f)
+      for (int64_t i = 0; i < m; ++i) p[i * r + k] = p[i * r + k] / nrm;
+  }
+  if (p_given)
+    for (int64_t x = 0; x < m * r; ++x) p[x] = p_given[x];
+  // Q = M^T P
+  for (int64_t jcol = 0; jcol < n; ++jcol)
+    for (int32_t k = 0; k < r; ++k) q[jcol * r + k] = (float)dot_rows(m, &M[jcol], n, p + k, r);
+  if (q_given)
+    for (int64_t x = 0; x < n * r; ++x) q[x] = q_given[x];
+  // E = M - P Q^T
+  for (int64_t i = 0; i < m; ++i)
+    for (int64_t jcol = 0; jcol < n; ++jcol) {
+      float s = 0.0f;
+      for (int32_t k = 0; k < r; ++k) s = s + p[i * r + k] * q[jcol * r + k];
+      e[i * n + jcol] = M[i * n + jcol] - s;
+    }
+  return 0;
+}
+
+// Receiver of a PowerSGD payload: out += P Q^T (same fp32 accumulation).
+int oracle_powersgd_decode_accumulate(int64_t m, int64_t n, int32_t r, const float* p,
+                                      const float* q, float* out) {
+  for (int64_t i = 0; i < m; ++i)
+    for (int64_t jcol = 0; jcol < n; ++jcol) {
+      float s = 0.0f;
+      for (int32_t k = 0; k < r; ++k) s = s + p[i * r + k] * q[jcol * r + k];
+      out[i * n + jcol] = out[i * n + jcol] + s;
+    }
+  return 0;
+}
+
 // ------------------------------------------------------------------ receivers
 // Sum of W workers' sparse payloads into a dense arena ([P4]: the received
 // gradient is the union of different sparse vectors; [P1]: all-gather of

@@ -35,6 +35,12 @@ MUTANTS = {
                                       ["test_sparse_accumulate_matches_numpy_add_at"]),
     "clip_ratio_inverted": ("const float c = max_norm / N;", "const float c = N / max_norm;",
                             ["test_clipping_scales_to_max_norm_and_leaves_small_tensors"]),
+    "powersgd_gs_sign": ("for (int64_t i = 0; i < m; ++i) p[i * r + k] = p[i * r + k] - d * p[i * r + j];",
+                         "for (int64_t i = 0; i < m; ++i) p[i * r + k] = p[i * r + k] + d * p[i * r + j];",
+                         ["test_powersgd_one_step_matches_numpy_and_keeps_the_residual"]),
+    "powersgd_q_transposed": ("q[jcol * r + k] = (float)dot_rows(m, &M[jcol], n, p + k, r);",
+                              "q[jcol * r + k] = (float)dot_rows(m, &M[jcol], 1, p + k, r);",
+                              ["test_powersgd_one_step_matches_numpy_and_keeps_the_residual"]),
     "randk_largest_keys": ("if (key[a] != key[b]) return key[a] < key[b];", "if (key[a] != key[b]) return key[a] > key[b];",
                            ["test_randk_selection_is_k_smallest_keys"]),
 }

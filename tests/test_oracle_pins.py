@@ -535,3 +535,59 @@ def test_clipping_scales_to_max_norm_and_leaves_small_tensors():
     e = np.full(5000, 1e-5, F32)
     idx, val, _, _, _ = oracle.clip_topk_tensor(g, e, 10, 0.0)
     assert np.all(np.abs(val) == F32(1e-5))
+
+
+# ----------------------------------------------------------------------------- PowerSGD
+
+def test_powersgd_one_step_matches_numpy_and_keeps_the_residual():
+    rng = np.random.default_rng(31)
+    m, n, r = 37, 53, 4
+    g = rng.standard_normal((m, n)).astype(F32)
+    e0 = (0.1 * rng.standard_normal((m, n))).astype(F32)
+    q0 = rng.standard_normal((n, r)).astype(F32)
+    e, q = e0.copy(), q0.copy()
+    p, p_raw = oracle.powersgd_tensor(g, e, q, r)
+    M = (g + e0).astype(np.float64)
+    assert np.allclose(p_raw, M @ q0.astype(np.float64), rtol=1e-6, atol=1e-5)   # numpy matmul
+    assert np.allclose(p.T.astype(np.float64) @ p, np.eye(r), atol=1e-5)          # orthonormal columns
+    # same column space as M Q (QR from numpy spans it too)
+    qr, _ = np.linalg.qr(M @ q0.astype(np.float64))
+    assert np.allclose(np.abs(qr.T @ p), np.eye(r), atol=1e-4)
+    assert np.allclose(q, M.T @ p.astype(np.float64), rtol=1e-5, atol=1e-4)
+    # nothing lost: M = P Q^T + E (to fp32 rounding)
+    assert np.allclose(p.astype(np.float64) @ q.T.astype(np.float64) + e, M, atol=1e-4)
+    out = np.zeros((m, n), F32)
+    oracle.powersgd_decode_accumulate(p, q, out)
+    assert np.array_equal(out + e, (g + e0)) or np.allclose(out + e, g + e0, atol=1e-5)
+
+
+def test_powersgd_reproduces_a_rank_r_matrix_and_converges_to_svd():
+    rng = np.random.default_rng(32)
+    m, n, r = 60, 40, 2
+    a, b = rng.standard_normal((m, r)), rng.standard_normal((n, r))
+    g = (a @ b.T).astype(F32)                       # exactly rank r (up to fp32)
+    e = np.zeros((m, n), F32)
+    q = rng.standard_normal((n, r)).astype(F32)
+    p, _ = oracle.powersgd_tensor(g, e, q, r)
+    assert np.abs(e).max() <= 1e-4 * np.abs(g).max()    # one step captures it
+    # a full-rank matrix: repeated steps (E reset) converge to the truncated SVD
+    # a full-rank matrix with a clear gap after the r-th singular value
+    u0, _ = np.linalg.qr(rng.standard_normal((m, n)))
+    v0, _ = np.linalg.qr(rng.standard_normal((n, n)))
+    spectrum = np.concatenate([[10.0, 7.0], np.linspace(1.0, 0.1, n - 2)])
+    h = ((u0 * spectrum) @ v0.T).astype(F32)
+    u, sv, vt = np.linalg.svd(h.astype(np.float64))
+    best = (u[:, :r] * sv[:r]) @ vt[:r]
+    q = rng.standard_normal((n, r)).astype(F32)
+    for _ in range(60):
+        e = np.zeros((m, n), F32)
+        p, _ = oracle.powersgd_tensor(h, e, q, r)
+    approx = p.astype(np.float64) @ q.T.astype(np.float64)
+    assert np.linalg.norm(approx - best) <= 1e-3 * np.linalg.norm(best)
+
+
+def test_powersgd_ratio_page_figure():
+    # mbrenndoerfer.com "Gradient Compression", PowerSGD: m = n = 4096, r = 4 gives 512x
+    m = n = 4096
+    r = 4
+    assert (m * n) / ((m + n) * r) == 512
