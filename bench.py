@@ -385,6 +385,7 @@ OPS = {
     "decompress": (5, "llama3_8b", 0.001, "scatter-add of W = 8 workers' sparse fp32 payloads", 0, 0, 0),
     "threshold": (3, "bert_large", 0.002, "threshold |acc| >= 1e-2 with EF, capped at 0.2% per tensor", 12, 8, 0),
     "clip": (3, "bert_large", 0.001, "DGC local clipping (max norm = half of ||g_t||) + EF Top-k 0.1%", 16, 8, 0),
+    "powersgd": (3, "bert_large", None, "PowerSGD rank 4 with EF on every weight matrix", 12, 0, 0),
 }
 
 
@@ -417,6 +418,22 @@ def run_op(args):
             else:
                 gc.ef_topk_compress_momentum(L, grads[it % 2], a, b, 0.9, idx, val, None, None, 5, it, 0, ws)
         algo = b_elem * N + b_kept * K
+    elif args.op == "powersgd":
+        mats = workloads.matrices_of(layout)
+        ml = gc.MatrixLayout([int(layout.off[t]) for t, _, _ in mats], [m for _, m, _ in mats],
+                             [n for _, _, n in mats], device=dev)
+        R = 4
+        e = torch.zeros(N, device=dev)
+        qv = torch.randn(int(ml.qoff[-1]) * R, device=dev)
+        pv = torch.empty(int(ml.poff[-1]) * R, device=dev)
+        ws = gc.powersgd_workspace(ml, R)
+
+        def step(it):
+            gc.powersgd_compress(ml, R, grads[it % 2], e, qv, pv, None, ws)
+        melems = sum(m * n for _, m, n in mats)
+        algo = 12 * melems + 4 * R * (int(ml.poff[-1]) + int(ml.qoff[-1]))
+        extra = {"matrices": len(mats), "matrix_elements": melems, "rank": R,
+                 "passes": "M = G + E and P = MQ (12 B/elt), Q = M^T P (4), E = M - PQ^T (8)"}
     elif args.op in ("threshold", "clip"):
         ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
         idx = torch.empty(K, dtype=torch.int32, device=dev)

@@ -29,6 +29,10 @@ class gc_layout(C.Structure):
     _fields_ = [("num_tensors", C.c_int32), ("off", C.c_void_p), ("k", C.c_void_p), ("koff", C.c_void_p)]
 
 
+class gc_matrix_layout(C.Structure):
+    _fields_ = [("num_tensors", C.c_int32), ("start", C.c_void_p), ("rows", C.c_void_p), ("cols", C.c_void_p)]
+
+
 class gc_diag(C.Structure):
     _fields_ = [("error_bits", C.c_uint32), ("exact_tensors", C.c_uint32),
                 ("overflow_tensors", C.c_uint32), ("reserved", C.c_uint32)]
@@ -61,6 +65,10 @@ def lib() -> C.CDLL:
         L.gc_ef_residual_materialize.argtypes = [LP, LP, P, P, P]
         L.gc_sign_compress_lazy.argtypes = [LP, LP, P, P, P, P, P, P, SZ, P]
         L.gc_sign_residual_materialize.argtypes = [LP, LP, P, P, P]
+        MLP = C.POINTER(gc_matrix_layout)
+        L.gc_powersgd_workspace_size.argtypes = [MLP, I32, C.POINTER(SZ)]
+        L.gc_powersgd_compress.argtypes = [MLP, MLP, I32, P, P, P, P, P, P, SZ, P]
+        L.gc_powersgd_decompress_accumulate.argtypes = [MLP, MLP, I32, P, P, P, P, SZ, P]
         L.gc_ef_topk_compress_clipped.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_threshold_compress.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_warmup_density.argtypes = [I64, I64, C.c_double, C.c_double, I32, I32]
@@ -78,7 +86,8 @@ def lib() -> C.CDLL:
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
                      "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
                      "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
-                     "gc_ef_topk_compress_clipped",
+                     "gc_ef_topk_compress_clipped", "gc_powersgd_workspace_size", "gc_powersgd_compress",
+                     "gc_powersgd_decompress_accumulate",
                      "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status"):
@@ -162,6 +171,48 @@ class Layout:
         if self._dev is None:
             raise RuntimeError("layout has no device copy")
         return C.byref(self._dev)
+
+
+class MatrixLayout:
+    """Matrices of an arena for PowerSGD: host arrays + device copies."""
+
+    def __init__(self, start, rows, cols, device="cuda"):
+        self.start = np.ascontiguousarray(start, dtype=np.int64)
+        self.rows = np.ascontiguousarray(rows, dtype=np.int64)
+        self.cols = np.ascontiguousarray(cols, dtype=np.int64)
+        self.T = int(self.start.size)
+        self.device = torch.device(device)
+        self._host = gc_matrix_layout(self.T, self.start.ctypes.data, self.rows.ctypes.data, self.cols.ctypes.data)
+        self._dev = None
+        if self.device.type == "cuda":
+            self._d = [torch.from_numpy(a).to(self.device) for a in (self.start, self.rows, self.cols)]
+            self._dev = gc_matrix_layout(self.T, *[_ptr(x) for x in self._d])
+        self.poff = np.zeros(self.T + 1, np.int64); self.poff[1:] = np.cumsum(self.rows)
+        self.qoff = np.zeros(self.T + 1, np.int64); self.qoff[1:] = np.cumsum(self.cols)
+
+    def host(self):
+        return C.byref(self._host)
+
+    def dev(self):
+        return C.byref(self._dev)
+
+
+def powersgd_workspace(ml: MatrixLayout, rank: int, device=None) -> torch.Tensor:
+    out = C.c_size_t(0)
+    _check(lib().gc_powersgd_workspace_size(ml.host(), int(rank), C.byref(out)), "gc_powersgd_workspace_size")
+    return torch.empty(max(int(out.value), 256), dtype=torch.uint8, device=device or ml.device)
+
+
+def powersgd_compress(ml, rank, g, e, q, p, p_raw, workspace, stream=None):
+    _check(lib().gc_powersgd_compress(ml.dev(), ml.host(), int(rank), _ptr(g), _ptr(e), _ptr(q), _ptr(p),
+                                      _ptr(p_raw), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_powersgd_compress")
+
+
+def powersgd_decompress_accumulate(ml, rank, p, q, out, workspace, stream=None):
+    _check(lib().gc_powersgd_decompress_accumulate(ml.dev(), ml.host(), int(rank), _ptr(p), _ptr(q), _ptr(out),
+                                                   _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_powersgd_decompress_accumulate")
 
 
 def workspace_size(layout: Layout, op: int, flags: int = 0) -> int:

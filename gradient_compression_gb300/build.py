@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgc.so")
-SOURCES = ["gc_api.cu", "gc_topk.cu", "gc_dense.cu", "gc_decompress.cu", "gc_noalloc.cu"]
+SOURCES = ["gc_api.cu", "gc_topk.cu", "gc_dense.cu", "gc_decompress.cu", "gc_noalloc.cu", "gc_powersgd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

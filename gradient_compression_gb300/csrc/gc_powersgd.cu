@@ -1,0 +1,495 @@
+// PowerSGD with error feedback (sm_103a).
+//
+// Method: mbrenndoerfer.com "Gradient Compression", PowerSGD section: each
+// gradient matrix G (m x n) is sent as P (m x r) and Q (n x r) with
+// G ~ P Q^T, found by power iteration (alternating updates of P and Q) with
+// error feedback on G - P Q^T; chipfoundryservices.com glossary: rank-4
+// PowerSGD.  One warm-started power-iteration step per call:
+//   M = G + E;  P = M Q;  orthonormalize P (modified Gram-Schmidt);
+//   Q = M^T P;  E = M - P Q^T.
+//
+// With r <= 4 the products are skinny (about one flop per byte of M), so
+// they are HBM-bound streaming passes on the CUDA cores, not tensor-core
+// GEMMs.  Passes over the matrices:
+//   k_pmq   warp per row: M = G + E (stored into E), P_raw = M Q
+//   k_porth one CTA per matrix: Gram-Schmidt on P (fixed-order fp64 sums)
+//   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
+//   k_pqred fixed-order sum of the partials -> Q
+//   k_pres  warp per row: E = M - P Q^T
+// Reductions are fp32 Neumaier per thread and fp64 across threads and tiles
+// in a fixed order (deterministic); elementwise steps are single fp32
+// roundings in the order the method states them.
+#include <cstring>
+
+#include "gc_common.cuh"
+#include "gc_host.h"
+
+namespace gc {
+
+constexpr int PS_RC = 256;   // rows per Q tile
+constexpr int PS_CC = 1024;  // columns per Q tile (256 threads x 4)
+
+struct PsArgs {
+  int T;
+  const int64_t* start;
+  const int64_t* rows;
+  const int64_t* cols;
+  const float* g;
+  float* e;
+  float* q;
+  float* p;
+  float* p_raw;
+  float* out;
+  uint32_t* diag;
+  int64_t* rowoff;   // [T+1] prefix of m
+  int64_t* coloff;   // [T+1] prefix of n
+  int64_t* tileoff;  // [T+1] prefix of Q tiles
+  int64_t* partoff;  // [T+1] prefix of ceil(m / PS_RC) * n
+  float* part;       // partial column sums, [partoff][R]
+  int64_t Mrows, Ncols, Tiles, Parts;
+};
+
+__device__ __forceinline__ bool ps_aborted(const PsArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
+
+__global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  int64_t carry[4] = {0, 0, 0, 0};
+  int64_t* outs[4] = {A.rowoff, A.coloff, A.tileoff, A.partoff};
+  for (int base = 0; base < A.T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    int64_t v[4] = {0, 0, 0, 0};
+    if (t < A.T) {
+      const int64_t m = A.rows[t], n = A.cols[t];
+      if (m < 1 || n < 1 || A.start[t] < 0) s_bad = 1;
+      const int64_t rc = (m + PS_RC - 1) / PS_RC;
+      v[0] = m;
+      v[1] = n;
+      v[2] = rc * ((n + PS_CC - 1) / PS_CC);
+      v[3] = rc * n;
+    }
+    for (int w = 0; w < 4; ++w) {
+      const unsigned lane = lane_id(), wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
+      int64_t x = v[w];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(FULL, x, d);
+        if (lane >= (unsigned)d) x += y;
+      }
+      if (lane == 31) s_warp[wi] = x;
+      __syncthreads();
+      if (wi == 0) {
+        int64_t z = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int64_t y = __shfl_up_sync(FULL, z, d);
+          if (lane >= (unsigned)d) z += y;
+        }
+        if (lane < nw) s_warp[lane] = z;
+      }
+      __syncthreads();
+      const int64_t excl = (wi == 0 ? 0 : s_warp[wi - 1]) + x - v[w];
+      const int64_t tot = s_warp[nw - 1];
+      __syncthreads();
+      if (t < A.T) outs[w][t] = carry[w] + excl;
+      carry[w] += tot;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < 4; ++w) outs[w][A.T] = carry[w];
+    if (s_bad || carry[0] != A.Mrows || carry[1] != A.Ncols || carry[2] != A.Tiles || carry[3] != A.Parts) {
+      A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
+      A.diag[DIAG_ABORT] = 1u;
+    }
+  }
+}
+
+struct Nm {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = __fadd_rn(s, x);
+    if (fabsf(s) >= fabsf(x))
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
+    else
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
+    s = t;
+  }
+  __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+};
+
+template <int R>
+__device__ __forceinline__ void load_row(const float* base, float v[R]) {
+#pragma unroll
+  for (int k = 0; k < R; ++k) v[k] = __ldg(base + k);
+}
+
+// M = G + E (stored into E) and P_raw = M Q, one warp per matrix row.
+template <int R>
+__global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
+  if (ps_aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < A.Mrows; gr += nwarps) {
+    const int t = find_segment(A.rowoff, A.T, gr);
+    const int64_t i = gr - A.rowoff[t], n = A.cols[t];
+    const int64_t rb = A.start[t] + i * n;
+    const float* qt = A.q + A.coloff[t] * R;
+    Nm acc[R];
+    if ((rb & 3) == 0 && (n & 3) == 0) {
+      const float4* g4 = reinterpret_cast<const float4*>(A.g + rb);
+      float4* e4 = reinterpret_cast<float4*>(A.e + rb);
+      for (int64_t v = lane; v < (n >> 2); v += 32) {
+        const float4 gv = ld_stream(g4 + v);
+        const float4 ev = ld_stream(e4 + v);
+        float4 mv;
+        mv.x = __fadd_rn(gv.x, ev.x);
+        mv.y = __fadd_rn(gv.y, ev.y);
+        mv.z = __fadd_rn(gv.z, ev.z);
+        mv.w = __fadd_rn(gv.w, ev.w);
+        st_stream(e4 + v, mv);
+        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float qv[R];
+          load_row<R>(qt + (4 * v + c) * R, qv);
+#pragma unroll
+          for (int k = 0; k < R; ++k) acc[k].add(__fmul_rn(mm[c], qv[k]));
+        }
+      }
+    } else {
+      for (int64_t j = lane; j < n; j += 32) {
+        const float mv = __fadd_rn(A.g[rb + j], A.e[rb + j]);
+        A.e[rb + j] = mv;
+        float qv[R];
+        load_row<R>(qt + j * R, qv);
+#pragma unroll
+        for (int k = 0; k < R; ++k) acc[k].add(__fmul_rn(mv, qv[k]));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      double x = acc[k].value();
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) x += __shfl_xor_sync(FULL, x, d);
+      if (lane == 0) {
+        const float pv = __double2float_rn(x);
+        A.p[(A.rowoff[t] + i) * R + k] = pv;
+        if (A.p_raw) A.p_raw[(A.rowoff[t] + i) * R + k] = pv;
+      }
+    }
+  }
+}
+
+// Sum over the block of per-thread fp64 values, fixed tree; all threads get it.
+__device__ double block_sum_f64(double v, double* sm) {
+  sm[threadIdx.x] = v;
+  __syncthreads();
+  for (int h = blockDim.x >> 1; h > 0; h >>= 1) {
+    if ((int)threadIdx.x < h) sm[threadIdx.x] += sm[threadIdx.x + h];
+    __syncthreads();
+  }
+  const double r = sm[0];
+  __syncthreads();
+  return r;
+}
+
+// Modified Gram-Schmidt on the columns of P (one CTA of 1024 threads per matrix).
+template <int R>
+__global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
+  __shared__ double sm[1024];
+  if (ps_aborted(A)) return;
+  const int t = blockIdx.x;
+  const int64_t m = A.rows[t];
+  float* P = A.p + A.rowoff[t] * R;
+  for (int k = 0; k < R; ++k) {
+    for (int j = 0; j < k; ++j) {
+      double s = 0.0;
+      for (int64_t i = threadIdx.x; i < m; i += blockDim.x) s += (double)P[i * R + j] * (double)P[i * R + k];
+      const float d = __double2float_rn(block_sum_f64(s, sm));
+      for (int64_t i = threadIdx.x; i < m; i += blockDim.x)
+        P[i * R + k] = __fsub_rn(P[i * R + k], __fmul_rn(d, P[i * R + j]));
+      __syncthreads();
+    }
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < m; i += blockDim.x) s += (double)P[i * R + k] * (double)P[i * R + k];
+    const float nrm = __double2float_rn(sqrt(block_sum_f64(s, sm)));
+    if (nrm > 0.0f)
+      for (int64_t i = threadIdx.x; i < m; i += blockDim.x) P[i * R + k] = __fdiv_rn(P[i * R + k], nrm);
+    __syncthreads();
+  }
+}
+
+// Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
+// thread = 4 consecutive columns.
+template <int R>
+__global__ void __launch_bounds__(256) k_pmtp(PsArgs A) {
+  if (ps_aborted(A)) return;
+  const int64_t tile = blockIdx.x;
+  const int t = find_segment(A.tileoff, A.T, tile);
+  const int64_t m = A.rows[t], n = A.cols[t];
+  const int64_t nd = (n + PS_CC - 1) / PS_CC;
+  const int64_t local = tile - A.tileoff[t];
+  const int64_t c = local / nd, d = local % nd;
+  const int64_t j0 = d * PS_CC + 4 * threadIdx.x;
+  const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
+  const float* P = A.p + A.rowoff[t] * R;
+  const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+  Nm acc[4][R];
+  if (j0 < n) {
+    for (int64_t i = i0; i < i1; ++i) {
+      const int64_t rb = A.start[t] + i * n;
+      float mm[4];
+      if (vec) {
+        const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
+        mm[0] = mv.x; mm[1] = mv.y; mm[2] = mv.z; mm[3] = mv.w;
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) mm[cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
+      }
+      float pv[R];
+      load_row<R>(P + i * R, pv);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int k = 0; k < R; ++k) acc[cc][k].add(__fmul_rn(mm[cc], pv[k]));
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      if (j0 + cc >= n) break;
+      float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
+#pragma unroll
+      for (int k = 0; k < R; ++k) dst[k] = __double2float_rn(acc[cc][k].value());
+    }
+  }
+}
+
+// Q_jk = sum over row tiles of the partials, in tile order (fp64).
+template <int R>
+__global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
+  if (ps_aborted(A)) return;
+  for (int64_t gc = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gc < A.Ncols;
+       gc += (int64_t)gridDim.x * blockDim.x) {
+    const int t = find_segment(A.coloff, A.T, gc);
+    const int64_t j = gc - A.coloff[t], n = A.cols[t];
+    const int64_t nc = (A.rows[t] + PS_RC - 1) / PS_RC;
+    double s[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) s[k] = 0.0;
+    for (int64_t c = 0; c < nc; ++c) {
+      const float* src = A.part + (A.partoff[t] + c * n + j) * R;
+#pragma unroll
+      for (int k = 0; k < R; ++k) s[k] += (double)src[k];
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) A.q[gc * R + k] = __double2float_rn(s[k]);
+  }
+}
+
+// s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, then
+//   E = M - s (residual) or out += s (receiver); warp per row.
+template <int R, bool DECODE>
+__global__ void __launch_bounds__(256) k_pres(PsArgs A) {
+  if (ps_aborted(A)) return;
+  const unsigned lane = lane_id();
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  float* dstbase = DECODE ? A.out : A.e;
+  for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < A.Mrows; gr += nwarps) {
+    const int t = find_segment(A.rowoff, A.T, gr);
+    const int64_t i = gr - A.rowoff[t], n = A.cols[t];
+    const int64_t rb = A.start[t] + i * n;
+    const float* qt = A.q + A.coloff[t] * R;
+    float pv[R];
+    load_row<R>(A.p + (A.rowoff[t] + i) * R, pv);
+    auto lowrank = [&](int64_t j) {
+      float qv[R];
+      load_row<R>(qt + j * R, qv);
+      float s = 0.0f;
+#pragma unroll
+      for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[k]));
+      return s;
+    };
+    if ((rb & 3) == 0 && (n & 3) == 0) {
+      float4* d4 = reinterpret_cast<float4*>(dstbase + rb);
+      for (int64_t v = lane; v < (n >> 2); v += 32) {
+        float4 x = ld_stream(d4 + v);
+        if (DECODE) {
+          x.x = __fadd_rn(x.x, lowrank(4 * v + 0));
+          x.y = __fadd_rn(x.y, lowrank(4 * v + 1));
+          x.z = __fadd_rn(x.z, lowrank(4 * v + 2));
+          x.w = __fadd_rn(x.w, lowrank(4 * v + 3));
+        } else {
+          x.x = __fsub_rn(x.x, lowrank(4 * v + 0));
+          x.y = __fsub_rn(x.y, lowrank(4 * v + 1));
+          x.z = __fsub_rn(x.z, lowrank(4 * v + 2));
+          x.w = __fsub_rn(x.w, lowrank(4 * v + 3));
+        }
+        st_stream(d4 + v, x);
+      }
+    } else {
+      for (int64_t j = lane; j < n; j += 32) {
+        const float x = dstbase[rb + j];
+        dstbase[rb + j] = DECODE ? __fadd_rn(x, lowrank(j)) : __fsub_rn(x, lowrank(j));
+      }
+    }
+  }
+}
+
+// ============================================================================ host
+
+struct PsTotals {
+  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, maxel = 0;
+};
+
+static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* z) {
+  if (!h || h->num_tensors < 1 || !h->start || !h->rows || !h->cols) return GC_ERR_INVALID_ARG;
+  if (rank != 1 && rank != 2 && rank != 4) return GC_ERR_INVALID_ARG;
+  for (int t = 0; t < h->num_tensors; ++t) {
+    const int64_t m = h->rows[t], n = h->cols[t];
+    if (m < 1 || n < 1 || h->start[t] < 0 || m > (INT64_C(1) << 40) / n) return GC_ERR_LAYOUT;
+    const int64_t rc = (m + PS_RC - 1) / PS_RC;
+    z->M += m;
+    z->N += n;
+    z->Tiles += rc * ((n + PS_CC - 1) / PS_CC);
+    z->Parts += rc * n;
+  }
+  return GC_OK;
+}
+
+struct PsCarve {
+  size_t o_row, o_col, o_tile, o_part_off, o_part, total;
+};
+
+static PsCarve ps_carve(int T, int R, const PsTotals& z) {
+  PsCarve c;
+  size_t p = DIAG_BYTES;
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes, 256);
+    return at;
+  };
+  c.o_row = take(8 * (size_t)(T + 1));
+  c.o_col = take(8 * (size_t)(T + 1));
+  c.o_tile = take(8 * (size_t)(T + 1));
+  c.o_part_off = take(8 * (size_t)(T + 1));
+  c.o_part = take(4 * (size_t)z.Parts * R);
+  c.total = p;
+  return c;
+}
+
+template <class K>
+static int ps_grid(K kernel, int64_t warps_of_work) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+  if (per_sm < 1) per_sm = 1;
+  int64_t want = (warps_of_work + 7) / 8;
+  int64_t grid = (int64_t)sms * per_sm;
+  if (grid > want) grid = want;
+  if (grid < 1) grid = 1;
+  return (int)grid;
+}
+
+template <int R>
+static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
+  k_psplan<<<1, 1024, 0, s>>>(A);
+  k_pmq<R><<<ps_grid(k_pmq<R>, A.Mrows), 256, 0, s>>>(A);
+  k_porth<R><<<A.T, 1024, 0, s>>>(A);
+  k_pmtp<R><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
+  k_pres<R, false><<<ps_grid(k_pres<R, false>, A.Mrows), 256, 0, s>>>(A);
+}
+
+static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* host, int32_t rank,
+                          void* ws, size_t ws_bytes, cudaStream_t s, PsArgs* A) {
+  PsTotals z;
+  const gc_status st = ps_validate(host, rank, &z);
+  if (st != GC_OK) return st;
+  if (!dev || !dev->start || !dev->rows || !dev->cols || dev->num_tensors != host->num_tensors)
+    return GC_ERR_INVALID_ARG;
+  const PsCarve c = ps_carve(host->num_tensors, rank, z);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  memset(A, 0, sizeof *A);
+  A->T = host->num_tensors;
+  A->start = dev->start;
+  A->rows = dev->rows;
+  A->cols = dev->cols;
+  A->diag = reinterpret_cast<uint32_t*>(w);
+  A->rowoff = reinterpret_cast<int64_t*>(w + c.o_row);
+  A->coloff = reinterpret_cast<int64_t*>(w + c.o_col);
+  A->tileoff = reinterpret_cast<int64_t*>(w + c.o_tile);
+  A->partoff = reinterpret_cast<int64_t*>(w + c.o_part_off);
+  A->part = reinterpret_cast<float*>(w + c.o_part);
+  A->Mrows = z.M;
+  A->Ncols = z.N;
+  A->Tiles = z.Tiles;
+  A->Parts = z.Parts;
+  if (cudaMemsetAsync(ws, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
+  return GC_OK;
+}
+
+}  // namespace gc
+
+using namespace gc;
+
+extern "C" gc_status gc_powersgd_workspace_size(const gc_matrix_layout* host, int32_t rank,
+                                                size_t* bytes) {
+  if (!bytes) return GC_ERR_INVALID_ARG;
+  PsTotals z;
+  const gc_status st = ps_validate(host, rank, &z);
+  if (st != GC_OK) return st;
+  *bytes = ps_carve(host->num_tensors, rank, z).total;
+  return GC_OK;
+}
+
+extern "C" gc_status gc_powersgd_compress(const gc_matrix_layout* dev, const gc_matrix_layout* host,
+                                          int32_t rank, const float* g, float* e, float* q, float* p,
+                                          float* p_raw, void* workspace, size_t ws_bytes,
+                                          void* stream) {
+  if (!g || !e || !q || !p) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(e) || !aligned16(q) || !aligned16(p)) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PsArgs A;
+  const gc_status st = ps_setup(dev, host, rank, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.g = g;
+  A.e = e;
+  A.q = q;
+  A.p = p;
+  A.p_raw = p_raw;
+  if (rank == 1)
+    ps_launch_compress<1>(A, s);
+  else if (rank == 2)
+    ps_launch_compress<2>(A, s);
+  else
+    ps_launch_compress<4>(A, s);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* dev,
+                                                       const gc_matrix_layout* host, int32_t rank,
+                                                       const float* p, const float* q, float* out,
+                                                       void* workspace, size_t ws_bytes,
+                                                       void* stream) {
+  if (!p || !q || !out) return GC_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(p)) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PsArgs A;
+  const gc_status st = ps_setup(dev, host, rank, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.p = const_cast<float*>(p);
+  A.q = const_cast<float*>(q);
+  A.out = out;
+  k_psplan<<<1, 1024, 0, s>>>(A);
+  if (rank == 1)
+    k_pres<1, true><<<ps_grid(k_pres<1, true>, A.Mrows), 256, 0, s>>>(A);
+  else if (rank == 2)
+    k_pres<2, true><<<ps_grid(k_pres<2, true>, A.Mrows), 256, 0, s>>>(A);
+  else
+    k_pres<4, true><<<ps_grid(k_pres<4, true>, A.Mrows), 256, 0, s>>>(A);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}

@@ -253,6 +253,48 @@ gc_status gc_ef_topk_compress_lazy(const gc_layout* dev, const gc_layout* host, 
 gc_status gc_ef_residual_materialize(const gc_layout* dev, const gc_layout* host, float* e,
                                      gc_residual_desc* rd, void* stream);
 
+/* Matrix layout for PowerSGD: matrix t is row-major rows[t] x cols[t] at
+ * element offset start[t] of the gradient arena (matrices must not overlap;
+ * vectors such as biases are left out and sent some other way). */
+typedef struct gc_matrix_layout {
+  int32_t num_tensors;  /* T >= 1 */
+  const int64_t* start; /* [T] element offset of matrix t */
+  const int64_t* rows;  /* [T] m_t >= 1 */
+  const int64_t* cols;  /* [T] n_t >= 1 */
+} gc_matrix_layout;
+
+/* Workspace bytes for gc_powersgd_compress / _decompress_accumulate. */
+gc_status gc_powersgd_workspace_size(const gc_matrix_layout* host, int32_t rank, size_t* bytes);
+
+/* PowerSGD with error feedback (mbrenndoerfer.com "Gradient Compression",
+ * PowerSGD section: G ~ P Q^T found by power iteration, error feedback on
+ * G - P Q^T; chipfoundryservices.com glossary: rank-4 PowerSGD).  One
+ * warm-started power-iteration step per call, per matrix:
+ *   M = G + E;  P = M Q;  orthonormalize P's columns (modified
+ *   Gram-Schmidt);  Q = M^T P;  E = M - P Q^T.
+ * Sums over rows or columns are reduced in a fixed order (fp32 compensated
+ * partials, fp64 across them); the elementwise steps are single fp32
+ * roundings: s_ij = sum_k P_ik Q_jk accumulated in k order, E = M - s.
+ *   rank: 1, 2 or 4.
+ *   g: device fp32 arena (read);  e: device fp32 arena, residual in/out.
+ *   q: device fp32[sum_t cols[t] * rank], row-major n_t x rank per matrix:
+ *      in, the previous call's Q (warm start; any full-rank start the first
+ *      time); out, this call's Q.
+ *   p: device fp32[sum_t rows[t] * rank] out, orthonormal columns.
+ *   p_raw: device fp32 like p, or NULL: receives P = M Q before
+ *      orthonormalization.
+ * Payload of a call: p and q ((m + n) * rank values per matrix). */
+gc_status gc_powersgd_compress(const gc_matrix_layout* dev, const gc_matrix_layout* host,
+                               int32_t rank, const float* g, float* e, float* q, float* p,
+                               float* p_raw, void* workspace, size_t ws_bytes, void* stream);
+
+/* Receiver of one PowerSGD payload: out += P Q^T per matrix, with the same
+ * fp32 accumulation as the residual (call once per worker, in order). */
+gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* dev,
+                                            const gc_matrix_layout* host, int32_t rank,
+                                            const float* p, const float* q, float* out,
+                                            void* workspace, size_t ws_bytes, void* stream);
+
 /* Size of the scratch array built into libgc for gc_ef_topk_compress_noalloc. */
 #define GC_NOALLOC_MAX_WORKSPACE_BYTES (32u << 20)
 

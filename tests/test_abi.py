@@ -108,3 +108,12 @@ def test_warmup_density_matches_oracle(gc):
             a = gc.warmup_density(step, 10, 0.25, 0.001, kind, 4)
             b = oracle.warmup_density(step, 10, 0.25, 0.001, kind)
             assert a == pytest.approx(b, rel=1e-15, abs=0)
+
+
+def test_powersgd_validation(gc):
+    ml = gc.MatrixLayout([0, 100], [10, 5], [10, 7], device="cpu")
+    out = C.c_size_t()
+    assert gc.lib().gc_powersgd_workspace_size(ml.host(), 4, C.byref(out)) == gc.GC_OK and out.value > 0
+    assert gc.lib().gc_powersgd_workspace_size(ml.host(), 3, C.byref(out)) == gc.GC_ERR_INVALID_ARG
+    bad = gc.MatrixLayout([0], [0], [5], device="cpu")
+    assert gc.lib().gc_powersgd_workspace_size(bad.host(), 1, C.byref(out)) == gc.GC_ERR_LAYOUT

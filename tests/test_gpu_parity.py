@@ -589,3 +589,77 @@ def test_clipped_topk_layouts(gc, flags_name):
             if int8:
                 assert np.array_equal(q.cpu().numpy()[ka:kb], rq) and sc.cpu().numpy()[t] == rs
         assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), f"it {it}: residual"
+
+
+# ----------------------------------------------------------------------------- PowerSGD
+
+PS_SHAPES = [(1, 1), (3, 5), (17, 33), (64, 4096), (300, 1024), (1024, 1000), (2000, 257)]
+
+
+@pytest.mark.parametrize("rank", [1, 2, 4])
+def test_powersgd_steps(gc, rank):
+    """Fixed-order reductions on the GPU vs fp64 in the oracle: P_raw = MQ and
+    Q = M^T P within 2e-6 of sum |M||.| (compensated fp32 partials), the
+    orthonormalized P within 1e-5 given the GPU's P_raw, and the residual
+    E = M - P Q^T bit-exact given the GPU's P and Q; three warm-started calls."""
+    rng = np.random.default_rng(40 + rank)
+    starts, pos = [], 0
+    for i, (m, n) in enumerate(PS_SHAPES):
+        pos += 3 * (i % 2)                      # gaps: some matrices start misaligned
+        starts.append(pos)
+        pos += m * n
+    N = pos
+    ml = gc.MatrixLayout(starts, [s[0] for s in PS_SHAPES], [s[1] for s in PS_SHAPES], device="cuda")
+    Msum, Nsum = int(ml.poff[-1]), int(ml.qoff[-1])
+    e_h = (0.1 * rng.standard_normal(N)).astype(F32)
+    q_h = rng.standard_normal(Nsum * rank).astype(F32)
+    e, q = torch.from_numpy(e_h).cuda(), torch.from_numpy(q_h).cuda()
+    p = torch.empty(Msum * rank, device="cuda")
+    p_raw = torch.empty(Msum * rank, device="cuda")
+    ws = gc.powersgd_workspace(ml, rank)
+    for it in range(3):
+        g_h = rng.standard_normal(N).astype(F32)
+        gc.powersgd_compress(ml, rank, torch.from_numpy(g_h).cuda(), e, q, p, p_raw, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        gp, gpr, gq, ge = p.cpu().numpy(), p_raw.cpu().numpy(), q.cpu().numpy(), e.cpu().numpy()
+        for t, (m, n) in enumerate(PS_SHAPES):
+            a = starts[t]
+            sl = slice(a, a + m * n)
+            ps_ = slice(int(ml.poff[t]) * rank, int(ml.poff[t + 1]) * rank)
+            qs_ = slice(int(ml.qoff[t]) * rank, int(ml.qoff[t + 1]) * rank)
+            Mh = (g_h[sl] + e_h[sl]).reshape(m, n)
+            q_in = q_h[qs_].reshape(n, rank)
+            # step 1: P_raw
+            e1, q1 = e_h[sl].reshape(m, n).copy(), q_in.copy()
+            _, pr_ref = oracle.powersgd_tensor(g_h[sl].reshape(m, n), e1, q1, rank)
+            bound = 2e-6 * (np.abs(Mh).astype(np.float64) @ np.abs(q_in).astype(np.float64)) + 1e-30
+            assert np.all(np.abs(gpr[ps_].reshape(m, rank) - pr_ref) <= bound), f"it {it} matrix {t}: P = MQ"
+            # step 2: Gram-Schmidt given the GPU's P_raw
+            e2, q2 = e_h[sl].reshape(m, n).copy(), q_in.copy()
+            p_ref, _ = oracle.powersgd_tensor(g_h[sl].reshape(m, n), e2, q2, rank,
+                                              p_raw_given=gpr[ps_].reshape(m, rank))
+            assert np.allclose(gp[ps_].reshape(m, rank), p_ref, rtol=0, atol=1e-5), f"it {it} matrix {t}: P orth"
+            # step 3: Q given the GPU's P
+            e3, q3 = e_h[sl].reshape(m, n).copy(), q_in.copy()
+            oracle.powersgd_tensor(g_h[sl].reshape(m, n), e3, q3, rank, p_given=gp[ps_].reshape(m, rank))
+            bound = 2e-6 * (np.abs(Mh).T.astype(np.float64) @ np.abs(gp[ps_].reshape(m, rank)).astype(np.float64)) + 1e-30
+            assert np.all(np.abs(gq[qs_].reshape(n, rank) - q3) <= bound), f"it {it} matrix {t}: Q = M^T P"
+            # step 4: residual given the GPU's P and Q, bit-exact
+            e4, q4 = e_h[sl].reshape(m, n).copy(), q_in.copy()
+            oracle.powersgd_tensor(g_h[sl].reshape(m, n), e4, q4, rank, p_given=gp[ps_].reshape(m, rank),
+                                   q_given=gq[qs_].reshape(n, rank))
+            assert np.array_equal(_bits(ge[sl]), _bits(e4.ravel())), f"it {it} matrix {t}: residual"
+        e_h = ge.copy()           # both sides continue from the same state
+        q_h = gq.copy()
+    # receiver: out += P Q^T, bit-exact
+    base = rng.standard_normal(N).astype(F32)
+    out = torch.from_numpy(base).cuda()
+    gc.powersgd_decompress_accumulate(ml, rank, p, q, out, ws)
+    ref = base.copy()
+    for t, (m, n) in enumerate(PS_SHAPES):
+        sl = slice(starts[t], starts[t] + m * n)
+        blk = ref[sl].reshape(m, n).copy()
+        oracle.powersgd_decode_accumulate(gp[int(ml.poff[t]) * rank:int(ml.poff[t + 1]) * rank].reshape(m, rank),
+                                          gq[int(ml.qoff[t]) * rank:int(ml.qoff[t + 1]) * rank].reshape(n, rank), blk)
+        ref[sl] = blk.ravel()
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))

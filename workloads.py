@@ -29,6 +29,7 @@ class Layout:
     name: str
     sizes: list[int]
     kinds: list[str] = field(default_factory=list)   # "w" (weight-like), "bn", "b"
+    shapes: list = field(default_factory=list)       # (rows, cols) of each tensor; (n,) for vectors
 
     @property
     def num_tensors(self) -> int:
@@ -86,15 +87,16 @@ def resnet50_layout() -> Layout:
 
 def bert_large_layout() -> Layout:
     h, ffn, vocab, layers = 1024, 4096, 30522, 24
-    sizes = [vocab * h, 512 * h, 2 * h, h, h]
+    shapes = [(vocab, h), (512, h), (2, h), (h,), (h,)]
     for _ in range(layers):
         for _ in range(4):                     # query, key, value, attention output
-            sizes += [h * h, h]
-        sizes += [h, h]                        # attention LayerNorm
-        sizes += [ffn * h, ffn, h * ffn, h]    # FFN in / out
-        sizes += [h, h]                        # output LayerNorm
-    sizes += [h * h, h]                        # pooler
-    return Layout("bert_large", sizes, ["w"] * len(sizes))
+            shapes += [(h, h), (h,)]
+        shapes += [(h,), (h,)]                 # attention LayerNorm
+        shapes += [(ffn, h), (ffn,), (h, ffn), (h,)]   # FFN in / out
+        shapes += [(h,), (h,)]                 # output LayerNorm
+    shapes += [(h, h), (h,)]                   # pooler
+    sizes = [int(np.prod(s)) for s in shapes]
+    return Layout("bert_large", sizes, ["w"] * len(sizes), shapes)
 
 
 def gpt2_medium_layout() -> Layout:
@@ -113,13 +115,19 @@ def gpt2_medium_layout() -> Layout:
 
 def llama3_8b_layout() -> Layout:
     d, ffn, layers, vocab, kv = 4096, 14336, 32, 128256, 1024
-    sizes = [vocab * d]
+    shapes = [(vocab, d)]
     for _ in range(layers):
-        sizes += [d * d, kv * d, kv * d, d * d]      # q, k, v, o
-        sizes += [ffn * d, ffn * d, d * ffn]         # gate, up, down
-        sizes += [d, d]                              # two RMSNorm weights
-    sizes += [d, vocab * d]                          # final norm, untied lm_head
-    return Layout("llama3_8b", sizes, ["w"] * len(sizes))
+        shapes += [(d, d), (kv, d), (kv, d), (d, d)]      # q, k, v, o
+        shapes += [(ffn, d), (ffn, d), (d, ffn)]          # gate, up, down
+        shapes += [(d,), (d,)]                            # two RMSNorm weights
+    shapes += [(d,), (vocab, d)]                          # final norm, untied lm_head
+    sizes = [int(np.prod(s)) for s in shapes]
+    return Layout("llama3_8b", sizes, ["w"] * len(sizes), shapes)
+
+
+def matrices_of(layout: Layout):
+    """(tensor index, rows, cols) of the 2-D tensors of a layout with shapes."""
+    return [(t, s[0], s[1]) for t, s in enumerate(layout.shapes) if len(s) == 2]
 
 
 # ----------------------------------------------------------------------------
