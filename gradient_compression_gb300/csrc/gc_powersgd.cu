@@ -16,9 +16,10 @@
 //   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
 //   k_pqred fixed-order sum of the partials -> Q
 //   k_pres  warp per row: E = M - P Q^T
-// Reductions are fp32 Neumaier per thread and fp64 across threads and tiles
-// in a fixed order (deterministic); elementwise steps are single fp32
-// roundings in the order the method states them.
+// Reductions: fp32 partial sums over 4 terms, added into a compensated fp32
+// accumulator per thread, then fp64 across threads and tiles in a fixed
+// order (deterministic); elementwise steps are single fp32 roundings in the
+// order the method states them.
 #include <cstring>
 
 #include "gc_common.cuh"
@@ -118,15 +119,36 @@ struct Nm {
     s = t;
   }
   __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+  // Combine with the same accumulator of lane (lane ^ d): fp32 addition is
+  // commutative and the compensation is symmetric in its operands, so both
+  // partners end with identical values (fixed butterfly order).
+  __device__ __forceinline__ void butterfly(int d) {
+    const float os = __shfl_xor_sync(FULL, s, d);
+    const float oc = __shfl_xor_sync(FULL, c, d);
+    add(os);
+    c = __fadd_rn(c, oc);
+  }
 };
 
+// The R values of row j of Q or P (16- or 8-byte aligned for R = 4, 2).
 template <int R>
 __device__ __forceinline__ void load_row(const float* base, float v[R]) {
+  if (R == 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(base));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if (R == 2) {
+    const float2 x = __ldg(reinterpret_cast<const float2*>(base));
+    v[0] = x.x; v[1] = x.y;
+  } else {
 #pragma unroll
-  for (int k = 0; k < R; ++k) v[k] = __ldg(base + k);
+    for (int k = 0; k < R; ++k) v[k] = __ldg(base + k);
+  }
 }
 
-// M = G + E (stored into E) and P_raw = M Q, one warp per matrix row.
+// M = G + E (stored into E) and P_raw = M Q, one warp per matrix row.  Lane
+// l takes columns l, l + 32, ... (coalesced M, one contiguous Q row each);
+// products are summed in fp32 over 4 columns, then added to a compensated
+// accumulator, then reduced across lanes in fp64 in a fixed order.
 template <int R>
 __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
   if (ps_aborted(A)) return;
@@ -139,43 +161,75 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
     const float* qt = A.q + A.coloff[t] * R;
     Nm acc[R];
     if ((rb & 3) == 0 && (n & 3) == 0) {
+      // 16-byte accesses: lane owns 4 consecutive columns of each 128-column group
       const float4* g4 = reinterpret_cast<const float4*>(A.g + rb);
       float4* e4 = reinterpret_cast<float4*>(A.e + rb);
-      for (int64_t v = lane; v < (n >> 2); v += 32) {
-        const float4 gv = ld_stream(g4 + v);
-        const float4 ev = ld_stream(e4 + v);
-        float4 mv;
-        mv.x = __fadd_rn(gv.x, ev.x);
-        mv.y = __fadd_rn(gv.y, ev.y);
-        mv.z = __fadd_rn(gv.z, ev.z);
-        mv.w = __fadd_rn(gv.w, ev.w);
-        st_stream(e4 + v, mv);
-        const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+      const int64_t nv = n >> 2;
+      for (int64_t v0 = lane; v0 < nv; v0 += 128) {
+        float4 mv[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float qv[R];
-          load_row<R>(qt + (4 * v + c) * R, qv);
+        for (int u = 0; u < 4; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            const float4 gv = ld_stream(g4 + v), ev = ld_stream(e4 + v);
+            mv[u].x = __fadd_rn(gv.x, ev.x);
+            mv[u].y = __fadd_rn(gv.y, ev.y);
+            mv[u].z = __fadd_rn(gv.z, ev.z);
+            mv[u].w = __fadd_rn(gv.w, ev.w);
+            st_stream(e4 + v, mv[u]);
+          }
+        }
 #pragma unroll
-          for (int k = 0; k < R; ++k) acc[k].add(__fmul_rn(mm[c], qv[k]));
+        for (int u = 0; u < 4; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            float qv[4][R];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) load_row<R>(qt + (4 * v + c) * R, qv[c]);
+            const float mm[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+              float part = __fmul_rn(mm[0], qv[0][k]);
+#pragma unroll
+              for (int c = 1; c < 4; ++c) part = __fadd_rn(part, __fmul_rn(mm[c], qv[c][k]));
+              acc[k].add(part);
+            }
+          }
         }
       }
-    } else {
-      for (int64_t j = lane; j < n; j += 32) {
-        const float mv = __fadd_rn(A.g[rb + j], A.e[rb + j]);
-        A.e[rb + j] = mv;
-        float qv[R];
-        load_row<R>(qt + j * R, qv);
+    } else
+    for (int64_t j0 = lane; j0 < n; j0 += 256) {
+      float mv[8], qv[8][R];
 #pragma unroll
-        for (int k = 0; k < R; ++k) acc[k].add(__fmul_rn(mv, qv[k]));
+      for (int u = 0; u < 8; ++u) {
+        const int64_t j = j0 + 32 * u;
+        if (j < n) {
+          mv[u] = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
+          __stcs(A.e + rb + j, mv[u]);
+          load_row<R>(qt + j * R, qv[u]);
+        } else {
+          mv[u] = 0.0f;
+#pragma unroll
+          for (int k = 0; k < R; ++k) qv[u][k] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float part = __fmul_rn(mv[4 * h], qv[4 * h][k]);
+#pragma unroll
+          for (int u = 1; u < 4; ++u) part = __fadd_rn(part, __fmul_rn(mv[4 * h + u], qv[4 * h + u][k]));
+          acc[k].add(part);
+        }
       }
     }
 #pragma unroll
     for (int k = 0; k < R; ++k) {
-      double x = acc[k].value();
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) x += __shfl_xor_sync(FULL, x, d);
+      for (int d = 16; d > 0; d >>= 1) acc[k].butterfly(d);
       if (lane == 0) {
-        const float pv = __double2float_rn(x);
+        const float pv = __double2float_rn(acc[k].value());
         A.p[(A.rowoff[t] + i) * R + k] = pv;
         if (A.p_raw) A.p_raw[(A.rowoff[t] + i) * R + k] = pv;
       }
@@ -225,7 +279,7 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
 // Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
 // thread = 4 consecutive columns.
 template <int R>
-__global__ void __launch_bounds__(256) k_pmtp(PsArgs A) {
+__global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
   if (ps_aborted(A)) return;
   const int64_t tile = blockIdx.x;
   const int t = find_segment(A.tileoff, A.T, tile);
@@ -239,22 +293,43 @@ __global__ void __launch_bounds__(256) k_pmtp(PsArgs A) {
   const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
   Nm acc[4][R];
   if (j0 < n) {
-    for (int64_t i = i0; i < i1; ++i) {
-      const int64_t rb = A.start[t] + i * n;
-      float mm[4];
-      if (vec) {
-        const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
-        mm[0] = mv.x; mm[1] = mv.y; mm[2] = mv.z; mm[3] = mv.w;
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) mm[cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
-      }
-      float pv[R];
-      load_row<R>(P + i * R, pv);
+    for (int64_t ib = i0; ib < i1; ib += 4) {
+      float part[4][R];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int k = 0; k < R; ++k) acc[cc][k].add(__fmul_rn(mm[cc], pv[k]));
+        for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
+      float mm[4][4], pv[4][R];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = ib + u;
+        if (i < i1) {
+          const int64_t rb = A.start[t] + i * n;
+          if (vec) {
+            const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
+            mm[u][0] = mv.x; mm[u][1] = mv.y; mm[u][2] = mv.z; mm[u][3] = mv.w;
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) mm[u][cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
+          }
+          load_row<R>(P + i * R, pv[u]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) mm[u][cc] = 0.0f;
+#pragma unroll
+          for (int k = 0; k < R; ++k) pv[u][k] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int k = 0; k < R; ++k) part[cc][k] = __fadd_rn(part[cc][k], __fmul_rn(mm[u][cc], pv[u][k]));
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
     }
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
@@ -303,35 +378,25 @@ __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
     const float* qt = A.q + A.coloff[t] * R;
     float pv[R];
     load_row<R>(A.p + (A.rowoff[t] + i) * R, pv);
-    auto lowrank = [&](int64_t j) {
-      float qv[R];
-      load_row<R>(qt + j * R, qv);
-      float s = 0.0f;
+    for (int64_t j0 = lane; j0 < n; j0 += 128) {
+      float qv[4][R], x[4];
 #pragma unroll
-      for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[k]));
-      return s;
-    };
-    if ((rb & 3) == 0 && (n & 3) == 0) {
-      float4* d4 = reinterpret_cast<float4*>(dstbase + rb);
-      for (int64_t v = lane; v < (n >> 2); v += 32) {
-        float4 x = ld_stream(d4 + v);
-        if (DECODE) {
-          x.x = __fadd_rn(x.x, lowrank(4 * v + 0));
-          x.y = __fadd_rn(x.y, lowrank(4 * v + 1));
-          x.z = __fadd_rn(x.z, lowrank(4 * v + 2));
-          x.w = __fadd_rn(x.w, lowrank(4 * v + 3));
-        } else {
-          x.x = __fsub_rn(x.x, lowrank(4 * v + 0));
-          x.y = __fsub_rn(x.y, lowrank(4 * v + 1));
-          x.z = __fsub_rn(x.z, lowrank(4 * v + 2));
-          x.w = __fsub_rn(x.w, lowrank(4 * v + 3));
+      for (int u = 0; u < 4; ++u) {
+        const int64_t j = j0 + 32 * u;
+        if (j < n) {
+          load_row<R>(qt + j * R, qv[u]);
+          x[u] = __ldcs(dstbase + rb + j);
         }
-        st_stream(d4 + v, x);
       }
-    } else {
-      for (int64_t j = lane; j < n; j += 32) {
-        const float x = dstbase[rb + j];
-        dstbase[rb + j] = DECODE ? __fadd_rn(x, lowrank(j)) : __fsub_rn(x, lowrank(j));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t j = j0 + 32 * u;
+        if (j < n) {
+          float s = 0.0f;
+#pragma unroll
+          for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[u][k]));
+          __stcs(dstbase + rb + j, DECODE ? __fadd_rn(x[u], s) : __fsub_rn(x[u], s));
+        }
       }
     }
   }
