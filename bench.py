@@ -43,11 +43,11 @@ WORKLOADS = {
     "flat_2p20": (1, 0.001, False, [0], 0),
 }
 CFG, RHO, INT8 = 5, 0.001, True
-# kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan, two
-# sample levels and their selects, the streaming pass, three candidate radix
-# levels plus the full-pass level-1 histogram with their selects, count,
-# scan, write
-LAUNCHES_PER_STEP = 16
+# kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan,
+# the sampled threshold estimate, the streaming pass, the level-1 select,
+# three histogram passes (full-pass level 1, candidate levels 2 and 3) with
+# their selects, count, scan, write
+LAUNCHES_PER_STEP = 13
 # bytes the streaming pass must move per element: read g, read e, write e
 STREAM_BYTES_PER_ELEM = 12
 
