@@ -50,6 +50,8 @@ CFG, RHO, INT8 = 5, 0.001, True
 LAUNCHES_PER_STEP = 13
 # bytes the streaming pass must move per element: read g, read e, write e
 STREAM_BYTES_PER_ELEM = 12
+# integer multiplies of one Philox4x32-10 word (random-k keys, QSGD rounding)
+IMAD_PER_ELEMENT = 10
 
 
 GRADIENT = {1: "student_t_nu3_x1e-3", 2: "laplace_loguniform_scale", 3: "student_t_nu2.5_x1e-3",
@@ -523,6 +525,18 @@ def run_op(args):
             "roofline": {"bound": "hbm", "kernel": "whole call", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "algorithmic_bytes": algo}, "clocks": clocks}
+    if args.op in ("qsgd", "randk"):
+        # Philox4x32-10 draws one 32-bit word per element: 10 rounds of two
+        # 32x32 -> 64-bit products per block of 4 words, each product an
+        # integer multiply-high and multiply-low, so 10 integer multiplies
+        # per element; the integer multiply-add rate is 64 per SM per clock.
+        sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        imad_peak = sm_count * 64 * mhz * 1e6
+        imad_done = IMAD_PER_ELEMENT * N / (ms * 1e-3)
+        line["alu"] = {"bound": "alu", "unit": "G int-mul/s", "per_element": IMAD_PER_ELEMENT,
+                       "achieved": imad_done / 1e9, "peak": imad_peak / 1e9, "frac": imad_done / imad_peak,
+                       "peak_from": "%d SMs x 64 per clock x %.0f MHz" % (sm_count, mhz)}
     line.update(extra)
     print(json.dumps(line), flush=True)
 

@@ -133,18 +133,56 @@ __device__ __forceinline__ uint32_t philox_word(uint64_t seed, uint64_t iter, ui
   return uint4_word(philox_block(seed, iter, i >> 2, purpose), (int)(i & 3));
 }
 
+// The ten round keys of a seed, computed once on the host and passed in a
+// kernel's parameters, so that each round XORs them straight from the
+// parameter bank instead of stepping the key in registers.
+struct PhiloxKey {
+  uint32_t k[20];  // k[2r], k[2r + 1]: the two key words of round r
+};
+
+inline PhiloxKey make_philox_key(uint64_t seed) {
+  PhiloxKey K;
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    K.k[2 * r] = k0;
+    K.k[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return K;
+}
+
+__device__ __forceinline__ uint4 philox_block(const PhiloxKey& K, uint64_t iter, uint64_t b, uint32_t purpose) {
+  uint4 c = make_uint4((uint32_t)b, (uint32_t)(b >> 32), (uint32_t)iter, purpose);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    // each 32 x 32 -> 64-bit product in one wide multiply
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k[2 * r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ K.k[2 * r + 1],
+                   (uint32_t)p0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t philox_word(const PhiloxKey& K, uint64_t iter, uint64_t i, uint32_t purpose) {
+  return uint4_word(philox_block(K, iter, i >> 2, purpose), (int)(i & 3));
+}
+
 constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
 // ---------------------------------------------------------------- rounding
-// Stochastic rounding of x >= 0: floor(x) + 1 iff r * 2^-32 < frac(x),
-// decided exactly: F = frac * 2^32 is exact (a power-of-two scaling of an
-// fp32 value below 1), and for an integer r, r < F iff r < ceil(F); since
-// frac <= 1 - 2^-24, ceil(F) <= 2^32 - 256 converts to uint32 exactly.
+// Stochastic rounding of 0 <= x < 2^23: floor(x) + 1 iff r * 2^-32 < frac(x),
+// decided exactly.  x + 2^23 rounded toward zero is 2^23 + floor(x) (the
+// sum's ulp is 1), which gives floor(x) both as an integer (its bit pattern
+// minus that of 2^23) and as a float; frac = x - floor(x) and F = frac * 2^32
+// are exact, and for an integer r, r < F iff r < ceil(F) <= 2^32 - 256.  One
+// float-to-integer conversion per value.
 __device__ __forceinline__ int stochastic_round(float x, uint32_t r) {
-  const float f = floorf(x);
-  const float frac = __fsub_rn(x, f);  // exact
-  const uint32_t c = __float2uint_rz(ceilf(__fmul_rn(frac, 4294967296.0f)));
-  return (int)f + (r < c ? 1 : 0);
+  const float t = __fadd_rz(x, 8388608.0f);
+  const int fl = (int)(__float_as_uint(t) - 0x4B000000u);
+  const float frac = __fsub_rn(x, __fsub_rn(t, 8388608.0f));
+  const uint32_t c = __float2uint_ru(__fmul_rn(frac, 4294967296.0f));
+  return fl + (r < c ? 1 : 0);
 }
 
 // int8 code of x for scale s (s == 0 gives 0).
@@ -156,6 +194,85 @@ __device__ __forceinline__ int int8_code(float x, float s, uint32_t r) {
   m = m > 127 ? 127 : m;
   return signbit(x) ? -m : m;
 }
+
+// Correctly rounded a / b for many a and one b, without a divide per a:
+// with y = RN(1/b), q = RN(a y) is within one ulp of a / b, the remainder
+// a - b q is exact (one FMA), and RN(q + (a - b q) y) is RN(a / b)
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The theorem needs
+// every intermediate in the normal range: b in [2^-125, 2^125], a >= 2^-100
+// and q in [2^-99, 2^125]; anything else takes the IEEE division.  The
+// bounds on a and q come from one per-divisor threshold on a.
+struct Divisor {
+  float b, rb, thr;
+  // qmax: an upper bound of a / b over the values this divisor will see
+  // (the fast path also needs q <= 2^125).  Values a >= thr take the fast
+  // path: then a >= 2^-100 and q >= 2^-98 (1 - 2^-23) > 2^-99.
+  __device__ __forceinline__ Divisor(float b_, float qmax) : b(b_) {
+    const bool fast = b_ >= 0x1p-125f && b_ <= 0x1p125f && qmax <= 0x1p125f;
+    rb = fast ? __frcp_rn(b_) : 0.0f;
+    thr = fast ? fmaxf(0x1p-100f, __fmul_rn(b_, 0x1p-98f)) : __int_as_float(0x7f800000);
+  }
+  // a >= 0
+  __device__ __forceinline__ float div(float a) const {
+    if (a >= thr) {
+      const float q = __fmul_rn(a, rb);
+      return __fmaf_rn(__fmaf_rn(-q, b, a), rb, q);
+    }
+    if (a == 0.0f) return 0.0f;
+    return __fdiv_rn(a, b);
+  }
+};
+
+// ---------------------------------------------------------------- sums
+// Per-lane sum of |x| (P = 1) or x^2 (P = 2) that neither overflows nor
+// underflows in fp32 for any finite x: terms are taken relative to a running
+// power of two 2^E that bounds every |x| seen so far (the scaled sum of
+// squares of LAPACK's xLASSQ, after S. Hammarling), summed with Neumaier
+// compensation, and the sum is rescaled exactly (a power of two) whenever E
+// grows.  A term below 2^-126 of the bound may lose bits; its square is
+// below 2^-252 of the largest square, far under fp64 resolution.
+template <int P>
+struct ScaledSum {
+  float s = 0.0f, c = 0.0f;
+  int E = -125;
+  // mk: max of mag_key over the terms about to be added
+  __device__ __forceinline__ void bound(uint32_t mk) {
+    int eg = (int)(mk >> 24) - 126;  // |x| < 2^eg
+    eg = eg < -125 ? -125 : (eg > 126 ? 126 : eg);
+    if (eg > E) {
+      const int sh = P * (E - eg);
+      if (sh < -120) {
+        s = 0.0f;  // the old terms are below 2^-110 of the new ones
+        c = 0.0f;
+      } else {
+        const float f = __int_as_float((127 + sh) << 23);
+        s = __fmul_rn(s, f);
+        c = __fmul_rn(c, f);
+      }
+      E = eg;
+    }
+  }
+  __device__ __forceinline__ float mult() const { return __int_as_float((127 - E) << 23); }
+  __device__ __forceinline__ void add(float x, float m) {
+    const float y = __fmul_rn(fabsf(x), m);
+    const float v = (P == 2) ? __fmul_rn(y, y) : y;
+    const float t = __fadd_rn(s, v);
+    if (fabsf(s) >= v)
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), v));
+    else
+      c = __fadd_rn(c, __fadd_rn(__fsub_rn(v, t), s));
+    s = t;
+  }
+  // one term at a time (tails)
+  __device__ __forceinline__ void add1(float x) {
+    bound(mag_key(x));
+    add(x, mult());
+  }
+  __device__ __forceinline__ double value() const {
+    return ((double)s + (double)c) * __longlong_as_double((long long)(1023 + P * E) << 52);
+  }
+};
 
 // ---------------------------------------------------------------- lookup
 // Largest t in [0, T) with offs[t] <= x (offs[0] <= x < offs[T]).

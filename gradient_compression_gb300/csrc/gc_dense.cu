@@ -10,8 +10,8 @@
 // Each compressor is two streaming passes over the arena (the per-tensor
 // scale must be known before any code or residual can be written):
 //   pass 1: acc = g (+ e, written back), per-unit partial of sum|acc| or
-//           sum acc^2 (fp32 Neumaier per lane, fp64 across lanes), or the
-//           per-tensor max key (int8)
+//           sum acc^2 (scaled compensated fp32 per lane, fp64 across
+//           lanes), or the per-tensor max key (int8)
 //   reduce: per tensor, unit partials summed in a fixed order in fp64
 //   pass 2: bits / codes and the EF residual
 #include <cmath>
@@ -36,6 +36,7 @@ struct DenseArgs {
   int8_t* codes;
   float* scale;  // mean_abs (sign), max/127 (int8), norm (QSGD)
   uint64_t seed, iter;
+  PhiloxKey pk;       // round keys of seed
   uint32_t* diag;
   uint32_t* maxkey;   // [T]
   int64_t* units_off; // [T+1]
@@ -106,17 +107,6 @@ __global__ void __launch_bounds__(1024) k_dplan(DenseArgs A) {
   }
 }
 
-struct Neumaier {
-  float s = 0.0f, c = 0.0f;
-  __device__ __forceinline__ void add(float x) {
-    const float t = __fadd_rn(s, x);
-    if (fabsf(s) >= fabsf(x))
-      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
-    else
-      c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
-    s = t;
-  }
-};
 
 __device__ __forceinline__ double warp_sum_f64(double v) {
 #pragma unroll
@@ -153,12 +143,11 @@ __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
   for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
     const UnitRef r = unit_ref(A, u);
     const int64_t g0 = r.base + r.lstart;
-    Neumaier acc_sum;
+    ScaledSum<OP == DOP_QSGD ? 2 : 1> acc_sum;  // sign: sum |acc|; QSGD: sum acc^2
     uint32_t mx = 0u;
-    auto take = [&](float x) {
-      if (OP == DOP_SIGN) acc_sum.add(fabsf(x));
-      else if (OP == DOP_QSGD) acc_sum.add(__fmul_rn(x, x));
-      else mx = max(mx, mag_key(x));
+    auto take1 = [&](float x) {
+      if (OP == DOP_INT8) mx = max(mx, mag_key(x));
+      else acc_sum.add1(x);
     };
     if ((g0 & 3) == 0) {
       const int nv = r.len >> 2;
@@ -169,24 +158,37 @@ __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int vi = v0 + 32 * j + (int)lane;
+          x[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           if (vi < nv) {
             x[j] = ld_stream(g4 + vi);
             if (EF) y[j] = ld_stream(e4 + vi);
           }
         }
+        uint32_t km = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int vi = v0 + 32 * j + (int)lane;
-          if (vi < nv) {
-            float4 a = x[j];
-            if (EF) {
-              a.x = __fadd_rn(a.x, y[j].x);
-              a.y = __fadd_rn(a.y, y[j].y);
-              a.z = __fadd_rn(a.z, y[j].z);
-              a.w = __fadd_rn(a.w, y[j].w);
-              st_stream(e4 + vi, a);
-            }
-            take(a.x); take(a.y); take(a.z); take(a.w);
+          if (vi < nv && EF) {
+            x[j].x = __fadd_rn(x[j].x, y[j].x);
+            x[j].y = __fadd_rn(x[j].y, y[j].y);
+            x[j].z = __fadd_rn(x[j].z, y[j].z);
+            x[j].w = __fadd_rn(x[j].w, y[j].w);
+            st_stream(e4 + vi, x[j]);
+          }
+          km = max(km, max(max(mag_key(x[j].x), mag_key(x[j].y)), max(mag_key(x[j].z), mag_key(x[j].w))));
+        }
+        if (OP == DOP_INT8) {
+          mx = max(mx, km);
+        } else {
+          // slots past the end hold zeros, which add nothing
+          acc_sum.bound(km);
+          const float m = acc_sum.mult();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc_sum.add(x[j].x, m);
+            acc_sum.add(x[j].y, m);
+            acc_sum.add(x[j].z, m);
+            acc_sum.add(x[j].w, m);
           }
         }
       }
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
           a = __fadd_rn(a, A.e[gi]);
           A.e[gi] = a;
         }
-        take(a);
+        take1(a);
       }
     } else {
       for (int i = (int)lane; i < r.len; i += 32) {
@@ -208,14 +210,14 @@ __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
           a = __fadd_rn(a, A.e[gi]);
           A.e[gi] = a;
         }
-        take(a);
+        take1(a);
       }
     }
     if (OP == DOP_INT8) {
       mx = warp_max_u32(mx);
       if (lane == 0) atomicMax(A.maxkey + r.t, mx);
     } else {
-      const double part = warp_sum_f64((double)acc_sum.s + (double)acc_sum.c);
+      const double part = warp_sum_f64(acc_sum.value());
       if (lane == 0) A.upart[u] = part;
     }
   }
@@ -246,17 +248,26 @@ __global__ void __launch_bounds__(256) k_dreduce(DenseArgs A) {
 }
 
 // Code of x for the dense quantizers; with DEC, *dec receives the decoded
-// value (needed only for the EF residual).
-template <int OP, bool DEC>
-__device__ __forceinline__ int dense_code(float x, float sc, int s_levels, uint32_t r, float* dec) {
+// value (needed only for the EF residual).  dv divides by the tensor's scale;
+// NZ: the caller has checked that the scale is not zero.
+template <int OP, bool DEC, bool NZ = false>
+__device__ __forceinline__ int dense_code(float x, const Divisor& dv, int s_levels, uint32_t r, float* dec) {
+  const float sc = dv.b;
   if (OP == DOP_INT8) {
-    const int c = int8_code(x, sc, r);
+    int c = 0;
+    if (NZ || sc != 0.0f) {
+      // |x| <= max|acc| keeps |x| / s near 127; the clamp (which cannot
+      // change min(127, .)) only guards the float -> int conversion
+      c = stochastic_round(fminf(dv.div(fabsf(x)), 128.0f), r);
+      c = c > 127 ? 127 : c;
+      c = signbit(x) ? -c : c;
+    }
     if (DEC) *dec = __fmul_rn((float)c, sc);
     return c;
   }
   int level = 0;
-  if (sc != 0.0f) {
-    float y = __fdiv_rn(__fmul_rn(fabsf(x), (float)s_levels), sc);
+  if (NZ || sc != 0.0f) {
+    float y = dv.div(__fmul_rn(fabsf(x), (float)s_levels));
     y = fminf(y, (float)s_levels + 1.0f);
     level = min(s_levels, stochastic_round(y, r));
   }
@@ -357,7 +368,7 @@ __global__ void __launch_bounds__(DTHREADS) k_sign_lazy(DenseArgs A, const float
     const float mp = PREV ? prev_mu[r.t] : 0.0f;
     uint32_t* wbase = A.bits + A.woff[r.t] + (r.lstart >> 5);
     const int nwords = (r.len + 31) >> 5;
-    Neumaier sum;
+    ScaledSum<1> sum;
     auto acc_of = [&](float gv, float ev) {
       if (PREV) ev = __fsub_rn(ev, signbit(ev) ? -mp : mp);
       return __fadd_rn(gv, ev);
@@ -385,17 +396,19 @@ __global__ void __launch_bounds__(DTHREADS) k_sign_lazy(DenseArgs A, const float
               st_stream(e4 + vi, a);
               nib = (signbit(a.x) ? 0u : 1u) | (signbit(a.y) ? 0u : 2u) | (signbit(a.z) ? 0u : 4u) |
                     (signbit(a.w) ? 0u : 8u);
-              sum.add(fabsf(a.x));
-              sum.add(fabsf(a.y));
-              sum.add(fabsf(a.z));
-              sum.add(fabsf(a.w));
+              sum.bound(max(max(mag_key(a.x), mag_key(a.y)), max(mag_key(a.z), mag_key(a.w))));
+              const float m = sum.mult();
+              sum.add(a.x, m);
+              sum.add(a.y, m);
+              sum.add(a.z, m);
+              sum.add(a.w, m);
             } else {
               for (int j = 0; li + j < r.len; ++j) {
                 const int64_t gi = g0 + li + j;
                 const float a = acc_of(A.g[gi], A.e[gi]);
                 A.e[gi] = a;
                 if (!signbit(a)) nib |= 1u << j;
-                sum.add(fabsf(a));
+                sum.add1(a);
               }
             }
           }
@@ -417,13 +430,13 @@ __global__ void __launch_bounds__(DTHREADS) k_sign_lazy(DenseArgs A, const float
         if (valid) {
           a = acc_of(A.g[g0 + i], A.e[g0 + i]);
           A.e[g0 + i] = a;
-          sum.add(fabsf(a));
+          sum.add1(a);
         }
         const unsigned w = __ballot_sync(FULL, valid && !signbit(a));
         if (lane == 0) wbase[i0 >> 5] = w;
       }
     }
-    const double part = warp_sum_f64((double)sum.s + (double)sum.c);
+    const double part = warp_sum_f64(sum.value());
     if (lane == 0) A.upart[u] = part;
   }
 }
@@ -441,7 +454,29 @@ __global__ void __launch_bounds__(256) k_sign_materialize(const int64_t* off, in
   }
 }
 
-// Pass 2 of the int8 / QSGD quantizers: codes and residual.
+// Pass 2 of the int8 / QSGD quantizers: codes and residual.  A lane takes
+// 4 float4 slots 32 apart per step; in full steps the four Philox blocks are
+// independent chains that the compiler interleaves.
+template <int OP, bool EF, bool NZ = false>
+__device__ __forceinline__ void quant_slot(const DenseArgs& A, const Divisor& dv, float4 x, uint4 rw,
+                                           char4* c4, float4* e4) {
+  float4 d;
+  char4 c;
+  c.x = (signed char)dense_code<OP, EF, NZ>(x.x, dv, A.s_levels, rw.x, &d.x);
+  c.y = (signed char)dense_code<OP, EF, NZ>(x.y, dv, A.s_levels, rw.y, &d.y);
+  c.z = (signed char)dense_code<OP, EF, NZ>(x.z, dv, A.s_levels, rw.z, &d.z);
+  c.w = (signed char)dense_code<OP, EF, NZ>(x.w, dv, A.s_levels, rw.w, &d.w);
+  __stcs(reinterpret_cast<int*>(c4), *reinterpret_cast<int*>(&c));
+  if (EF) {
+    float4 res;
+    res.x = __fsub_rn(x.x, d.x);
+    res.y = __fsub_rn(x.y, d.y);
+    res.z = __fsub_rn(x.z, d.z);
+    res.w = __fsub_rn(x.w, d.w);
+    st_stream(e4, res);
+  }
+}
+
 template <int OP, bool EF>
 __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
   if (aborted(A)) return;
@@ -453,39 +488,42 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
   for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
     const UnitRef r = unit_ref(A, u);
     const int64_t g0 = r.base + r.lstart;
-    const float sc = A.scale[r.t];
+    // |acc| <= ||acc|| gives a / N <= s (QSGD); |acc| <= max|acc| gives |acc| / s <= 127 (int8)
+    const Divisor dv(A.scale[r.t], 256.0f);
     if ((g0 & 3) == 0) {
       const int nv = r.len >> 2;
       const float4* s4 = reinterpret_cast<const float4*>(src + g0);
       float4* e4 = reinterpret_cast<float4*>(A.e + g0);
       char4* c4 = reinterpret_cast<char4*>(A.codes + g0);
+      const uint64_t b0 = (uint64_t)(g0 >> 2);
       for (int v0 = 0; v0 < nv; v0 += 128) {
         float4 x[4];
+        if (v0 + 128 <= nv && dv.b == 0.0f) {
+          // zero scale: every code is 0 and the residual stays acc
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int vi = v0 + 32 * j + (int)lane;
-          if (vi < nv) x[j] = ld_stream(s4 + vi);
-        }
+          for (int j = 0; j < 4; ++j) __stcs(reinterpret_cast<int*>(c4 + v0 + 32 * j + (int)lane), 0);
+        } else if (v0 + 128 <= nv) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int vi = v0 + 32 * j + (int)lane;
-          if (vi < nv) {
-            const uint4 rw = philox_block(A.seed, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, purpose);
-            float4 d;
-            char4 c;
-            c.x = (signed char)dense_code<OP, EF>(x[j].x, sc, A.s_levels, rw.x, &d.x);
-            c.y = (signed char)dense_code<OP, EF>(x[j].y, sc, A.s_levels, rw.y, &d.y);
-            c.z = (signed char)dense_code<OP, EF>(x[j].z, sc, A.s_levels, rw.z, &d.z);
-            c.w = (signed char)dense_code<OP, EF>(x[j].w, sc, A.s_levels, rw.w, &d.w);
-            __stcs(reinterpret_cast<int*>(c4 + vi), *reinterpret_cast<int*>(&c));
-            if (EF) {
-              float4 res;
-              res.x = __fsub_rn(x[j].x, d.x);
-              res.y = __fsub_rn(x[j].y, d.y);
-              res.z = __fsub_rn(x[j].z, d.z);
-              res.w = __fsub_rn(x[j].w, d.w);
-              st_stream(e4 + vi, res);
-            }
+          for (int j = 0; j < 4; ++j) x[j] = ld_stream(s4 + v0 + 32 * j + (int)lane);
+          uint4 rw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) rw[j] = philox_block(A.pk, A.iter, b0 + (uint64_t)(v0 + 32 * j + (int)lane), purpose);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int vi = v0 + 32 * j + (int)lane;
+            quant_slot<OP, EF, true>(A, dv, x[j], rw[j], c4 + vi, e4 + vi);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int vi = v0 + 32 * j + (int)lane;
+            if (vi < nv) x[j] = ld_stream(s4 + vi);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int vi = v0 + 32 * j + (int)lane;
+            if (vi < nv) quant_slot<OP, EF>(A, dv, x[j], philox_block(A.pk, A.iter, b0 + (uint64_t)vi, purpose),
+                                            c4 + vi, e4 + vi);
           }
         }
       }
@@ -494,7 +532,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + 4 * nv + lane;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, A.iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     } else {
@@ -502,7 +540,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + i;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, sc, A.s_levels, philox_word(A.seed, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, A.iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     }
@@ -680,6 +718,7 @@ extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layou
   A.codes = codes;
   A.scale = scale;
   A.seed = seed;
+  A.pk = make_philox_key(seed);
   A.iter = iter;
   if (mode == GC_Q_INT8) {
     if (e) launch_quant<DOP_INT8, true>(A, s);

@@ -11,15 +11,17 @@
 // With r <= 4 the products are skinny (about one flop per byte of M), so
 // they are HBM-bound streaming passes on the CUDA cores, not tensor-core
 // GEMMs.  Passes over the matrices:
-//   k_pmq   warp per row: M = G + E (stored into E), P_raw = M Q
-//   k_porth one CTA per matrix: Gram-Schmidt on P (fixed-order fp64 sums)
+//   k_pmq   warp per PS_RB rows: M = G + E (stored into E), P_raw = M Q
+//   k_porth one CTA per matrix: Gram-Schmidt on P (fixed-order sums)
 //   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
 //   k_pqred fixed-order sum of the partials -> Q
 //   k_pres  warp per row: E = M - P Q^T
-// Reductions: fp32 partial sums over 4 terms, added into a compensated fp32
-// accumulator per thread, then fp64 across threads and tiles in a fixed
-// order (deterministic); elementwise steps are single fp32 roundings in the
-// order the method states them.
+// Reductions: fused multiply-add partial sums in fp32 over a few terms,
+// added into a compensated fp32 accumulator per thread, then combined across
+// lanes, warps and tiles by compensated fp32 additions in a fixed order
+// (deterministic; no fp64 arithmetic, which is slow on this part);
+// elementwise steps are single fp32 roundings in the order the method
+// states them.
 #include <cstring>
 
 #include "gc_common.cuh"
@@ -29,6 +31,24 @@ namespace gc {
 
 constexpr int PS_RC = 256;   // rows per Q tile
 constexpr int PS_CC = 1024;  // columns per Q tile (256 threads x 4)
+// Launch shapes of the streaming passes (compile-time; the defaults are the
+// measured best on the BERT-large weight matrices).
+#ifndef GC_PS_RB
+#define GC_PS_RB 2
+#endif
+#ifndef GC_PS_CU
+#define GC_PS_CU 1
+#endif
+#ifndef GC_PS_RS
+#define GC_PS_RS 4
+#endif
+#ifndef GC_PS_RESVEC
+#define GC_PS_RESVEC 0
+#endif
+constexpr int PS_RB = GC_PS_RB;        // rows per warp in P = M Q
+constexpr int PS_CU = GC_PS_CU;        // 128-column groups per step in P = M Q
+constexpr int PS_RS = GC_PS_RS;        // rows per step in M^T P
+constexpr bool PS_RESVEC = GC_PS_RESVEC != 0;  // 16-byte accesses in E = M - P Q^T
 
 struct PsArgs {
   int T;
@@ -46,8 +66,9 @@ struct PsArgs {
   int64_t* coloff;   // [T+1] prefix of n
   int64_t* tileoff;  // [T+1] prefix of Q tiles
   int64_t* partoff;  // [T+1] prefix of ceil(m / PS_RC) * n
+  int64_t* blkoff;   // [T+1] prefix of ceil(m / PS_RB)
   float* part;       // partial column sums, [partoff][R]
-  int64_t Mrows, Ncols, Tiles, Parts;
+  int64_t Mrows, Ncols, Tiles, Parts, Blocks;
 };
 
 __device__ __forceinline__ bool ps_aborted(const PsArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
@@ -57,11 +78,11 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  int64_t carry[4] = {0, 0, 0, 0};
-  int64_t* outs[4] = {A.rowoff, A.coloff, A.tileoff, A.partoff};
+  int64_t carry[5] = {0, 0, 0, 0, 0};
+  int64_t* outs[5] = {A.rowoff, A.coloff, A.tileoff, A.partoff, A.blkoff};
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
-    int64_t v[4] = {0, 0, 0, 0};
+    int64_t v[5] = {0, 0, 0, 0, 0};
     if (t < A.T) {
       const int64_t m = A.rows[t], n = A.cols[t];
       if (m < 1 || n < 1 || A.start[t] < 0) s_bad = 1;
@@ -70,8 +91,9 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
       v[1] = n;
       v[2] = rc * ((n + PS_CC - 1) / PS_CC);
       v[3] = rc * n;
+      v[4] = (m + PS_RB - 1) / PS_RB;
     }
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 5; ++w) {
       const unsigned lane = lane_id(), wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
       int64_t x = v[w];
 #pragma unroll
@@ -100,8 +122,9 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 0; w < 4; ++w) outs[w][A.T] = carry[w];
-    if (s_bad || carry[0] != A.Mrows || carry[1] != A.Ncols || carry[2] != A.Tiles || carry[3] != A.Parts) {
+    for (int w = 0; w < 5; ++w) outs[w][A.T] = carry[w];
+    if (s_bad || carry[0] != A.Mrows || carry[1] != A.Ncols || carry[2] != A.Tiles || carry[3] != A.Parts ||
+        carry[4] != A.Blocks) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -118,7 +141,9 @@ struct Nm {
       c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
     s = t;
   }
-  __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+  // RN(s + c): the sum rounded once to fp32 (no fp64 arithmetic, which is
+  // slow on this part)
+  __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
   // Combine with the same accumulator of lane (lane ^ d): fp32 addition is
   // commutative and the compensation is symmetric in its operands, so both
   // partners end with identical values (fixed butterfly order).
@@ -145,141 +170,254 @@ __device__ __forceinline__ void load_row(const float* base, float v[R]) {
   }
 }
 
-// M = G + E (stored into E) and P_raw = M Q, one warp per matrix row.  Lane
-// l takes columns l, l + 32, ... (coalesced M, one contiguous Q row each);
-// products are summed in fp32 over 4 columns, then added to a compensated
-// accumulator, then reduced across lanes in fp64 in a fixed order.
+// Store row i's P_raw from the lane-distributed accumulators (lane 0 writes).
+template <int R>
+__device__ __forceinline__ void pmq_emit(const PsArgs& A, int t, int64_t i, Nm acc[R], unsigned lane) {
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) acc[k].butterfly(d);
+    if (lane == 0) {
+      const float pv = acc[k].value();
+      A.p[(A.rowoff[t] + i) * R + k] = pv;
+      if (A.p_raw) A.p_raw[(A.rowoff[t] + i) * R + k] = pv;
+    }
+  }
+}
+
+// M = G + E (stored into E) and P_raw = M Q.  A warp takes a block of PS_RB
+// consecutive rows of one matrix; lane l owns 4 consecutive columns of every
+// 128-column group, so each Q row it loads serves all the block's rows.
+// Products are fused multiply-adds summed in fp32 over 8 columns, then
+// added to a compensated accumulator per row, then reduced across lanes (a
+// fixed butterfly) and rounded once to fp32: a fixed order throughout.
+// Matrices with misaligned rows take a scalar path, one row at a time.
 template <int R>
 __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
   if (ps_aborted(A)) return;
   const unsigned lane = lane_id();
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < A.Mrows; gr += nwarps) {
-    const int t = find_segment(A.rowoff, A.T, gr);
-    const int64_t i = gr - A.rowoff[t], n = A.cols[t];
-    const int64_t rb = A.start[t] + i * n;
+  for (int64_t gb = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gb < A.Blocks; gb += nwarps) {
+    const int t = find_segment(A.blkoff, A.T, gb);
+    const int64_t m = A.rows[t], n = A.cols[t];
+    const int64_t i0 = (gb - A.blkoff[t]) * PS_RB;
+    const int nr = (int)min((int64_t)PS_RB, m - i0);
     const float* qt = A.q + A.coloff[t] * R;
-    Nm acc[R];
-    if ((rb & 3) == 0 && (n & 3) == 0) {
-      // 16-byte accesses: lane owns 4 consecutive columns of each 128-column group
-      const float4* g4 = reinterpret_cast<const float4*>(A.g + rb);
-      float4* e4 = reinterpret_cast<float4*>(A.e + rb);
+    if ((A.start[t] & 3) == 0 && (n & 3) == 0) {
+      Nm acc[PS_RB][R];
+      float part[PS_RB][R];
+#pragma unroll
+      for (int r = 0; r < PS_RB; ++r)
+#pragma unroll
+        for (int k = 0; k < R; ++k) part[r][k] = 0.0f;
       const int64_t nv = n >> 2;
-      for (int64_t v0 = lane; v0 < nv; v0 += 128) {
-        float4 mv[4];
+      int half = 0;
+      for (int64_t v0 = lane; v0 < nv; v0 += 32 * PS_CU) {
+        float4 mv[PS_CU][PS_RB];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t v = v0 + 32 * u;
-          if (v < nv) {
-            const float4 gv = ld_stream(g4 + v), ev = ld_stream(e4 + v);
-            mv[u].x = __fadd_rn(gv.x, ev.x);
-            mv[u].y = __fadd_rn(gv.y, ev.y);
-            mv[u].z = __fadd_rn(gv.z, ev.z);
-            mv[u].w = __fadd_rn(gv.w, ev.w);
-            st_stream(e4 + v, mv[u]);
-          }
-        }
+        for (int cu = 0; cu < PS_CU; ++cu) {
+          const int64_t v = v0 + 32 * cu;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t v = v0 + 32 * u;
-          if (v < nv) {
-            float qv[4][R];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) load_row<R>(qt + (4 * v + c) * R, qv[c]);
-            const float mm[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
-#pragma unroll
-            for (int k = 0; k < R; ++k) {
-              float part = __fmul_rn(mm[0], qv[0][k]);
-#pragma unroll
-              for (int c = 1; c < 4; ++c) part = __fadd_rn(part, __fmul_rn(mm[c], qv[c][k]));
-              acc[k].add(part);
+          for (int r = 0; r < PS_RB; ++r) {
+            if (r < nr && v < nv) {
+              const int64_t o = A.start[t] + (i0 + r) * n + 4 * v;
+              const float4 gv = ld_stream(reinterpret_cast<const float4*>(A.g + o));
+              const float4 ev = ld_stream(reinterpret_cast<const float4*>(A.e + o));
+              mv[cu][r].x = __fadd_rn(gv.x, ev.x);
+              mv[cu][r].y = __fadd_rn(gv.y, ev.y);
+              mv[cu][r].z = __fadd_rn(gv.z, ev.z);
+              mv[cu][r].w = __fadd_rn(gv.w, ev.w);
+              st_stream(reinterpret_cast<float4*>(A.e + o), mv[cu][r]);
+            } else {
+              mv[cu][r] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
           }
         }
-      }
-    } else
-    for (int64_t j0 = lane; j0 < n; j0 += 256) {
-      float mv[8], qv[8][R];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t j = j0 + 32 * u;
-        if (j < n) {
-          mv[u] = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
-          __stcs(A.e + rb + j, mv[u]);
-          load_row<R>(qt + j * R, qv[u]);
-        } else {
-          mv[u] = 0.0f;
+        for (int cu = 0; cu < PS_CU; ++cu) {
+          const int64_t v = v0 + 32 * cu;
+          float qv[4][R];
 #pragma unroll
-          for (int k = 0; k < R; ++k) qv[u][k] = 0.0f;
+          for (int c = 0; c < 4; ++c) {
+            if (v < nv) {
+              load_row<R>(qt + (4 * v + c) * R, qv[c]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < R; ++k) qv[c][k] = 0.0f;
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < PS_RB; ++r) {
+            const float mm[4] = {mv[cu][r].x, mv[cu][r].y, mv[cu][r].z, mv[cu][r].w};
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) part[r][k] = __fmaf_rn(mm[c], qv[c][k], part[r][k]);
+          }
+          if (half) {
+#pragma unroll
+            for (int r = 0; r < PS_RB; ++r)
+#pragma unroll
+              for (int k = 0; k < R; ++k) {
+                acc[r][k].add(part[r][k]);
+                part[r][k] = 0.0f;
+              }
+          }
+          half ^= 1;
         }
       }
 #pragma unroll
-      for (int k = 0; k < R; ++k) {
+      for (int r = 0; r < PS_RB; ++r) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float part = __fmul_rn(mv[4 * h], qv[4 * h][k]);
-#pragma unroll
-          for (int u = 1; u < 4; ++u) part = __fadd_rn(part, __fmul_rn(mv[4 * h + u], qv[4 * h + u][k]));
-          acc[k].add(part);
-        }
+        for (int k = 0; k < R; ++k) acc[r][k].add(part[r][k]);
+        if (r < nr) pmq_emit<R>(A, t, i0 + r, acc[r], lane);
       }
-    }
+    } else {
+      for (int r = 0; r < nr; ++r) {
+        const int64_t i = i0 + r;
+        const int64_t rb = A.start[t] + i * n;
+        Nm acc[R];
+        for (int64_t j0 = lane; j0 < n; j0 += 256) {
+          float mv[8], qv[8][R];
 #pragma unroll
-    for (int k = 0; k < R; ++k) {
+          for (int u = 0; u < 8; ++u) {
+            const int64_t j = j0 + 32 * u;
+            if (j < n) {
+              mv[u] = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
+              __stcs(A.e + rb + j, mv[u]);
+              load_row<R>(qt + j * R, qv[u]);
+            } else {
+              mv[u] = 0.0f;
 #pragma unroll
-      for (int d = 16; d > 0; d >>= 1) acc[k].butterfly(d);
-      if (lane == 0) {
-        const float pv = __double2float_rn(acc[k].value());
-        A.p[(A.rowoff[t] + i) * R + k] = pv;
-        if (A.p_raw) A.p_raw[(A.rowoff[t] + i) * R + k] = pv;
+              for (int k = 0; k < R; ++k) qv[u][k] = 0.0f;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < R; ++k) {
+            float part = 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) part = __fmaf_rn(mv[u], qv[u][k], part);
+            acc[k].add(part);
+          }
+        }
+        pmq_emit<R>(A, t, i, acc, lane);
       }
     }
   }
 }
 
-// Sum over the block of per-thread fp64 values, fixed tree; all threads get it.
-__device__ double block_sum_f64(double v, double* sm) {
-  sm[threadIdx.x] = v;
-  __syncthreads();
-  for (int h = blockDim.x >> 1; h > 0; h >>= 1) {
-    if ((int)threadIdx.x < h) sm[threadIdx.x] += sm[threadIdx.x + h];
-    __syncthreads();
-  }
-  const double r = sm[0];
-  __syncthreads();
+// Modified Gram-Schmidt on the columns of P, one CTA of 1024 threads per
+// matrix.  Every reduction is one pass over P's rows, and the update that
+// uses a reduction's result (P_ik -= d P_ij, or P_ik /= nrm) is applied to
+// each row as the next pass reads it: the same per-element operations in the
+// same order as separate update loops.  Per-thread sums are the error-free
+// product (fp32 product plus its exact FMA remainder) added to a compensated
+// fp32 accumulator (Ogita, Rump and Oishi, "Accurate sum and dot product",
+// 2005, Dot2); threads are combined by a fixed compensated butterfly in each
+// warp and then across warps.
+template <int R>
+__device__ __forceinline__ float pick(const float v[R], int k) {
+  float r = v[0];
+#pragma unroll
+  for (int c = 1; c < R; ++c)
+    if (c == k) r = v[c];
   return r;
 }
 
-// Modified Gram-Schmidt on the columns of P (one CTA of 1024 threads per matrix).
+template <int R>
+__device__ __forceinline__ void porth_row(float* row, float v[R], int ukind, int uk, int uj, float uval) {
+  if (R == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(row);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if (R == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(row);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int k = 0; k < R; ++k) v[k] = row[k];
+  }
+  if (ukind != 0) {
+    const float vk = pick<R>(v, uk);
+    const float nv = (ukind == 1) ? __fsub_rn(vk, __fmul_rn(uval, pick<R>(v, uj))) : __fdiv_rn(vk, uval);
+#pragma unroll
+    for (int k = 0; k < R; ++k)
+      if (k == uk) v[k] = nv;
+    row[uk] = nv;
+  }
+}
+
 template <int R>
 __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
-  __shared__ double sm[1024];
+  __shared__ float s_ws[32], s_wc[32];
+  __shared__ float s_tot;
   if (ps_aborted(A)) return;
   const int t = blockIdx.x;
   const int64_t m = A.rows[t];
   float* P = A.p + A.rowoff[t] * R;
+  const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  int ukind = 0, uk = 0, uj = 0;  // pending update: 0 none, 1 P_k -= d P_j, 2 P_k /= nrm
+  float uval = 0.0f;
   for (int k = 0; k < R; ++k) {
-    for (int j = 0; j < k; ++j) {
-      double s = 0.0;
-      for (int64_t i = threadIdx.x; i < m; i += blockDim.x) s += (double)P[i * R + j] * (double)P[i * R + k];
-      const float d = __double2float_rn(block_sum_f64(s, sm));
-      for (int64_t i = threadIdx.x; i < m; i += blockDim.x)
-        P[i * R + k] = __fsub_rn(P[i * R + k], __fmul_rn(d, P[i * R + j]));
+    for (int j = 0; j <= k; ++j) {  // j < k: d = <P_j, P_k>;  j == k: |P_k|^2
+      Nm acc;
+      for (int64_t i0 = threadIdx.x; i0 < m; i0 += 4 * 1024) {
+        float v[4][R];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + 1024 * u;
+          if (i < m) porth_row<R>(P + i * R, v[u], ukind, uk, uj, uval);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + 1024 * u;
+          if (i < m) {
+            const float a = pick<R>(v[u], j), b = pick<R>(v[u], k);
+            const float pr = __fmul_rn(a, b);
+            acc.add(pr);
+            acc.c = __fadd_rn(acc.c, __fmaf_rn(a, b, -pr));
+          }
+        }
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) acc.butterfly(d);
+      if (lane == 0) {
+        s_ws[warp] = acc.s;
+        s_wc[warp] = acc.c;
+      }
       __syncthreads();
+      if (warp == 0) {
+        Nm w;
+        w.s = s_ws[lane];
+        w.c = s_wc[lane];
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) w.butterfly(d);
+        if (lane == 0) s_tot = w.value();
+      }
+      __syncthreads();
+      const float tot = s_tot;
+      __syncthreads();
+      if (j < k) {
+        ukind = 1; uk = k; uj = j; uval = tot;
+      } else {
+        const float nrm = __fsqrt_rn(tot);
+        ukind = nrm > 0.0f ? 2 : 0; uk = k; uval = nrm;
+      }
     }
-    double s = 0.0;
-    for (int64_t i = threadIdx.x; i < m; i += blockDim.x) s += (double)P[i * R + k] * (double)P[i * R + k];
-    const float nrm = __double2float_rn(sqrt(block_sum_f64(s, sm)));
-    if (nrm > 0.0f)
-      for (int64_t i = threadIdx.x; i < m; i += blockDim.x) P[i * R + k] = __fdiv_rn(P[i * R + k], nrm);
-    __syncthreads();
   }
+  if (ukind != 0)
+    for (int64_t i = threadIdx.x; i < m; i += 1024) {
+      float v[R];
+      porth_row<R>(P + i * R, v, ukind, uk, uj, uval);
+    }
 }
 
 // Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
-// thread = 4 consecutive columns.
+// thread = 4 consecutive columns.  PS_RS rows are loaded per step (fused
+// multiply-adds summed in fp32 over those rows, then added to compensated
+// accumulators).
 template <int R>
-__global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
+__global__ void __launch_bounds__(256, PS_RS > 4 ? 2 : 3) k_pmtp(PsArgs A) {
+  constexpr int RS = PS_RS;  // rows per step
   if (ps_aborted(A)) return;
   const int64_t tile = blockIdx.x;
   const int t = find_segment(A.tileoff, A.T, tile);
@@ -293,15 +431,10 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
   const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
   Nm acc[4][R];
   if (j0 < n) {
-    for (int64_t ib = i0; ib < i1; ib += 4) {
-      float part[4][R];
+    for (int64_t ib = i0; ib < i1; ib += RS) {
+      float mm[RS][4], pv[RS][R];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
-      float mm[4][4], pv[4][R];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < RS; ++u) {
         const int64_t i = ib + u;
         if (i < i1) {
           const int64_t rb = A.start[t] + i * n;
@@ -321,27 +454,26 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int k = 0; k < R; ++k) part[cc][k] = __fadd_rn(part[cc][k], __fmul_rn(mm[u][cc], pv[u][k]));
-#pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
+        for (int k = 0; k < R; ++k) {
+          float part = 0.0f;
+#pragma unroll
+          for (int u = 0; u < RS; ++u) part = __fmaf_rn(mm[u][cc], pv[u][k], part);
+          acc[cc][k].add(part);
+        }
     }
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
       if (j0 + cc >= n) break;
       float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
 #pragma unroll
-      for (int k = 0; k < R; ++k) dst[k] = __double2float_rn(acc[cc][k].value());
+      for (int k = 0; k < R; ++k) dst[k] = acc[cc][k].value();
     }
   }
 }
 
-// Q_jk = sum over row tiles of the partials, in tile order (fp64).
+// Q_jk = sum over row tiles of the partials, in tile order (compensated fp32).
 template <int R>
 __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
   if (ps_aborted(A)) return;
@@ -350,21 +482,41 @@ __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
     const int t = find_segment(A.coloff, A.T, gc);
     const int64_t j = gc - A.coloff[t], n = A.cols[t];
     const int64_t nc = (A.rows[t] + PS_RC - 1) / PS_RC;
-    double s[R];
+    Nm s[R];
+    const float* src = A.part + (A.partoff[t] + j) * R;
+    int64_t c = 0;
+    for (; c + 8 <= nc; c += 8) {  // eight row tiles' loads in flight, summed in tile order
+      float v[8][R];
 #pragma unroll
-    for (int k = 0; k < R; ++k) s[k] = 0.0;
-    for (int64_t c = 0; c < nc; ++c) {
-      const float* src = A.part + (A.partoff[t] + c * n + j) * R;
+      for (int u = 0; u < 8; ++u) load_row<R>(src + (c + u) * n * R, v[u]);
 #pragma unroll
-      for (int k = 0; k < R; ++k) s[k] += (double)src[k];
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int k = 0; k < R; ++k) s[k].add(v[u][k]);
+    }
+    for (; c < nc; ++c) {
+      float v[R];
+      load_row<R>(src + c * n * R, v);
+#pragma unroll
+      for (int k = 0; k < R; ++k) s[k].add(v[k]);
     }
 #pragma unroll
-    for (int k = 0; k < R; ++k) A.q[gc * R + k] = __double2float_rn(s[k]);
+    for (int k = 0; k < R; ++k) A.q[gc * R + k] = s[k].value();
   }
 }
 
 // s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, then
-//   E = M - s (residual) or out += s (receiver); warp per row.
+//   E = M - s (residual) or out += s (receiver); warp per row, lane per
+//   column (each lane's Q row is one 16-byte load, coalesced across the
+//   warp); with PS_RESVEC aligned rows go 4 columns per lane instead.
+template <int R, bool DECODE>
+__device__ __forceinline__ float pres_one(float x, const float pv[R], const float qv[R]) {
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[k]));
+  return DECODE ? __fadd_rn(x, s) : __fsub_rn(x, s);
+}
+
 template <int R, bool DECODE>
 __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
   if (ps_aborted(A)) return;
@@ -378,24 +530,49 @@ __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
     const float* qt = A.q + A.coloff[t] * R;
     float pv[R];
     load_row<R>(A.p + (A.rowoff[t] + i) * R, pv);
-    for (int64_t j0 = lane; j0 < n; j0 += 128) {
-      float qv[4][R], x[4];
+    if (PS_RESVEC && (rb & 3) == 0 && (n & 3) == 0) {
+      float4* d4 = reinterpret_cast<float4*>(dstbase + rb);
+      const int64_t nv = n >> 2;
+      for (int64_t v0 = lane; v0 < nv; v0 += 64) {
+        float4 x[2];
+        float qv[2][4][R];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t j = j0 + 32 * u;
-        if (j < n) {
-          load_row<R>(qt + j * R, qv[u]);
-          x[u] = __ldcs(dstbase + rb + j);
+        for (int u = 0; u < 2; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            x[u] = ld_stream(d4 + v);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) load_row<R>(qt + (4 * v + c) * R, qv[u][c]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int64_t v = v0 + 32 * u;
+          if (v < nv) {
+            float4 y;
+            y.x = pres_one<R, DECODE>(x[u].x, pv, qv[u][0]);
+            y.y = pres_one<R, DECODE>(x[u].y, pv, qv[u][1]);
+            y.z = pres_one<R, DECODE>(x[u].z, pv, qv[u][2]);
+            y.w = pres_one<R, DECODE>(x[u].w, pv, qv[u][3]);
+            st_stream(d4 + v, y);
+          }
         }
       }
+    } else {
+      for (int64_t j0 = lane; j0 < n; j0 += 128) {
+        float qv[4][R], x[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t j = j0 + 32 * u;
-        if (j < n) {
-          float s = 0.0f;
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = j0 + 32 * u;
+          if (j < n) {
+            load_row<R>(qt + j * R, qv[u]);
+            x[u] = __ldcs(dstbase + rb + j);
+          }
+        }
 #pragma unroll
-          for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[u][k]));
-          __stcs(dstbase + rb + j, DECODE ? __fadd_rn(x[u], s) : __fsub_rn(x[u], s));
+        for (int u = 0; u < 4; ++u) {
+          const int64_t j = j0 + 32 * u;
+          if (j < n) __stcs(dstbase + rb + j, pres_one<R, DECODE>(x[u], pv, qv[u]));
         }
       }
     }
@@ -405,7 +582,7 @@ __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
 // ============================================================================ host
 
 struct PsTotals {
-  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, maxel = 0;
+  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, Blocks = 0, maxel = 0;
 };
 
 static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* z) {
@@ -419,12 +596,13 @@ static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* 
     z->N += n;
     z->Tiles += rc * ((n + PS_CC - 1) / PS_CC);
     z->Parts += rc * n;
+    z->Blocks += (m + PS_RB - 1) / PS_RB;
   }
   return GC_OK;
 }
 
 struct PsCarve {
-  size_t o_row, o_col, o_tile, o_part_off, o_part, total;
+  size_t o_row, o_col, o_tile, o_part_off, o_blk, o_part, total;
 };
 
 static PsCarve ps_carve(int T, int R, const PsTotals& z) {
@@ -439,6 +617,7 @@ static PsCarve ps_carve(int T, int R, const PsTotals& z) {
   c.o_col = take(8 * (size_t)(T + 1));
   c.o_tile = take(8 * (size_t)(T + 1));
   c.o_part_off = take(8 * (size_t)(T + 1));
+  c.o_blk = take(8 * (size_t)(T + 1));
   c.o_part = take(4 * (size_t)z.Parts * R);
   c.total = p;
   return c;
@@ -461,7 +640,7 @@ static int ps_grid(K kernel, int64_t warps_of_work) {
 template <int R>
 static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
   k_psplan<<<1, 1024, 0, s>>>(A);
-  k_pmq<R><<<ps_grid(k_pmq<R>, A.Mrows), 256, 0, s>>>(A);
+  k_pmq<R><<<ps_grid(k_pmq<R>, A.Blocks), 256, 0, s>>>(A);
   k_porth<R><<<A.T, 1024, 0, s>>>(A);
   k_pmtp<R><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
   k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
@@ -488,11 +667,13 @@ static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* h
   A->coloff = reinterpret_cast<int64_t*>(w + c.o_col);
   A->tileoff = reinterpret_cast<int64_t*>(w + c.o_tile);
   A->partoff = reinterpret_cast<int64_t*>(w + c.o_part_off);
+  A->blkoff = reinterpret_cast<int64_t*>(w + c.o_blk);
   A->part = reinterpret_cast<float*>(w + c.o_part);
   A->Mrows = z.M;
   A->Ncols = z.N;
   A->Tiles = z.Tiles;
   A->Parts = z.Parts;
+  A->Blocks = z.Blocks;
   if (cudaMemsetAsync(ws, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
   return GC_OK;
 }

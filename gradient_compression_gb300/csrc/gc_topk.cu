@@ -55,6 +55,7 @@ struct TopkArgs {
   int8_t* q;
   float* scale;
   uint64_t seed, iter;
+  PhiloxKey pk;          // round keys of seed
   gc_residual_desc* rd;  // pending-residual descriptors (lazy mode), else null
   const float* tau;      // per-tensor magnitude thresholds (threshold mode), else null
   int64_t* count_out;    // per-tensor kept counts (threshold mode)
@@ -233,7 +234,7 @@ __device__ __forceinline__ const float* value_source(const TopkArgs& A) {
 
 template <int MODE>
 __device__ __forceinline__ uint32_t key_of(const TopkArgs& A, float value, int64_t gi) {
-  if (MODE == MODE_RANDK) return ~philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_RANDK);
+  if (MODE == MODE_RANDK) return ~philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_RANDK);
   return mag_key(value);
 }
 
@@ -291,19 +292,8 @@ __device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64
 
 // ============================================================================ local clipping
 
-struct Neumaier32 {
-  float s = 0.0f, c = 0.0f;
-  __device__ __forceinline__ void add(float x) {
-    const float t = __fadd_rn(s, x);
-    if (fabsf(s) >= fabsf(x))
-      c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
-    else
-      c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
-    s = t;
-  }
-};
 
-// Per-unit partial sums of g^2 (fp32 Neumaier per lane, fp64 across lanes).
+// Per-unit partial sums of g^2 (scaled compensated fp32 per lane, fp64 across lanes).
 __global__ void __launch_bounds__(256) k_gnorm(TopkArgs A) {
   if (aborted(A)) return;
   const unsigned lane = lane_id();
@@ -314,28 +304,36 @@ __global__ void __launch_bounds__(256) k_gnorm(TopkArgs A) {
     const int64_t lstart = (u - A.units_off[t]) << UNIT_SHIFT;
     const int len = (int)min((int64_t)UNIT, n - lstart);
     const int64_t g0 = base + lstart;
-    Neumaier32 acc;
+    ScaledSum<2> acc;
     if ((g0 & 3) == 0) {
       const int nv = len >> 2;
       const float4* g4 = reinterpret_cast<const float4*>(A.g + g0);
-      for (int vi = (int)lane; vi < nv; vi += 32) {
-        const float4 x = ld_stream(g4 + vi);
-        acc.add(__fmul_rn(x.x, x.x));
-        acc.add(__fmul_rn(x.y, x.y));
-        acc.add(__fmul_rn(x.z, x.z));
-        acc.add(__fmul_rn(x.w, x.w));
+      for (int v0 = 0; v0 < nv; v0 += 128) {
+        float4 x[4];
+        uint32_t km = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int vi = v0 + 32 * j + (int)lane;
+          x[j] = vi < nv ? ld_stream(g4 + vi) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          km = max(km, max(max(mag_key(x[j].x), mag_key(x[j].y)), max(mag_key(x[j].z), mag_key(x[j].w))));
+        acc.bound(km);
+        const float m = acc.mult();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // zeros past the end add nothing
+          acc.add(x[j].x, m);
+          acc.add(x[j].y, m);
+          acc.add(x[j].z, m);
+          acc.add(x[j].w, m);
+        }
       }
-      if ((int)lane < (len & 3)) {
-        const float x = A.g[g0 + 4 * nv + lane];
-        acc.add(__fmul_rn(x, x));
-      }
+      if ((int)lane < (len & 3)) acc.add1(A.g[g0 + 4 * nv + lane]);
     } else {
-      for (int i = (int)lane; i < len; i += 32) {
-        const float x = A.g[g0 + i];
-        acc.add(__fmul_rn(x, x));
-      }
+      for (int i = (int)lane; i < len; i += 32) acc.add1(A.g[g0 + i]);
     }
-    double part = (double)acc.s + (double)acc.c;
+    double part = acc.value();
 #pragma unroll
     for (int dd = 16; dd > 0; dd >>= 1) part += __shfl_xor_sync(FULL, part, dd);
     if (lane == 0) A.upart[u] = part;
@@ -700,17 +698,25 @@ __device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t li, int
     }
   }
   *value = x;
-  *key = (MODE == MODE_RANDK) ? ~philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_RANDK)
+  *key = (MODE == MODE_RANDK) ? ~philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_RANDK)
                               : mag_key(x);
 }
 
 constexpr int STREAM_THREADS = 256;
 constexpr int STREAM_WARPS = STREAM_THREADS / 32;
-constexpr int STREAM_UNROLL = 4;
+// Loads in flight per lane and resident blocks per SM of the streaming pass
+// (compile-time; defaults measured best on the Llama-3-8B arena).
+#ifndef GC_STREAM_UNROLL
+#define GC_STREAM_UNROLL 2
+#endif
+#ifndef GC_STREAM_MINB
+#define GC_STREAM_MINB 4
+#endif
+constexpr int STREAM_UNROLL = GC_STREAM_UNROLL;
 constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
 
 template <int MODE, bool EF, bool LOADG, bool LAZY>
-__global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_stream(TopkArgs A) {
+__global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? GC_STREAM_MINB : 2) k_stream(TopkArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
@@ -804,7 +810,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? 3 : 2) k_s
           }
           unsigned m = 0u;
           if (MODE == MODE_RANDK) {
-            const uint4 w = philox_block(A.seed, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, PURPOSE_RANDK);
+            const uint4 w = philox_block(A.pk, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, PURPOSE_RANDK);
             kk[0] = ~w.x; kk[1] = ~w.y; kk[2] = ~w.z; kk[3] = ~w.w;
           } else {
 #pragma unroll
@@ -1096,7 +1102,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
   }
   float* res = (MODE == MODE_MOM) ? A.v : ((A.ef && !A.rd) ? A.e : nullptr);
   if (A.int8) {
-    const int c = int8_code(x, s, philox_word(A.seed, A.iter, (uint64_t)gi, PURPOSE_INT8));
+    const int c = int8_code(x, s, philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_INT8));
     const float d = __fmul_rn((float)c, s);
     A.q[pos] = (int8_t)c;
     if (A.val) A.val[pos] = d;
@@ -1398,6 +1404,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.q = q;
   A.scale = scale;
   A.seed = seed;
+  A.pk = make_philox_key(seed);
   A.iter = iter;
   A.rd = rd;
   A.tau = tau;

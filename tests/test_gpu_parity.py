@@ -315,6 +315,99 @@ def test_quantize_zero_tensor(gc):
         _quant_check(gc, L, np.zeros(137, F32), None, mode, s, seed=0, it=0)
 
 
+def _extreme_tensors():
+    """Tensors whose squares (or sums) leave the fp32 range, or whose
+    quotients by the scale are tiny: huge values (norm above 2^125), values
+    near the subnormal range, values spread over 2^-149 .. 2^10, values
+    whose squares underflow fp32, zeros of both signs."""
+    rng = np.random.default_rng(123)
+
+    def signed(x):
+        return np.where(rng.random(x.size) < 0.5, -x, x).astype(F32)
+    parts = [
+        signed(1e36 * rng.uniform(0.5, 1.0, 5001)),             # ||g|| ~ 5e37 > 2^125
+        signed(1e-40 * rng.uniform(0.5, 1.0, 3000)),            # subnormal values, norm < 2^-125
+        signed(np.exp2(rng.uniform(-149, 10, 20000))),          # quotients down to the subnormal range
+        signed(1e-25 * rng.uniform(0.5, 1.0, 7000)),            # squares underflow fp32
+        np.zeros(1, F32),
+        np.concatenate([np.asarray([0.0, -0.0, 1e-45, -1e-45], F32), signed(rng.uniform(0, 1, 29))]),
+        signed(1e30 * rng.standard_t(3, 4100)),                 # heavy tail, squares overflow fp32
+    ]
+    return [p.size for p in parts], np.concatenate(parts).astype(F32)
+
+
+def test_dense_extreme_magnitudes(gc):
+    """Scales and codes stay exact-to-the-oracle where fp32 squares or sums
+    of the values would overflow or underflow, and where the quotient by the
+    scale leaves the range of the fast division."""
+    sizes, g = _extreme_tensors()
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    for mode, s in (("qsgd", 16), ("int8", 0), ("qsgd", 1)):
+        _quant_check(gc, L, g, None, mode, s, seed=13, it=0)
+    _quant_check(gc, L, g, np.zeros_like(g), "qsgd", 16, seed=13, it=1)
+    _sign_check(gc, L, g, np.zeros_like(g))
+    # single-pass sign: the same mean |acc| and bits
+    ws = gc.alloc_workspace(L, gc.GC_OP_SIGN)
+    bits = torch.empty(L.words, dtype=torch.int32, device="cuda")
+    mu = torch.empty(L.T, dtype=torch.float32, device="cuda")
+    gc.sign_compress_lazy(L, torch.from_numpy(g).cuda(), torch.zeros(L.numel, device="cuda"), None, bits, mu, ws)
+    gb, gm = bits.cpu().numpy().view(np.uint32), mu.cpu().numpy()
+    woff = workloads.prefix((np.diff(L.off) + 31) // 32)
+    for t in range(L.T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        _, mu_ref = oracle.sign_tensor(g[a:b], np.zeros(b - a, F32))
+        assert abs(float(gm[t]) - mu_ref) <= REL_TOL * abs(mu_ref), f"lazy sign tensor {t}: mean |acc|"
+        rb, _ = oracle.sign_tensor(g[a:b], np.zeros(b - a, F32), mu_given=float(gm[t]))
+        assert np.array_equal(gb[woff[t]:woff[t + 1]], rb), f"lazy sign tensor {t}: bits"
+
+
+def test_int8_rounding_boundaries(gc):
+    """Dense int8 with max |x| = 127, so the scale is exactly 1 and |x| / s is
+    |x| itself: integers, values just above and below them, fractions that
+    are small multiples of 2^-32, subnormals; codes bit-exact against the
+    oracle (the random words decide against exactly these fractions)."""
+    rng = np.random.default_rng(77)
+    k = rng.integers(0, 127, 2000).astype(np.float64)
+    parts = [np.asarray([127.0]), k, k + 2.0 ** -20, k + 0.5, k + (1 - 2.0 ** -17), k + 2.0 ** -23 * 3,
+             2.0 ** -32 * rng.integers(1, 4096, 1000), np.exp2(rng.uniform(-149, -126, 500)),
+             rng.uniform(0, 127, 3000)]
+    g = np.concatenate(parts).astype(F32)
+    g = np.where(rng.random(g.size) < 0.5, -g, g).astype(F32)
+    g[0] = 127.0
+    L = _layout(gc, [g.size], k=[0])
+    for it in range(3):
+        _quant_check(gc, L, g, None, "int8", 0, seed=21, it=it)
+
+
+def test_clipping_extreme_magnitudes(gc):
+    sizes, g_h = _extreme_tensors()
+    L = _layout(gc, sizes, rho=0.01)
+    n, K, T = L.numel, L.total_k, L.T
+    e_ref = np.zeros(n, F32)
+    e = torch.zeros(n, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    val = torch.empty(K, device="cuda")
+    norm = torch.empty(T, device="cuda")
+    gn = [float(np.linalg.norm(g_h[int(L.off[t]):int(L.off[t + 1])].astype(np.float64))) for t in range(T)]
+    cap = np.asarray([0.5 * x for x in gn], F32)
+    gc.ef_topk_compress_clipped(L, torch.from_numpy(g_h).cuda(), e, torch.from_numpy(cap).cuda(), norm,
+                                idx, val, None, None, 8, 0, gc.GC_EF, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    gi, gv, gno = idx.cpu().numpy(), val.cpu().numpy(), norm.cpu().numpy()
+    for t in range(T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+        _, _, _, _, nref = oracle.clip_topk_tensor(g_h[a:b], e_ref[a:b].copy(), int(L.k[t]), float(cap[t]),
+                                                   base=a, int8=False, seed=8, it=0)
+        assert abs(float(gno[t]) - nref) <= 1e-6 * nref, f"tensor {t}: norm"
+        ri, rv, _, _, _ = oracle.clip_topk_tensor(g_h[a:b], e_ref[a:b], int(L.k[t]), float(cap[t]), base=a,
+                                                  int8=False, seed=8, it=0, norm_given=float(gno[t]))
+        assert np.array_equal(gi[ka:kb], ri), f"tensor {t}: indices"
+        assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"tensor {t}: values"
+    assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), "residual"
+
+
 # ----------------------------------------------------------------------------- receivers
 
 @pytest.mark.parametrize("int8", [False, True])
