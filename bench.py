@@ -376,6 +376,9 @@ def measure_e2e(gc, L, layout, k, g, e, comp, flags, dev, args):
 
 # ---------------------------------------------------------------------------- other rows
 
+# layout name -> generator config of workloads.LAYOUTS
+LAYOUT_CFG = {"resnet50": 2, "bert_large": 3, "gpt2_medium": 4, "llama3_8b": 5}
+
 OPS = {
     # op: (generator config, layout, density, what, algorithmic bytes per element, per kept, per tensor)
     "randk": (2, "resnet50", 0.01, "random-k (Philox keys) with EF", 12, 8, 0),
@@ -398,6 +401,8 @@ def run_op(args):
 
     dev = torch.device("cuda", 0)
     cfg, lname, rho, what, b_elem, b_kept, b_tensor = OPS[args.op]
+    if args.layout:
+        cfg, lname = LAYOUT_CFG[args.layout], args.layout
     layout = workloads.LAYOUTS[cfg]()
     N, T = layout.numel, layout.num_tensors
     k = workloads.k_per_tensor(layout.sizes, rho) if rho else np.zeros(T, np.int64)
@@ -551,6 +556,8 @@ def main():
                     help="the measured workload is llama3_8b; the others are smaller cases for profiling")
     ap.add_argument("--op", choices=("topk",) + tuple(OPS), default="topk",
                     help="topk is the measured headline; the others measure the remaining compression rows")
+    ap.add_argument("--layout", choices=sorted(LAYOUT_CFG), default=None,
+                    help="with --op: run that row on another layout (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -712,7 +712,9 @@ constexpr int STREAM_WARPS = STREAM_THREADS / 32;
 #ifndef GC_STREAM_MINB
 #define GC_STREAM_MINB 4
 #endif
-constexpr int STREAM_UNROLL = GC_STREAM_UNROLL;
+// Top-k (GC_STREAM_UNROLL) or the other modes (4): loads in flight per lane.
+template <int MODE>
+constexpr int stream_unroll() { return MODE == 0 ? GC_STREAM_UNROLL : 4; }
 constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
 
 template <int MODE, bool EF, bool LOADG, bool LAZY>
@@ -745,10 +747,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? GC_STREAM_
       float4* e4 = reinterpret_cast<float4*>(A.e + g0);
       float4* u4 = reinterpret_cast<float4*>(A.u + g0);
       float4* v4 = reinterpret_cast<float4*>(A.v + g0);
-      for (int v0 = 0; v0 < nv; v0 += 32 * STREAM_UNROLL) {
-        float4 x[STREAM_UNROLL], y[STREAM_UNROLL], z[STREAM_UNROLL];
+      constexpr int SU = stream_unroll<MODE>();
+      for (int v0 = 0; v0 < nv; v0 += 32 * SU) {
+        float4 x[SU], y[SU], z[SU];
 #pragma unroll
-        for (int j = 0; j < STREAM_UNROLL; ++j) {
+        for (int j = 0; j < SU; ++j) {
           const int vi = v0 + j * 32 + (int)lane;
           if (vi < nv) {
             if (LOADG || MODE == MODE_MOM) x[j] = ld_stream(g4 + vi);
@@ -761,7 +764,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? GC_STREAM_
           }
         }
 #pragma unroll
-        for (int j = 0; j < STREAM_UNROLL; ++j) {
+        for (int j = 0; j < SU; ++j) {
           const int vi = v0 + j * 32 + (int)lane;
           const bool valid = vi < nv;
           float a[4] = {0.f, 0.f, 0.f, 0.f};
