@@ -42,6 +42,9 @@ constexpr int PS_CC = 1024;  // columns per Q tile (256 threads x 4)
 #ifndef GC_PS_RS
 #define GC_PS_RS 4
 #endif
+#ifndef GC_PS_PMTP_MINB
+#define GC_PS_PMTP_MINB 3
+#endif
 #ifndef GC_PS_RESVEC
 #define GC_PS_RESVEC 0
 #endif
@@ -49,6 +52,10 @@ constexpr int PS_RB = GC_PS_RB;        // rows per warp in P = M Q
 constexpr int PS_CU = GC_PS_CU;        // 128-column groups per step in P = M Q
 constexpr int PS_RS = GC_PS_RS;        // rows per step in M^T P
 constexpr bool PS_RESVEC = GC_PS_RESVEC != 0;  // 16-byte accesses in E = M - P Q^T
+// Terms summed in plain fp32 (fused multiply-adds) before each compensated
+// addition in P = M Q and M^T P: the partial's rounding error is at most
+// (PS_FLUSH - 1) u of the sum of |terms| (u = 2^-24), below 1e-6 of it.
+constexpr int PS_FLUSH = 16;
 
 struct PsArgs {
   int T;
@@ -188,7 +195,7 @@ __device__ __forceinline__ void pmq_emit(const PsArgs& A, int t, int64_t i, Nm a
 // M = G + E (stored into E) and P_raw = M Q.  A warp takes a block of PS_RB
 // consecutive rows of one matrix; lane l owns 4 consecutive columns of every
 // 128-column group, so each Q row it loads serves all the block's rows.
-// Products are fused multiply-adds summed in fp32 over 8 columns, then
+// Products are fused multiply-adds summed in fp32 over PS_FLUSH columns, then
 // added to a compensated accumulator per row, then reduced across lanes (a
 // fixed butterfly) and rounded once to fp32: a fixed order throughout.
 // Matrices with misaligned rows take a scalar path, one row at a time.
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
 #pragma unroll
               for (int c = 0; c < 4; ++c) part[r][k] = __fmaf_rn(mm[c], qv[c][k], part[r][k]);
           }
-          if (half) {
+          if (++half * 4 >= PS_FLUSH) {
 #pragma unroll
             for (int r = 0; r < PS_RB; ++r)
 #pragma unroll
@@ -262,8 +269,8 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
                 acc[r][k].add(part[r][k]);
                 part[r][k] = 0.0f;
               }
+            half = 0;
           }
-          half ^= 1;
         }
       }
 #pragma unroll
@@ -412,11 +419,11 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
 }
 
 // Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
-// thread = 4 consecutive columns.  PS_RS rows are loaded per step (fused
-// multiply-adds summed in fp32 over those rows, then added to compensated
-// accumulators).
+// thread = 4 consecutive columns.  PS_RS rows are loaded per step; fused
+// multiply-adds are summed in fp32 over PS_FLUSH rows, then added to
+// compensated accumulators.
 template <int R>
-__global__ void __launch_bounds__(256, PS_RS > 4 ? 2 : 3) k_pmtp(PsArgs A) {
+__global__ void __launch_bounds__(256, GC_PS_PMTP_MINB) k_pmtp(PsArgs A) {
   constexpr int RS = PS_RS;  // rows per step
   if (ps_aborted(A)) return;
   const int64_t tile = blockIdx.x;
@@ -430,7 +437,13 @@ __global__ void __launch_bounds__(256, PS_RS > 4 ? 2 : 3) k_pmtp(PsArgs A) {
   const float* P = A.p + A.rowoff[t] * R;
   const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
   Nm acc[4][R];
+  float part[4][R];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
   if (j0 < n) {
+    int step = 0;
     for (int64_t ib = i0; ib < i1; ib += RS) {
       float mm[RS][4], pv[RS][R];
 #pragma unroll
@@ -456,13 +469,24 @@ __global__ void __launch_bounds__(256, PS_RS > 4 ? 2 : 3) k_pmtp(PsArgs A) {
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-          float part = 0.0f;
+        for (int k = 0; k < R; ++k)
 #pragma unroll
-          for (int u = 0; u < RS; ++u) part = __fmaf_rn(mm[u][cc], pv[u][k], part);
-          acc[cc][k].add(part);
-        }
+          for (int u = 0; u < RS; ++u) part[cc][k] = __fmaf_rn(mm[u][cc], pv[u][k], part[cc][k]);
+      if (++step * RS >= PS_FLUSH) {  // fp32 partials span PS_FLUSH rows
+        step = 0;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int k = 0; k < R; ++k) {
+            acc[cc][k].add(part[cc][k]);
+            part[cc][k] = 0.0f;
+          }
+      }
     }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+      for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
       if (j0 + cc >= n) break;

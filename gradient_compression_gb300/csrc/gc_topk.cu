@@ -712,13 +712,14 @@ constexpr int STREAM_WARPS = STREAM_THREADS / 32;
 #ifndef GC_STREAM_MINB
 #define GC_STREAM_MINB 4
 #endif
-// Top-k (GC_STREAM_UNROLL) or the other modes (4): loads in flight per lane.
-template <int MODE>
-constexpr int stream_unroll() { return MODE == 0 ? GC_STREAM_UNROLL : 4; }
+// Loads in flight per lane: eager Top-k GC_STREAM_UNROLL; the other modes
+// and the lazy-residual pass (more registers per element) 4.
+template <int MODE, bool LAZY>
+constexpr int stream_unroll() { return (MODE == 0 && !LAZY) ? GC_STREAM_UNROLL : 4; }
 constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
 
 template <int MODE, bool EF, bool LOADG, bool LAZY>
-__global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? GC_STREAM_MINB : 2) k_stream(TopkArgs A) {
+__global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? (LAZY ? 3 : GC_STREAM_MINB) : 2) k_stream(TopkArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
@@ -747,7 +748,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? GC_STREAM_
       float4* e4 = reinterpret_cast<float4*>(A.e + g0);
       float4* u4 = reinterpret_cast<float4*>(A.u + g0);
       float4* v4 = reinterpret_cast<float4*>(A.v + g0);
-      constexpr int SU = stream_unroll<MODE>();
+      constexpr int SU = stream_unroll<MODE, LAZY>();
       for (int v0 = 0; v0 < nv; v0 += 32 * SU) {
         float4 x[SU], y[SU], z[SU];
 #pragma unroll
