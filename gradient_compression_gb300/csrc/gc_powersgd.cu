@@ -11,11 +11,13 @@
 // With r <= 4 the products are skinny (about one flop per byte of M), so
 // they are HBM-bound streaming passes on the CUDA cores, not tensor-core
 // GEMMs.  Passes over the matrices:
-//   k_pmq   warp per PS_RB rows: M = G + E (stored into E), P_raw = M Q
+//   k_pmq   PS_RC x PS_CC tiles, Q^T in shared memory: M = G + E (stored
+//           into E), row partials of P_raw = M Q per column tile
+//   k_ppred fixed-order sum of the row partials -> P_raw
 //   k_porth one CTA per matrix: Gram-Schmidt on P (fixed-order sums)
 //   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
 //   k_pqred fixed-order sum of the partials -> Q
-//   k_pres  warp per row: E = M - P Q^T
+//   k_pres  the same tiles, Q^T staged in shared memory: E = M - P Q^T
 // Reductions: fused multiply-add partial sums in fp32 over a few terms,
 // added into a compensated fp32 accumulator per thread, then combined across
 // lanes, warps and tiles by compensated fp32 additions in a fixed order
@@ -29,29 +31,20 @@
 
 namespace gc {
 
-constexpr int PS_RC = 256;   // rows per Q tile
+#ifndef GC_PS_RC
+#define GC_PS_RC 256
+#endif
+constexpr int PS_RC = GC_PS_RC;  // rows per tile
 constexpr int PS_CC = 1024;  // columns per Q tile (256 threads x 4)
 // Launch shapes of the streaming passes (compile-time; the defaults are the
 // measured best on the BERT-large weight matrices).
-#ifndef GC_PS_RB
-#define GC_PS_RB 2
-#endif
-#ifndef GC_PS_CU
-#define GC_PS_CU 1
-#endif
 #ifndef GC_PS_RS
 #define GC_PS_RS 4
 #endif
 #ifndef GC_PS_PMTP_MINB
 #define GC_PS_PMTP_MINB 3
 #endif
-#ifndef GC_PS_RESVEC
-#define GC_PS_RESVEC 0
-#endif
-constexpr int PS_RB = GC_PS_RB;        // rows per warp in P = M Q
-constexpr int PS_CU = GC_PS_CU;        // 128-column groups per step in P = M Q
 constexpr int PS_RS = GC_PS_RS;        // rows per step in M^T P
-constexpr bool PS_RESVEC = GC_PS_RESVEC != 0;  // 16-byte accesses in E = M - P Q^T
 // Terms summed in plain fp32 (fused multiply-adds) before each compensated
 // addition in P = M Q and M^T P: the partial's rounding error is at most
 // (PS_FLUSH - 1) u of the sum of |terms| (u = 2^-24), below 1e-6 of it.
@@ -73,9 +66,10 @@ struct PsArgs {
   int64_t* coloff;   // [T+1] prefix of n
   int64_t* tileoff;  // [T+1] prefix of Q tiles
   int64_t* partoff;  // [T+1] prefix of ceil(m / PS_RC) * n
-  int64_t* blkoff;   // [T+1] prefix of ceil(m / PS_RB)
-  float* part;       // partial column sums, [partoff][R]
-  int64_t Mrows, Ncols, Tiles, Parts, Blocks;
+  int64_t* ppoff;    // [T+1] prefix of m * ceil(n / PS_CC)
+  float* part;       // partial column sums of M^T P, [partoff][R]
+  float* ppart;      // partial row sums of M Q per column tile, [ppoff][R]
+  int64_t Mrows, Ncols, Tiles, Parts, PParts;
 };
 
 __device__ __forceinline__ bool ps_aborted(const PsArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
@@ -86,7 +80,7 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   int64_t carry[5] = {0, 0, 0, 0, 0};
-  int64_t* outs[5] = {A.rowoff, A.coloff, A.tileoff, A.partoff, A.blkoff};
+  int64_t* outs[5] = {A.rowoff, A.coloff, A.tileoff, A.partoff, A.ppoff};
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
     int64_t v[5] = {0, 0, 0, 0, 0};
@@ -98,7 +92,7 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
       v[1] = n;
       v[2] = rc * ((n + PS_CC - 1) / PS_CC);
       v[3] = rc * n;
-      v[4] = (m + PS_RB - 1) / PS_RB;
+      v[4] = m * ((n + PS_CC - 1) / PS_CC);
     }
     for (int w = 0; w < 5; ++w) {
       const unsigned lane = lane_id(), wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -131,7 +125,7 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   if (threadIdx.x == 0) {
     for (int w = 0; w < 5; ++w) outs[w][A.T] = carry[w];
     if (s_bad || carry[0] != A.Mrows || carry[1] != A.Ncols || carry[2] != A.Tiles || carry[3] != A.Parts ||
-        carry[4] != A.Blocks) {
+        carry[4] != A.PParts) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -177,138 +171,142 @@ __device__ __forceinline__ void load_row(const float* base, float v[R]) {
   }
 }
 
-// Store row i's P_raw from the lane-distributed accumulators (lane 0 writes).
-template <int R>
-__device__ __forceinline__ void pmq_emit(const PsArgs& A, int t, int64_t i, Nm acc[R], unsigned lane) {
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) acc[k].butterfly(d);
-    if (lane == 0) {
-      const float pv = acc[k].value();
-      A.p[(A.rowoff[t] + i) * R + k] = pv;
-      if (A.p_raw) A.p_raw[(A.rowoff[t] + i) * R + k] = pv;
-    }
-  }
-}
-
-// M = G + E (stored into E) and P_raw = M Q.  A warp takes a block of PS_RB
-// consecutive rows of one matrix; lane l owns 4 consecutive columns of every
-// 128-column group, so each Q row it loads serves all the block's rows.
-// Products are fused multiply-adds summed in fp32 over PS_FLUSH columns, then
-// added to a compensated accumulator per row, then reduced across lanes (a
-// fixed butterfly) and rounded once to fp32: a fixed order throughout.
-// Matrices with misaligned rows take a scalar path, one row at a time.
+// M = G + E (stored into E) and partial sums of P_raw = M Q over the tiles
+// of M^T P (PS_RC rows x PS_CC columns).  The tile's Q columns are staged
+// transposed in shared memory; a warp takes a row and a lane 4 consecutive
+// columns of each 128-column group (16-byte g, e and Q^T accesses, four
+// groups of g and e in flight).  Fused multiply-adds are summed in fp32
+// over PS_FLUSH columns into compensated accumulators, reduced across lanes
+// by a fixed butterfly, and lane 0 stores the row's partial for this column
+// tile.  Matrices with misaligned rows go one column per lane.
 template <int R>
 __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
+  constexpr int PG = 4;  // 128-column groups per step: PG * 4 = PS_FLUSH columns per lane
+  static_assert(PG * 4 == PS_FLUSH, "one compensated addition per step");
+  __shared__ __align__(16) float sq[R][PS_CC];
   if (ps_aborted(A)) return;
-  const unsigned lane = lane_id();
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t gb = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gb < A.Blocks; gb += nwarps) {
-    const int t = find_segment(A.blkoff, A.T, gb);
+  for (int64_t tile = blockIdx.x; tile < A.Tiles; tile += gridDim.x) {
+    const int t = find_segment(A.tileoff, A.T, tile);
     const int64_t m = A.rows[t], n = A.cols[t];
-    const int64_t i0 = (gb - A.blkoff[t]) * PS_RB;
-    const int nr = (int)min((int64_t)PS_RB, m - i0);
-    const float* qt = A.q + A.coloff[t] * R;
-    if ((A.start[t] & 3) == 0 && (n & 3) == 0) {
-      Nm acc[PS_RB][R];
-      float part[PS_RB][R];
+    const int64_t nd = (n + PS_CC - 1) / PS_CC;
+    const int64_t local = tile - A.tileoff[t];
+    const int64_t c = local / nd, d = local % nd;
+    const int64_t jb = d * PS_CC;
+    const int cw = (int)min((int64_t)PS_CC, n - jb);
+    const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
+    const float* qt = A.q + (A.coloff[t] + jb) * R;
+    for (int j = threadIdx.x; j < cw; j += blockDim.x) {
+      float v[R];
+      load_row<R>(qt + (int64_t)j * R, v);
 #pragma unroll
-      for (int r = 0; r < PS_RB; ++r)
+      for (int k = 0; k < R; ++k) sq[k][j] = v[k];
+    }
+    __syncthreads();
+    const unsigned lane = lane_id();
+    const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+    const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+    for (int64_t i = i0 + warp; i < i1; i += nwarp) {
+      const int64_t rb = A.start[t] + i * n + jb;
+      Nm acc[R];
+      float part[R];
 #pragma unroll
-        for (int k = 0; k < R; ++k) part[r][k] = 0.0f;
-      const int64_t nv = n >> 2;
-      int half = 0;
-      for (int64_t v0 = lane; v0 < nv; v0 += 32 * PS_CU) {
-        float4 mv[PS_CU][PS_RB];
+      for (int k = 0; k < R; ++k) part[k] = 0.0f;
+      if (vec) {
+        const float4* g4 = reinterpret_cast<const float4*>(A.g + rb);
+        float4* e4 = reinterpret_cast<float4*>(A.e + rb);
+        const int nv = cw >> 2;
+        for (int v0 = (int)lane; v0 < nv; v0 += 32 * PG) {
+          float4 mv[PG];
 #pragma unroll
-        for (int cu = 0; cu < PS_CU; ++cu) {
-          const int64_t v = v0 + 32 * cu;
-#pragma unroll
-          for (int r = 0; r < PS_RB; ++r) {
-            if (r < nr && v < nv) {
-              const int64_t o = A.start[t] + (i0 + r) * n + 4 * v;
-              const float4 gv = ld_stream(reinterpret_cast<const float4*>(A.g + o));
-              const float4 ev = ld_stream(reinterpret_cast<const float4*>(A.e + o));
-              mv[cu][r].x = __fadd_rn(gv.x, ev.x);
-              mv[cu][r].y = __fadd_rn(gv.y, ev.y);
-              mv[cu][r].z = __fadd_rn(gv.z, ev.z);
-              mv[cu][r].w = __fadd_rn(gv.w, ev.w);
-              st_stream(reinterpret_cast<float4*>(A.e + o), mv[cu][r]);
-            } else {
-              mv[cu][r] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
-          }
-        }
-#pragma unroll
-        for (int cu = 0; cu < PS_CU; ++cu) {
-          const int64_t v = v0 + 32 * cu;
-          float qv[4][R];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (v < nv) {
-              load_row<R>(qt + (4 * v + c) * R, qv[c]);
-            } else {
-#pragma unroll
-              for (int k = 0; k < R; ++k) qv[c][k] = 0.0f;
+          for (int u = 0; u < PG; ++u) {
+            const int vi = v0 + 32 * u;
+            mv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (vi < nv) {
+              const float4 gv = ld_stream(g4 + vi), ev = ld_stream(e4 + vi);
+              mv[u].x = __fadd_rn(gv.x, ev.x);
+              mv[u].y = __fadd_rn(gv.y, ev.y);
+              mv[u].z = __fadd_rn(gv.z, ev.z);
+              mv[u].w = __fadd_rn(gv.w, ev.w);
+              st_stream(e4 + vi, mv[u]);
             }
           }
 #pragma unroll
-          for (int r = 0; r < PS_RB; ++r) {
-            const float mm[4] = {mv[cu][r].x, mv[cu][r].y, mv[cu][r].z, mv[cu][r].w};
-#pragma unroll
-            for (int k = 0; k < R; ++k)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) part[r][k] = __fmaf_rn(mm[c], qv[c][k], part[r][k]);
-          }
-          if (++half * 4 >= PS_FLUSH) {
-#pragma unroll
-            for (int r = 0; r < PS_RB; ++r)
+          for (int u = 0; u < PG; ++u) {
+            const int vi = v0 + 32 * u;
+            if (vi < nv) {
 #pragma unroll
               for (int k = 0; k < R; ++k) {
-                acc[r][k].add(part[r][k]);
-                part[r][k] = 0.0f;
+                const float4 qk = *reinterpret_cast<const float4*>(&sq[k][4 * vi]);
+                part[k] = __fmaf_rn(mv[u].x, qk.x, part[k]);
+                part[k] = __fmaf_rn(mv[u].y, qk.y, part[k]);
+                part[k] = __fmaf_rn(mv[u].z, qk.z, part[k]);
+                part[k] = __fmaf_rn(mv[u].w, qk.w, part[k]);
               }
-            half = 0;
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < PS_RB; ++r) {
-#pragma unroll
-        for (int k = 0; k < R; ++k) acc[r][k].add(part[r][k]);
-        if (r < nr) pmq_emit<R>(A, t, i0 + r, acc[r], lane);
-      }
-    } else {
-      for (int r = 0; r < nr; ++r) {
-        const int64_t i = i0 + r;
-        const int64_t rb = A.start[t] + i * n;
-        Nm acc[R];
-        for (int64_t j0 = lane; j0 < n; j0 += 256) {
-          float mv[8], qv[8][R];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int64_t j = j0 + 32 * u;
-            if (j < n) {
-              mv[u] = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
-              __stcs(A.e + rb + j, mv[u]);
-              load_row<R>(qt + j * R, qv[u]);
-            } else {
-              mv[u] = 0.0f;
-#pragma unroll
-              for (int k = 0; k < R; ++k) qv[u][k] = 0.0f;
             }
           }
 #pragma unroll
           for (int k = 0; k < R; ++k) {
-            float part = 0.0f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) part = __fmaf_rn(mv[u], qv[u][k], part);
-            acc[k].add(part);
+            acc[k].add(part[k]);
+            part[k] = 0.0f;
           }
         }
-        pmq_emit<R>(A, t, i, acc, lane);
+      } else {
+        int fl = 0;
+        for (int j = (int)lane; j < cw; j += 32) {
+          const float mvj = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
+          __stcs(A.e + rb + j, mvj);
+#pragma unroll
+          for (int k = 0; k < R; ++k) part[k] = __fmaf_rn(mvj, sq[k][j], part[k]);
+          if (++fl == PS_FLUSH) {
+            fl = 0;
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+              acc[k].add(part[k]);
+              part[k] = 0.0f;
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < R; ++k) acc[k].add(part[k]);
       }
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+#pragma unroll
+        for (int dd = 16; dd > 0; dd >>= 1) acc[k].butterfly(dd);
+      }
+      if (lane == 0) {
+        float* dst = A.ppart + (A.ppoff[t] + i * nd + d) * R;
+#pragma unroll
+        for (int k = 0; k < R; ++k) dst[k] = acc[k].value();
+      }
+    }
+    __syncthreads();  // the next tile restages the shared Q^T
+  }
+}
+
+// P_raw = sum over column tiles of the row partials, in tile order
+// (compensated fp32); thread per row.
+template <int R>
+__global__ void __launch_bounds__(256) k_ppred(PsArgs A) {
+  if (ps_aborted(A)) return;
+  for (int64_t gr = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gr < A.Mrows;
+       gr += (int64_t)gridDim.x * blockDim.x) {
+    const int t = find_segment(A.rowoff, A.T, gr);
+    const int64_t i = gr - A.rowoff[t];
+    const int64_t nd = (A.cols[t] + PS_CC - 1) / PS_CC;
+    const float* src = A.ppart + (A.ppoff[t] + i * nd) * R;
+    Nm s[R];
+    for (int64_t d = 0; d < nd; ++d) {
+      float v[R];
+      load_row<R>(src + d * R, v);
+#pragma unroll
+      for (int k = 0; k < R; ++k) s[k].add(v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      const float pv = s[k].value();
+      A.p[gr * R + k] = pv;
+      if (A.p_raw) A.p_raw[gr * R + k] = pv;
     }
   }
 }
@@ -426,73 +424,74 @@ template <int R>
 __global__ void __launch_bounds__(256, GC_PS_PMTP_MINB) k_pmtp(PsArgs A) {
   constexpr int RS = PS_RS;  // rows per step
   if (ps_aborted(A)) return;
-  const int64_t tile = blockIdx.x;
-  const int t = find_segment(A.tileoff, A.T, tile);
-  const int64_t m = A.rows[t], n = A.cols[t];
-  const int64_t nd = (n + PS_CC - 1) / PS_CC;
-  const int64_t local = tile - A.tileoff[t];
-  const int64_t c = local / nd, d = local % nd;
-  const int64_t j0 = d * PS_CC + 4 * threadIdx.x;
-  const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
-  const float* P = A.p + A.rowoff[t] * R;
-  const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
-  Nm acc[4][R];
-  float part[4][R];
+  for (int64_t tile = blockIdx.x; tile < A.Tiles; tile += gridDim.x) {
+    const int t = find_segment(A.tileoff, A.T, tile);
+    const int64_t m = A.rows[t], n = A.cols[t];
+    const int64_t nd = (n + PS_CC - 1) / PS_CC;
+    const int64_t local = tile - A.tileoff[t];
+    const int64_t c = local / nd, d = local % nd;
+    const int64_t j0 = d * PS_CC + 4 * threadIdx.x;
+    const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
+    const float* P = A.p + A.rowoff[t] * R;
+    const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+    Nm acc[4][R];
+    float part[4][R];
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc)
+    for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-    for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
-  if (j0 < n) {
-    int step = 0;
-    for (int64_t ib = i0; ib < i1; ib += RS) {
-      float mm[RS][4], pv[RS][R];
+      for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
+    if (j0 < n) {
+      int step = 0;
+      for (int64_t ib = i0; ib < i1; ib += RS) {
+        float mm[RS][4], pv[RS][R];
 #pragma unroll
-      for (int u = 0; u < RS; ++u) {
-        const int64_t i = ib + u;
-        if (i < i1) {
-          const int64_t rb = A.start[t] + i * n;
-          if (vec) {
-            const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
-            mm[u][0] = mv.x; mm[u][1] = mv.y; mm[u][2] = mv.z; mm[u][3] = mv.w;
+        for (int u = 0; u < RS; ++u) {
+          const int64_t i = ib + u;
+          if (i < i1) {
+            const int64_t rb = A.start[t] + i * n;
+            if (vec) {
+              const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
+              mm[u][0] = mv.x; mm[u][1] = mv.y; mm[u][2] = mv.z; mm[u][3] = mv.w;
+            } else {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) mm[u][cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
+            }
+            load_row<R>(P + i * R, pv[u]);
           } else {
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) mm[u][cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
+            for (int cc = 0; cc < 4; ++cc) mm[u][cc] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < R; ++k) pv[u][k] = 0.0f;
           }
-          load_row<R>(P + i * R, pv[u]);
-        } else {
+        }
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) mm[u][cc] = 0.0f;
+        for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int k = 0; k < R; ++k) pv[u][k] = 0.0f;
+          for (int k = 0; k < R; ++k)
+#pragma unroll
+            for (int u = 0; u < RS; ++u) part[cc][k] = __fmaf_rn(mm[u][cc], pv[u][k], part[cc][k]);
+        if (++step * RS >= PS_FLUSH) {  // fp32 partials span PS_FLUSH rows
+          step = 0;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+              acc[cc][k].add(part[cc][k]);
+              part[cc][k] = 0.0f;
+            }
         }
       }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-        for (int k = 0; k < R; ++k)
+        for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
 #pragma unroll
-          for (int u = 0; u < RS; ++u) part[cc][k] = __fmaf_rn(mm[u][cc], pv[u][k], part[cc][k]);
-      if (++step * RS >= PS_FLUSH) {  // fp32 partials span PS_FLUSH rows
-        step = 0;
+      for (int cc = 0; cc < 4; ++cc) {
+        if (j0 + cc >= n) break;
+        float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int k = 0; k < R; ++k) {
-            acc[cc][k].add(part[cc][k]);
-            part[cc][k] = 0.0f;
-          }
+        for (int k = 0; k < R; ++k) dst[k] = acc[cc][k].value();
       }
-    }
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-      for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      if (j0 + cc >= n) break;
-      float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
-#pragma unroll
-      for (int k = 0; k < R; ++k) dst[k] = acc[cc][k].value();
     }
   }
 }
@@ -529,10 +528,8 @@ __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
   }
 }
 
-// s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, then
-//   E = M - s (residual) or out += s (receiver); warp per row, lane per
-//   column (each lane's Q row is one 16-byte load, coalesced across the
-//   warp); with PS_RESVEC aligned rows go 4 columns per lane instead.
+// s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, as the method
+// states, then E = M - s (residual) or out += s (receiver).
 template <int R, bool DECODE>
 __device__ __forceinline__ float pres_one(float x, const float pv[R], const float qv[R]) {
   float s = 0.0f;
@@ -541,63 +538,75 @@ __device__ __forceinline__ float pres_one(float x, const float pv[R], const floa
   return DECODE ? __fadd_rn(x, s) : __fsub_rn(x, s);
 }
 
+// E = M - P Q^T (or out += P Q^T) over the same PS_RC x PS_CC tiles as
+// M^T P.  The tile's Q columns are staged transposed in shared memory
+// (Q^T[k][c]), so a lane reads the R values of its 4 consecutive columns
+// with one conflict-free 16-byte load per k; a warp takes a row, and M (or
+// out) moves in 16-byte vectors, four per lane in flight.  Matrices with
+// misaligned rows go one column per lane.
 template <int R, bool DECODE>
 __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
+  constexpr int PG = 4;  // 128-column groups per step
+  __shared__ __align__(16) float sq[R][PS_CC];
   if (ps_aborted(A)) return;
-  const unsigned lane = lane_id();
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t tile = blockIdx.x;
+  const int t = find_segment(A.tileoff, A.T, tile);
+  const int64_t m = A.rows[t], n = A.cols[t];
+  const int64_t nd = (n + PS_CC - 1) / PS_CC;
+  const int64_t local = tile - A.tileoff[t];
+  const int64_t c = local / nd, d = local % nd;
+  const int64_t jb = d * PS_CC;
+  const int cw = (int)min((int64_t)PS_CC, n - jb);
+  const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
+  const float* qt = A.q + (A.coloff[t] + jb) * R;
+  for (int j = threadIdx.x; j < cw; j += blockDim.x) {
+    float v[R];
+    load_row<R>(qt + (int64_t)j * R, v);
+#pragma unroll
+    for (int k = 0; k < R; ++k) sq[k][j] = v[k];
+  }
+  __syncthreads();
   float* dstbase = DECODE ? A.out : A.e;
-  for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < A.Mrows; gr += nwarps) {
-    const int t = find_segment(A.rowoff, A.T, gr);
-    const int64_t i = gr - A.rowoff[t], n = A.cols[t];
-    const int64_t rb = A.start[t] + i * n;
-    const float* qt = A.q + A.coloff[t] * R;
+  const unsigned lane = lane_id();
+  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+  for (int64_t i = i0 + warp; i < i1; i += nwarp) {
+    const int64_t rb = A.start[t] + i * n + jb;
     float pv[R];
     load_row<R>(A.p + (A.rowoff[t] + i) * R, pv);
-    if (PS_RESVEC && (rb & 3) == 0 && (n & 3) == 0) {
+    if (vec) {
       float4* d4 = reinterpret_cast<float4*>(dstbase + rb);
-      const int64_t nv = n >> 2;
-      for (int64_t v0 = lane; v0 < nv; v0 += 64) {
-        float4 x[2];
-        float qv[2][4][R];
+      const int nv = cw >> 2;
+      for (int v0 = (int)lane; v0 < nv; v0 += 32 * PG) {
+        float4 x[PG];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int64_t v = v0 + 32 * u;
-          if (v < nv) {
-            x[u] = ld_stream(d4 + v);
+        for (int u = 0; u < PG; ++u)
+          if (v0 + 32 * u < nv) x[u] = ld_stream(d4 + v0 + 32 * u);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) load_row<R>(qt + (4 * v + c) * R, qv[u][c]);
-          }
-        }
+        for (int u = 0; u < PG; ++u) {
+          const int vi = v0 + 32 * u;
+          if (vi < nv) {
+            float qv[4][R];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int64_t v = v0 + 32 * u;
-          if (v < nv) {
+            for (int k = 0; k < R; ++k) {
+              const float4 qk = *reinterpret_cast<const float4*>(&sq[k][4 * vi]);
+              qv[0][k] = qk.x; qv[1][k] = qk.y; qv[2][k] = qk.z; qv[3][k] = qk.w;
+            }
             float4 y;
-            y.x = pres_one<R, DECODE>(x[u].x, pv, qv[u][0]);
-            y.y = pres_one<R, DECODE>(x[u].y, pv, qv[u][1]);
-            y.z = pres_one<R, DECODE>(x[u].z, pv, qv[u][2]);
-            y.w = pres_one<R, DECODE>(x[u].w, pv, qv[u][3]);
-            st_stream(d4 + v, y);
+            y.x = pres_one<R, DECODE>(x[u].x, pv, qv[0]);
+            y.y = pres_one<R, DECODE>(x[u].y, pv, qv[1]);
+            y.z = pres_one<R, DECODE>(x[u].z, pv, qv[2]);
+            y.w = pres_one<R, DECODE>(x[u].w, pv, qv[3]);
+            st_stream(d4 + vi, y);
           }
         }
       }
     } else {
-      for (int64_t j0 = lane; j0 < n; j0 += 128) {
-        float qv[4][R], x[4];
+      for (int j = (int)lane; j < cw; j += 32) {
+        float qv[R];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t j = j0 + 32 * u;
-          if (j < n) {
-            load_row<R>(qt + j * R, qv[u]);
-            x[u] = __ldcs(dstbase + rb + j);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t j = j0 + 32 * u;
-          if (j < n) __stcs(dstbase + rb + j, pres_one<R, DECODE>(x[u], pv, qv[u]));
-        }
+        for (int k = 0; k < R; ++k) qv[k] = sq[k][j];
+        __stcs(dstbase + rb + j, pres_one<R, DECODE>(__ldcs(dstbase + rb + j), pv, qv));
       }
     }
   }
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
 // ============================================================================ host
 
 struct PsTotals {
-  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, Blocks = 0, maxel = 0;
+  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, PParts = 0, maxel = 0;
 };
 
 static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* z) {
@@ -620,13 +629,13 @@ static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* 
     z->N += n;
     z->Tiles += rc * ((n + PS_CC - 1) / PS_CC);
     z->Parts += rc * n;
-    z->Blocks += (m + PS_RB - 1) / PS_RB;
+    z->PParts += m * ((n + PS_CC - 1) / PS_CC);
   }
   return GC_OK;
 }
 
 struct PsCarve {
-  size_t o_row, o_col, o_tile, o_part_off, o_blk, o_part, total;
+  size_t o_row, o_col, o_tile, o_part_off, o_pp_off, o_part, o_ppart, total;
 };
 
 static PsCarve ps_carve(int T, int R, const PsTotals& z) {
@@ -641,34 +650,37 @@ static PsCarve ps_carve(int T, int R, const PsTotals& z) {
   c.o_col = take(8 * (size_t)(T + 1));
   c.o_tile = take(8 * (size_t)(T + 1));
   c.o_part_off = take(8 * (size_t)(T + 1));
-  c.o_blk = take(8 * (size_t)(T + 1));
+  c.o_pp_off = take(8 * (size_t)(T + 1));
   c.o_part = take(4 * (size_t)z.Parts * R);
+  c.o_ppart = take(4 * (size_t)z.PParts * R);
   c.total = p;
   return c;
 }
 
+// Resident CTAs of a tile kernel: k_pmq and k_pmtp stride over the tiles
+// with a persistent grid (measured no slower than one tile per CTA, and
+// k_pmq 6% faster); k_pres keeps one tile per CTA (the loop costs it
+// registers and 15%).
 template <class K>
-static int ps_grid(K kernel, int64_t warps_of_work) {
+static unsigned ps_tile_grid(K kernel, size_t smem, int64_t tiles) {
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem);
   if (per_sm < 1) per_sm = 1;
-  int64_t want = (warps_of_work + 7) / 8;
-  int64_t grid = (int64_t)sms * per_sm;
-  if (grid > want) grid = want;
-  if (grid < 1) grid = 1;
-  return (int)grid;
+  const int64_t grid = std::min<int64_t>((int64_t)sms * per_sm, tiles);
+  return (unsigned)std::max<int64_t>(grid, 1);
 }
 
 template <int R>
 static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
   k_psplan<<<1, 1024, 0, s>>>(A);
-  k_pmq<R><<<ps_grid(k_pmq<R>, A.Blocks), 256, 0, s>>>(A);
+  k_pmq<R><<<ps_tile_grid(k_pmq<R>, 0, A.Tiles), 256, 0, s>>>(A);
+  k_ppred<R><<<(unsigned)std::min<int64_t>((A.Mrows + 255) / 256, 65535), 256, 0, s>>>(A);
   k_porth<R><<<A.T, 1024, 0, s>>>(A);
-  k_pmtp<R><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  k_pmtp<R><<<ps_tile_grid(k_pmtp<R>, 0, A.Tiles), 256, 0, s>>>(A);
   k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
-  k_pres<R, false><<<ps_grid(k_pres<R, false>, A.Mrows), 256, 0, s>>>(A);
+  k_pres<R, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
 }
 
 static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* host, int32_t rank,
@@ -691,13 +703,14 @@ static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* h
   A->coloff = reinterpret_cast<int64_t*>(w + c.o_col);
   A->tileoff = reinterpret_cast<int64_t*>(w + c.o_tile);
   A->partoff = reinterpret_cast<int64_t*>(w + c.o_part_off);
-  A->blkoff = reinterpret_cast<int64_t*>(w + c.o_blk);
+  A->ppoff = reinterpret_cast<int64_t*>(w + c.o_pp_off);
+  A->ppart = reinterpret_cast<float*>(w + c.o_ppart);
   A->part = reinterpret_cast<float*>(w + c.o_part);
   A->Mrows = z.M;
   A->Ncols = z.N;
   A->Tiles = z.Tiles;
   A->Parts = z.Parts;
-  A->Blocks = z.Blocks;
+  A->PParts = z.PParts;
   if (cudaMemsetAsync(ws, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
   return GC_OK;
 }
@@ -756,10 +769,10 @@ extern "C" gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* d
   A.out = out;
   k_psplan<<<1, 1024, 0, s>>>(A);
   if (rank == 1)
-    k_pres<1, true><<<ps_grid(k_pres<1, true>, A.Mrows), 256, 0, s>>>(A);
+    k_pres<1, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
   else if (rank == 2)
-    k_pres<2, true><<<ps_grid(k_pres<2, true>, A.Mrows), 256, 0, s>>>(A);
+    k_pres<2, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
   else
-    k_pres<4, true><<<ps_grid(k_pres<4, true>, A.Mrows), 256, 0, s>>>(A);
+    k_pres<4, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

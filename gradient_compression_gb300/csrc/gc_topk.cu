@@ -544,7 +544,6 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
     if (phase == PH_C1 && A.rd && threadIdx.x == 0) A.rd[t] = gc_residual_desc{0u, 0u, 0, 0.0f, 0ull, 0ull};
     return;
   }
-  const int64_t k = A.kk[t];
   uint32_t* row = A.hist + (size_t)t * NBINS;
   uint32_t rank = st->rank;
 
