@@ -31,20 +31,10 @@
 
 namespace gc {
 
-#ifndef GC_PS_RC
-#define GC_PS_RC 256
-#endif
-constexpr int PS_RC = GC_PS_RC;  // rows per tile
-constexpr int PS_CC = 1024;  // columns per Q tile (256 threads x 4)
-// Launch shapes of the streaming passes (compile-time; the defaults are the
-// measured best on the BERT-large weight matrices).
-#ifndef GC_PS_RS
-#define GC_PS_RS 4
-#endif
-#ifndef GC_PS_PMTP_MINB
-#define GC_PS_PMTP_MINB 3
-#endif
-constexpr int PS_RS = GC_PS_RS;        // rows per step in M^T P
+// Tiles of the three streaming passes: PS_RC rows x PS_CC columns (256
+// threads x 4 columns); 128-row tiles measured the same as 256.
+constexpr int PS_RC = 256;
+constexpr int PS_CC = 1024;
 // Terms summed in plain fp32 (fused multiply-adds) before each compensated
 // addition in P = M Q and M^T P: the partial's rounding error is at most
 // (PS_FLUSH - 1) u of the sum of |terms| (u = 2^-24), below 1e-6 of it.
@@ -417,81 +407,123 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
 }
 
 // Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
-// thread = 4 consecutive columns.  PS_RS rows are loaded per step; fused
-// multiply-adds are summed in fp32 over PS_FLUSH rows, then added to
-// compensated accumulators.
+// a thread owns 4 consecutive columns.  Aligned matrices stream M through a
+// cp.async pipeline: each thread copies its own 16-byte slice of the next
+// rows into shared memory PT_NS - 1 stages ahead (no registers held for
+// data in flight, no thread reads another's slice), then computes from
+// shared memory.  Fused multiply-adds are summed in fp32 over PS_FLUSH rows,
+// then added to compensated accumulators; the tile's partials go to A.part.
+constexpr int PT_RS = 4;  // rows per stage
+constexpr int PT_NS = 3;  // stages (48 KB of shared memory per CTA)
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
 template <int R>
-__global__ void __launch_bounds__(256, GC_PS_PMTP_MINB) k_pmtp(PsArgs A) {
-  constexpr int RS = PS_RS;  // rows per step
+__device__ __forceinline__ void pmtp_rows(float part[4][R], const float mm[4], const float pv[R]) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int k = 0; k < R; ++k) part[cc][k] = __fmaf_rn(mm[cc], pv[k], part[cc][k]);
+}
+
+template <int R>
+__device__ __forceinline__ void pmtp_flush(Nm acc[4][R], float part[4][R]) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      acc[cc][k].add(part[cc][k]);
+      part[cc][k] = 0.0f;
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
+  __shared__ __align__(16) float4 sbuf[PT_NS * PT_RS * 256];
   if (ps_aborted(A)) return;
+  const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < A.Tiles; tile += gridDim.x) {
     const int t = find_segment(A.tileoff, A.T, tile);
     const int64_t m = A.rows[t], n = A.cols[t];
     const int64_t nd = (n + PS_CC - 1) / PS_CC;
     const int64_t local = tile - A.tileoff[t];
     const int64_t c = local / nd, d = local % nd;
-    const int64_t j0 = d * PS_CC + 4 * threadIdx.x;
+    const int64_t j0 = d * PS_CC + 4 * tid;
     const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
     const float* P = A.p + A.rowoff[t] * R;
     const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+    if (j0 >= n) continue;
     Nm acc[4][R];
     float part[4][R];
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
       for (int k = 0; k < R; ++k) part[cc][k] = 0.0f;
-    if (j0 < n) {
-      int step = 0;
-      for (int64_t ib = i0; ib < i1; ib += RS) {
-        float mm[RS][4], pv[RS][R];
+    if (vec) {
+      const float* ecol = A.e + A.start[t] + j0;  // row i at ecol + i * n, 16-byte aligned
+      const int nsteps = (int)((i1 - i0 + PT_RS - 1) / PT_RS);
+      auto issue = [&](int st) {
+        if (st < nsteps) {
 #pragma unroll
-        for (int u = 0; u < RS; ++u) {
-          const int64_t i = ib + u;
-          if (i < i1) {
-            const int64_t rb = A.start[t] + i * n;
-            if (vec) {
-              const float4 mv = ld_stream(reinterpret_cast<const float4*>(A.e + rb + j0));
-              mm[u][0] = mv.x; mm[u][1] = mv.y; mm[u][2] = mv.z; mm[u][3] = mv.w;
-            } else {
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) mm[u][cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
-            }
-            load_row<R>(P + i * R, pv[u]);
-          } else {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) mm[u][cc] = 0.0f;
-#pragma unroll
-            for (int k = 0; k < R; ++k) pv[u][k] = 0.0f;
+          for (int u = 0; u < PT_RS; ++u) {
+            const int64_t i = i0 + (int64_t)st * PT_RS + u;
+            if (i < i1) cp_async16(&sbuf[((st % PT_NS) * PT_RS + u) * 256 + tid], ecol + i * n);
           }
         }
+        cp_async_commit();
+      };
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+      for (int st = 0; st < PT_NS - 1; ++st) issue(st);
+      int fl = 0;
+      for (int st = 0; st < nsteps; ++st) {
+        issue(st + PT_NS - 1);
+        cp_async_wait<PT_NS - 1>();  // this thread's copies of stage st have landed
 #pragma unroll
-          for (int k = 0; k < R; ++k)
-#pragma unroll
-            for (int u = 0; u < RS; ++u) part[cc][k] = __fmaf_rn(mm[u][cc], pv[u][k], part[cc][k]);
-        if (++step * RS >= PS_FLUSH) {  // fp32 partials span PS_FLUSH rows
-          step = 0;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int k = 0; k < R; ++k) {
-              acc[cc][k].add(part[cc][k]);
-              part[cc][k] = 0.0f;
-            }
+        for (int u = 0; u < PT_RS; ++u) {
+          const int64_t i = i0 + (int64_t)st * PT_RS + u;
+          if (i < i1) {
+            const float4 mv = sbuf[((st % PT_NS) * PT_RS + u) * 256 + tid];
+            const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+            float pv[R];
+            load_row<R>(P + i * R, pv);
+            pmtp_rows<R>(part, mm, pv);
+          }
+        }
+        if (++fl * PT_RS >= PS_FLUSH) {
+          fl = 0;
+          pmtp_flush<R>(acc, part);
         }
       }
+      cp_async_wait<0>();
+    } else {
+      int fl = 0;
+      for (int64_t i = i0; i < i1; ++i) {
+        const int64_t rb = A.start[t] + i * n;
+        float mm[4];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-        for (int k = 0; k < R; ++k) acc[cc][k].add(part[cc][k]);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        if (j0 + cc >= n) break;
-        float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
-#pragma unroll
-        for (int k = 0; k < R; ++k) dst[k] = acc[cc][k].value();
+        for (int cc = 0; cc < 4; ++cc) mm[cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
+        float pv[R];
+        load_row<R>(P + i * R, pv);
+        pmtp_rows<R>(part, mm, pv);
+        if (++fl == PS_FLUSH) {
+          fl = 0;
+          pmtp_flush<R>(acc, part);
+        }
       }
+    }
+    pmtp_flush<R>(acc, part);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      if (j0 + cc >= n) break;
+      float* dst = A.part + (A.partoff[t] + c * n + j0 + cc) * R;
+#pragma unroll
+      for (int k = 0; k < R; ++k) dst[k] = acc[cc][k].value();
     }
   }
 }
