@@ -252,19 +252,27 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
         float4* e4 = reinterpret_cast<float4*>(A.e + rb);
         const int nv = cw >> 2;
         for (int v0 = (int)lane; v0 < nv; v0 += 32 * PG) {
-          float4 mv[PG];
+          // every load of the step is issued before the first store (the
+          // stores to E could alias later loads as far as the compiler knows)
+          float4 mv[PG], ev[PG];
 #pragma unroll
           for (int u = 0; u < PG; ++u) {
             const int vi = v0 + 32 * u;
             mv[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            ev[u] = mv[u];
             if (vi < nv) {
-              const float4 gv = ld_stream(g4 + vi), ev = ld_stream(e4 + vi);
-              mv[u].x = __fadd_rn(gv.x, ev.x);
-              mv[u].y = __fadd_rn(gv.y, ev.y);
-              mv[u].z = __fadd_rn(gv.z, ev.z);
-              mv[u].w = __fadd_rn(gv.w, ev.w);
-              st_stream(e4 + vi, mv[u]);
+              mv[u] = ld_stream(g4 + vi);
+              ev[u] = ld_stream(e4 + vi);
             }
+          }
+#pragma unroll
+          for (int u = 0; u < PG; ++u) {
+            const int vi = v0 + 32 * u;
+            mv[u].x = __fadd_rn(mv[u].x, ev[u].x);
+            mv[u].y = __fadd_rn(mv[u].y, ev[u].y);
+            mv[u].z = __fadd_rn(mv[u].z, ev[u].z);
+            mv[u].w = __fadd_rn(mv[u].w, ev[u].w);
+            if (vi < nv) st_stream(e4 + vi, mv[u]);
           }
 #pragma unroll
           for (int u = 0; u < PG; ++u) {
