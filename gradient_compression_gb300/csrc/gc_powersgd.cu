@@ -14,7 +14,8 @@
 //   k_pmq   PS_RC x PS_CC tiles, Q^T in shared memory: M = G + E (stored
 //           into E), row partials of P_raw = M Q per column tile
 //   k_ppred fixed-order sum of the row partials -> P_raw
-//   k_porth one CTA per matrix: Gram-Schmidt on P (fixed-order sums)
+//   k_porth Gram-Schmidt on P (fixed-order sums): one CTA per matrix, or a
+//           cluster of PORTH_CL CTAs for matrices of more than PORTH_BIG rows
 //   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
 //   k_pqred fixed-order sum of the partials -> Q
 //   k_pres  the same tiles, Q^T staged in shared memory: E = M - P Q^T
@@ -24,6 +25,7 @@
 // (deterministic; no fp64 arithmetic, which is slow on this part);
 // elementwise steps are single fp32 roundings in the order the method
 // states them.
+#include <cooperative_groups.h>
 #include <cstring>
 
 #include "gc_common.cuh"
@@ -39,6 +41,11 @@ constexpr int PS_CC = 1024;
 // addition in P = M Q and M^T P: the partial's rounding error is at most
 // (PS_FLUSH - 1) u of the sum of |terms| (u = 2^-24), below 1e-6 of it.
 constexpr int PS_FLUSH = 16;
+// Gram-Schmidt of matrices with more than PORTH_BIG rows runs on a cluster of
+// PORTH_CL CTAs (rows split over the cluster, sums combined through
+// distributed shared memory).
+constexpr int64_t PORTH_BIG = 8192;
+constexpr int PORTH_CL = 8;
 
 struct PsArgs {
   int T;
@@ -59,7 +66,8 @@ struct PsArgs {
   int64_t* ppoff;    // [T+1] prefix of m * ceil(n / PS_CC)
   float* part;       // partial column sums of M^T P, [partoff][R]
   float* ppart;      // partial row sums of M Q per column tile, [ppoff][R]
-  int64_t Mrows, Ncols, Tiles, Parts, PParts;
+  int64_t* bigoff;    // [T+1] prefix count of matrices with more than PORTH_BIG rows
+  int64_t Mrows, Ncols, Tiles, Parts, PParts, Big;
 };
 
 __device__ __forceinline__ bool ps_aborted(const PsArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
@@ -69,11 +77,11 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  int64_t carry[5] = {0, 0, 0, 0, 0};
-  int64_t* outs[5] = {A.rowoff, A.coloff, A.tileoff, A.partoff, A.ppoff};
+  int64_t carry[6] = {0, 0, 0, 0, 0, 0};
+  int64_t* outs[6] = {A.rowoff, A.coloff, A.tileoff, A.partoff, A.ppoff, A.bigoff};
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
-    int64_t v[5] = {0, 0, 0, 0, 0};
+    int64_t v[6] = {0, 0, 0, 0, 0, 0};
     if (t < A.T) {
       const int64_t m = A.rows[t], n = A.cols[t];
       if (m < 1 || n < 1 || A.start[t] < 0) s_bad = 1;
@@ -83,8 +91,9 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
       v[2] = rc * ((n + PS_CC - 1) / PS_CC);
       v[3] = rc * n;
       v[4] = m * ((n + PS_CC - 1) / PS_CC);
+      v[5] = m > PORTH_BIG ? 1 : 0;
     }
-    for (int w = 0; w < 5; ++w) {
+    for (int w = 0; w < 6; ++w) {
       const unsigned lane = lane_id(), wi = threadIdx.x >> 5, nw = blockDim.x >> 5;
       int64_t x = v[w];
 #pragma unroll
@@ -113,9 +122,9 @@ __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 0; w < 5; ++w) outs[w][A.T] = carry[w];
+    for (int w = 0; w < 6; ++w) outs[w][A.T] = carry[w];
     if (s_bad || carry[0] != A.Mrows || carry[1] != A.Ncols || carry[2] != A.Tiles || carry[3] != A.Parts ||
-        carry[4] != A.PParts) {
+        carry[4] != A.PParts || carry[5] != A.Big) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -388,30 +397,38 @@ __device__ __forceinline__ void porth_row(float* row, float v[R], int ukind, int
   }
 }
 
-template <int R>
-__global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
+// Gram-Schmidt of matrix t by one CTA (CL = 1) or by cluster rank `rank` of
+// CL CTAs: thread g of the CL * blockDim.x threads owns rows g, g + CL *
+// blockDim.x, ...  Each pass's block sum is a compensated pair; with CL > 1
+// every CTA publishes its pair in shared memory (slot alternating by pass),
+// the cluster barrier orders it, and every CTA adds the CL pairs in rank
+// order, so all CTAs hold the same value.
+template <int R, int CL>
+__device__ __forceinline__ void porth_matrix(const PsArgs& A, int t, int rank) {
   __shared__ float s_ws[32], s_wc[32];
   __shared__ float s_tot;
-  if (ps_aborted(A)) return;
-  const int t = blockIdx.x;
+  __shared__ float s_slot[2][2];
   const int64_t m = A.rows[t];
   float* P = A.p + A.rowoff[t] * R;
   const unsigned lane = lane_id(), warp = threadIdx.x >> 5;
+  const int64_t nthr = (int64_t)CL * blockDim.x;
+  const int64_t g0 = (int64_t)rank * blockDim.x + threadIdx.x;
   int ukind = 0, uk = 0, uj = 0;  // pending update: 0 none, 1 P_k -= d P_j, 2 P_k /= nrm
   float uval = 0.0f;
+  int pass = 0;
   for (int k = 0; k < R; ++k) {
-    for (int j = 0; j <= k; ++j) {  // j < k: d = <P_j, P_k>;  j == k: |P_k|^2
+    for (int j = 0; j <= k; ++j, ++pass) {  // j < k: d = <P_j, P_k>;  j == k: |P_k|^2
       Nm acc;
-      for (int64_t i0 = threadIdx.x; i0 < m; i0 += 4 * 1024) {
+      for (int64_t i0 = g0; i0 < m; i0 += 4 * nthr) {
         float v[4][R];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int64_t i = i0 + 1024 * u;
+          const int64_t i = i0 + nthr * u;
           if (i < m) porth_row<R>(P + i * R, v[u], ukind, uk, uj, uval);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int64_t i = i0 + 1024 * u;
+          const int64_t i = i0 + nthr * u;
           if (i < m) {
             const float a = pick<R>(v[u], j), b = pick<R>(v[u], k);
             const float pr = __fmul_rn(a, b);
@@ -429,11 +446,32 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
       __syncthreads();
       if (warp == 0) {
         Nm w;
-        w.s = s_ws[lane];
-        w.c = s_wc[lane];
+        w.s = lane < (blockDim.x >> 5) ? s_ws[lane] : 0.0f;
+        w.c = lane < (blockDim.x >> 5) ? s_wc[lane] : 0.0f;
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) w.butterfly(d);
-        if (lane == 0) s_tot = w.value();
+        if (lane == 0) {
+          if (CL == 1) {
+            s_tot = w.value();
+          } else {
+            s_slot[pass & 1][0] = w.s;
+            s_slot[pass & 1][1] = w.c;
+          }
+        }
+      }
+      if (CL > 1) {
+        cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+        cluster.sync();
+        if (threadIdx.x == 0) {
+          Nm z;
+#pragma unroll
+          for (int r = 0; r < CL; ++r) {
+            const float* peer = cluster.map_shared_rank(&s_slot[pass & 1][0], r);
+            z.add(peer[0]);
+            z.c = __fadd_rn(z.c, peer[1]);
+          }
+          s_tot = z.value();
+        }
       }
       __syncthreads();
       const float tot = s_tot;
@@ -446,11 +484,34 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A) {
       }
     }
   }
+  // no CTA may exit while a peer could still be reading its slots
+  if (CL > 1) cooperative_groups::this_cluster().sync();
   if (ukind != 0)
-    for (int64_t i = threadIdx.x; i < m; i += 1024) {
+    for (int64_t i = g0; i < m; i += nthr) {
       float v[R];
       porth_row<R>(P + i * R, v, ukind, uk, uj, uval);
     }
+}
+
+// One CTA per matrix: those of at most PORTH_BIG rows (big = 0), or the
+// larger ones (big = 1, used only if the cluster launch is refused).
+template <int R>
+__global__ void __launch_bounds__(1024) k_porth(PsArgs A, int big) {
+  if (ps_aborted(A)) return;
+  const int t = blockIdx.x;
+  if ((A.rows[t] > PORTH_BIG) != (big != 0)) return;
+  porth_matrix<R, 1>(A, t, 0);
+}
+
+// One cluster of PORTH_CL CTAs per matrix of more than PORTH_BIG rows.  Every
+// CTA of a cluster runs the same passes (the abort flag, set before this
+// launch, reads the same in all of them), so all reach every barrier.
+template <int R>
+__global__ void __launch_bounds__(1024) k_porthc(PsArgs A) {
+  if (ps_aborted(A)) return;
+  const int64_t ci = blockIdx.x / PORTH_CL;
+  const int t = find_segment(A.bigoff, A.T, ci);
+  porth_matrix<R, PORTH_CL>(A, t, (int)(blockIdx.x % PORTH_CL));
 }
 
 // Partial column sums of M^T P over a tile of PS_RC rows x PS_CC columns;
@@ -694,7 +755,7 @@ __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
 // ============================================================================ host
 
 struct PsTotals {
-  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, PParts = 0, maxel = 0;
+  int64_t M = 0, N = 0, Tiles = 0, Parts = 0, PParts = 0, Big = 0, maxel = 0;
 };
 
 static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* z) {
@@ -709,12 +770,13 @@ static gc_status ps_validate(const gc_matrix_layout* h, int32_t rank, PsTotals* 
     z->Tiles += rc * ((n + PS_CC - 1) / PS_CC);
     z->Parts += rc * n;
     z->PParts += m * ((n + PS_CC - 1) / PS_CC);
+    z->Big += m > PORTH_BIG ? 1 : 0;
   }
   return GC_OK;
 }
 
 struct PsCarve {
-  size_t o_row, o_col, o_tile, o_part_off, o_pp_off, o_part, o_ppart, total;
+  size_t o_row, o_col, o_tile, o_part_off, o_pp_off, o_big, o_part, o_ppart, total;
 };
 
 static PsCarve ps_carve(int T, int R, const PsTotals& z) {
@@ -730,6 +792,7 @@ static PsCarve ps_carve(int T, int R, const PsTotals& z) {
   c.o_tile = take(8 * (size_t)(T + 1));
   c.o_part_off = take(8 * (size_t)(T + 1));
   c.o_pp_off = take(8 * (size_t)(T + 1));
+  c.o_big = take(8 * (size_t)(T + 1));
   c.o_part = take(4 * (size_t)z.Parts * R);
   c.o_ppart = take(4 * (size_t)z.PParts * R);
   c.total = p;
@@ -756,7 +819,25 @@ static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
   k_psplan<<<1, 1024, 0, s>>>(A);
   k_pmq<R><<<ps_tile_grid(k_pmq<R>, 0, A.Tiles), 256, 0, s>>>(A);
   k_ppred<R><<<(unsigned)std::min<int64_t>((A.Mrows + 255) / 256, 65535), 256, 0, s>>>(A);
-  k_porth<R><<<A.T, 1024, 0, s>>>(A);
+  k_porth<R><<<A.T, 1024, 0, s>>>(A, 0);
+  if (A.Big > 0) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(A.Big * PORTH_CL));
+    cfg.blockDim = dim3(1024);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PORTH_CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_porthc<R>, A) != cudaSuccess) {
+      (void)cudaGetLastError();  // cluster refused: one CTA per large matrix instead
+      k_porth<R><<<A.T, 1024, 0, s>>>(A, 1);
+    }
+  }
   k_pmtp<R><<<ps_tile_grid(k_pmtp<R>, 0, A.Tiles), 256, 0, s>>>(A);
   k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
   k_pres<R, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
@@ -783,6 +864,7 @@ static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* h
   A->tileoff = reinterpret_cast<int64_t*>(w + c.o_tile);
   A->partoff = reinterpret_cast<int64_t*>(w + c.o_part_off);
   A->ppoff = reinterpret_cast<int64_t*>(w + c.o_pp_off);
+  A->bigoff = reinterpret_cast<int64_t*>(w + c.o_big);
   A->ppart = reinterpret_cast<float*>(w + c.o_ppart);
   A->part = reinterpret_cast<float*>(w + c.o_part);
   A->Mrows = z.M;
@@ -790,6 +872,7 @@ static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* h
   A->Tiles = z.Tiles;
   A->Parts = z.Parts;
   A->PParts = z.PParts;
+  A->Big = z.Big;
   if (cudaMemsetAsync(ws, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
   return GC_OK;
 }

@@ -695,7 +695,19 @@ def test_powersgd_steps(gc, rank):
     Q = M^T P within 2e-6 of sum |M||.| (compensated fp32 partials), the
     orthonormalized P within 1e-5 given the GPU's P_raw, and the residual
     E = M - P Q^T bit-exact given the GPU's P and Q; three warm-started calls."""
-    rng = np.random.default_rng(40 + rank)
+    _powersgd_check(gc, rank, PS_SHAPES, 40 + rank, iters=3)
+
+
+@pytest.mark.parametrize("rank", [1, 4])
+def test_powersgd_tall_matrices(gc, rank):
+    """Matrices taller than 8192 rows (Gram-Schmidt on a cluster of CTAs),
+    between small ones, one with a misaligned start."""
+    _powersgd_check(gc, rank, [(5, 7), (9000, 16), (16385, 5), (30522, 12), (100, 3)], 60 + rank, iters=2)
+
+
+def _powersgd_check(gc, rank, shapes, seed, iters):
+    PS_SHAPES = shapes
+    rng = np.random.default_rng(seed)
     starts, pos = [], 0
     for i, (m, n) in enumerate(PS_SHAPES):
         pos += 3 * (i % 2)                      # gaps: some matrices start misaligned
@@ -710,7 +722,7 @@ def test_powersgd_steps(gc, rank):
     p = torch.empty(Msum * rank, device="cuda")
     p_raw = torch.empty(Msum * rank, device="cuda")
     ws = gc.powersgd_workspace(ml, rank)
-    for it in range(3):
+    for it in range(iters):
         g_h = rng.standard_normal(N).astype(F32)
         gc.powersgd_compress(ml, rank, torch.from_numpy(g_h).cuda(), e, q, p, p_raw, ws)
         assert gc.get_device_status(ws).error_bits == 0
