@@ -519,10 +519,11 @@ __global__ void __launch_bounds__(1024) k_porthc(PsArgs A) {
 // cp.async pipeline: each thread copies its own 16-byte slice of the next
 // rows into shared memory PT_NS - 1 stages ahead (no registers held for
 // data in flight, no thread reads another's slice), then computes from
-// shared memory.  Fused multiply-adds are summed in fp32 over PS_FLUSH rows,
-// then added to compensated accumulators; the tile's partials go to A.part.
-constexpr int PT_RS = 4;  // rows per stage
-constexpr int PT_NS = 3;  // stages (48 KB of shared memory per CTA)
+// shared memory, with the tile's rows of P staged there once.  Fused
+// multiply-adds are summed in fp32 over PS_FLUSH rows, then added to
+// compensated accumulators; the tile's partials go to A.part.
+constexpr int PT_RS = 2;  // rows per stage
+constexpr int PT_NS = 5;  // stages (40 KB of shared memory per CTA, 8 rows in flight)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -554,6 +555,7 @@ __device__ __forceinline__ void pmtp_flush(Nm acc[4][R], float part[4][R]) {
 template <int R>
 __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
   __shared__ __align__(16) float4 sbuf[PT_NS * PT_RS * 256];
+  __shared__ __align__(16) float sp[PS_RC * R];  // the tile's rows of P
   if (ps_aborted(A)) return;
   const int tid = threadIdx.x;
   for (int64_t tile = blockIdx.x; tile < A.Tiles; tile += gridDim.x) {
@@ -566,6 +568,9 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
     const int64_t i0 = c * PS_RC, i1 = min(m, i0 + PS_RC);
     const float* P = A.p + A.rowoff[t] * R;
     const bool vec = ((A.start[t] & 3) == 0) && ((n & 3) == 0);
+    __syncthreads();  // the previous tile's readers of sp are done
+    for (int x = tid; x < (int)(i1 - i0) * R; x += blockDim.x) sp[x] = P[i0 * R + x];
+    __syncthreads();
     if (j0 >= n) continue;
     Nm acc[4][R];
     float part[4][R];
@@ -599,7 +604,8 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
             const float4 mv = sbuf[((st % PT_NS) * PT_RS + u) * 256 + tid];
             const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
             float pv[R];
-            load_row<R>(P + i * R, pv);
+#pragma unroll
+            for (int k = 0; k < R; ++k) pv[k] = sp[(i - i0) * R + k];
             pmtp_rows<R>(part, mm, pv);
           }
         }
@@ -617,7 +623,8 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) mm[cc] = (j0 + cc < n) ? A.e[rb + j0 + cc] : 0.0f;
         float pv[R];
-        load_row<R>(P + i * R, pv);
+#pragma unroll
+        for (int k = 0; k < R; ++k) pv[k] = sp[(i - i0) * R + k];
         pmtp_rows<R>(part, mm, pv);
         if (++fl == PS_FLUSH) {
           fl = 0;
