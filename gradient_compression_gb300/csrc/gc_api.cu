@@ -40,6 +40,7 @@ extern "C" gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32
 
 extern "C" gc_status gc_get_device_status(const void* workspace, size_t ws_bytes, void* stream,
                                           gc_diag* out) {
+  NvtxRange nvtx_range("gc_get_device_status");
   if (!workspace || ws_bytes < DIAG_BYTES || !out) return GC_ERR_INVALID_ARG;
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);

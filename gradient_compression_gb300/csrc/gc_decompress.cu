@@ -66,6 +66,7 @@ extern "C" gc_status gc_sparse_decompress_accumulate(const gc_layout* dev, const
                                                      const float* const* scale, float* out,
                                                      void* workspace, size_t ws_bytes,
                                                      void* stream) {
+  NvtxRange nvtx_range("gc_sparse_decompress_accumulate");
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->koff || dev->num_tensors != host->num_tensors) return GC_ERR_INVALID_ARG;

@@ -678,6 +678,7 @@ using namespace gc;
 extern "C" gc_status gc_sign_compress(const gc_layout* dev, const gc_layout* host, const float* g,
                                       float* e, uint32_t* bits, float* mean_abs, void* workspace,
                                       size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_sign_compress");
   if (!g || !bits || !mean_abs) return GC_ERR_INVALID_ARG;
   if (!aligned16(g) || (e && !aligned16(e))) return GC_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -702,6 +703,7 @@ extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layou
                                             int32_t mode, int32_t s_levels, uint64_t seed,
                                             uint64_t iter, void* workspace, size_t ws_bytes,
                                             void* stream) {
+  NvtxRange nvtx_range("gc_quantize_stochastic");
   if (!g || !codes || !scale) return GC_ERR_INVALID_ARG;
   if (mode != GC_Q_INT8 && mode != GC_Q_QSGD) return GC_ERR_INVALID_ARG;
   if (mode == GC_Q_QSGD && (s_levels < 1 || s_levels > 127)) return GC_ERR_INVALID_ARG;
@@ -736,6 +738,7 @@ extern "C" gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const 
                                                     const float* const* scale, float* out,
                                                     void* workspace, size_t ws_bytes,
                                                     void* stream) {
+  NvtxRange nvtx_range("gc_dense_decompress_accumulate");
   if (W < 0 || !out || (W > 0 && (!data || !scale))) return GC_ERR_INVALID_ARG;
   if (kind != GC_DENSE_SIGN && kind != GC_DENSE_INT8 && kind != GC_DENSE_QSGD) return GC_ERR_INVALID_ARG;
   if (kind == GC_DENSE_QSGD && (s_levels < 1 || s_levels > 127)) return GC_ERR_INVALID_ARG;
@@ -762,6 +765,7 @@ extern "C" gc_status gc_sign_compress_lazy(const gc_layout* dev, const gc_layout
                                            const float* g, float* e, const float* prev_mean_abs,
                                            uint32_t* bits, float* mean_abs, void* workspace,
                                            size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_sign_compress_lazy");
   if (!g || !e || !bits || !mean_abs) return GC_ERR_INVALID_ARG;
   if (!aligned16(g) || !aligned16(e)) return GC_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -784,6 +788,7 @@ extern "C" gc_status gc_sign_compress_lazy(const gc_layout* dev, const gc_layout
 
 extern "C" gc_status gc_sign_residual_materialize(const gc_layout* dev, const gc_layout* host,
                                                   float* e, const float* mean_abs, void* stream) {
+  NvtxRange nvtx_range("gc_sign_residual_materialize");
   const gc_status st = validate_layout(host, false);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || dev->num_tensors != host->num_tensors || !e || !mean_abs) return GC_ERR_INVALID_ARG;

@@ -1,12 +1,23 @@
 // Host-side helpers of libgc: argument validation and workspace sizing.
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/gc.h"
 
 namespace gc {
+
+// Names the enclosing host scope (an entry point, or the enqueueing of one
+// phase of it) in profiler timelines: an NVTX range, which costs nothing
+// when no profiler is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0u; }

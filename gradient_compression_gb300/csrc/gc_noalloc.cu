@@ -61,6 +61,7 @@ extern "C" gc_status gc_ef_topk_compress_noalloc(const gc_layout* dev, const gc_
                                                  float* val, int8_t* q, float* scale,
                                                  uint64_t seed, uint64_t iter, uint32_t flags,
                                                  void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_noalloc");
   const gc_status lst = validate_layout(host, true);
   if (lst != GC_OK) return lst;
   const size_t need = topk_workspace_bytes(host, !(flags & GC_RANDK));

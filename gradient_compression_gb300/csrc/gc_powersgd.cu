@@ -902,6 +902,7 @@ extern "C" gc_status gc_powersgd_compress(const gc_matrix_layout* dev, const gc_
                                           int32_t rank, const float* g, float* e, float* q, float* p,
                                           float* p_raw, void* workspace, size_t ws_bytes,
                                           void* stream) {
+  NvtxRange nvtx_range("gc_powersgd_compress");
   if (!g || !e || !q || !p) return GC_ERR_INVALID_ARG;
   if (!aligned16(g) || !aligned16(e) || !aligned16(q) || !aligned16(p)) return GC_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -927,6 +928,7 @@ extern "C" gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* d
                                                        const float* p, const float* q, float* out,
                                                        void* workspace, size_t ws_bytes,
                                                        void* stream) {
+  NvtxRange nvtx_range("gc_powersgd_decompress_accumulate");
   if (!p || !q || !out) return GC_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(p)) return GC_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1476,6 +1476,7 @@ extern "C" gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* 
                                          int8_t* q, float* scale, uint64_t seed, uint64_t iter,
                                          uint32_t flags, void* workspace, size_t ws_bytes,
                                          void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress");
   return topk_entry(dev, host, g, e, idx, val, q, scale, seed, iter, flags, workspace, ws_bytes,
                     stream, PhaseEvents{});
 }
@@ -1486,6 +1487,7 @@ extern "C" gc_status gc_ef_topk_compress_profiled(const gc_layout* dev, const gc
                                                   uint64_t seed, uint64_t iter, uint32_t flags,
                                                   void* workspace, size_t ws_bytes, void* stream,
                                                   void* const* events, int32_t n_events) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_profiled");
   if (n_events < 0 || n_events > 32 || (n_events > 0 && !events)) return GC_ERR_INVALID_ARG;
   PhaseEvents pe;
   pe.ev = events;
@@ -1500,6 +1502,7 @@ extern "C" gc_status gc_ef_topk_compress_momentum(const gc_layout* dev, const gc
                                                   float* scale, uint64_t seed, uint64_t iter,
                                                   uint32_t flags, void* workspace,
                                                   size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_momentum");
   const uint32_t known = GC_INT8 | GC_NO_MASK | GC_FORCE_EXACT;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   if (!u || !v) return GC_ERR_INVALID_ARG;
@@ -1512,6 +1515,7 @@ extern "C" gc_status gc_ef_topk_compress_lazy(const gc_layout* dev, const gc_lay
                                               int32_t* idx, float* val, int8_t* q, float* scale,
                                               uint64_t seed, uint64_t iter, uint32_t flags,
                                               void* workspace, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_lazy");
   const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   if (!e || !rd) return GC_ERR_INVALID_ARG;
@@ -1543,6 +1547,7 @@ __global__ void k_clear_desc(gc_residual_desc* rd, int T) {
 
 extern "C" gc_status gc_ef_residual_materialize(const gc_layout* dev, const gc_layout* host, float* e,
                                                 gc_residual_desc* rd, void* stream) {
+  NvtxRange nvtx_range("gc_ef_residual_materialize");
   const gc_status st = validate_layout(host, false);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || dev->num_tensors != host->num_tensors || !e || !rd) return GC_ERR_INVALID_ARG;
@@ -1559,6 +1564,7 @@ extern "C" gc_status gc_ef_threshold_compress(const gc_layout* dev, const gc_lay
                                               float* scale, uint64_t seed, uint64_t iter,
                                               uint32_t flags, void* workspace, size_t ws_bytes,
                                               void* stream) {
+  NvtxRange nvtx_range("gc_ef_threshold_compress");
   const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   if (!tau || !count) return GC_ERR_INVALID_ARG;
@@ -1574,6 +1580,7 @@ extern "C" gc_status gc_ef_topk_compress_clipped(const gc_layout* dev, const gc_
                                                  float* scale, uint64_t seed, uint64_t iter,
                                                  uint32_t flags, void* workspace, size_t ws_bytes,
                                                  void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_clipped");
   const uint32_t known = GC_EF | GC_INT8 | GC_FORCE_EXACT;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   if (!(flags & GC_EF) || !e || !max_norm || !norm) return GC_ERR_INVALID_ARG;
