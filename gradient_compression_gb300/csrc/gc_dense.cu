@@ -14,6 +14,8 @@
 //           lanes), or the per-tensor max key (int8)
 //   reduce: per tensor, unit partials summed in a fixed order in fp64
 //   pass 2: bits / codes and the EF residual
+// The single-pass sign variant (k_sign_lazy) writes bits, acc and the
+// partials in one pass and leaves the residual's -+mean to the next call.
 #include <cmath>
 #include <cstring>
 

@@ -9,9 +9,11 @@
 // Pipeline for one call (all tensors of the arena at once, stream-ordered):
 //   plan       per-tensor prefix tables (units, unit blocks, candidate and
 //              sample regions) from the device layout
-//   sample1/2  a strided sample of acc per tensor -> a threshold estimate
-//              t_est well below the k-th magnitude (Top-k, momentum only;
-//              random-k keys are uniform, so t_est is set analytically)
+//   sample     a strided sample of acc per tensor, two shared-memory radix
+//              levels -> a threshold estimate t_est below the k-th magnitude
+//              (Top-k, momentum, threshold; random-k keys are uniform, so
+//              t_est is set analytically by the plan)
+//   [clip]     per-tensor ||g|| and the clipping multiplier (local clipping)
 //   stream     THE pass over HBM: acc = g + e (or the momentum update),
 //              write-back of e (u, v), and emission of every element whose
 //              key >= t_est into an index-ordered per-unit candidate chunk,
