@@ -428,16 +428,19 @@ __device__ uint32_t find_bucket(const uint32_t* row, uint32_t rank, uint32_t* ab
   return b;
 }
 
-// Threshold estimate t_est from a strided sample of acc, one CTA of 1024
-// threads per tensor.  The sample is runs of RUN = 128 consecutive elements
-// (one warp, 16 bytes per lane per input) spaced `stride` apart; small
-// tensors are sampled completely.  Level 1: shared-memory histogram of the
+// Threshold estimate t_est from a strided sample of acc, one CTA of 512
+// threads per tensor (two CTAs per SM, so that every tensor's CTA starts in
+// the first wave; each warp keeps SRUNS runs in flight).  The sample is runs
+// of RUN = 128 consecutive elements (one warp, 16 bytes per lane per input)
+// spaced `stride` apart; small tensors are sampled completely.  Level 1: shared-memory histogram of the
 // sample keys' top 11 bits -> the bucket of the j-th largest sample key.
 // Level 2: the next 11 bits of the sample keys in that bucket (re-read from
 // the sample key buffer) -> t_est = the lower edge of that level-2 bucket,
 // which is <= the j-th largest sample key.
+constexpr int SRUNS = 4;  // sample runs per warp per step
+
 template <int MODE>
-__global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
+__global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t sh[NBINS];
@@ -469,11 +472,11 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
   const bool vec = (base & 3) == 0;
   uint32_t* sk = A.skey + A.soff[t];
   const int64_t nwarp = blockDim.x >> 5;
-  for (int64_t r0 = threadIdx.x >> 5; r0 < runs; r0 += 2 * nwarp) {
-    float a[2][4];
-    bool ok[2][4];
+  for (int64_t r0 = threadIdx.x >> 5; r0 < runs; r0 += SRUNS * nwarp) {
+    float a[SRUNS][4];
+    bool ok[SRUNS][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < SRUNS; ++h) {
       const int64_t r = r0 + h * nwarp;
       if (r < runs) {
         acc4_from_inputs<MODE>(A, t, base, n, sample_run_start(r, stride) + 4 * lane, vec, a[h], ok[h]);
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < SRUNS; ++h) {
       const int64_t r = r0 + h * nwarp;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(1024) k_sample(TopkArgs A) {
     return;
   }
   const uint32_t rank2 = (uint32_t)j - above;
-  constexpr int U8 = 8;
+  constexpr int U8 = 16;
   for (int64_t i0 = 0; i0 < m; i0 += (int64_t)blockDim.x * U8) {
     uint32_t kk[U8];
 #pragma unroll
@@ -1319,7 +1322,7 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
   }
   pe.done(A.sampled ? 0 : 1, s);
   if (A.sampled) {
-    k_sample<MODE><<<T, 1024, 0, s>>>(A);
+    k_sample<MODE><<<T, 512, 0, s>>>(A);
     pe.done(1, s);
   }
   if (MODE == MODE_MOM) {
