@@ -77,6 +77,8 @@ def lib() -> C.CDLL:
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
         L.gc_quantize_stochastic.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, U64, P, SZ, P]
+        L.gc_quantize_stochastic_dev_iter.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, P, P, SZ, P]
+        L.gc_ef_topk_compress_dev_iter.argtypes = [LP, LP, P, P, P, P, P, P, U64, P, U32, P, SZ, P]
         L.gc_sparse_decompress_accumulate.argtypes = [LP, LP, I32, P, P, P, P, P, P, SZ, P]
         L.gc_dense_decompress_accumulate.argtypes = [LP, LP, I32, I32, I32, P, P, P, P, SZ, P]
         L.gc_get_device_status.argtypes = [P, SZ, P, C.POINTER(gc_diag)]
@@ -90,7 +92,8 @@ def lib() -> C.CDLL:
                      "gc_powersgd_decompress_accumulate",
                      "gc_ef_topk_compress_momentum",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
-                     "gc_dense_decompress_accumulate", "gc_get_device_status"):
+                     "gc_dense_decompress_accumulate", "gc_get_device_status",
+                     "gc_ef_topk_compress_dev_iter", "gc_quantize_stochastic_dev_iter"):
             getattr(L, name).restype = I32
         _lib = L
     return _lib
@@ -300,6 +303,28 @@ def ef_topk_compress_profiled(layout, g, e, idx, val, q, scale, seed, it, flags,
                                               _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
                                               _ptr(workspace), workspace.numel(), _stream(stream), arr,
                                               len(events)), "gc_ef_topk_compress_profiled")
+
+
+def ef_topk_compress_dev_iter(layout, g, e, idx, val, q, scale, seed, iter_dev, flags, workspace, stream=None):
+    """ef_topk_compress with the iteration counter in a device int64 tensor
+    (`iter_dev`, one element), read by the kernels and advanced by one at
+    the end of the call: capturable in a CUDA graph that replays as
+    successive steps."""
+    _check(lib().gc_ef_topk_compress_dev_iter(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx),
+                                              _ptr(val), _ptr(q), _ptr(scale), int(seed), _ptr(iter_dev),
+                                              int(flags), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_ef_topk_compress_dev_iter")
+
+
+def quantize_stochastic_dev_iter(layout, g, e, codes, scale, mode, s_levels, seed, iter_dev, workspace,
+                                 stream=None):
+    """quantize_stochastic with the iteration counter in a device int64 tensor
+    (see ef_topk_compress_dev_iter)."""
+    _check(lib().gc_quantize_stochastic_dev_iter(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(codes),
+                                                 _ptr(scale), int(mode), int(s_levels), int(seed),
+                                                 _ptr(iter_dev), _ptr(workspace), workspace.numel(),
+                                                 _stream(stream)),
+           "gc_quantize_stochastic_dev_iter")
 
 
 def ef_topk_compress_momentum(layout, g, u, v, beta, idx, val, q, scale, seed, it, flags, workspace,

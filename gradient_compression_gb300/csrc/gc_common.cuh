@@ -170,6 +170,10 @@ __device__ __forceinline__ uint32_t philox_word(const PhiloxKey& K, uint64_t ite
 
 constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
+// Advances a device-resident iteration counter by one (the last kernel of a
+// *_dev_iter call).
+static __global__ void k_iter_advance(uint64_t* iter) { *iter += 1u; }
+
 // ---------------------------------------------------------------- rounding
 // Stochastic rounding of 0 <= x < 2^23: floor(x) + 1 iff r * 2^-32 < frac(x),
 // decided exactly.  x + 2^23 rounded toward zero is 2^23 + floor(x) (the

@@ -38,6 +38,7 @@ struct DenseArgs {
   int8_t* codes;
   float* scale;  // mean_abs (sign), max/127 (int8), norm (QSGD)
   uint64_t seed, iter;
+  const uint64_t* iter_dev;  // iteration counter in device memory (graph capture), else null
   PhiloxKey pk;       // round keys of seed
   uint32_t* diag;
   uint32_t* maxkey;   // [T]
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
   const int64_t nwarps = (int64_t)gridDim.x * DWARPS;
   const float* src = EF ? A.e : A.g;
   const uint32_t purpose = (OP == DOP_INT8) ? PURPOSE_INT8 : PURPOSE_QSGD;
+  const uint64_t iter = A.iter_dev ? *A.iter_dev : A.iter;
   for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
     const UnitRef r = unit_ref(A, u);
     const int64_t g0 = r.base + r.lstart;
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
           for (int j = 0; j < 4; ++j) x[j] = ld_stream(s4 + v0 + 32 * j + (int)lane);
           uint4 rw[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) rw[j] = philox_block(A.pk, A.iter, b0 + (uint64_t)(v0 + 32 * j + (int)lane), purpose);
+          for (int j = 0; j < 4; ++j) rw[j] = philox_block(A.pk, iter, b0 + (uint64_t)(v0 + 32 * j + (int)lane), purpose);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int vi = v0 + 32 * j + (int)lane;
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int vi = v0 + 32 * j + (int)lane;
-            if (vi < nv) quant_slot<OP, EF>(A, dv, x[j], philox_block(A.pk, A.iter, b0 + (uint64_t)vi, purpose),
+            if (vi < nv) quant_slot<OP, EF>(A, dv, x[j], philox_block(A.pk, iter, b0 + (uint64_t)vi, purpose),
                                             c4 + vi, e4 + vi);
           }
         }
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + 4 * nv + lane;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     } else {
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
         const int64_t gi = g0 + i;
         const float x = src[gi];
         float d;
-        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, A.iter, (uint64_t)gi, purpose), &d);
+        A.codes[gi] = (int8_t)dense_code<OP, EF>(x, dv, A.s_levels, philox_word(A.pk, iter, (uint64_t)gi, purpose), &d);
         if (EF) A.e[gi] = __fsub_rn(x, d);
       }
     }
@@ -700,12 +702,10 @@ extern "C" gc_status gc_sign_compress(const gc_layout* dev, const gc_layout* hos
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
-extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layout* host,
-                                            const float* g, float* e, int8_t* codes, float* scale,
-                                            int32_t mode, int32_t s_levels, uint64_t seed,
-                                            uint64_t iter, void* workspace, size_t ws_bytes,
-                                            void* stream) {
-  NvtxRange nvtx_range("gc_quantize_stochastic");
+static gc_status quantize_entry(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
+                                int8_t* codes, float* scale, int32_t mode, int32_t s_levels, uint64_t seed,
+                                uint64_t iter, uint64_t* iter_dev, void* workspace, size_t ws_bytes,
+                                void* stream) {
   if (!g || !codes || !scale) return GC_ERR_INVALID_ARG;
   if (mode != GC_Q_INT8 && mode != GC_Q_QSGD) return GC_ERR_INVALID_ARG;
   if (mode == GC_Q_QSGD && (s_levels < 1 || s_levels > 127)) return GC_ERR_INVALID_ARG;
@@ -724,6 +724,7 @@ extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layou
   A.seed = seed;
   A.pk = make_philox_key(seed);
   A.iter = iter;
+  A.iter_dev = iter_dev;
   if (mode == GC_Q_INT8) {
     if (e) launch_quant<DOP_INT8, true>(A, s);
     else launch_quant<DOP_INT8, false>(A, s);
@@ -731,7 +732,29 @@ extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layou
     if (e) launch_quant<DOP_QSGD, true>(A, s);
     else launch_quant<DOP_QSGD, false>(A, s);
   }
+  if (iter_dev) k_iter_advance<<<1, 1, 0, s>>>(iter_dev);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layout* host,
+                                            const float* g, float* e, int8_t* codes, float* scale,
+                                            int32_t mode, int32_t s_levels, uint64_t seed,
+                                            uint64_t iter, void* workspace, size_t ws_bytes,
+                                            void* stream) {
+  NvtxRange nvtx_range("gc_quantize_stochastic");
+  return quantize_entry(dev, host, g, e, codes, scale, mode, s_levels, seed, iter, nullptr, workspace,
+                        ws_bytes, stream);
+}
+
+extern "C" gc_status gc_quantize_stochastic_dev_iter(const gc_layout* dev, const gc_layout* host,
+                                                     const float* g, float* e, int8_t* codes, float* scale,
+                                                     int32_t mode, int32_t s_levels, uint64_t seed,
+                                                     uint64_t* iter_dev, void* workspace, size_t ws_bytes,
+                                                     void* stream) {
+  NvtxRange nvtx_range("gc_quantize_stochastic_dev_iter");
+  if (!iter_dev || ((uintptr_t)iter_dev & 7u)) return GC_ERR_INVALID_ARG;
+  return quantize_entry(dev, host, g, e, codes, scale, mode, s_levels, seed, 0, iter_dev, workspace,
+                        ws_bytes, stream);
 }
 
 extern "C" gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const gc_layout* host,

@@ -57,6 +57,7 @@ struct TopkArgs {
   int8_t* q;
   float* scale;
   uint64_t seed, iter;
+  const uint64_t* iter_dev;  // iteration counter in device memory (graph capture), else null
   PhiloxKey pk;          // round keys of seed
   gc_residual_desc* rd;  // pending-residual descriptors (lazy mode), else null
   const float* tau;      // per-tensor magnitude thresholds (threshold mode), else null
@@ -234,9 +235,14 @@ __device__ __forceinline__ const float* value_source(const TopkArgs& A) {
   return A.ef ? A.e : A.g;
 }
 
+// The call's iteration counter: the argument, or the device-resident counter
+// of the *_dev_iter entry points (read where used, so a captured call sees
+// each replay's value).
+__device__ __forceinline__ uint64_t iter_of(const TopkArgs& A) { return A.iter_dev ? *A.iter_dev : A.iter; }
+
 template <int MODE>
 __device__ __forceinline__ uint32_t key_of(const TopkArgs& A, float value, int64_t gi) {
-  if (MODE == MODE_RANDK) return ~philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_RANDK);
+  if (MODE == MODE_RANDK) return ~philox_word(A.pk, iter_of(A), (uint64_t)gi, PURPOSE_RANDK);
   return mag_key(value);
 }
 
@@ -652,7 +658,7 @@ __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
         A.scale[t] = sc;
       }
       // last_tie is filled in by the payload write
-      if (A.rd) A.rd[t] = gc_residual_desc{1u | (A.int8 ? 2u : 0u), st->thr, -1, sc, A.seed, A.iter};
+      if (A.rd) A.rd[t] = gc_residual_desc{1u | (A.int8 ? 2u : 0u), st->thr, -1, sc, A.seed, iter_of(A)};
       break;
     }
   }
@@ -702,7 +708,7 @@ __device__ __forceinline__ void stream_scalar(const TopkArgs& A, int64_t li, int
     }
   }
   *value = x;
-  *key = (MODE == MODE_RANDK) ? ~philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_RANDK)
+  *key = (MODE == MODE_RANDK) ? ~philox_word(A.pk, iter_of(A), (uint64_t)gi, PURPOSE_RANDK)
                               : mag_key(x);
 }
 
@@ -731,6 +737,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? (LAZY ? 3 
   uint32_t* skey = reinterpret_cast<uint32_t*>(smem + (size_t)STREAM_WARPS * WCAP * 4) + warp * WCAP;
   uint16_t* spos = reinterpret_cast<uint16_t*>(smem + (size_t)STREAM_WARPS * WCAP * 8) + warp * WCAP;
   if (aborted(A)) return;
+  const uint64_t iter = iter_of(A);
   const int64_t nwarps = (int64_t)gridDim.x * STREAM_WARPS;
   for (int64_t u = (int64_t)blockIdx.x * STREAM_WARPS + warp; u < A.U; u += nwarps) {
     const int t = find_segment(A.units_off, A.T, u);
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? (LAZY ? 3 
           }
           unsigned m = 0u;
           if (MODE == MODE_RANDK) {
-            const uint4 w = philox_block(A.pk, A.iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, PURPOSE_RANDK);
+            const uint4 w = philox_block(A.pk, iter, (uint64_t)(g0 >> 2) + (uint64_t)vi, PURPOSE_RANDK);
             kk[0] = ~w.x; kk[1] = ~w.y; kk[2] = ~w.z; kk[3] = ~w.w;
           } else {
 #pragma unroll
@@ -1110,7 +1117,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
   }
   float* res = (MODE == MODE_MOM) ? A.v : ((A.ef && !A.rd) ? A.e : nullptr);
   if (A.int8) {
-    const int c = int8_code(x, s, philox_word(A.pk, A.iter, (uint64_t)gi, PURPOSE_INT8));
+    const int c = int8_code(x, s, philox_word(A.pk, iter_of(A), (uint64_t)gi, PURPOSE_INT8));
     const float d = __fmul_rn((float)c, s);
     A.q[pos] = (int8_t)c;
     if (A.val) A.val[pos] = d;
@@ -1372,7 +1379,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
                           void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe,
                           gc_residual_desc* rd = nullptr, const float* tau = nullptr,
                           int64_t* count_out = nullptr, const float* clip = nullptr,
-                          float* norm_out = nullptr) {
+                          float* norm_out = nullptr, uint64_t* iter_dev = nullptr) {
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
@@ -1414,6 +1421,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.seed = seed;
   A.pk = make_philox_key(seed);
   A.iter = iter;
+  A.iter_dev = iter_dev;
   A.rd = rd;
   A.tau = tau;
   A.count_out = count_out;
@@ -1454,6 +1462,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
     launch_pipeline<MODE_RANDK>(A, s, pe);
   else
     launch_pipeline<MODE_MOM>(A, s, pe);
+  if (iter_dev) k_iter_advance<<<1, 1, 0, s>>>(iter_dev);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
@@ -1464,7 +1473,7 @@ using namespace gc;
 static gc_status topk_entry(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
                             int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                             uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
-                            void* stream, const PhaseEvents& pe) {
+                            void* stream, const PhaseEvents& pe, uint64_t* iter_dev = nullptr) {
   const uint32_t known = GC_EF | GC_INT8 | GC_RANDK | GC_UNBIASED | GC_FORCE_EXACT;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   const bool randk = (flags & GC_RANDK) != 0u;
@@ -1473,7 +1482,18 @@ static gc_status topk_entry(const gc_layout* dev, const gc_layout* host, const f
   if ((flags & GC_EF) && !e) return GC_ERR_INVALID_ARG;
   return run_topk(randk ? MODE_RANDK : MODE_TOPK, dev, host, g, (flags & GC_EF) ? e : nullptr,
                   nullptr, nullptr, 0.0f, idx, val, q, scale, seed, iter, flags, workspace,
-                  ws_bytes, stream, pe);
+                  ws_bytes, stream, pe, nullptr, nullptr, nullptr, nullptr, nullptr, iter_dev);
+}
+
+extern "C" gc_status gc_ef_topk_compress_dev_iter(const gc_layout* dev, const gc_layout* host,
+                                                  const float* g, float* e, int32_t* idx, float* val,
+                                                  int8_t* q, float* scale, uint64_t seed,
+                                                  uint64_t* iter_dev, uint32_t flags, void* workspace,
+                                                  size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_dev_iter");
+  if (!iter_dev || ((uintptr_t)iter_dev & 7u)) return GC_ERR_INVALID_ARG;
+  return topk_entry(dev, host, g, e, idx, val, q, scale, seed, 0, flags, workspace, ws_bytes, stream,
+                    PhaseEvents{}, iter_dev);
 }
 
 extern "C" gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host,

@@ -130,6 +130,18 @@ typedef struct gc_diag {
 #define GC_DIAG_INDEX_RANGE 0x4u     /* decompress met a payload index >= n_t; entry skipped */
 #define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold or clipping norm was negative or NaN */
 
+/* CUDA-graph capture.  gc_ef_topk_compress_dev_iter and
+ * gc_quantize_stochastic_dev_iter are gc_ef_topk_compress and
+ * gc_quantize_stochastic with the iteration counter in device memory: the
+ * kernels read *iter_dev where the other entry points take `iter`, and the
+ * call ends by adding 1 to *iter_dev.  A call captured once into a graph
+ * therefore replays as successive steps (fresh random-k keys and stochastic
+ * rounding draws), with results bit-identical to calling the plain entry
+ * point with iter = 0, 1, 2, ... from the counter's starting value.  The
+ * calls enqueue only kernels and memsets on `stream` (no allocation, no
+ * synchronization), so they can be captured.
+ *   iter_dev: device uint64, 8-byte aligned; nothing else may write it
+ *             while the call runs.  Other arguments as the plain entry. */
 /* Bytes of workspace that operation `op` needs for layout `host` and
  * `flags`.  *bytes is set on GC_OK. */
 gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32_t flags, size_t* bytes);
@@ -153,6 +165,10 @@ gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const
                               int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                               uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
                               void* stream);
+gc_status gc_ef_topk_compress_dev_iter(const gc_layout* dev, const gc_layout* host, const float* g,
+                                       float* e, int32_t* idx, float* val, int8_t* q, float* scale,
+                                       uint64_t seed, uint64_t* iter_dev, uint32_t flags,
+                                       void* workspace, size_t ws_bytes, void* stream);
 
 /* EF Top-k with DGC local gradient clipping (genomic glossary "Gradient
  * Compression", DGC: local gradient clipping normalizes the gradient's
@@ -368,6 +384,10 @@ gc_status gc_quantize_stochastic(const gc_layout* dev, const gc_layout* host, co
                                  float* e, int8_t* codes, float* scale, int32_t mode,
                                  int32_t s_levels, uint64_t seed, uint64_t iter, void* workspace,
                                  size_t ws_bytes, void* stream);
+gc_status gc_quantize_stochastic_dev_iter(const gc_layout* dev, const gc_layout* host, const float* g,
+                                          float* e, int8_t* codes, float* scale, int32_t mode,
+                                          int32_t s_levels, uint64_t seed, uint64_t* iter_dev,
+                                          void* workspace, size_t ws_bytes, void* stream);
 
 /* Receiver of W workers' sparse payloads (mbrenndoerfer.com: the union of
  * different sparse vectors; zh glossary: all-gather of indices and values):
