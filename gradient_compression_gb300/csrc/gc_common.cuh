@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/gc.h"
@@ -26,6 +27,12 @@ constexpr int64_t SMALL_N = 65536;
 // Expected number of Top-k members in a tensor's sample.
 constexpr int64_t SAMPLE_HITS = 128;
 constexpr int RUN = 128;  // sampled elements per contiguous run (one warp, one float4 per lane)
+// Threshold estimate from the sample: pilot runs, shared-memory key list
+// (the pilot's keys, then the keys above the pilot's floor), and the
+// smallest sample that takes the filtered search.
+constexpr int SPILOT = 64;
+constexpr int SLIST = SPILOT * RUN;
+constexpr int64_t SFILTER_RUNS = 256;
 
 // Tensor state flags.
 constexpr uint32_t TS_NOEMIT = 1u;    // k_t == 0: nothing is selected
@@ -48,16 +55,23 @@ struct alignas(16) TensorState {
   uint32_t keff;        // elements kept (k_t, or fewer under a threshold)
   float gmul;           // multiplier applied to g (local clipping), else 1
   uint32_t cnt_tau;     // elements with |acc| >= tau (threshold mode, full-pass path)
-  uint32_t pad[5];
+  uint32_t pad0;
+  uint32_t s_runs;      // sample plan (set by the planner; 16-byte aligned): runs of RUN elements,
+  uint32_t s_stride;    //   their spacing,
+  uint32_t s_j;         //   the rank of the sample key that bounds t_est,
+  uint32_t s_rp;        //   and the rank in the pilot of the filtered search
 };
 static_assert(sizeof(TensorState) == 64, "TensorState is 64 bytes");
+static_assert(offsetof(TensorState, s_runs) % 16 == 0, "sample plan is one 16-byte load");
 
 // ---------------------------------------------------------------- sizing
-// Candidate capacity of a tensor, identical on host and device.
+// Candidate capacity of a tensor, identical on host and device.  The sampled
+// threshold yields about 1.6k candidates for a large tensor, with a relative
+// spread of about 7%, so 3k + 4096 is many standard deviations above it.
 __host__ __device__ inline int64_t cand_capacity(int64_t n, int64_t k) {
   if (k <= 0) return 0;
   if (n <= SMALL_N) return n;
-  int64_t c = 2 * k + 4096;
+  int64_t c = 3 * k + 4096;
   return c < n ? c : n;
 }
 
@@ -94,7 +108,7 @@ __host__ __device__ inline int64_t sample_run_start(int64_t r, int64_t stride) {
   const int64_t slack = (stride - RUN) >> 2;
   if (slack <= 0) return r * stride;
   const uint32_t h = (uint32_t)r * 2654435761u;
-  return r * stride + 4 * (int64_t)(h % (uint32_t)(slack + 1));
+  return r * stride + 4 * (int64_t)(((uint64_t)h * (uint64_t)(slack + 1)) >> 32);
 }
 
 // ---------------------------------------------------------------- keys

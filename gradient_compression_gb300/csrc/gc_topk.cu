@@ -131,13 +131,29 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       nu = units_of(n);
       nb = ublocks_of(n);
       nc = cand_capacity(n, k);
+      TensorState st;
+      memset(&st, 0, sizeof st);
       if (sampled && k > 0) {
         int64_t runs, stride, m;
         sample_plan(n, k, &runs, &stride, &m);
         ns = m;
+        // the sample key of rank j bounds t_est: j = k for a complete sample,
+        // else the expected count lam of Top-k members in the sample plus six
+        // standard deviations (and 8), so that fewer than k candidates needs
+        // about a 5-sigma sample (with four, about one tensor-step in 10^4
+        // fell short under error feedback and took the full-pass path)
+        int64_t j = k;
+        if (m < n) {
+          const double lam = (double)k * (double)m / (double)n;
+          j = (int64_t)ceil(lam + 6.0 * sqrt(lam) + 8.0);
+        }
+        st.s_runs = (uint32_t)runs;
+        st.s_stride = (uint32_t)stride;
+        st.s_j = (uint32_t)min(j, m + 1);
+        // pilot rank whose count scales to about 4j over the whole sample
+        const int64_t rp = (4 * j * (int64_t)SPILOT + runs - 1) / runs + 4;
+        st.s_rp = (uint32_t)min(rp, (int64_t)SLIST);
       }
-      TensorState st;
-      memset(&st, 0, sizeof st);
       if (k <= 0) st.flags = TS_NOEMIT;
       if (A.mode == MODE_RANDK && k > 0) {
         // keys ~kappa, kappa uniform on 32-bit words: emit kappa < tau with
@@ -254,12 +270,12 @@ __device__ __forceinline__ bool aborted(const TopkArgs& A) { return A.diag[DIAG_
 // `base`), read with one 16-byte load per input when aligned and complete.
 template <int MODE>
 __device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64_t base, int64_t n,
-                                                 int64_t li, bool vec, float a[4], bool ok[4]) {
+                                                 int64_t li, bool vec, float gmul, float a[4], bool ok[4]) {
   const int64_t gi = base + li;
   if (vec && li + 4 <= n) {
     float4 g4 = ld_stream(reinterpret_cast<const float4*>(A.g + gi));
     if (MODE != MODE_MOM) {
-      const float c = A.ts[t].gmul;
+      const float c = gmul;
       g4.x = __fmul_rn(c, g4.x);
       g4.y = __fmul_rn(c, g4.y);
       g4.z = __fmul_rn(c, g4.z);
@@ -438,18 +454,112 @@ __device__ uint32_t find_bucket(const uint32_t* row, uint32_t rank, uint32_t* ab
 // threads per tensor (two CTAs per SM, so that every tensor's CTA starts in
 // the first wave; each warp keeps SRUNS runs in flight).  The sample is runs
 // of RUN = 128 consecutive elements (one warp, 16 bytes per lane per input)
-// spaced `stride` apart; small tensors are sampled completely.  Level 1: shared-memory histogram of the
-// sample keys' top 11 bits -> the bucket of the j-th largest sample key.
-// Level 2: the next 11 bits of the sample keys in that bucket (re-read from
-// the sample key buffer) -> t_est = the lower edge of that level-2 bucket,
-// which is <= the j-th largest sample key.
-constexpr int SRUNS = 4;  // sample runs per warp per step
+// spaced `stride` apart; small tensors are sampled completely.
+//
+// t_est is the lower edge of the level-2 bucket (top 22 bits of the key) of
+// the j-th largest sample key, so t_est <= that key.  It is found from a
+// radix pass of two levels (top 11 bits, next 11 bits) over the sample keys
+// that matter:
+//  * filtered path (samples of at least SFILTER_RUNS runs): a pilot of
+//    SPILOT runs spread evenly over the sample gives a floor F, the level-2
+//    edge of the pilot key whose rank scales to about 4j in the whole sample;
+//    one pass over the sample then keeps only the keys >= F (histogram of
+//    their top bits, list in shared memory).  When at least j keys pass, the
+//    j-th largest and its buckets lie among them and every key above it is
+//    counted, so both levels give the same buckets as over the whole sample;
+//  * direct path (small samples, or a filter that kept fewer than j keys or
+//    more than the list holds): both levels over every sample key, the keys
+//    stored in the sample key buffer between the levels.
+
+// Keys of the sample runs r = (r0 + h * rstep) * rmul, h < SR, r0 + h * rstep < rend;
+// bit c of okm[h] flags key[h][c] as a sample element.  Every run's loads
+// are issued before any is used, so that a warp keeps SR runs in flight;
+// runs that are not whole aligned float4s per lane (the tensor's tail, an
+// unaligned tensor) and the pending-residual mode (which rebuilds e per
+// element) take the per-run path.
+template <int MODE>
+constexpr int sample_runs_in_flight() { return MODE == MODE_MOM ? 2 : 4; }
+
+template <int MODE, int SR>
+__device__ __forceinline__ void sample_keys(const TopkArgs& A, int t, int64_t base, int64_t n, int64_t stride,
+                                            int r0, int rstep, int rend, int rmul, bool vec, float gmul,
+                                            unsigned lane, uint32_t key[SR][4], unsigned okm[SR]) {
+  constexpr bool MOM = MODE == MODE_MOM;
+  if (!MOM && A.rd) {
+    // pending residual: one run at a time
+#pragma unroll
+    for (int h = 0; h < SR; ++h) {
+      const int ri = r0 + h * rstep;
+      float a[4];
+      bool ok[4] = {false, false, false, false};
+      if (ri < rend)
+        acc4_from_inputs<MODE>(A, t, base, n, sample_run_start((int64_t)ri * rmul, stride) + 4 * lane, vec, gmul,
+                               a, ok);
+      okm[h] = (ok[0] ? 1u : 0u) | (ok[1] ? 2u : 0u) | (ok[2] ? 4u : 0u) | (ok[3] ? 8u : 0u);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) key[h][c] = ok[c] ? mag_key(a[c]) : 0u;
+    }
+    return;
+  }
+  const float* gp = A.g + base;
+  const float* ep = MOM ? A.u + base : A.e + base;  // second input (e, or u)
+  const float* vp = A.v + base;
+  const bool ef = MOM || A.ef;
+  float4 x[SR], y[SR], z[SR];
+  int li[SR];  // n < 2^31
+#pragma unroll
+  for (int h = 0; h < SR; ++h) {
+    const int ri = r0 + h * rstep;
+    li[h] = ri < rend ? (int)sample_run_start((int64_t)ri * rmul, stride) + 4 * (int)lane : (int)n;
+    if (vec && (int64_t)li[h] + 4 <= n) {
+      x[h] = ld_stream(reinterpret_cast<const float4*>(gp + li[h]));
+      if (ef) y[h] = ld_stream(reinterpret_cast<const float4*>(ep + li[h]));
+      if (MOM) z[h] = ld_stream(reinterpret_cast<const float4*>(vp + li[h]));
+    } else {
+      // tail or unaligned tensor: element loads, zero past the end
+      float xs[4] = {0.f, 0.f, 0.f, 0.f}, ys[4] = {0.f, 0.f, 0.f, 0.f}, zs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if ((int64_t)li[h] + c < n) {
+          xs[c] = gp[li[h] + c];
+          if (ef) ys[c] = ep[li[h] + c];
+          if (MOM) zs[c] = vp[li[h] + c];
+        }
+      }
+      x[h] = make_float4(xs[0], xs[1], xs[2], xs[3]);
+      y[h] = make_float4(ys[0], ys[1], ys[2], ys[3]);
+      z[h] = make_float4(zs[0], zs[1], zs[2], zs[3]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < SR; ++h) {
+    const float g4[4] = {x[h].x, x[h].y, x[h].z, x[h].w}, e4[4] = {y[h].x, y[h].y, y[h].z, y[h].w};
+    unsigned m = 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float a;
+      if (MOM) {
+        const float v4[4] = {z[h].x, z[h].y, z[h].z, z[h].w};
+        a = __fadd_rn(v4[c], __fadd_rn(__fmul_rn(A.beta, e4[c]), g4[c]));
+      } else {
+        const float gv = __fmul_rn(gmul, g4[c]);
+        a = ef ? __fadd_rn(gv, e4[c]) : gv;
+      }
+      const bool ok = (int64_t)li[h] + c < n;
+      m |= (ok ? 1u : 0u) << c;
+      key[h][c] = ok ? mag_key(a) : 0u;
+    }
+    okm[h] = m;
+  }
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[2];
+  __shared__ uint32_t s_cnt;
   __shared__ uint32_t sh[NBINS];
+  __shared__ uint32_t sl[SLIST];
   const int t = blockIdx.x;
   if (aborted(A)) return;
   TensorState* st = A.ts + t;
@@ -459,55 +569,122 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   if (k >= n) return;  // t_est set by the planner
   // threshold mode: never below the threshold's own key
   const uint32_t floor_key = A.tau ? mag_key(A.tau[t]) : 0u;
-  int64_t runs, stride, m;
-  sample_plan(n, k, &runs, &stride, &m);
-  int64_t j;
-  if (m >= n) {
-    j = k;
-  } else {
-    const double lam = (double)k * (double)m / (double)n;
-    j = (int64_t)ceil(lam + 4.0 * sqrt(lam) + 4.0);
-  }
+  const uint4 plan = *reinterpret_cast<const uint4*>(&st->s_runs);  // runs, stride, j, rp
+  const int runs = (int)plan.x;
+  const int64_t stride = plan.y, j = plan.z;
+  const int64_t m = min((int64_t)runs * RUN, n);
+  const float gmul = st->gmul;
   if (j > m) {
     if (threadIdx.x == 0) st->t_est = floor_key;
     return;
   }
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  __syncthreads();
   const unsigned lane = lane_id();
   const bool vec = (base & 3) == 0;
-  uint32_t* sk = A.skey + A.soff[t];
-  const int64_t nwarp = blockDim.x >> 5;
-  for (int64_t r0 = threadIdx.x >> 5; r0 < runs; r0 += SRUNS * nwarp) {
-    float a[SRUNS][4];
-    bool ok[SRUNS][4];
+  const int nwarp = blockDim.x >> 5, w = threadIdx.x >> 5;
+  constexpr int SR = sample_runs_in_flight<MODE>();
+  uint32_t key[SR][4];
+  unsigned okm[SR];
+  uint32_t b1 = 0xFFFFFFFFu, above = 0u, lvl2_n = 0u;
+  const uint32_t* lvl2 = nullptr;  // keys for level 2 (shared list or sample buffer)
+  bool filtered = false;
+
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  if (runs >= SFILTER_RUNS) {
+    // pilot: runs i * ps, i < SPILOT, keys kept in sl
+    const int ps = runs / SPILOT;
+    for (int i0 = w; i0 < SPILOT; i0 += SR * nwarp) {
+      sample_keys<MODE, SR>(A, t, base, n, stride, i0, nwarp, SPILOT, ps, vec, gmul, lane, key, okm);
 #pragma unroll
-    for (int h = 0; h < SRUNS; ++h) {
-      const int64_t r = r0 + h * nwarp;
-      if (r < runs) {
-        acc4_from_inputs<MODE>(A, t, base, n, sample_run_start(r, stride) + 4 * lane, vec, a[h], ok[h]);
-      } else {
-        ok[h][0] = ok[h][1] = ok[h][2] = ok[h][3] = false;
-      }
-    }
+      for (int h = 0; h < SR; ++h) {
+        const int i = i0 + h * nwarp;
+        if (i < SPILOT) {
 #pragma unroll
-    for (int h = 0; h < SRUNS; ++h) {
-      const int64_t r = r0 + h * nwarp;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t key = mag_key(a[h][c]);
-        if (ok[h][c]) {
-          sk[r * RUN + 4 * lane + c] = key;
-          atomicAdd(sh + (key >> 21), 1u);
+          for (int c = 0; c < 4; ++c) sl[i * RUN + 4 * lane + c] = key[h][c];
         }
       }
     }
+    __syncthreads();
+    for (int i = threadIdx.x; i < SLIST; i += blockDim.x) atomicAdd(sh + (sl[i] >> 21), 1u);
+    __syncthreads();
+    const uint32_t rp = plan.w;
+    uint32_t pabove;
+    const uint32_t p1 = find_bucket(sh, rp, &pabove, s_warp, s_res);
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+    __syncthreads();
+    uint32_t F = 0u;
+    if (p1 != 0xFFFFFFFFu) {
+      for (int i = threadIdx.x; i < SLIST; i += blockDim.x) {
+        const uint32_t kk = sl[i];
+        if ((kk >> 21) == p1) atomicAdd(sh + ((kk >> 10) & 0x7FFu), 1u);
+      }
+      __syncthreads();
+      uint32_t pabove2;
+      const uint32_t p2 = find_bucket(sh, rp - pabove, &pabove2, s_warp, s_res);
+      F = (p1 << 21) | (p2 == 0xFFFFFFFFu ? 0u : (p2 << 10));
+      for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+    }
+    if (threadIdx.x == 0) s_cnt = 0u;
+    __syncthreads();
+    // filtered pass: histogram of the keys >= F, list of them in sl
+    for (int r0 = w; r0 < runs; r0 += SR * nwarp) {
+      sample_keys<MODE, SR>(A, t, base, n, stride, r0, nwarp, runs, 1, vec, gmul, lane, key, okm);
+#pragma unroll
+      for (int h = 0; h < SR; ++h) {
+        unsigned msk = 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) msk |= (((okm[h] >> c) & 1u) && key[h][c] >= F ? 1u : 0u) << c;
+        if (__any_sync(FULL, msk != 0u)) {
+          unsigned pre, tot;
+          warp_count_scan(__popc(msk), lane, &pre, &tot);
+          uint32_t at = 0u;
+          if (lane == 0) at = atomicAdd(&s_cnt, tot);
+          at = __shfl_sync(FULL, at, 0) + pre;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if ((msk >> c) & 1u) {
+              atomicAdd(sh + (key[h][c] >> 21), 1u);
+              if (at < (uint32_t)SLIST) sl[at] = key[h][c];
+              ++at;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t c = s_cnt;
+    if (c >= (uint32_t)j && c <= (uint32_t)SLIST) {
+      filtered = true;
+      lvl2 = sl;
+      lvl2_n = c;
+      b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
+    }
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+    __syncthreads();
   }
-  __syncthreads();
-  uint32_t above;
-  const uint32_t b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
-  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  __syncthreads();
+  if (!filtered) {
+    // direct path: level 1 over every sample key, keys kept in the sample buffer
+    uint32_t* sk = A.skey + A.soff[t];
+    for (int r0 = w; r0 < runs; r0 += SR * nwarp) {
+      sample_keys<MODE, SR>(A, t, base, n, stride, r0, nwarp, runs, 1, vec, gmul, lane, key, okm);
+#pragma unroll
+      for (int h = 0; h < SR; ++h) {
+        const int64_t r = r0 + h * nwarp;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if ((okm[h] >> c) & 1u) {
+            sk[r * RUN + 4 * lane + c] = key[h][c];
+            atomicAdd(sh + (key[h][c] >> 21), 1u);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+    __syncthreads();
+    lvl2 = sk;
+    lvl2_n = (uint32_t)m;
+  }
   if (b1 == 0xFFFFFFFFu) {
     if (threadIdx.x == 0) {
       atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
@@ -517,17 +694,17 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   }
   const uint32_t rank2 = (uint32_t)j - above;
   constexpr int U8 = 16;
-  for (int64_t i0 = 0; i0 < m; i0 += (int64_t)blockDim.x * U8) {
+  for (uint32_t i0 = 0; i0 < lvl2_n; i0 += blockDim.x * U8) {
     uint32_t kk[U8];
 #pragma unroll
     for (int u = 0; u < U8; ++u) {
-      const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
-      kk[u] = i < m ? __ldcg(sk + i) : 0u;
+      const uint32_t i = i0 + u * blockDim.x + threadIdx.x;
+      kk[u] = i < lvl2_n ? (filtered ? lvl2[i] : __ldcg(lvl2 + i)) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < U8; ++u) {
-      const int64_t i = i0 + (int64_t)u * blockDim.x + threadIdx.x;
-      smem_hist_add(sh, (kk[u] >> 10) & 0x7FFu, i < m && (kk[u] >> 21) == b1);
+      const uint32_t i = i0 + u * blockDim.x + threadIdx.x;
+      smem_hist_add(sh, (kk[u] >> 10) & 0x7FFu, i < lvl2_n && (kk[u] >> 21) == b1);
     }
   }
   __syncthreads();
@@ -1001,6 +1178,20 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
   }
 }
 
+// The candidate chunks of a warp's 32 units are walked as one concatenated
+// sequence, 32 entries per step with one entry per lane, so that loads are
+// contiguous and no lane idles on a short chunk.  `off` is this lane's
+// exclusive prefix of the chunk lengths; returns the lane whose chunk holds
+// entry e (e below the total): the last lane with off <= e, which skips
+// empty chunks.
+__device__ __forceinline__ int chunk_owner(uint32_t off, uint32_t e) {
+  int o = 0;
+#pragma unroll
+  for (int b = 16; b >= 1; b >>= 1)
+    if (__shfl_sync(FULL, off, o + b) <= e) o += b;
+  return o;
+}
+
 // Per-unit counts of keys above / equal to the k-th key, and their sums
 // per unit block.
 template <int MODE>
@@ -1037,23 +1228,37 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
           s_eq[ui] = eq;
         }
       }
-    } else if (tid < ub.nu) {
-      const uint2 ch = A.chunk[ub.u0 + tid];
-      const uint32_t* ck = A.ckey + A.cand_off[ub.t] + ch.x;
-      uint32_t gt = 0u, eq = 0u;
-      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
-        uint32_t kk[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ch.y ? __ldcs(ck + j0 + u) : 0u;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool v = j0 + u < ch.y;
-          gt += v && kk[u] > st.thr;
-          eq += v && kk[u] == st.thr;
+    } else {
+      // the warp's 32 chunks walked as one sequence (see chunk_owner)
+      const unsigned lane = lane_id();
+      const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
+      unsigned L;
+      const uint32_t off = warp_excl_scan(ch.y, lane, &L);
+      const uint32_t* ck = A.ckey + A.cand_off[ub.t];
+      uint32_t Gc = 0u, Ec = 0u, gs = 0u, es = 0u;
+      for (uint32_t ws = 0; ws < L; ws += 32u) {
+        const uint32_t e = ws + lane;
+        const int o = chunk_owner(off, e);
+        const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
+        const bool act = e < L;
+        const uint32_t key = act ? __ldcs(ck + chx_o + (e - off_o)) : 0u;
+        const unsigned gtm = __ballot_sync(FULL, act && key > st.thr);
+        const unsigned eqm = __ballot_sync(FULL, act && key == st.thr);
+        if (off - ws < 32u) {  // this unit's first entry is in this step
+          const unsigned below = (1u << (off - ws)) - 1u;
+          gs = Gc + __popc(gtm & below);
+          es = Ec + __popc(eqm & below);
         }
+        Gc += __popc(gtm);
+        Ec += __popc(eqm);
       }
-      s_gt[tid] = gt;
-      s_eq[tid] = eq;
+      if (off >= L) {  // empty units after the last entry
+        gs = Gc;
+        es = Ec;
+      }
+      const uint32_t gn = __shfl_down_sync(FULL, gs, 1), en = __shfl_down_sync(FULL, es, 1);
+      s_gt[tid] = (lane == 31u ? Gc : gn) - gs;
+      s_eq[tid] = (lane == 31u ? Ec : en) - es;
     }
   }
   __syncthreads();
@@ -1180,35 +1385,54 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
         eqrun += __popc(eqm);
       }
     }
-  } else if (tid < ub.nu) {
-    const uint2 ch = A.chunk[ub.u0 + tid];
-    const int64_t cb = A.cand_off[ub.t] + ch.x;
-    const uint32_t eqb = s_eq[tid];
-    int64_t selpos = (int64_t)s_gt[tid] + min(eqb, r_eq);
-    uint32_t eqrun = 0u;
-    for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
-      uint32_t kk[8];
-      int32_t ci[8];
-      float cv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool v = j0 + u < ch.y;
-        kk[u] = v ? __ldcs(A.ckey + cb + j0 + u) : 0u;
-        ci[u] = v ? __ldcs(A.cidx + cb + j0 + u) : 0;
-        cv[u] = v ? __ldcs(A.cval + cb + j0 + u) : 0.0f;
+  } else {
+    // the warp's 32 chunks walked as one sequence (see chunk_owner); kept
+    // and tie counts inside a unit are differences of running counts over
+    // the sequence, taken at the unit's first entry
+    const unsigned lane = lane_id();
+    const unsigned lt = (1u << lane) - 1u;
+    const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
+    const uint32_t eqb = s_eq[tid];                   // ties before this unit
+    const uint32_t sel0 = s_gt[tid] + min(eqb, r_eq);  // kept before this unit
+    unsigned L;
+    const uint32_t off = warp_excl_scan(ch.y, lane, &L);
+    const int64_t cb = A.cand_off[ub.t];
+    uint32_t Kc = 0u, Ec = 0u, ks = 0u, es = 0u;
+    for (uint32_t ws = 0; ws < L; ws += 32u) {
+      const uint32_t e = ws + lane;
+      const int o = chunk_owner(off, e);
+      const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
+      const uint32_t eqb_o = __shfl_sync(FULL, eqb, o), sel0_o = __shfl_sync(FULL, sel0, o);
+      const uint32_t es_o = __shfl_sync(FULL, es, o), ks_o = __shfl_sync(FULL, ks, o);
+      const bool act = e < L;
+      uint32_t key = 0u;
+      int32_t li = 0;
+      float x = 0.0f;
+      if (act) {
+        const int64_t c = cb + chx_o + (e - off_o);
+        key = __ldcs(A.ckey + c);
+        li = __ldcs(A.cidx + c);
+        x = __ldcs(A.cval + c);
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (j0 + u >= ch.y) break;
-        const bool iseq = kk[u] == thr;
-        const bool sel = kk[u] > thr || (iseq && eqb + eqrun < r_eq);
-        const bool last = iseq && eqb + eqrun + 1u == r_eq;
-        eqrun += iseq;
-        if (sel) {
-          emit_kept<MODE>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
-          ++selpos;
-        }
+      const bool iseq = act && key == thr;
+      const unsigned eqm = __ballot_sync(FULL, iseq);
+      // the owner's first entry is in this step (off_o - ws <= 31 for every lane)
+      const bool here = off_o >= ws;
+      const unsigned below_o = (1u << ((off_o - ws) & 31u)) - 1u;
+      const uint32_t eqr = eqb_o + (Ec + __popc(eqm & lt) - (here ? Ec + __popc(eqm & below_o) : es_o));
+      const bool sel = act && (key > thr || (iseq && eqr < r_eq));
+      const unsigned selm = __ballot_sync(FULL, sel);
+      if (sel) {
+        const uint32_t kin = Kc + __popc(selm & lt) - (here ? Kc + __popc(selm & below_o) : ks_o);
+        emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + sel0_o + kin, s, iseq && eqr + 1u == r_eq);
       }
+      if (off - ws < 32u) {
+        const unsigned below = (1u << (off - ws)) - 1u;
+        ks = Kc + __popc(selm & below);
+        es = Ec + __popc(eqm & below);
+      }
+      Kc += __popc(selm);
+      Ec += __popc(eqm);
     }
   }
 }
