@@ -66,7 +66,7 @@ static_assert(offsetof(TensorState, s_runs) % 16 == 0, "sample plan is one 16-by
 
 // ---------------------------------------------------------------- sizing
 // Candidate capacity of a tensor, identical on host and device.  The sampled
-// threshold yields about 1.6k candidates for a large tensor, with a relative
+// threshold yields about 1.5k candidates for a large tensor, with a relative
 // spread of about 7%, so 3k + 4096 is many standard deviations above it.
 __host__ __device__ inline int64_t cand_capacity(int64_t n, int64_t k) {
   if (k <= 0) return 0;

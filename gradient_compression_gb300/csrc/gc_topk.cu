@@ -138,14 +138,16 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
         sample_plan(n, k, &runs, &stride, &m);
         ns = m;
         // the sample key of rank j bounds t_est: j = k for a complete sample,
-        // else the expected count lam of Top-k members in the sample plus six
-        // standard deviations (and 8), so that fewer than k candidates needs
-        // about a 5-sigma sample (with four, about one tensor-step in 10^4
-        // fell short under error feedback and took the full-pass path)
+        // else the expected count lam of Top-k members in the sample plus five
+        // standard deviations (and 6).  Fewer than k candidates then needs a
+        // Poisson(lam) count of at least j (about 1e-7 at lam = 128); with four
+        // (and 4) about one tensor-step in 10^4 fell short under error
+        // feedback and took the full-pass path.  Each standard deviation of
+        // margin costs about 7% more candidates.
         int64_t j = k;
         if (m < n) {
           const double lam = (double)k * (double)m / (double)n;
-          j = (int64_t)ceil(lam + 6.0 * sqrt(lam) + 8.0);
+          j = (int64_t)ceil(lam + 5.0 * sqrt(lam) + 6.0);
         }
         st.s_runs = (uint32_t)runs;
         st.s_stride = (uint32_t)stride;
@@ -1092,6 +1094,52 @@ __device__ __forceinline__ UnitBlock unit_block(const TopkArgs& A) {
   return r;
 }
 
+// Full-pass walk of one unit (tensors selected without candidates): the warp
+// takes 128 elements per step, four consecutive per lane, and issues the
+// loads of DSTEPS steps before using any.  f(o, key, x, ok) runs on every
+// lane for each step in index order: o is the unit-local offset of the
+// lane's first element, bit c of ok flags element o + c as inside the unit.
+template <int MODE, bool LOADX, int DSTEPS = 4, class F>
+__device__ __forceinline__ void dense_unit_walk(const TopkArgs& A, const float* src, int64_t g0, int len,
+                                                unsigned lane, F&& f) {
+  const bool vec = (g0 & 3) == 0;
+  for (int i0 = 0; i0 < len; i0 += 128 * DSTEPS) {
+    float x[DSTEPS][4];
+#pragma unroll
+    for (int st = 0; st < DSTEPS; ++st) {
+      const int o = i0 + st * 128 + 4 * (int)lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[st][c] = 0.0f;
+      if (LOADX) {
+        if (vec && o + 4 <= len) {
+          const float4 v = __ldcs(reinterpret_cast<const float4*>(src + g0 + o));
+          x[st][0] = v.x;
+          x[st][1] = v.y;
+          x[st][2] = v.z;
+          x[st][3] = v.w;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (o + c < len) x[st][c] = src[g0 + o + c];
+        }
+      }
+    }
+#pragma unroll
+    for (int st = 0; st < DSTEPS; ++st) {
+      const int o = i0 + st * 128 + 4 * (int)lane;
+      uint32_t key[4];
+      unsigned ok = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool in = o + c < len;
+        ok |= (in ? 1u : 0u) << c;
+        key[c] = in ? key_of<MODE>(A, x[st][c], g0 + o + c) : 0u;
+      }
+      f(o, key, x[st], ok);
+    }
+  }
+}
+
 // Histogram level `level` (1, 2, 3) of the keys matching the tensor's
 // prefix.  Level 1 runs only for tensors selected by full passes (the
 // candidate level-1 histogram comes from the streaming pass).
@@ -1124,23 +1172,20 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
     for (int ui = threadIdx.x >> 5; ui < ub.nu; ui += blockDim.x >> 5) {
       const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
       const int len = (int)min((int64_t)UNIT, ub.n - lstart);
-      for (int i0 = 0; i0 < len; i0 += 32) {
-        const int64_t li = lstart + i0 + lane;
-        const bool valid = i0 + (int)lane < len;
-        uint32_t key = 0u;
-        if (valid) {
-          const int64_t gi = ub.base + li;
-          const float x = (MODE == MODE_RANDK) ? 0.0f : src[gi];
-          key = key_of<MODE>(A, x, gi);
-        }
-        const bool hit = valid && (level == 1 || (key >> shift_prev) == st.prefix);
-        if (valid) mx = max(mx, key);
-        if (count_tau) {
-          const unsigned c = __popc(__ballot_sync(FULL, valid && key >= tkey));
-          if (lane == 0 && c) atomicAdd(&s_tau, c);
-        }
-        smem_hist_add(sh, (key >> shift) & mask, hit);
-      }
+      dense_unit_walk<MODE, MODE != MODE_RANDK>(
+          A, src, ub.base + lstart, len, lane, [&](int, const uint32_t* key, const float*, unsigned ok) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const bool valid = (ok >> c) & 1u;
+              const bool hit = valid && (level == 1 || (key[c] >> shift_prev) == st.prefix);
+              if (valid) mx = max(mx, key[c]);
+              if (count_tau) {
+                const unsigned cnt = __popc(__ballot_sync(FULL, valid && key[c] >= tkey));
+                if (lane == 0 && cnt) atomicAdd(&s_tau, cnt);
+              }
+              smem_hist_add(sh, (key[c] >> shift) & mask, hit);
+            }
+          });
     }
     if (level == 1) {
       mx = warp_max_u32(mx);
@@ -1213,16 +1258,17 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
         const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
         const int len = (int)min((int64_t)UNIT, ub.n - lstart);
         uint32_t gt = 0u, eq = 0u;
-        for (int i0 = 0; i0 < len; i0 += 32) {
-          const bool valid = i0 + (int)lane < len;
-          uint32_t key = 0u;
-          if (valid) {
-            const int64_t gi = ub.base + lstart + i0 + lane;
-            key = key_of<MODE>(A, (MODE == MODE_RANDK) ? 0.0f : src[gi], gi);
-          }
-          gt += __popc(__ballot_sync(FULL, valid && key > st.thr));
-          eq += __popc(__ballot_sync(FULL, valid && key == st.thr));
-        }
+        dense_unit_walk<MODE, MODE != MODE_RANDK>(
+            A, src, ub.base + lstart, len, lane, [&](int, const uint32_t* key, const float*, unsigned ok) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const bool valid = (ok >> c) & 1u;
+                gt += (valid && key[c] > st.thr) ? 1u : 0u;
+                eq += (valid && key[c] == st.thr) ? 1u : 0u;
+              }
+            });
+        gt = __reduce_add_sync(FULL, gt);
+        eq = __reduce_add_sync(FULL, eq);
         if (lane == 0) {
           s_gt[ui] = gt;
           s_eq[ui] = eq;
@@ -1356,34 +1402,43 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
   const uint32_t thr = st.thr, r_eq = st.r_eq;
   if (st.flags & TS_DENSE) {
     const unsigned lane = lane_id();
-    const unsigned lt = (1u << lane) - 1u;
     const float* src = value_source<MODE>(A);
     for (int ui = tid >> 5; ui < ub.nu; ui += blockDim.x >> 5) {
       const int64_t lstart = (ub.u0 + ui - A.units_off[ub.t]) << UNIT_SHIFT;
       const int len = (int)min((int64_t)UNIT, ub.n - lstart);
       const uint32_t eqb = s_eq[ui];
       int64_t selpos = (int64_t)s_gt[ui] + min(eqb, r_eq);
-      uint32_t eqrun = 0u;
-      for (int i0 = 0; i0 < len; i0 += 32) {
-        const int64_t li = lstart + i0 + lane;
-        const bool valid = i0 + (int)lane < len;
-        float x = 0.0f;
-        uint32_t key = 0u;
-        if (valid) {
-          const int64_t gi = ub.base + li;
-          x = (MODE == MODE_RANDK && A.unbiased) ? 0.0f : src[gi];
-          key = key_of<MODE>(A, x, gi);
-        }
-        const bool isgt = valid && key > thr, iseq = valid && key == thr;
-        const unsigned eqm = __ballot_sync(FULL, iseq);
-        const bool sel = isgt || (iseq && eqb + eqrun + __popc(eqm & lt) < r_eq);
-        const unsigned selm = __ballot_sync(FULL, sel);
-        if (sel)
-          emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + selpos + __popc(selm & lt), s,
-                          iseq && eqb + eqrun + __popc(eqm & lt) + 1u == r_eq);
-        selpos += __popc(selm);
-        eqrun += __popc(eqm);
-      }
+      uint32_t eqrun = 0u;  // ties before this step in the unit
+      dense_unit_walk<MODE, true, 2>(
+          A, src, ub.base + lstart, len, lane, [&](int o, const uint32_t* key, const float* x, unsigned ok) {
+            unsigned eqm = 0u, gtm = 0u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const bool valid = (ok >> c) & 1u;
+              eqm |= (valid && key[c] == thr ? 1u : 0u) << c;
+              gtm |= (valid && key[c] > thr ? 1u : 0u) << c;
+            }
+            unsigned epre, etot;
+            warp_count_scan(__popc(eqm), lane, &epre, &etot);
+            unsigned selm = gtm;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t rank = eqb + eqrun + epre + __popc(eqm & ((1u << c) - 1u));
+              if (((eqm >> c) & 1u) && rank < r_eq) selm |= 1u << c;
+            }
+            unsigned spre, stot;
+            warp_count_scan(__popc(selm), lane, &spre, &stot);
+            for (unsigned m = selm; m != 0u; m &= m - 1u) {  // one emit site, no unrolling
+              const int c = __ffs(m) - 1;
+              const unsigned below = (1u << c) - 1u;
+              const bool last = ((eqm >> c) & 1u) && eqb + eqrun + epre + __popc(eqm & below) + 1u == r_eq;
+              const float xv = c == 0 ? x[0] : (c == 1 ? x[1] : (c == 2 ? x[2] : x[3]));
+              emit_kept<MODE>(A, ub.t, ub.base, ub.n, lstart + o + c, xv, kbase + selpos + spre + __popc(selm & below),
+                              s, last);
+            }
+            selpos += stot;
+            eqrun += etot;
+          });
     }
   } else {
     // the warp's 32 chunks walked as one sequence (see chunk_owner); kept
