@@ -1325,37 +1325,25 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
           s_eq[ui] = eq;
         }
       }
-    } else {
-      // the warp's 32 chunks walked as one sequence (see chunk_owner)
-      const unsigned lane = lane_id();
-      const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
-      unsigned L;
-      const uint32_t off = warp_excl_scan(ch.y, lane, &L);
-      const uint32_t* ck = A.ckey + A.cand_off[ub.t];
-      uint32_t Gc = 0u, Ec = 0u, gs = 0u, es = 0u;
-      for (uint32_t ws = 0; ws < L; ws += 32u) {
-        const uint32_t e = ws + lane;
-        const int o = chunk_owner(off, e);
-        const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
-        const bool act = e < L;
-        const uint32_t key = act ? __ldcs(ck + chx_o + (e - off_o)) : 0u;
-        const unsigned gtm = __ballot_sync(FULL, act && key > st.thr);
-        const unsigned eqm = __ballot_sync(FULL, act && key == st.thr);
-        if (off - ws < 32u) {  // this unit's first entry is in this step
-          const unsigned below = (1u << (off - ws)) - 1u;
-          gs = Gc + __popc(gtm & below);
-          es = Ec + __popc(eqm & below);
+    } else if (tid < ub.nu) {
+      // a thread per unit (the concatenated walk of k_write measured slower
+      // here: counting costs less per entry than finding its unit)
+      const uint2 ch = A.chunk[ub.u0 + tid];
+      const uint32_t* ck = A.ckey + A.cand_off[ub.t] + ch.x;
+      uint32_t gt = 0u, eq = 0u;
+      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
+        uint32_t kk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ch.y ? __ldcs(ck + j0 + u) : 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool v = j0 + u < ch.y;
+          gt += v && kk[u] > st.thr;
+          eq += v && kk[u] == st.thr;
         }
-        Gc += __popc(gtm);
-        Ec += __popc(eqm);
       }
-      if (off >= L) {  // empty units after the last entry
-        gs = Gc;
-        es = Ec;
-      }
-      const uint32_t gn = __shfl_down_sync(FULL, gs, 1), en = __shfl_down_sync(FULL, es, 1);
-      s_gt[tid] = (lane == 31u ? Gc : gn) - gs;
-      s_eq[tid] = (lane == 31u ? Ec : en) - es;
+      s_gt[tid] = gt;
+      s_eq[tid] = eq;
     }
   }
   __syncthreads();
@@ -1411,7 +1399,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(256) k_write(TopkArgs A) {
+__global__ void __launch_bounds__(256, MODE == MODE_TOPK ? 5 : 4) k_write(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
@@ -1471,9 +1459,13 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
           });
     }
   } else {
-    // the warp's 32 chunks walked as one sequence (see chunk_owner); kept
-    // and tie counts inside a unit are differences of running counts over
-    // the sequence, taken at the unit's first entry
+    // Candidate path.  Long chunks (the warp's units average 40 or more
+    // candidates): a thread walks its unit's chunk.  Short chunks: the warp's
+    // 32 chunks are walked as one sequence (see chunk_owner), and kept and
+    // tie counts inside a unit are differences of running counts over the
+    // sequence, taken at the unit's first entry; this keeps every lane busy
+    // when a few long chunks would otherwise hold the warp (measured faster
+    // at 0.1-0.5% density, slower at 1%: random-k on ResNet-50).
     const unsigned lane = lane_id();
     const unsigned lt = (1u << lane) - 1u;
     const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
@@ -1482,6 +1474,36 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
     unsigned L;
     const uint32_t off = warp_excl_scan(ch.y, lane, &L);
     const int64_t cb = A.cand_off[ub.t];
+    if (L >= 32u * 40u) {
+      const int64_t cu = cb + ch.x;
+      int64_t selpos = sel0;
+      uint32_t eqrun = 0u;
+      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
+        uint32_t kk[8];
+        int32_t ci[8];
+        float cv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool v = j0 + u < ch.y;
+          kk[u] = v ? __ldcs(A.ckey + cu + j0 + u) : 0u;
+          ci[u] = v ? __ldcs(A.cidx + cu + j0 + u) : 0;
+          cv[u] = v ? __ldcs(A.cval + cu + j0 + u) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (j0 + u >= ch.y) break;
+          const bool iseq = kk[u] == thr;
+          const bool sel = kk[u] > thr || (iseq && eqb + eqrun < r_eq);
+          const bool last = iseq && eqb + eqrun + 1u == r_eq;
+          eqrun += iseq;
+          if (sel) {
+            emit_kept<MODE>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
+            ++selpos;
+          }
+        }
+      }
+      return;
+    }
     uint32_t Kc = 0u, Ec = 0u, ks = 0u, es = 0u;
     for (uint32_t ws = 0; ws < L; ws += 32u) {
       const uint32_t e = ws + lane;

@@ -148,6 +148,27 @@ def test_topk_ties(gc, kind, exact):
         assert d.overflow_tensors >= 1 and d.exact_tensors >= 1
 
 
+@pytest.mark.parametrize("rho", [0.001, 0.01])
+@pytest.mark.parametrize("flags_name", ["ef", "ef_int8"])
+def test_topk_boundary_ties(gc, rho, flags_name):
+    """A group of equal magnitudes straddles the k-th rank (ties kept by lowest
+    index); 0.1% gives short candidate chunks per unit, 1% long ones, so both
+    candidate walks of the payload write meet a partial tie group."""
+    n = 300_000
+    flags = gc.GC_EF | (gc.GC_INT8 if flags_name == "ef_int8" else 0)
+    L = _layout(gc, [n, 4099], rho=rho)
+    g = _grad(L.numel, 21).numpy()
+    k0 = int(L.k[0])
+    mag = np.sort(np.abs(g[:n]))[::-1]
+    v = mag[k0 - 40]
+    rng = np.random.default_rng(22)
+    pos = rng.choice(n, 120, replace=False)
+    g[pos] = np.where(rng.random(120) < 0.5, -v, v).astype(F32)
+    e = np.zeros(L.numel, F32)
+    _, d = _topk_check(gc, L, g, e, flags, seed=9, it=0, expect_exact=0)
+    assert d.overflow_tensors == 0
+
+
 def test_topk_flat_2p20_ten_iterations(gc):
     """One flat fp32 gradient of 2^20 elements at 0.1% (k = 1049), EF, 10 fresh gradients."""
     lay = workloads.flat_layout(1 << 20)
