@@ -46,8 +46,8 @@ CFG, RHO, INT8 = 5, 0.001, True
 # kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan,
 # the sampled threshold estimate, the streaming pass, the level-1 select,
 # three histogram passes (full-pass level 1, candidate levels 2 and 3) with
-# their selects, count (ending with the scan), write
-LAUNCHES_PER_STEP = 12
+# their selects, count, scan, write
+LAUNCHES_PER_STEP = 13
 # bytes the streaming pass must move per element: read g, read e, write e
 STREAM_BYTES_PER_ELEM = 12
 # integer multiplies of one Philox4x32-10 word (random-k keys, QSGD rounding)

@@ -55,7 +55,7 @@ struct alignas(16) TensorState {
   uint32_t keff;        // elements kept (k_t, or fewer under a threshold)
   float gmul;           // multiplier applied to g (local clipping), else 1
   uint32_t cnt_tau;     // elements with |acc| >= tau (threshold mode, full-pass path)
-  uint32_t done;        // CTAs of the current kernel finished on this tensor (0 between kernels)
+  uint32_t pad0;
   uint32_t s_runs;      // sample plan (set by the planner; 16-byte aligned): runs of RUN elements,
   uint32_t s_stride;    //   their spacing,
   uint32_t s_j;         //   the rank of the sample key that bounds t_est,
