@@ -41,6 +41,10 @@ MUTANTS = {
     "powersgd_q_transposed": ("q[jcol * r + k] = (float)dot_rows(m, &M[jcol], n, p + k, r);",
                               "q[jcol * r + k] = (float)dot_rows(m, &M[jcol], 1, p + k, r);",
                               ["test_powersgd_one_step_matches_numpy_and_keeps_the_residual"]),
+    "int8_decode_scale_dropped": ("      d = (float)codes[i] * sc;", "      d = (float)codes[i];",
+                                  ["test_int8_decode_exact_on_a_representable_grid_and_restores_acc"]),
+    "momentum_int8_residual_zeroed": ("      v[i] = v[i] - d;", "      v[i] = 0.0f;",
+                                      ["test_momentum_int8_reduces_to_ef_topk_int8_and_keeps_quantization_error"]),
     "randk_largest_keys": ("if (key[a] != key[b]) return key[a] < key[b];", "if (key[a] != key[b]) return key[a] > key[b];",
                            ["test_randk_selection_is_k_smallest_keys"]),
 }

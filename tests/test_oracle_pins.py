@@ -591,3 +591,64 @@ def test_powersgd_ratio_page_figure():
     m = n = 4096
     r = 4
     assert (m * n) / ((m + n) * r) == 512
+
+
+# ----------------------------------------------------------------------------- int8 receivers and momentum + int8
+
+def test_int8_decode_exact_on_a_representable_grid_and_restores_acc():
+    # A tensor on the grid s * {-127..127} with max |x| = 127 s is quantized
+    # without rounding (every |x| / s is an integer), so decoding returns x
+    # exactly: genomic glossary "Gradient Compression", 8-bit quantization,
+    # code * scale.  s = 0.5 (not 1), so a decoder that forgets the scale fails.
+    rng = np.random.default_rng(41)
+    steps = rng.integers(-127, 128, size=2000)
+    steps[7] = 127
+    x = (steps * 0.5).astype(F32)
+    codes, s = oracle.quantize_tensor(x, None, "int8", seed=3, it=2)
+    assert s == F32(0.5) and np.array_equal(codes.astype(np.int64), steps)
+    base = rng.integers(-1000, 1000, size=x.size).astype(F32)   # integers: every sum below is exact
+    out = base.copy()
+    oracle.codes_decode_accumulate(codes, s, "int8", out)
+    assert np.array_equal(out, base + x)
+    # Off the grid: the receiver's value plus the sender's residual gives acc
+    # back to within half an ulp of the residual (the EF identity, nothing lost).
+    g = (rng.standard_t(3, 4000) * 1e-3).astype(F32)
+    e0 = (rng.standard_normal(4000) * 1e-5).astype(F32)
+    e = e0.copy()
+    codes, s = oracle.quantize_tensor(g, e, "int8", seed=5, it=9)
+    dec = np.zeros(4000, F32)
+    oracle.codes_decode_accumulate(codes, s, "int8", dec)
+    acc = (g + e0).astype(np.float64)
+    err = np.abs(acc - (dec.astype(np.float64) + e.astype(np.float64)))
+    assert np.all(err <= 0.5 * np.spacing(np.abs(e)).astype(np.float64))
+    assert np.abs(dec - acc).max() <= float(s) * (1 + 2 ** -20)     # one quantization step at most
+
+
+def test_momentum_int8_reduces_to_ef_topk_int8_and_keeps_quantization_error():
+    rng = np.random.default_rng(42)
+    n, k = 3000, 40
+    g = (rng.standard_t(3, n) * 1e-3).astype(F32)
+    v0 = (rng.standard_normal(n) * 1e-4).astype(F32)
+    # beta = 0: u' = g, v' = v + g, which is EF Top-k + int8 with e = v
+    u = rng.standard_normal(n).astype(F32)
+    v, e = v0.copy(), v0.copy()
+    i1, x1, q1, s1 = oracle.momentum_topk_tensor(g, u, v, k, 0.0, int8=True, seed=11, it=4)
+    i2, x2, q2, s2 = oracle.ef_topk_tensor(g, e, k, int8=True, seed=11, it=4)
+    assert np.array_equal(i1, i2) and np.array_equal(q1, q2) and s1 == s2 and np.array_equal(x1, x2)
+    assert np.array_equal(v.view(np.uint32), e.view(np.uint32))
+    # beta = 0.9: the kept entries' velocity keeps exactly the quantization
+    # error (v' + q s restores v to half an ulp of v'); the rest keep v; u is
+    # cleared on the kept set (factor masking)
+    u0 = (rng.standard_normal(n) * 1e-3).astype(F32)
+    u, v = u0.copy(), v0.copy()
+    idx, val, q, s = oracle.momentum_topk_tensor(g, u, v, k, 0.9, int8=True, seed=12, it=5)
+    u_new = F32(0.9) * u0 + g
+    v_pre = v0 + u_new
+    assert idx.tolist() == _brute_topk(v_pre, k)
+    deq = q.astype(F32) * F32(s)
+    assert np.array_equal(val, deq)
+    err = np.abs(v_pre[idx].astype(np.float64) - (deq.astype(np.float64) + v[idx].astype(np.float64)))
+    assert np.all(err <= 0.5 * np.spacing(np.abs(v[idx])).astype(np.float64))
+    assert np.all(np.abs(v[idx]) <= F32(s) * (1 + 2 ** -20))
+    rest = np.setdiff1d(np.arange(n), idx)
+    assert np.array_equal(v[rest], v_pre[rest]) and np.all(u[idx] == 0) and np.array_equal(u[rest], u_new[rest])
