@@ -43,6 +43,10 @@ def _declare(L):
     L.oracle_momentum_topk_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _F, _I32, _P, _P, _P, _P,
                                               _U64, _U64, _I32, _I32]
     L.oracle_sign_tensor.argtypes = [_I64, _P, _P, _P, _P, _P]
+    L.oracle_ef_topk_quantized_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32,
+                                                  _U64, _U64, _I32]
+    L.oracle_momentum_topk_quantized_tensor.argtypes = [_I64, _I64, _U64, _P, _P, _P, _F, _I32, _P, _P, _P, _P,
+                                                        _P, _P, _I32, _I32, _U64, _U64, _I32]
     L.oracle_quantize_tensor.argtypes = [_I64, _U64, _P, _P, _P, _P, _I32, _I32, _U64, _U64, _P]
     L.oracle_sparse_accumulate.argtypes = [_I32, _P, _P, _I32, _P, _P, _P, _P, _P]
     L.oracle_sign_decode_accumulate.argtypes = [_I64, _P, _F, _P]
@@ -52,6 +56,7 @@ def _declare(L):
     for name in ("oracle_select", "oracle_ef_topk_tensor", "oracle_randk_tensor", "oracle_threshold_tensor", "oracle_clip_topk_tensor",
                  "oracle_powersgd_tensor", "oracle_powersgd_decode_accumulate",
                  "oracle_momentum_topk_tensor", "oracle_sign_tensor", "oracle_quantize_tensor",
+                 "oracle_ef_topk_quantized_tensor", "oracle_momentum_topk_quantized_tensor",
                  "oracle_sparse_accumulate", "oracle_sign_decode_accumulate",
                  "oracle_codes_decode_accumulate"):
         getattr(L, name).restype = C.c_int
@@ -194,6 +199,50 @@ def momentum_topk_tensor(g, u, v, k, beta, masking=True, base=0, int8=False, see
                                              _p(idx), _p(val), _p(q), _p(sc), seed, it, int(int8), method),
            "momentum")
     return idx, val, q, (float(sc[0]) if int8 else None)
+
+
+KEPT_KINDS = {"qsgd": 2, "sign": 3}
+
+
+def _kept_buffers(k, kind):
+    q = np.zeros(k, np.int8) if kind == "qsgd" else None
+    bits = np.zeros((k + 31) // 32, np.uint32) if kind == "sign" else None
+    return q, bits
+
+
+def ef_topk_quantized_tensor(g, e, k, kind, s_levels=16, base=0, seed=0, it=0, scale_given=None, method=1):
+    """EF Top-k, then QSGD ('qsgd') or sign ('sign') of the kept values.
+    Returns (idx, decoded values, codes or None, bits or None, scale computed);
+    e (if given) is updated in place."""
+    g = _c(g, np.float32); n = g.size
+    if e is not None:
+        assert e.dtype == np.float32 and e.flags.c_contiguous and e.size == n
+    idx = np.zeros(k, np.int32); val = np.zeros(k, np.float32)
+    q, bits = _kept_buffers(k, kind)
+    sc = np.zeros(1, np.float32)
+    sg = None if scale_given is None else np.asarray([scale_given], np.float32)
+    _check(lib().oracle_ef_topk_quantized_tensor(n, k, base, _p(g), _p(e), _p(idx), _p(val), _p(q), _p(bits),
+                                                 _p(sc), _p(sg), KEPT_KINDS[kind], s_levels, seed, it, method),
+           "ef_topk_quantized")
+    return idx, val, q, bits, float(sc[0])
+
+
+def momentum_topk_quantized_tensor(g, u, v, k, beta, kind, s_levels=16, masking=True, base=0, seed=0, it=0,
+                                   scale_given=None, method=1):
+    """Momentum correction + Top-k, then QSGD or sign of the kept velocity.
+    Returns (idx, decoded values, codes or None, bits or None, scale computed)."""
+    g = _c(g, np.float32); n = g.size
+    for a in (u, v):
+        assert a.dtype == np.float32 and a.flags.c_contiguous and a.size == n
+    idx = np.zeros(k, np.int32); val = np.zeros(k, np.float32)
+    q, bits = _kept_buffers(k, kind)
+    sc = np.zeros(1, np.float32)
+    sg = None if scale_given is None else np.asarray([scale_given], np.float32)
+    _check(lib().oracle_momentum_topk_quantized_tensor(n, k, base, _p(g), _p(u), _p(v), float(beta), int(masking),
+                                                       _p(idx), _p(val), _p(q), _p(bits), _p(sc), _p(sg),
+                                                       KEPT_KINDS[kind], s_levels, seed, it, method),
+           "momentum_topk_quantized")
+    return idx, val, q, bits, float(sc[0])
 
 
 def sign_tensor(g, e, mu_given=None):

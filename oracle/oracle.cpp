@@ -388,6 +388,126 @@ int oracle_momentum_topk_tensor(int64_t n, int64_t k, uint64_t base, const float
   return 0;
 }
 
+// ------------------------------------------------------------------ quantized kept values
+// QSGD or sign quantization applied after Top-k ([P4] QSGD eq.
+// Q_s(g) = ||g|| sgn(g) xi(g, s) and its stochastic rounding; [P4] 1-bit SGD
+// eq. sign(g) ||g||_1 / d with one scalar; [P1] the Top-k + 8-bit pipeline,
+// quantization applied to the values that sparsification kept).  The
+// quantized vector is the kept one: its d entries are the k kept values x_j,
+// in ascending index order.
+//   kind 2, QSGD: N = (float)sqrt(sum_j x_j^2) (fp64 in index order);
+//     y = (|x_j| * s_levels) / N; level = min(s_levels, SR(y)) with the
+//     Philox word of purpose 2 at the element's arena index; code =
+//     sgn * level (int8); decoded value sgn * ((level * N) / s_levels).
+//     N == 0 gives level 0.
+//   kind 3, sign: mu = (float)(sum_j |x_j| / k) (fp64 in index order, 0 when
+//     k == 0); bit j = 1 iff x_j has a clear sign bit, packed LSB-first 32 per
+//     word (pad bits 0); decoded value bit ? mu : -mu.
+// res[i] (the EF residual or the velocity) becomes x - decoded on the kept
+// set.  scale_given != NULL replaces the computed N or mu.
+namespace {
+const int32_t KEPT_QSGD = 2, KEPT_SIGN = 3;
+
+int quantize_kept(int32_t kind, int32_t s_levels, const std::vector<int64_t>& S, const float* x,
+                  float* res, uint64_t base, uint64_t seed, uint64_t iter, int8_t* q, uint32_t* bits,
+                  float* val, float* scale_out, const float* scale_given) {
+  const int64_t k = (int64_t)S.size();
+  float sc;
+  if (kind == KEPT_QSGD) {
+    double ss = 0.0;
+    for (int64_t i : S) ss += (double)x[i] * (double)x[i];
+    sc = (float)std::sqrt(ss);
+  } else {
+    double sa = 0.0;
+    for (int64_t i : S) sa += std::fabs((double)x[i]);
+    sc = k > 0 ? (float)(sa / (double)k) : 0.0f;
+  }
+  if (scale_out) *scale_out = sc;
+  if (scale_given) sc = *scale_given;
+  if (kind == KEPT_SIGN)
+    for (int64_t w = 0; w < (k + 31) / 32; ++w) bits[w] = 0u;
+  for (int64_t j = 0; j < k; ++j) {
+    const int64_t i = S[j];
+    const bool neg = std::signbit(x[i]);
+    float d;
+    if (kind == KEPT_QSGD) {
+      int level = 0;
+      if (sc != 0.0f) {
+        const float y = (std::fabs(x[i]) * (float)s_levels) / sc;
+        double m = stochastic_round(y, draw_u32(seed, iter, base + (uint64_t)i, PURPOSE_QSGD));
+        if (m > (double)s_levels) m = (double)s_levels;
+        level = (int)m;
+      }
+      q[j] = (int8_t)(neg ? -level : level);
+      const float mag = ((float)level * sc) / (float)s_levels;
+      d = neg ? -mag : mag;
+    } else {
+      if (!neg) bits[j / 32] |= 1u << (j % 32);
+      d = neg ? -sc : sc;
+    }
+    if (val) val[j] = d;
+    if (res) res[i] = x[i] - d;
+  }
+  return 0;
+}
+}  // namespace
+
+// EF Top-k, then QSGD (kind 2) or sign (kind 3) of the kept values:
+//   acc = g + e (e may be NULL: no EF); S = Top-k of acc by |acc|;
+//   idx = S ascending; codes / bits and scale[0] of quantize_kept over acc[S];
+//   e' = acc off S, acc - decoded on S (the residual keeps the quantization
+//   error, as with int8).  `val`, when given, receives the decoded values.
+int oracle_ef_topk_quantized_tensor(int64_t n, int64_t k, uint64_t base, const float* g, float* e,
+                                    int32_t* idx, float* val, int8_t* q, uint32_t* bits,
+                                    float* scale_out, const float* scale_given, int32_t kind,
+                                    int32_t s_levels, uint64_t seed, uint64_t iter, int32_t method) {
+  if (n < 0 || k < 0 || k > n) return 1;
+  if (kind != KEPT_QSGD && kind != KEPT_SIGN) return 1;
+  if (kind == KEPT_QSGD && (!q || s_levels < 1 || s_levels > 127)) return 1;
+  if (kind == KEPT_SIGN && !bits) return 1;
+  std::vector<float> acc(n);
+  for (int64_t i = 0; i < n; ++i) acc[i] = e ? g[i] + e[i] : g[i];
+  std::vector<uint32_t> key(n);
+  for (int64_t i = 0; i < n; ++i) key[i] = magnitude_key(acc[i]);
+  std::vector<int64_t> S = select_k<LargerFirst>(n, k, key.data(), method);
+  for (size_t j = 0; j < S.size(); ++j) idx[j] = (int32_t)S[j];
+  std::vector<float> res(acc);
+  quantize_kept(kind, s_levels, S, acc.data(), res.data(), base, seed, iter, q, bits, val, scale_out,
+                scale_given);
+  if (e)
+    for (int64_t i = 0; i < n; ++i) e[i] = res[i];
+  return 0;
+}
+
+// Momentum correction + Top-k, then QSGD or sign of the kept velocity
+// (the update of oracle_momentum_topk_tensor; v'[S] = v' - decoded, u'[S] = +0
+// with masking).
+int oracle_momentum_topk_quantized_tensor(int64_t n, int64_t k, uint64_t base, const float* g,
+                                          float* u, float* v, float beta, int32_t masking,
+                                          int32_t* idx, float* val, int8_t* q, uint32_t* bits,
+                                          float* scale_out, const float* scale_given, int32_t kind,
+                                          int32_t s_levels, uint64_t seed, uint64_t iter,
+                                          int32_t method) {
+  if (n < 0 || k < 0 || k > n) return 1;
+  if (kind != KEPT_QSGD && kind != KEPT_SIGN) return 1;
+  if (kind == KEPT_QSGD && (!q || s_levels < 1 || s_levels > 127)) return 1;
+  if (kind == KEPT_SIGN && !bits) return 1;
+  for (int64_t i = 0; i < n; ++i) {
+    float bu = beta * u[i];
+    u[i] = bu + g[i];
+    v[i] = v[i] + u[i];
+  }
+  std::vector<uint32_t> key(n);
+  for (int64_t i = 0; i < n; ++i) key[i] = magnitude_key(v[i]);
+  std::vector<int64_t> S = select_k<LargerFirst>(n, k, key.data(), method);
+  for (size_t j = 0; j < S.size(); ++j) idx[j] = (int32_t)S[j];
+  std::vector<float> x(v, v + n);
+  quantize_kept(kind, s_levels, S, x.data(), v, base, seed, iter, q, bits, val, scale_out, scale_given);
+  if (masking)
+    for (int64_t i : S) u[i] = 0.0f;
+  return 0;
+}
+
 // ------------------------------------------------------------------ sign
 // 1-bit SGD ([P4] eq. Q(g) = sign(g) ||g||_1 / d, with a per-layer scalar):
 //   acc = g + e (EF; e may be NULL)

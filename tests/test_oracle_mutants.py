@@ -45,6 +45,16 @@ MUTANTS = {
                                   ["test_int8_decode_exact_on_a_representable_grid_and_restores_acc"]),
     "momentum_int8_residual_zeroed": ("      v[i] = v[i] - d;", "      v[i] = 0.0f;",
                                       ["test_momentum_int8_reduces_to_ef_topk_int8_and_keeps_quantization_error"]),
+    "kept_qsgd_norm_by_position": ("for (int64_t i : S) ss += (double)x[i] * (double)x[i];",
+                                   "for (size_t i = 0; i < S.size(); ++i) ss += (double)x[i] * (double)x[i];",
+                                   ["test_kept_qsgd_norm_is_over_the_kept_set_and_one_kept_value_is_sent_exactly"]),
+    "kept_qsgd_draw_purpose": ("const float y = (std::fabs(x[i]) * (float)s_levels) / sc;\n        double m = stochastic_round(y, draw_u32(seed, iter, base + (uint64_t)i, PURPOSE_QSGD));",
+                               "const float y = (std::fabs(x[i]) * (float)s_levels) / sc;\n        double m = stochastic_round(y, draw_u32(seed, iter, base + (uint64_t)i, PURPOSE_INT8));",
+                               ["test_kept_quantizers_with_every_element_kept_are_the_dense_quantizers"]),
+    "kept_sign_bit_inverted": ("      if (!neg) bits[j / 32] |= 1u << (j % 32);", "      if (neg) bits[j / 32] |= 1u << (j % 32);",
+                               ["test_kept_sign_bits_mean_and_residual"]),
+    "kept_residual_dropped": ("    if (res) res[i] = x[i] - d;", "    if (res) res[i] = 0.0f;",
+                              ["test_kept_sign_bits_mean_and_residual"]),
     "randk_largest_keys": ("if (key[a] != key[b]) return key[a] < key[b];", "if (key[a] != key[b]) return key[a] > key[b];",
                            ["test_randk_selection_is_k_smallest_keys"]),
 }

@@ -652,3 +652,116 @@ def test_momentum_int8_reduces_to_ef_topk_int8_and_keeps_quantization_error():
     assert np.all(np.abs(v[idx]) <= F32(s) * (1 + 2 ** -20))
     rest = np.setdiff1d(np.arange(n), idx)
     assert np.array_equal(v[rest], v_pre[rest]) and np.all(u[idx] == 0) and np.array_equal(u[rest], u_new[rest])
+
+
+# ----------------------------------------------------------------------------- QSGD / sign of the kept values
+
+def _tensor(seed, n, scale=1e-3):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_t(3, n) * scale).astype(F32), (rng.standard_normal(n) * scale * 0.1).astype(F32)
+
+
+def test_kept_quantizers_with_every_element_kept_are_the_dense_quantizers():
+    # k = n: the quantized vector is the whole tensor, so QSGD / sign of the
+    # kept values must be the dense QSGD / 1-bit SGD of acc (mbrenndoerfer.com
+    # QSGD and 1-bit SGD equations), with the same draws at the same arena
+    # indices and the same EF residual
+    for n, base in ((1, 0), (33, 7), (1000, 4097), (4099, 123456789)):
+        g, e0 = _tensor(50 + n, n)
+        e1, e2 = e0.copy(), e0.copy()
+        idx, val, q, _, N = oracle.ef_topk_quantized_tensor(g, e1, n, "qsgd", 16, base=base, seed=3, it=5)
+        codes, N2 = oracle.quantize_tensor(g, e2, "qsgd", 16, base=base, seed=3, it=5)
+        assert idx.tolist() == list(range(n)) and N == N2
+        assert np.array_equal(q, codes) and np.array_equal(e1.view(np.uint32), e2.view(np.uint32))
+        dec = np.zeros(n, F32)
+        oracle.codes_decode_accumulate(codes, N2, "qsgd", dec, 16)
+        assert np.array_equal(val, dec)
+        e1, e2 = e0.copy(), e0.copy()
+        idx, val, _, bits, mu = oracle.ef_topk_quantized_tensor(g, e1, n, "sign", base=base)
+        bits2, mu2 = oracle.sign_tensor(g, e2)
+        assert mu == mu2 and np.array_equal(bits, bits2)
+        assert np.array_equal(e1.view(np.uint32), e2.view(np.uint32))
+
+
+def test_kept_qsgd_norm_is_over_the_kept_set_and_one_kept_value_is_sent_exactly():
+    g, e0 = _tensor(61, 5000)
+    acc = g + e0
+    for k in (1, 7, 50, 4999):
+        e = e0.copy()
+        idx, val, q, _, N = oracle.ef_topk_quantized_tensor(g, e, k, "qsgd", 16, seed=2, it=1)
+        assert idx.tolist() == _brute_topk(acc, k)
+        ref = np.linalg.norm(acc[idx].astype(np.float64))
+        assert abs(N - ref) <= 1e-6 * ref
+        assert N < np.linalg.norm(acc.astype(np.float64))          # not the whole tensor's norm
+        assert np.all(np.abs(q) <= 16) and np.all(np.sign(q) * np.sign(acc[idx]) >= 0)
+        # residual keeps the quantization error; nothing is lost
+        err = np.abs(acc[idx].astype(np.float64) - (val.astype(np.float64) + e[idx].astype(np.float64)))
+        assert np.all(err <= 0.5 * np.spacing(np.abs(e[idx])).astype(np.float64))
+        rest = np.setdiff1d(np.arange(5000), idx)
+        assert np.array_equal(e[rest], acc[rest])
+        if k == 1:
+            # a single kept value: N = |x| and the level is s (s = 16, so
+            # |x| * s / N is exact): the receiver gets x itself, e' = +0
+            i = idx[0]
+            assert N == abs(acc[i]) and abs(int(q[0])) == 16 and val[0] == acc[i] and e[i] == 0.0
+
+
+def test_kept_qsgd_is_unbiased():
+    g, _ = _tensor(62, 400, scale=1.0)
+    k, trials, s = 40, 3000, 4
+    tot = np.zeros(k)
+    first = None
+    for it in range(trials):
+        idx, val, q, _, N = oracle.ef_topk_quantized_tensor(g, None, k, "qsgd", s, seed=9, it=it)
+        first = idx if first is None else first
+        assert np.array_equal(idx, first)
+        tot += val
+    x = g[first].astype(np.float64)
+    step = float(N) / s
+    y = np.abs(x) / step
+    frac = y - np.floor(y)
+    sd = np.sqrt(frac * (1 - frac) / trials) * step
+    assert np.all(np.abs(tot / trials - x) <= 5 * sd + 4 * np.spacing(np.abs(x)))
+
+
+def test_kept_sign_bits_mean_and_residual():
+    g, e0 = _tensor(63, 3001)
+    g[::13] = -0.0
+    acc = g + e0
+    for k in (1, 31, 32, 33, 100, 3001):
+        e = e0.copy()
+        idx, val, _, bits, mu = oracle.ef_topk_quantized_tensor(g, e, k, "sign")
+        assert idx.tolist() == _brute_topk(acc, k)
+        x = acc[idx]
+        pos = ~np.signbit(x)
+        packed = np.packbits(pos.astype(np.uint8), bitorder="little")
+        packed = np.concatenate([packed, np.zeros((-packed.size) % 4, np.uint8)]).view("<u4")
+        assert np.array_equal(bits, packed)
+        ref = np.mean(np.abs(x.astype(np.float64)))
+        assert abs(mu - ref) <= 1e-6 * ref
+        d = np.where(pos, F32(mu), F32(-mu))
+        assert np.array_equal(val, d) and np.array_equal(e[idx], x - d)
+        rest = np.setdiff1d(np.arange(3001), idx)
+        assert np.array_equal(e[rest], acc[rest])
+    # all kept values positive: every bit set, the decoded values are their mean
+    y = np.linspace(1.0, 2.0, 64).astype(F32)
+    idx, val, _, bits, mu = oracle.ef_topk_quantized_tensor(y, None, 40, "sign")
+    assert bits.tolist() == [0xFFFFFFFF, 0xFF] and np.all(val == F32(mu))
+    assert abs(mu - np.mean(y[idx].astype(np.float64))) <= 1e-6 * mu
+    # nothing kept: scale 0, no bits
+    _, _, _, bits, mu = oracle.ef_topk_quantized_tensor(y, None, 0, "sign")
+    assert bits.size == 0 and mu == 0.0
+
+
+def test_momentum_quantized_reduces_to_ef_topk_quantized():
+    g, v0 = _tensor(64, 2000)
+    rng = np.random.default_rng(65)
+    for kind in ("qsgd", "sign"):
+        u = rng.standard_normal(2000).astype(F32)
+        v, e = v0.copy(), v0.copy()
+        a = oracle.momentum_topk_quantized_tensor(g, u, v, 25, 0.0, kind, 16, seed=4, it=2)
+        b = oracle.ef_topk_quantized_tensor(g, e, 25, kind, 16, seed=4, it=2)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[4] == b[4]
+        assert (a[2] is None or np.array_equal(a[2], b[2])) and (a[3] is None or np.array_equal(a[3], b[3]))
+        assert np.array_equal(v.view(np.uint32), e.view(np.uint32))
+        assert np.all(u[a[0]] == 0) and np.array_equal(np.delete(u, a[0]), np.delete(g, a[0]))
