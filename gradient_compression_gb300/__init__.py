@@ -74,6 +74,7 @@ def lib() -> C.CDLL:
         L.gc_warmup_density.argtypes = [I64, I64, C.c_double, C.c_double, I32, I32]
         L.gc_warmup_density.restype = C.c_double
         L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
+        L.gc_ef_topk_compress_noalloc_status.argtypes = [P, C.POINTER(gc_diag)]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
         L.gc_quantize_stochastic.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, U64, P, SZ, P]
@@ -86,7 +87,8 @@ def lib() -> C.CDLL:
         L.gc_status_string.restype = C.c_char_p
         L.gc_version.restype = I32
         for name in ("gc_workspace_size", "gc_ef_topk_compress", "gc_ef_topk_compress_profiled",
-                     "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
+                     "gc_ef_topk_compress_noalloc", "gc_ef_topk_compress_noalloc_status",
+                     "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
                      "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
                      "gc_ef_topk_compress_clipped", "gc_powersgd_workspace_size", "gc_powersgd_compress",
                      "gc_powersgd_decompress_accumulate",
@@ -290,6 +292,15 @@ def ef_topk_compress_noalloc(layout, g, e, idx, val, q, scale, seed, it, flags, 
     _check(lib().gc_ef_topk_compress_noalloc(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx),
                                              _ptr(val), _ptr(q), _ptr(scale), int(seed), int(it), int(flags),
                                              _stream(stream)), "gc_ef_topk_compress_noalloc")
+
+
+def noalloc_device_status(stream=None, raise_on_error=True) -> gc_diag:
+    """Diagnostics of the last ef_topk_compress_noalloc call on the current device."""
+    d = gc_diag()
+    st = lib().gc_ef_topk_compress_noalloc_status(_stream(stream), C.byref(d))
+    if st != GC_OK and (raise_on_error or st != GC_ERR_DEVICE):
+        raise GCError(st, f"gc_ef_topk_compress_noalloc_status (error bits 0x{d.error_bits:x})")
+    return d
 
 
 def ef_topk_compress_profiled(layout, g, e, idx, val, q, scale, seed, it, flags, workspace, events,

@@ -72,3 +72,13 @@ extern "C" gc_status gc_ef_topk_compress_noalloc(const gc_layout* dev, const gc_
   return gc_ef_topk_compress(dev, host, g, e, idx, val, q, scale, seed, iter, flags, scratch,
                              kStaticBytes, stream);
 }
+
+extern "C" gc_status gc_ef_topk_compress_noalloc_status(void* stream, gc_diag* out) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_noalloc_status");
+  if (!out) return GC_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const gc_status st = scratch_for_current_device(&scratch);
+  if (st != GC_OK) return st;
+  // the diagnostic words sit at the head of the scratch, as in a workspace
+  return gc_get_device_status(scratch, kStaticBytes, stream, out);
+}

@@ -333,6 +333,16 @@ gc_status gc_ef_topk_compress_noalloc(const gc_layout* dev, const gc_layout* hos
                                       float* e, int32_t* idx, float* val, int8_t* q, float* scale,
                                       uint64_t seed, uint64_t iter, uint32_t flags, void* stream);
 
+/* Diagnostics of the last gc_ef_topk_compress_noalloc call on the current
+ * device: waits for `stream`, then reads the diagnostic words at the head of
+ * the built-in scratch (what gc_get_device_status reads from a caller's
+ * workspace).  It reports, for instance, GC_DIAG_LAYOUT_MISMATCH when that
+ * call's device and host layouts disagreed (its kernels then did nothing),
+ * and the exact_tensors / overflow_tensors counts.  A later noalloc call on
+ * any stream of the device overwrites them.  Returns GC_ERR_DEVICE if an error
+ * bit is set; allocates nothing. */
+gc_status gc_ef_topk_compress_noalloc_status(void* stream, gc_diag* out);
+
 /* DGC momentum correction + Top-k (inferensys.com "Gradient Sparsification",
  * momentum correction and momentum factor masking; genomic glossary, DGC):
  *   u = beta * u + g;  v = v + u;  S = Top-k of |v|;  payload v[S] (or int8);

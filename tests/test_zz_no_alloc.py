@@ -67,6 +67,10 @@ def test_noalloc_matches_workspace_entry_on_two_calls(gc, case):
             assert torch.equal(a[2], b[2]), f"call {it}: int8 codes"
             assert np.array_equal(_bits(a[3]), _bits(b[3])), f"call {it}: scales"
         assert np.array_equal(_bits(e_ws), _bits(e_na)), f"call {it}: residual"
+        # the built-in scratch's diagnostics are this call's, and match the workspace's
+        d_ws, d_na = gc.get_device_status(ws), gc.noalloc_device_status()
+        assert d_na.error_bits == 0
+        assert (d_na.exact_tensors, d_na.overflow_tensors) == (d_ws.exact_tensors, d_ws.overflow_tensors)
 
 
 def test_noalloc_rejects_layout_beyond_its_scratch(gc):
@@ -82,3 +86,32 @@ def test_noalloc_rejects_layout_beyond_its_scratch(gc):
     st = gc.lib().gc_ef_topk_compress_noalloc(L.dev(), L.host(), g.data_ptr(), g.data_ptr(), g.data_ptr(),
                                               g.data_ptr(), None, None, 0, 0, gc.GC_EF, None)
     assert st == gc.GC_ERR_WORKSPACE
+
+
+def test_noalloc_status_reports_layout_mismatch_then_clears(gc):
+    """A noalloc call whose device layout disagrees with the host mirror does
+    nothing and says so through gc_ef_topk_compress_noalloc_status, like a
+    workspace call through gc_get_device_status; the next good call's status
+    is clean, and with GC_FORCE_EXACT it counts every selecting tensor."""
+    sizes = [1000, 2000]
+    k = [10, 20]
+    L = gc.Layout(workloads.prefix(sizes), k, device="cuda")
+    bad = gc.Layout(workloads.prefix([1000, 3000]), k, device="cuda")
+    L._dev_off.copy_(bad._dev_off)                 # device copy disagrees with the host mirror
+    g = torch.zeros(3000, device="cuda")
+    e = torch.zeros(3000, device="cuda")
+    idx = torch.full((30,), -7, dtype=torch.int32, device="cuda")
+    val = torch.zeros(30, device="cuda")
+    gc.ef_topk_compress_noalloc(L, g, e, idx, val, None, None, 0, 0, gc.GC_EF)
+    d = gc.noalloc_device_status(raise_on_error=False)
+    assert d.error_bits & gc.GC_DIAG_LAYOUT_MISMATCH
+    with pytest.raises(gc.GCError) as ei:
+        gc.noalloc_device_status()
+    assert ei.value.status == gc.GC_ERR_DEVICE
+    assert (idx.cpu() == -7).all()
+    good = gc.Layout(workloads.prefix(sizes), k, device="cuda")
+    g = torch.randn(3000, device="cuda")
+    gc.ef_topk_compress_noalloc(good, g, e, idx, val, None, None, 0, 1, gc.GC_EF | gc.GC_FORCE_EXACT)
+    d = gc.noalloc_device_status()
+    assert d.error_bits == 0 and d.exact_tensors == 2 and d.overflow_tensors == 0
+    assert (idx.cpu() >= 0).all()
