@@ -21,6 +21,7 @@ GC_EF, GC_INT8, GC_RANDK, GC_UNBIASED, GC_NO_MASK, GC_FORCE_EXACT = 0x1, 0x2, 0x
 GC_OP_TOPK, GC_OP_MOMENTUM, GC_OP_SIGN, GC_OP_QUANTIZE, GC_OP_DECOMPRESS = range(5)
 GC_Q_INT8, GC_Q_QSGD = 0, 1
 GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
+GC_KEPT_INT8, GC_KEPT_QSGD, GC_KEPT_SIGN = 1, 2, 3
 GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE, GC_DIAG_BAD_THRESHOLD = 0x1, 0x2, 0x4, 0x8
 GC_NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 
@@ -76,6 +77,9 @@ def lib() -> C.CDLL:
         L.gc_ef_topk_compress_noalloc.argtypes = [LP, LP, P, P, P, P, P, P, U64, U64, U32, P]
         L.gc_ef_topk_compress_noalloc_status.argtypes = [P, C.POINTER(gc_diag)]
         L.gc_ef_topk_compress_momentum.argtypes = [LP, LP, P, P, P, F, P, P, P, P, U64, U64, U32, P, SZ, P]
+        L.gc_ef_topk_compress_quantized.argtypes = [LP, LP, P, P, P, P, P, P, P, I32, I32, U64, U64, U32, P, SZ, P]
+        L.gc_ef_topk_compress_momentum_quantized.argtypes = [LP, LP, P, P, P, F, P, P, P, P, P, I32, I32, U64, U64,
+                                                             U32, P, SZ, P]
         L.gc_sign_compress.argtypes = [LP, LP, P, P, P, P, P, SZ, P]
         L.gc_quantize_stochastic.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, U64, P, SZ, P]
         L.gc_quantize_stochastic_dev_iter.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, P, P, SZ, P]
@@ -92,7 +96,8 @@ def lib() -> C.CDLL:
                      "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
                      "gc_ef_topk_compress_clipped", "gc_powersgd_workspace_size", "gc_powersgd_compress",
                      "gc_powersgd_decompress_accumulate",
-                     "gc_ef_topk_compress_momentum",
+                     "gc_ef_topk_compress_momentum", "gc_ef_topk_compress_quantized",
+                     "gc_ef_topk_compress_momentum_quantized",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
                      "gc_dense_decompress_accumulate", "gc_get_device_status",
                      "gc_ef_topk_compress_dev_iter", "gc_quantize_stochastic_dev_iter"):
@@ -163,6 +168,11 @@ class Layout:
     @property
     def total_k(self) -> int:
         return int(self.koff[-1]) if self.koff is not None else 0
+
+    @property
+    def kept_words(self) -> int:
+        """uint32 words of the kept-value sign bits: sum of ceil(k_t / 32)."""
+        return int(((self.k + 31) // 32).sum())
 
     @property
     def words(self) -> int:
@@ -345,6 +355,26 @@ def ef_topk_compress_momentum(layout, g, u, v, beta, idx, val, q, scale, seed, i
                                               int(seed), int(it), int(flags), _ptr(workspace),
                                               workspace.numel(), _stream(stream)),
            "gc_ef_topk_compress_momentum")
+
+
+def ef_topk_compress_quantized(layout, g, e, idx, val, q, bits, scale, kind, s_levels, seed, it, flags, workspace,
+                               stream=None):
+    """EF Top-k, then GC_KEPT_INT8 / GC_KEPT_QSGD / GC_KEPT_SIGN of the kept values."""
+    _check(lib().gc_ef_topk_compress_quantized(layout.dev(), layout.host(), _ptr(g), _ptr(e), _ptr(idx), _ptr(val),
+                                               _ptr(q), _ptr(bits), _ptr(scale), int(kind), int(s_levels), int(seed),
+                                               int(it), int(flags), _ptr(workspace), workspace.numel(),
+                                               _stream(stream)), "gc_ef_topk_compress_quantized")
+
+
+def ef_topk_compress_momentum_quantized(layout, g, u, v, beta, idx, val, q, bits, scale, kind, s_levels, seed, it,
+                                        flags, workspace, stream=None):
+    """Momentum correction + Top-k, then a quantizer of the kept velocity."""
+    _check(lib().gc_ef_topk_compress_momentum_quantized(layout.dev(), layout.host(), _ptr(g), _ptr(u), _ptr(v),
+                                                        float(beta), _ptr(idx), _ptr(val), _ptr(q), _ptr(bits),
+                                                        _ptr(scale), int(kind), int(s_levels), int(seed), int(it),
+                                                        int(flags), _ptr(workspace), workspace.numel(),
+                                                        _stream(stream)),
+           "gc_ef_topk_compress_momentum_quantized")
 
 
 def sign_compress(layout, g, e, bits, mean_abs, workspace, stream=None):

@@ -34,6 +34,9 @@
 namespace gc {
 
 enum { MODE_TOPK = 0, MODE_RANDK = 1, MODE_MOM = 2 };
+// Quantizer of the kept values beyond int8 (A.int8): QSGD levels with the
+// norm of the kept vector, or sign bits with the mean |kept value|.
+enum { KQ_NONE = 0, KQ_QSGD = 2, KQ_SIGN = 3 };
 enum { PH_C1 = 0, PH_C1D = 1, PH_C2 = 2, PH_C3 = 3 };
 
 struct TopkArgs {
@@ -65,7 +68,12 @@ struct TopkArgs {
   int sampled;           // threshold estimated by sampling (Top-k and momentum)
   const float* clip;     // per-tensor maximum L2 norm of g (local clipping), else null
   float* norm_out;       // per-tensor ||g||_2 (local clipping)
-  double* upart;         // per-unit partial sums of g^2 (local clipping)
+  double* upart;         // per-unit partial sums of g^2 (local clipping); per-unit-block sums
+                         // over the kept values (QSGD / sign of the kept values)
+  int qkind;             // KQ_*: QSGD or sign of the kept values
+  int slev;              // QSGD levels
+  uint32_t* bits;        // sign bits of the kept values (KQ_SIGN)
+  int64_t* kwoff;        // [T+1] first word of each tensor's kept-value sign bits
   // workspace
   uint32_t* diag;
   TensorState* ts;
@@ -119,11 +127,11 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0;
+  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0, carry_w = 0;
   const bool sampled = A.sampled != 0;
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
-    int64_t nu = 0, nb = 0, nc = 0, ns = 0;
+    int64_t nu = 0, nb = 0, nc = 0, ns = 0, nw = 0;
     if (t < A.T) {
       const int64_t n = A.off[t + 1] - A.off[t];
       const int64_t k = A.kk[t];
@@ -131,6 +139,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       nu = units_of(n);
       nb = ublocks_of(n);
       nc = cand_capacity(n, k);
+      nw = k > 0 ? (k + 31) >> 5 : 0;
       TensorState st;
       memset(&st, 0, sizeof st);
       if (sampled && k > 0) {
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       st.gmul = 1.0f;
       A.ts[t] = st;
       if (A.count_out && (st.flags & TS_NOEMIT)) A.count_out[t] = 0;
-      if (A.int8 && k <= 0) A.scale[t] = 0.0f;
+      if ((A.int8 || A.qkind != KQ_NONE) && k <= 0) A.scale[t] = 0.0f;
     }
     int64_t tot;
     int64_t eu = block_excl_scan_i64(nu, s_warp, &tot);
@@ -193,6 +202,9 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     int64_t es = block_excl_scan_i64(ns, s_warp, &tot);
     if (t < A.T) A.soff[t] = carry_s + es;
     carry_s += tot;
+    int64_t ew = block_excl_scan_i64(nw, s_warp, &tot);
+    if (t < A.T) A.kwoff[t] = carry_w + ew;
+    carry_w += tot;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -200,6 +212,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     A.ublk_off[A.T] = carry_b;
     A.cand_off[A.T] = carry_c;
     A.soff[A.T] = carry_s;
+    A.kwoff[A.T] = carry_w;
     if (s_bad || carry_u != A.U || carry_b != A.UB || carry_c != A.C || carry_s != A.S ||
         A.off[0] != 0 || A.off[A.T] != A.N || A.koff[0] != 0 || A.koff[A.T] != A.K) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
@@ -1269,11 +1282,38 @@ __device__ __forceinline__ int chunk_owner(uint32_t off, uint32_t e) {
   return o;
 }
 
+// Term of the kept-set reduction for one kept magnitude (the key holds |x|
+// exactly): x^2 for the QSGD norm, |x| for the sign scale.  Both are exact
+// in fp64.
+__device__ __forceinline__ double kept_term(int qkind, uint32_t key) {
+  const double m = (double)key_magnitude(key);
+  return qkind == KQ_QSGD ? m * m : m;
+}
+
+// Sum of one fp64 value per thread over the CTA in a fixed order (a shuffle
+// tree per warp, then the warps in index order), so that the result does
+// not depend on timing.  Valid in thread 0.
+__device__ double block_sum_f64(double v, double* s_d) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(FULL, v, d);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane_id() == 0) s_d[w] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < nw; ++i) r += s_d[i];
+  return r;
+}
+
 // Exclusive scan of the unit-block sums of each tensor (one CTA each).  Doing
 // it in the last CTA of each tensor in k_count instead (one launch fewer)
 // measured slower on the Llama-3-8B arena: 64.7 against 46.5 + 5.3 us.
+// For QSGD / sign of the kept values it also sets the tensor's scale: the
+// unit blocks' sums in a fixed order plus the kept ties, then
+// N = (float)sqrt(sum x^2) or mu = (float)(sum |x| / k).
 __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
   __shared__ uint32_t s_warp[33];
+  __shared__ double s_d[32];
   if (aborted(A)) return;
   const int t = blockIdx.x;
   const int64_t b0 = A.ublk_off[t], b1 = A.ublk_off[t + 1];
@@ -1292,18 +1332,36 @@ __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
     carry_g += tg;
     carry_e += te;
   }
+  if (A.qkind != KQ_NONE) {
+    double part = 0.0;
+    for (int64_t b = b0 + threadIdx.x; b < b1; b += blockDim.x) part += A.upart[b];
+    const double tot = block_sum_f64(part, s_d);
+    if (threadIdx.x == 0) {
+      const TensorState st = A.ts[t];
+      if (!(st.flags & TS_NOEMIT)) {
+        const double sum = tot + (double)st.r_eq * kept_term(A.qkind, st.thr);
+        A.scale[t] = A.qkind == KQ_QSGD ? __double2float_rn(sqrt(sum))
+                                        : __double2float_rn(sum / (double)st.keff);
+      }
+    }
+  }
 }
 
 // Per-unit counts of keys above / equal to the k-th key, and their sums
-// per unit block.
-template <int MODE>
+// per unit block.  For QSGD / sign of the kept values, also each unit
+// block's fp64 sum of x^2 or |x| over its elements above the k-th key (the
+// kept ties, all of magnitude |k-th key|, are added per tensor by k_scan).
+template <int MODE, bool KSUM>
 __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
+  __shared__ double s_d[32];
   if (aborted(A)) return;
   const UnitBlock ub = unit_block(A);
   const TensorState st = A.ts[ub.t];
   const int tid = threadIdx.x;
+  constexpr bool kq = KSUM;  // QSGD / sign of the kept values (A.qkind != KQ_NONE)
+  double ksum = 0.0;
   s_gt[tid] = 0u;
   s_eq[tid] = 0u;
   __syncthreads();
@@ -1322,6 +1380,7 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
                 const bool valid = (ok >> c) & 1u;
                 gt += (valid && key[c] > st.thr) ? 1u : 0u;
                 eq += (valid && key[c] == st.thr) ? 1u : 0u;
+                if (kq && valid && key[c] > st.thr) ksum += kept_term(A.qkind, key[c]);
               }
             });
         gt = __reduce_add_sync(FULL, gt);
@@ -1346,6 +1405,7 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
           const bool v = j0 + u < ch.y;
           gt += v && kk[u] > st.thr;
           eq += v && kk[u] == st.thr;
+          if (kq && v && kk[u] > st.thr) ksum += kept_term(A.qkind, kk[u]);
         }
       }
       s_gt[tid] = gt;
@@ -1365,10 +1425,14 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
     A.bgt[blockIdx.x] = tg;
     A.beq[blockIdx.x] = te;
   }
+  if (kq) {
+    const double r = block_sum_f64(ksum, s_d);
+    if (tid == 0) A.upart[blockIdx.x] = r;
+  }
 }
 
 // Writes one kept element: payload slot `pos` (absolute), residual.
-template <int MODE>
+template <int MODE, int KQ>
 __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base, int64_t n,
                                           int64_t li, float x, int64_t pos, float s, bool last_tie) {
   if (A.rd && last_tie) A.rd[t].last_tie = (int32_t)li;
@@ -1389,7 +1453,31 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
     return;
   }
   float* res = (MODE == MODE_MOM) ? A.v : ((A.ef && !A.rd) ? A.e : nullptr);
-  if (A.int8) {
+  if (KQ == KQ_QSGD) {
+    // s = N: level = min(L, SR((|x| L) / N)), decoded sgn ((level N) / L)
+    const float L = (float)A.slev;
+    int level = 0;
+    if (s != 0.0f) {
+      // (|x| L) / N <= L because |x| <= N; the clamp (which cannot change
+      // min(L, .)) only guards the float -> int conversion
+      const float y = fminf(__fdiv_rn(__fmul_rn(fabsf(x), L), s), L + 1.0f);
+      level = min(A.slev, stochastic_round(y, philox_word(A.pk, iter_of(A), (uint64_t)gi, PURPOSE_QSGD)));
+    }
+    const bool neg = signbit(x);
+    const float mag = __fdiv_rn(__fmul_rn((float)level, s), L);
+    const float d = neg ? -mag : mag;
+    A.q[pos] = (int8_t)(neg ? -level : level);
+    if (A.val) A.val[pos] = d;
+    if (res) res[gi] = __fsub_rn(x, d);
+  } else if (KQ == KQ_SIGN) {
+    // s = mu: bit j of the tensor's words = sign bit of x clear; decoded +-mu
+    const bool neg = signbit(x);
+    const int64_t j = pos - A.koff[t];
+    if (!neg) atomicOr(A.bits + A.kwoff[t] + (j >> 5), 1u << (j & 31));
+    const float d = neg ? -s : s;
+    if (A.val) A.val[pos] = d;
+    if (res) res[gi] = __fsub_rn(x, d);
+  } else if (A.int8) {
     const int c = int8_code(x, s, philox_word(A.pk, iter_of(A), (uint64_t)gi, PURPOSE_INT8));
     const float d = __fmul_rn((float)c, s);
     A.q[pos] = (int8_t)c;
@@ -1402,7 +1490,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
   if (MODE == MODE_MOM && A.masking) A.u[gi] = 0.0f;
 }
 
-template <int MODE>
+template <int MODE, int KQ>
 __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
@@ -1420,7 +1508,7 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
   s_eq[tid] = A.beq[blockIdx.x] + pe;
   __syncthreads();
   const int64_t kbase = A.koff[ub.t];
-  const float s = A.int8 ? A.scale[ub.t] : 0.0f;
+  const float s = (A.int8 || KQ != KQ_NONE) ? A.scale[ub.t] : 0.0f;
   const uint32_t thr = st.thr, r_eq = st.r_eq;
   if (st.flags & TS_DENSE) {
     const unsigned lane = lane_id();
@@ -1455,7 +1543,7 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
               const unsigned below = (1u << c) - 1u;
               const bool last = ((eqm >> c) & 1u) && eqb + eqrun + epre + __popc(eqm & below) + 1u == r_eq;
               const float xv = c == 0 ? x[0] : (c == 1 ? x[1] : (c == 2 ? x[2] : x[3]));
-              emit_kept<MODE>(A, ub.t, ub.base, ub.n, lstart + o + c, xv, kbase + selpos + spre + __popc(selm & below),
+              emit_kept<MODE, KQ>(A, ub.t, ub.base, ub.n, lstart + o + c, xv, kbase + selpos + spre + __popc(selm & below),
                               s, last);
             }
             selpos += stot;
@@ -1501,7 +1589,7 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
           const bool last = iseq && eqb + eqrun + 1u == r_eq;
           eqrun += iseq;
           if (sel) {
-            emit_kept<MODE>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
+            emit_kept<MODE, KQ>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
             ++selpos;
           }
         }
@@ -1535,7 +1623,7 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
       const unsigned selm = __ballot_sync(FULL, sel);
       if (sel) {
         const uint32_t kin = Kc + __popc(selm & lt) - (here ? Kc + __popc(selm & below_o) : ks_o);
-        emit_kept<MODE>(A, ub.t, ub.base, ub.n, li, x, kbase + sel0_o + kin, s, iseq && eqr + 1u == r_eq);
+        emit_kept<MODE, KQ>(A, ub.t, ub.base, ub.n, li, x, kbase + sel0_o + kin, s, iseq && eqr + 1u == r_eq);
       }
       if (off - ws < 32u) {
         const unsigned below = (1u << (off - ws)) - 1u;
@@ -1576,7 +1664,7 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
 struct TopkCarve {
   size_t zero_bytes = 0, total = 0;
   size_t o_ts, o_hist, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
-      o_cidx, o_cval, o_skey, o_upart;
+      o_cidx, o_cval, o_skey, o_upart, o_kwoff;
 };
 
 static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
@@ -1604,6 +1692,7 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   c.o_cval = take(4 * (size_t)z.C);
   c.o_skey = take(4 * (size_t)z.S);
   c.o_upart = take(8 * (size_t)z.U);
+  c.o_kwoff = take(8 * (size_t)(T + 1));
   c.total = p;
   return c;
 }
@@ -1704,13 +1793,29 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
   pe.done(0, s);
   k_select<<<T, 256, 0, s>>>(A, PH_C3);
   pe.done(3, s);
-  k_count<MODE><<<UBg, 256, 0, s>>>(A);
+  if (MODE != MODE_RANDK && A.qkind != KQ_NONE)
+    k_count<MODE, MODE != MODE_RANDK><<<UBg, 256, 0, s>>>(A);
+  else
+    k_count<MODE, false><<<UBg, 256, 0, s>>>(A);
   pe.done(0, s);
   k_scan<<<T, 256, 0, s>>>(A);
   pe.done(0, s);
-  k_write<MODE><<<UBg, 256, 0, s>>>(A);
+  if (MODE != MODE_RANDK && A.qkind == KQ_QSGD)
+    k_write<MODE, MODE != MODE_RANDK ? KQ_QSGD : KQ_NONE><<<UBg, 256, 0, s>>>(A);
+  else if (MODE != MODE_RANDK && A.qkind == KQ_SIGN)
+    k_write<MODE, MODE != MODE_RANDK ? KQ_SIGN : KQ_NONE><<<UBg, 256, 0, s>>>(A);
+  else
+    k_write<MODE, KQ_NONE><<<UBg, 256, 0, s>>>(A);
   pe.done(4, s);
 }
+
+// QSGD or sign quantization of the kept values (kind KQ_*), its levels and
+// the sign-bit output.
+struct KeptQuant {
+  int kind = KQ_NONE;
+  int slev = 0;
+  uint32_t* bits = nullptr;
+};
 
 static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host, const float* g,
                           float* e, float* u, float* v, float beta, int32_t* idx, float* val,
@@ -1718,7 +1823,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
                           void* ws, size_t ws_bytes, void* stream, const PhaseEvents& pe,
                           gc_residual_desc* rd = nullptr, const float* tau = nullptr,
                           int64_t* count_out = nullptr, const float* clip = nullptr,
-                          float* norm_out = nullptr, uint64_t* iter_dev = nullptr) {
+                          float* norm_out = nullptr, uint64_t* iter_dev = nullptr,
+                          const KeptQuant& kq = KeptQuant{}) {
   gc_status st = validate_layout(host, true);
   if (st != GC_OK) return st;
   if (!dev || !dev->off || !dev->k || !dev->koff || dev->num_tensors != host->num_tensors)
@@ -1726,7 +1832,11 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   const bool int8 = (flags & GC_INT8) != 0u;
   if (!g || !idx) return GC_ERR_INVALID_ARG;
   if (int8 && (!q || !scale)) return GC_ERR_INVALID_ARG;
-  if (!int8 && !val) return GC_ERR_INVALID_ARG;
+  if (kq.kind != KQ_NONE) {
+    if (int8 || !scale || (kq.kind == KQ_QSGD && !q) || (kq.kind == KQ_SIGN && !kq.bits)) return GC_ERR_INVALID_ARG;
+  } else if (!int8 && !val) {
+    return GC_ERR_INVALID_ARG;
+  }
   if (!aligned16(g) || (e && !aligned16(e)) || (u && !aligned16(u)) || (v && !aligned16(v)))
     return GC_ERR_ALIGNMENT;
   const bool sampled = mode != MODE_RANDK;
@@ -1784,6 +1894,10 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.upart = reinterpret_cast<double*>(w + c.o_upart);
   A.clip = clip;
   A.norm_out = norm_out;
+  A.qkind = kq.kind;
+  A.slev = kq.slev;
+  A.bits = kq.bits;
+  A.kwoff = reinterpret_cast<int64_t*>(w + c.o_kwoff);
   A.U = z.U;
   A.UB = z.UB;
   A.C = z.C;
@@ -1795,6 +1909,12 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   pe.start(s);
   if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
   pe.done(0, s);
+  if (kq.kind == KQ_SIGN) {
+    // the payload write sets the bits of the positive kept values
+    int64_t words = 0;
+    for (int t = 0; t < host->num_tensors; ++t) words += (host->k[t] + 31) / 32;
+    if (words > 0 && cudaMemsetAsync(kq.bits, 0, (size_t)words * 4u, s) != cudaSuccess) return GC_ERR_CUDA;
+  }
   if (mode == MODE_TOPK)
     launch_pipeline<MODE_TOPK>(A, s, pe);
   else if (mode == MODE_RANDK)
@@ -1872,6 +1992,64 @@ extern "C" gc_status gc_ef_topk_compress_momentum(const gc_layout* dev, const gc
   if (!u || !v) return GC_ERR_INVALID_ARG;
   return run_topk(MODE_MOM, dev, host, g, nullptr, u, v, beta, idx, val, q, scale, seed, iter,
                   flags, workspace, ws_bytes, stream, PhaseEvents{});
+}
+
+// Kept-value quantizer of the *_quantized entry points: int8 goes through the
+// GC_INT8 path, QSGD and sign through KeptQuant.
+static gc_status kept_quant_of(int32_t kind, int32_t s_levels, uint32_t* bits, uint32_t* flags,
+                               KeptQuant* kq) {
+  switch (kind) {
+    case GC_KEPT_INT8:
+      *flags |= GC_INT8;
+      return GC_OK;
+    case GC_KEPT_QSGD:
+      if (s_levels < 1 || s_levels > 127) return GC_ERR_INVALID_ARG;
+      kq->kind = KQ_QSGD;
+      kq->slev = s_levels;
+      return GC_OK;
+    case GC_KEPT_SIGN:
+      if (!bits) return GC_ERR_INVALID_ARG;
+      kq->kind = KQ_SIGN;
+      kq->bits = bits;
+      return GC_OK;
+    default:
+      return GC_ERR_INVALID_ARG;
+  }
+}
+
+extern "C" gc_status gc_ef_topk_compress_quantized(const gc_layout* dev, const gc_layout* host,
+                                                   const float* g, float* e, int32_t* idx,
+                                                   float* val, int8_t* q, uint32_t* bits,
+                                                   float* scale, int32_t kind, int32_t s_levels,
+                                                   uint64_t seed, uint64_t iter, uint32_t flags,
+                                                   void* workspace, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_quantized");
+  const uint32_t known = GC_EF | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if ((flags & GC_EF) && !e) return GC_ERR_INVALID_ARG;
+  KeptQuant kq;
+  const gc_status st = kept_quant_of(kind, s_levels, bits, &flags, &kq);
+  if (st != GC_OK) return st;
+  return run_topk(MODE_TOPK, dev, host, g, (flags & GC_EF) ? e : nullptr, nullptr, nullptr, 0.0f,
+                  idx, val, q, scale, seed, iter, flags, workspace, ws_bytes, stream, PhaseEvents{},
+                  nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kq);
+}
+
+extern "C" gc_status gc_ef_topk_compress_momentum_quantized(
+    const gc_layout* dev, const gc_layout* host, const float* g, float* u, float* v, float beta,
+    int32_t* idx, float* val, int8_t* q, uint32_t* bits, float* scale, int32_t kind,
+    int32_t s_levels, uint64_t seed, uint64_t iter, uint32_t flags, void* workspace,
+    size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_ef_topk_compress_momentum_quantized");
+  const uint32_t known = GC_NO_MASK | GC_FORCE_EXACT;
+  if (flags & ~known) return GC_ERR_INVALID_ARG;
+  if (!u || !v) return GC_ERR_INVALID_ARG;
+  KeptQuant kq;
+  const gc_status st = kept_quant_of(kind, s_levels, bits, &flags, &kq);
+  if (st != GC_OK) return st;
+  return run_topk(MODE_MOM, dev, host, g, nullptr, u, v, beta, idx, val, q, scale, seed, iter,
+                  flags, workspace, ws_bytes, stream, PhaseEvents{}, nullptr, nullptr, nullptr,
+                  nullptr, nullptr, nullptr, kq);
 }
 
 extern "C" gc_status gc_ef_topk_compress_lazy(const gc_layout* dev, const gc_layout* host,

@@ -343,6 +343,53 @@ gc_status gc_ef_topk_compress_noalloc(const gc_layout* dev, const gc_layout* hos
  * bit is set; allocates nothing. */
 gc_status gc_ef_topk_compress_noalloc_status(void* stream, gc_diag* out);
 
+/* Quantizers of the kept values, for the *_quantized entry points. */
+#define GC_KEPT_INT8 1 /* as GC_INT8: scale = max|kept| / 127, code = sgn * min(127, SR(|x| / scale)) */
+#define GC_KEPT_QSGD 2 /* scale = N = ||kept||_2, code = sgn * min(s, SR((|x| * s) / N)) */
+#define GC_KEPT_SIGN 3 /* scale = mu = mean |kept|, one bit per kept value (1 = sign bit clear) */
+
+/* EF Top-k, then a quantizer applied to the kept values (zh glossary
+ * "Gradient Compression": the Top-k + 8-bit pipeline, quantization after
+ * sparsification; mbrenndoerfer.com "Gradient Compression": QSGD equation
+ * Q_s(g) = ||g|| sgn(g) xi(g, s), 1-bit SGD equation sign(g) ||g||_1 / d with
+ * one scalar).  The quantized vector of tensor t is its k_t kept values x_j
+ * in ascending index order:
+ *   GC_KEPT_QSGD: scale[t] = N = (float)sqrt(sum_j x_j^2), the sum in fp64 in
+ *     a fixed order (within 1e-6 relative of any order); q[koff[t] + j] =
+ *     sgn(x_j) * min(s, SR((|x_j| * s) / N)), stochastic rounding with the
+ *     Philox word of purpose 2 at the element's arena index; decoded value
+ *     sgn * ((|q| * N) / s).  N = 0 gives codes 0.
+ *   GC_KEPT_SIGN: scale[t] = mu = (float)(sum_j |x_j| / k_t) (fp64 sum);
+ *     bit j of tensor t's words is 1 iff x_j has a clear sign bit; tensor t's
+ *     bits start at word sum_{t' < t} ceil(k_t' / 32), LSB first, pad bits 0;
+ *     decoded value bit ? mu : -mu.
+ *   GC_KEPT_INT8: gc_ef_topk_compress with GC_INT8.
+ *   residual (GC_EF): e = acc off S, acc - decoded value on S.
+ *   k_t = 0 gives scale[t] = 0.
+ * idx: device int32[sum k].  val: device fp32[sum k] or NULL: the decoded
+ * values.  q: device int8[sum k] (QSGD, INT8; else may be NULL).  bits:
+ * device uint32[sum ceil(k_t/32)] (SIGN; else may be NULL), fully written.
+ * scale: device fp32[T].  s_levels: 1..127 (QSGD).  flags: GC_EF,
+ * GC_FORCE_EXACT.  Workspace: gc_workspace_size(GC_OP_TOPK). */
+gc_status gc_ef_topk_compress_quantized(const gc_layout* dev, const gc_layout* host, const float* g,
+                                        float* e, int32_t* idx, float* val, int8_t* q,
+                                        uint32_t* bits, float* scale, int32_t kind,
+                                        int32_t s_levels, uint64_t seed, uint64_t iter,
+                                        uint32_t flags, void* workspace, size_t ws_bytes,
+                                        void* stream);
+
+/* gc_ef_topk_compress_momentum followed by the kept-value quantizer of
+ * gc_ef_topk_compress_quantized, applied to the kept velocity v[S]; v[S]
+ * keeps v - decoded value, u[S] = +0 unless GC_NO_MASK.  flags: GC_NO_MASK,
+ * GC_FORCE_EXACT.  Workspace: gc_workspace_size(GC_OP_MOMENTUM). */
+gc_status gc_ef_topk_compress_momentum_quantized(const gc_layout* dev, const gc_layout* host,
+                                                 const float* g, float* u, float* v, float beta,
+                                                 int32_t* idx, float* val, int8_t* q,
+                                                 uint32_t* bits, float* scale, int32_t kind,
+                                                 int32_t s_levels, uint64_t seed, uint64_t iter,
+                                                 uint32_t flags, void* workspace, size_t ws_bytes,
+                                                 void* stream);
+
 /* DGC momentum correction + Top-k (inferensys.com "Gradient Sparsification",
  * momentum correction and momentum factor masking; genomic glossary, DGC):
  *   u = beta * u + g;  v = v + u;  S = Top-k of |v|;  payload v[S] (or int8);

@@ -130,6 +130,150 @@ def test_topk_layouts(gc, name, flags_name):
         e, _ = _topk_check(gc, L, g, e, flags, seed=5, it=it, ws=ws)
 
 
+def _kept_quant_check(gc, L, g_h, state, kind, flags, seed, it, ws, momentum=False, beta=0.9, s_levels=16):
+    """One GPU call of the Top-k + QSGD / sign entry points against the oracle.
+    Protocol: indices bit-exact; each tensor's scale (a norm or mean over the
+    kept values, reduced in a different order) within 1e-6 relative; then the
+    oracle re-run with the GPU's scale, and codes or bits, decoded values and
+    the residual (velocity) bit-exact.  `state` is e, or (u, v) with momentum;
+    the oracle's updated state is returned."""
+    dev = L.device
+    K, T = L.total_k, L.T
+    kq = {"qsgd": gc.GC_KEPT_QSGD, "sign": gc.GC_KEPT_SIGN}[kind]
+    g = torch.from_numpy(g_h).to(dev)
+    idx = torch.full((max(K, 1),), -1, dtype=torch.int32, device=dev)
+    val = torch.empty(max(K, 1), dtype=torch.float32, device=dev)
+    q = torch.full((max(K, 1),), 99, dtype=torch.int8, device=dev) if kind == "qsgd" else None
+    bits = torch.full((max(L.kept_words, 1),), -1, dtype=torch.int32, device=dev) if kind == "sign" else None
+    sc = torch.full((T,), -1.0, dtype=torch.float32, device=dev)
+    if momentum:
+        u_h, v_h = state
+        u, v = torch.from_numpy(u_h).to(dev), torch.from_numpy(v_h).to(dev)
+        gc.ef_topk_compress_momentum_quantized(L, g, u, v, beta, idx, val, q, bits, sc, kq, s_levels, seed, it,
+                                               flags, ws)
+    else:
+        e = torch.from_numpy(state).to(dev) if state is not None else None
+        gc.ef_topk_compress_quantized(L, g, e, idx, val, q, bits, sc, kq, s_levels, seed, it, flags, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    gi, gv, gsc = idx.cpu().numpy()[:K], val.cpu().numpy()[:K], sc.cpu().numpy()
+    gq = q.cpu().numpy()[:K] if q is not None else None
+    gb = bits.cpu().numpy().view(np.uint32) if bits is not None else None
+    kw = workloads.prefix((L.k + 31) // 32)
+    if momentum:
+        u_ref, v_ref = u_h.copy(), v_h.copy()
+    else:
+        e_ref = state.copy() if state is not None else None
+    for t in range(T):
+        a, b = int(L.off[t]), int(L.off[t + 1])
+        ka, kb, kt = int(L.koff[t]), int(L.koff[t + 1]), int(L.k[t])
+        if momentum:
+            args = (g_h[a:b], u_ref[a:b].copy(), v_ref[a:b].copy(), kt, beta, kind, s_levels)
+            _, _, _, _, s_ref = oracle.momentum_topk_quantized_tensor(*args, base=a, seed=seed, it=it)
+        else:
+            args = (g_h[a:b], None if e_ref is None else e_ref[a:b].copy(), kt, kind, s_levels)
+            _, _, _, _, s_ref = oracle.ef_topk_quantized_tensor(*args, base=a, seed=seed, it=it)
+        assert abs(float(gsc[t]) - s_ref) <= REL_TOL * abs(s_ref), f"tensor {t}: scale {gsc[t]} vs {s_ref}"
+        # everything downstream of the scale, given the GPU's scale
+        if momentum:
+            ut, vt = u_ref[a:b], v_ref[a:b]
+            ri, rv, rq, rb, _ = oracle.momentum_topk_quantized_tensor(g_h[a:b], ut, vt, kt, beta, kind, s_levels,
+                                                                      base=a, seed=seed, it=it,
+                                                                      scale_given=float(gsc[t]))
+        else:
+            et = None if e_ref is None else e_ref[a:b]
+            ri, rv, rq, rb, _ = oracle.ef_topk_quantized_tensor(g_h[a:b], et, kt, kind, s_levels, base=a, seed=seed,
+                                                                it=it, scale_given=float(gsc[t]))
+        assert np.array_equal(gi[ka:kb], ri), f"tensor {t}: indices differ"
+        assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"tensor {t}: decoded values differ"
+        if kind == "qsgd":
+            assert np.array_equal(gq[ka:kb], rq), f"tensor {t}: QSGD codes differ"
+        else:
+            assert np.array_equal(gb[kw[t]:kw[t + 1]], rb), f"tensor {t}: sign bits differ"
+        if kt == 0:
+            assert gsc[t] == 0.0
+    if momentum:
+        assert np.array_equal(_bits(u.cpu().numpy()), _bits(u_ref)), "u differs"
+        assert np.array_equal(_bits(v.cpu().numpy()), _bits(v_ref)), "v differs"
+        return (u_ref, v_ref)
+    if e_ref is not None:
+        assert np.array_equal(_bits(e.cpu().numpy()), _bits(e_ref)), "residual differs"
+    return e_ref
+
+
+@pytest.mark.parametrize("name", ["tiny_ragged", "misaligned", "many_small", "medium"])
+@pytest.mark.parametrize("kind", ["qsgd", "sign"])
+@pytest.mark.parametrize("flags_name", ["ef", "noef", "ef_exact"])
+def test_topk_kept_quantizers(gc, name, kind, flags_name):
+    """EF Top-k + QSGD / sign of the kept values, three chained calls, with
+    k = n and k = 0 tensors and ragged, misaligned tensor starts."""
+    sizes = LAYOUTS[name]
+    flags = {"ef": gc.GC_EF, "noef": 0, "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT}[flags_name]
+    rng = np.random.default_rng(len(sizes) + 7)
+    k = [int(min(n, max(0, int(rng.integers(0, 3)) if n < 8 else int(np.ceil(0.01 * n))))) for n in sizes]
+    if len(sizes) > 2:
+        k[0] = sizes[0]
+        k[-1] = 0
+    L = _layout(gc, sizes, k=k)
+    n = L.numel
+    e = (np.random.default_rng(4).standard_normal(n) * 1e-4).astype(F32) if flags & gc.GC_EF else None
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    for it in range(3):
+        g = _grad(n, 20 + it).numpy()
+        e = _kept_quant_check(gc, L, g, e, kind, flags, seed=6, it=it, ws=ws, s_levels=16 if it != 1 else 5)
+
+
+@pytest.mark.parametrize("kind", ["qsgd", "sign"])
+@pytest.mark.parametrize("exact", [False, True])
+def test_momentum_kept_quantizers(gc, kind, exact):
+    sizes = LAYOUTS["misaligned"] + [70_000]
+    L = _layout(gc, sizes, rho=0.005)
+    n = L.numel
+    flags = gc.GC_FORCE_EXACT if exact else 0
+    rng = np.random.default_rng(9)
+    state = ((rng.standard_normal(n) * 1e-4).astype(F32), (rng.standard_normal(n) * 1e-4).astype(F32))
+    ws = gc.alloc_workspace(L, gc.GC_OP_MOMENTUM, flags)
+    for it in range(3):
+        g = _grad(n, 30 + it).numpy()
+        state = _kept_quant_check(gc, L, g, state, kind, flags, seed=7, it=it, ws=ws, momentum=True)
+
+
+@pytest.mark.parametrize("kind", ["qsgd", "sign"])
+def test_kept_quantizers_ties_and_extremes(gc, kind):
+    """Ties straddling the k-th magnitude (kept ties enter the norm / mean),
+    signed zeros, and magnitudes near the fp32 limits."""
+    sizes = [10_000, 4096, 333, 70_000]
+    L = _layout(gc, sizes, k=[37, 4096, 1, 700])
+    n = L.numel
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    e = np.zeros(n, F32)
+    for it, gk in enumerate(["ties", "zeros", "ties"]):
+        g = _grad(n, 40 + it, gk).numpy()
+        e = _kept_quant_check(gc, L, g, e, kind, gc.GC_EF, seed=8, it=it, ws=ws)
+    rng = np.random.default_rng(10)
+    # the kept set's L2 norm must stay finite in fp32 (it is the payload's
+    # scale): 700 kept values near 4e35 give N near 1e37
+    big = (rng.standard_normal(n) * 1e35).astype(F32)
+    tiny = (rng.standard_normal(n) * 1e-40).astype(F32)     # subnormal magnitudes
+    for it, g in enumerate([big, tiny]):
+        _kept_quant_check(gc, L, g, None, kind, 0, seed=9, it=it, ws=ws)
+
+
+def test_kept_quantizer_arguments(gc):
+    L = _layout(gc, [1000, 77], k=[10, 3])
+    g = torch.zeros(1077, device="cuda")
+    idx = torch.empty(13, dtype=torch.int32, device="cuda")
+    q = torch.empty(13, dtype=torch.int8, device="cuda")
+    sc = torch.empty(2, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, 0)
+    for kind, s_levels, qq, bb, flags in [(gc.GC_KEPT_QSGD, 0, q, None, 0), (gc.GC_KEPT_QSGD, 128, q, None, 0),
+                                          (gc.GC_KEPT_QSGD, 16, None, None, 0), (gc.GC_KEPT_SIGN, 0, None, None, 0),
+                                          (7, 16, q, None, 0), (gc.GC_KEPT_QSGD, 16, q, None, gc.GC_INT8),
+                                          (gc.GC_KEPT_QSGD, 16, q, None, gc.GC_RANDK)]:
+        with pytest.raises(gc.GCError) as ei:
+            gc.ef_topk_compress_quantized(L, g, None, idx, None, qq, bb, sc, kind, s_levels, 0, 0, flags, ws)
+        assert ei.value.status == gc.GC_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("kind", ["ties", "zeros"])
 @pytest.mark.parametrize("exact", [False, True])
 def test_topk_ties(gc, kind, exact):
