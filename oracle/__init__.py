@@ -49,6 +49,7 @@ def _declare(L):
                                                         _P, _P, _I32, _I32, _U64, _U64, _I32]
     L.oracle_quantize_tensor.argtypes = [_I64, _U64, _P, _P, _P, _P, _I32, _I32, _U64, _U64, _P]
     L.oracle_sparse_accumulate.argtypes = [_I32, _P, _P, _I32, _P, _P, _P, _P, _P]
+    L.oracle_sparse_accumulate_quantized.argtypes = [_I32, _P, _P, _I32, _P, _P, _P, _P, _I32, _I32, _P]
     L.oracle_sign_decode_accumulate.argtypes = [_I64, _P, _F, _P]
     L.oracle_warmup_density.argtypes = [_I64, _I64, C.c_double, C.c_double, _I32, _I32]
     L.oracle_warmup_density.restype = C.c_double
@@ -57,7 +58,8 @@ def _declare(L):
                  "oracle_powersgd_tensor", "oracle_powersgd_decode_accumulate",
                  "oracle_momentum_topk_tensor", "oracle_sign_tensor", "oracle_quantize_tensor",
                  "oracle_ef_topk_quantized_tensor", "oracle_momentum_topk_quantized_tensor",
-                 "oracle_sparse_accumulate", "oracle_sign_decode_accumulate",
+                 "oracle_sparse_accumulate", "oracle_sparse_accumulate_quantized",
+                 "oracle_sign_decode_accumulate",
                  "oracle_codes_decode_accumulate"):
         getattr(L, name).restype = C.c_int
 
@@ -288,6 +290,28 @@ def sparse_accumulate(off, koff, idx_list, val_list, q_list, scale_list, out):
         sp = (C.c_void_p * W)(*[a.ctypes.data for a in ss])
     assert out.dtype == np.float32 and out.flags.c_contiguous
     _check(lib().oracle_sparse_accumulate(T, _p(off), _p(koff), W, ip, vp, qp, sp, _p(out)), "sparse_accumulate")
+    return out
+
+
+def sparse_accumulate_quantized(off, koff, kind, idx_list, q_list, bits_list, scale_list, out, s_levels=16):
+    """kind 'int8', 'qsgd' or 'sign': the receiver of the quantized kept-value payloads."""
+    off = _c(off, np.int64); koff = _c(koff, np.int64)
+    T = off.size - 1; W = len(idx_list)
+    keep = [_c(a, np.int32) for a in idx_list]
+    ip = (C.c_void_p * W)(*[a.ctypes.data for a in keep])
+    qp = bp = None
+    if q_list is not None:
+        qs = [_c(a, np.int8) for a in q_list]; keep += qs
+        qp = (C.c_void_p * W)(*[a.ctypes.data for a in qs])
+    if bits_list is not None:
+        bs = [_c(a, np.uint32) for a in bits_list]; keep += bs
+        bp = (C.c_void_p * W)(*[a.ctypes.data for a in bs])
+    ss = [_c(a, np.float32) for a in scale_list]; keep += ss
+    sp = (C.c_void_p * W)(*[a.ctypes.data for a in ss])
+    assert out.dtype == np.float32 and out.flags.c_contiguous
+    k = {"int8": 1, "qsgd": 2, "sign": 3}[kind]
+    _check(lib().oracle_sparse_accumulate_quantized(T, _p(off), _p(koff), W, ip, qp, bp, sp, k, s_levels, _p(out)),
+           "sparse_accumulate_quantized")
     return out
 
 

@@ -689,6 +689,47 @@ int oracle_sparse_accumulate(int32_t T, const int64_t* off, const int64_t* koff,
   return 0;
 }
 
+// Receiver of W workers' quantized sparse payloads (the payloads of the
+// quantized kept values above): as oracle_sparse_accumulate, with entry j of
+// tensor t (j counted from koff[t]) decoded from its code:
+//   kind 1, int8: q * scale[t]
+//   kind 2, QSGD: sgn(q) * ((|q| * scale[t]) / s_levels), +0 for q = 0
+//   kind 3, sign: bit j of tensor t's words ? scale[t] : -scale[t], tensor t's
+//     words starting at sum_{t' < t} ceil(k_t' / 32).
+int oracle_sparse_accumulate_quantized(int32_t T, const int64_t* off, const int64_t* koff, int32_t W,
+                                       const int32_t* const* idx, const int8_t* const* q,
+                                       const uint32_t* const* bits, const float* const* scale,
+                                       int32_t kind, int32_t s_levels, float* out) {
+  if (kind < 1 || kind > 3 || (kind == 2 && (s_levels < 1 || s_levels > 127))) return 1;
+  for (int32_t w = 0; w < W; ++w) {
+    int64_t word0 = 0;  // first sign-bit word of tensor t
+    for (int32_t t = 0; t < T; ++t) {
+      const int64_t n = off[t + 1] - off[t];
+      for (int64_t p = koff[t]; p < koff[t + 1]; ++p) {
+        const int64_t i = idx[w][p];
+        if (i < 0 || i >= n) return 2;
+        const float sc = scale[w][t];
+        float v;
+        if (kind == 1) {
+          v = (float)q[w][p] * sc;
+        } else if (kind == 2) {
+          const int c = q[w][p];
+          const int level = c < 0 ? -c : c;
+          const float mag = ((float)level * sc) / (float)s_levels;
+          v = c < 0 ? -mag : mag;
+        } else {
+          const int64_t j = p - koff[t];
+          const bool bit = (bits[w][word0 + j / 32] >> (j % 32)) & 1u;
+          v = bit ? sc : -sc;
+        }
+        out[off[t] + i] = out[off[t] + i] + v;
+      }
+      word0 += (koff[t + 1] - koff[t] + 31) / 32;
+    }
+  }
+  return 0;
+}
+
 // Dense receivers: out += decode(payload) for one tensor.
 //   sign: bit ? mu : -mu
 //   int8: code * s

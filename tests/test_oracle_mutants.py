@@ -55,6 +55,11 @@ MUTANTS = {
                                ["test_kept_sign_bits_mean_and_residual"]),
     "kept_residual_dropped": ("    if (res) res[i] = x[i] - d;", "    if (res) res[i] = 0.0f;",
                               ["test_kept_sign_bits_mean_and_residual"]),
+    "receiver_sign_words_not_offset": ("      word0 += (koff[t + 1] - koff[t] + 31) / 32;", "      word0 += 0;",
+                                       ["test_quantized_sparse_receiver_restores_the_senders_decoded_values"]),
+    "receiver_qsgd_levels_not_divided": ("          const float mag = ((float)level * sc) / (float)s_levels;\n          v = c < 0 ? -mag : mag;",
+                                         "          const float mag = ((float)level * sc);\n          v = c < 0 ? -mag : mag;",
+                                         ["test_quantized_sparse_receiver_restores_the_senders_decoded_values"]),
     "randk_largest_keys": ("if (key[a] != key[b]) return key[a] < key[b];", "if (key[a] != key[b]) return key[a] > key[b];",
                            ["test_randk_selection_is_k_smallest_keys"]),
 }

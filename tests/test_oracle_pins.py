@@ -765,3 +765,38 @@ def test_momentum_quantized_reduces_to_ef_topk_quantized():
         assert (a[2] is None or np.array_equal(a[2], b[2])) and (a[3] is None or np.array_equal(a[3], b[3]))
         assert np.array_equal(v.view(np.uint32), e.view(np.uint32))
         assert np.all(u[a[0]] == 0) and np.array_equal(np.delete(u, a[0]), np.delete(g, a[0]))
+
+
+def test_quantized_sparse_receiver_restores_the_senders_decoded_values():
+    # One worker's payload of the kept-value quantizers, summed into a zero
+    # arena, gives back exactly the values the sender decoded (its `val`) at
+    # the sent indices, so out + e' restores acc to half an ulp (nothing lost:
+    # mbrenndoerfer.com residual equation); several tensors check the
+    # per-tensor word offsets of the sign bits.
+    sizes = [1000, 77, 4099, 31]
+    k = np.array([37, 0, 40, 31], np.int64)
+    off, koff = workloads.prefix(sizes), workloads.prefix(k)
+    rng = np.random.default_rng(66)
+    g = (rng.standard_t(3, int(off[-1])) * 1e-3).astype(F32)
+    e0 = (rng.standard_normal(int(off[-1])) * 1e-5).astype(F32)
+    for kind in ("qsgd", "sign"):
+        e = e0.copy()
+        idx, val, q, bits, sc = [], [], [], [], []
+        for t in range(len(sizes)):
+            a, b = int(off[t]), int(off[t + 1])
+            i_, v_, q_, b_, s_ = oracle.ef_topk_quantized_tensor(g[a:b], e[a:b], int(k[t]), kind, 16, base=a, seed=1)
+            idx.append(i_); val.append(v_); sc.append(s_)
+            q.append(q_ if q_ is not None else np.zeros(0, np.int8))
+            bits.append(b_ if b_ is not None else np.zeros(0, np.uint32))
+        out = np.zeros(int(off[-1]), F32)
+        oracle.sparse_accumulate_quantized(off, koff, kind, [np.concatenate(idx)],
+                                           [np.concatenate(q)] if kind == "qsgd" else None,
+                                           [np.concatenate(bits)] if kind == "sign" else None,
+                                           [np.asarray(sc, F32)], out)
+        sent = np.zeros(int(off[-1]), F32)
+        for t in range(len(sizes)):
+            sent[int(off[t]) + idx[t]] = val[t]
+        assert np.all(out == sent)
+        acc = (g + e0).astype(np.float64)
+        err = np.abs(acc - (out.astype(np.float64) + e.astype(np.float64)))
+        assert np.all(err <= 0.5 * np.spacing(np.abs(e)).astype(np.float64))
