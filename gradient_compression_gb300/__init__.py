@@ -23,6 +23,7 @@ GC_Q_INT8, GC_Q_QSGD = 0, 1
 GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
 GC_KEPT_INT8, GC_KEPT_QSGD, GC_KEPT_SIGN = 1, 2, 3
 GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE, GC_DIAG_BAD_THRESHOLD = 0x1, 0x2, 0x4, 0x8
+GC_DIAG_INDEX_ORDER = 0x10
 GC_NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 
 
@@ -85,6 +86,7 @@ def lib() -> C.CDLL:
         L.gc_quantize_stochastic_dev_iter.argtypes = [LP, LP, P, P, P, P, I32, I32, U64, P, P, SZ, P]
         L.gc_ef_topk_compress_dev_iter.argtypes = [LP, LP, P, P, P, P, P, P, U64, P, U32, P, SZ, P]
         L.gc_sparse_decompress_accumulate.argtypes = [LP, LP, I32, P, P, P, P, P, P, SZ, P]
+        L.gc_sparse_decompress_accumulate_quantized.argtypes = [LP, LP, I32, I32, I32, P, P, P, P, P, P, SZ, P]
         L.gc_dense_decompress_accumulate.argtypes = [LP, LP, I32, I32, I32, P, P, P, P, SZ, P]
         L.gc_get_device_status.argtypes = [P, SZ, P, C.POINTER(gc_diag)]
         L.gc_status_string.argtypes = [I32]
@@ -99,6 +101,7 @@ def lib() -> C.CDLL:
                      "gc_ef_topk_compress_momentum", "gc_ef_topk_compress_quantized",
                      "gc_ef_topk_compress_momentum_quantized",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
+                     "gc_sparse_decompress_accumulate_quantized",
                      "gc_dense_decompress_accumulate", "gc_get_device_status",
                      "gc_ef_topk_compress_dev_iter", "gc_quantize_stochastic_dev_iter"):
             getattr(L, name).restype = I32
@@ -414,6 +417,17 @@ def sparse_decompress_accumulate(layout, idx_list, val_list, q_list, scale_list,
     _check(lib().gc_sparse_decompress_accumulate(layout.dev(), layout.host(), W, ip, vp, qp, sp, _ptr(out),
                                                  _ptr(workspace), workspace.numel(), _stream(stream)),
            "gc_sparse_decompress_accumulate")
+
+
+def sparse_decompress_accumulate_quantized(layout, kind, s_levels, idx_list, q_list, bits_list, scale_list, out,
+                                           workspace, stream=None):
+    """Receiver of the GC_KEPT_* payloads of W workers (lists of device tensors)."""
+    W = len(idx_list)
+    _check(lib().gc_sparse_decompress_accumulate_quantized(layout.dev(), layout.host(), W, int(kind), int(s_levels),
+                                                           _ptr_array(idx_list), _ptr_array(q_list),
+                                                           _ptr_array(bits_list), _ptr_array(scale_list), _ptr(out),
+                                                           _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_sparse_decompress_accumulate_quantized")
 
 
 def dense_decompress_accumulate(layout, kind, s_levels, data_list, scale_list, out, workspace, stream=None):

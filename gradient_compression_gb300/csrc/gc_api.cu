@@ -28,9 +28,16 @@ extern "C" gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32
       return GC_OK;
     }
     case GC_OP_DECOMPRESS: {
-      const gc_status st = validate_layout(host, false);
+      gc_status st = validate_layout(host, false);
       if (st != GC_OK) return st;
-      *bytes = dense_workspace_bytes(host);
+      size_t b = dense_workspace_bytes(host);
+      if (host->k && host->koff) {  // sparse receivers: window tables and starts
+        st = validate_layout(host, true);
+        if (st != GC_OK) return st;
+        const size_t sb = sparse_decompress_workspace_bytes(host);
+        b = sb > b ? sb : b;
+      }
+      *bytes = b;
       return GC_OK;
     }
     default:

@@ -44,5 +44,6 @@ inline gc_status validate_layout(const gc_layout* h, bool sparse) {
 // Defined by the operation files.
 size_t topk_workspace_bytes(const gc_layout* h, bool sampled);
 size_t dense_workspace_bytes(const gc_layout* h);
+size_t sparse_decompress_workspace_bytes(const gc_layout* h);
 
 }  // namespace gc

@@ -129,6 +129,8 @@ typedef struct gc_diag {
 #define GC_DIAG_SELECT 0x2u          /* internal selection inconsistency (should never be set) */
 #define GC_DIAG_INDEX_RANGE 0x4u     /* decompress met a payload index >= n_t; entry skipped */
 #define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold or clipping norm was negative or NaN */
+#define GC_DIAG_INDEX_ORDER 0x10u    /* decompress met a worker's indices not ascending within a
+                                        tensor; see gc_sparse_decompress_accumulate */
 
 /* CUDA-graph capture.  gc_ef_topk_compress_dev_iter and
  * gc_quantize_stochastic_dev_iter are gc_ef_topk_compress and
@@ -450,15 +452,39 @@ gc_status gc_quantize_stochastic_dev_iter(const gc_layout* dev, const gc_layout*
  * different sparse vectors; zh glossary: all-gather of indices and values):
  *   for w = 0..W-1 in order: out[off[t] + idx_w[j]] += value_w[j],
  *   value = val_w[j], or q_w[j] * scale_w[t] when val is NULL.
+ * Each element's contributions are added in worker order (fp32, one rounding
+ * each), so the result equals that sequential loop bit for bit.
  * idx, val, q, scale: HOST arrays of W device pointers (val NULL, or q and
- * scale NULL).  Indices within one worker's tensor must be distinct; an
- * index >= n_t is skipped and flagged (GC_DIAG_INDEX_RANGE).  out: device
- * fp32[N], caller-initialised, accumulated into; it must not alias a payload. */
+ * scale NULL).  Each worker's indices of a tensor must be strictly
+ * ascending, as every compressor of this library emits them.  An index
+ * outside [0, n_t) is skipped and flagged (GC_DIAG_INDEX_RANGE); indices out
+ * of order are flagged (GC_DIAG_INDEX_ORDER), and an entry of that worker
+ * may then be skipped, so the sum is defined only for ascending payloads.
+ * out: device fp32[N], caller-initialised, accumulated into; it must not
+ * alias a payload.  Workspace: gc_workspace_size(GC_OP_DECOMPRESS) with the
+ * layout's k and koff. */
 gc_status gc_sparse_decompress_accumulate(const gc_layout* dev, const gc_layout* host, int32_t W,
                                           const int32_t* const* idx, const float* const* val,
                                           const int8_t* const* q, const float* const* scale,
                                           float* out, void* workspace, size_t ws_bytes,
                                           void* stream);
+
+/* Receiver of W workers' payloads of gc_ef_topk_compress_quantized (or its
+ * momentum form), as gc_sparse_decompress_accumulate with the value of entry
+ * j of tensor t decoded as the sender's decoded value:
+ *   GC_KEPT_INT8: q_w[j] * scale_w[t]
+ *   GC_KEPT_QSGD: sgn(q) * ((|q| * scale_w[t]) / s_levels)  (+0 for q = 0)
+ *   GC_KEPT_SIGN: bit (j - koff[t]) of tensor t's words of bits_w ? scale_w[t]
+ *                 : -scale_w[t]  (words as in gc_ef_topk_compress_quantized)
+ * idx, q, bits, scale: HOST arrays of W device pointers (q for INT8 / QSGD,
+ * bits for SIGN; the other may be NULL). */
+gc_status gc_sparse_decompress_accumulate_quantized(const gc_layout* dev, const gc_layout* host,
+                                                    int32_t W, int32_t kind, int32_t s_levels,
+                                                    const int32_t* const* idx,
+                                                    const int8_t* const* q,
+                                                    const uint32_t* const* bits,
+                                                    const float* const* scale, float* out,
+                                                    void* workspace, size_t ws_bytes, void* stream);
 
 /* Receiver of W workers' dense payloads, out += decode(payload_w) in order
  * w = 0..W-1.  kind GC_DENSE_SIGN: data = uint32 bits (word layout above),

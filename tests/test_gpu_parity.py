@@ -608,6 +608,128 @@ def test_sparse_decompress(gc, int8):
     assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))
 
 
+def _receiver_ref(L, kind, pays, base, s_levels=16):
+    ref = base.copy()
+    idx = [p["idx"].cpu().numpy() for p in pays]
+    if kind == "f32":
+        oracle.sparse_accumulate(L.off, L.koff, idx, [p["val"].cpu().numpy() for p in pays], None, None, ref)
+    else:
+        oracle.sparse_accumulate_quantized(L.off, L.koff, kind, idx,
+                                           [p["q"].cpu().numpy() for p in pays] if kind != "sign" else None,
+                                           [p["bits"].cpu().numpy().view(np.uint32) for p in pays]
+                                           if kind == "sign" else None,
+                                           [p["scale"].cpu().numpy() for p in pays], ref, s_levels)
+    return ref
+
+
+def _receiver_run(gc, L, kind, pays, out, ws, s_levels=16):
+    idx = [p["idx"] for p in pays]
+    if kind == "f32":
+        gc.sparse_decompress_accumulate(L, idx, [p["val"] for p in pays], None, None, out, ws)
+    else:
+        k = {"int8": gc.GC_KEPT_INT8, "qsgd": gc.GC_KEPT_QSGD, "sign": gc.GC_KEPT_SIGN}[kind]
+        gc.sparse_decompress_accumulate_quantized(L, k, s_levels, idx,
+                                                  [p["q"] for p in pays] if kind != "sign" else None,
+                                                  [p["bits"] for p in pays] if kind == "sign" else None,
+                                                  [p["scale"] for p in pays], out, ws)
+
+
+def _random_payload(L, rng, kind, clustered=False):
+    """One worker's payload: ascending distinct local indices per tensor (a
+    uniform subset, or the first k_t indices when clustered), values of the
+    given kind."""
+    idx = []
+    for t in range(L.T):
+        n, k = int(L.off[t + 1] - L.off[t]), int(L.k[t])
+        sel = np.arange(k) if clustered else np.sort(rng.choice(n, size=k, replace=False))
+        idx.append(sel.astype(np.int32))
+    p = {"idx": torch.from_numpy(np.concatenate(idx)).cuda()}
+    K = L.total_k
+    p["val"] = torch.from_numpy((rng.standard_normal(K) * 1e-3).astype(F32)).cuda()
+    p["q"] = torch.from_numpy(rng.integers(-16 if kind == "qsgd" else -127, 17 if kind == "qsgd" else 128,
+                                           K).astype(np.int8)).cuda()
+    p["bits"] = torch.from_numpy(rng.integers(0, 2 ** 32, max(L.kept_words, 1), dtype=np.uint64)
+                                 .astype(np.uint32).view(np.int32)).cuda()
+    p["scale"] = torch.from_numpy(rng.uniform(1e-4, 1e-2, L.T).astype(F32)).cuda()
+    return p
+
+
+@pytest.mark.parametrize("kind", ["f32", "int8", "qsgd", "sign"])
+@pytest.mark.parametrize("W", [1, 3, 8, 11])
+def test_sparse_receiver_merged_windows(gc, kind, W):
+    """Workers merged per window (W = 11 takes two launch groups), densities
+    from one entry per tensor to k = n, tensors with k = 0, misaligned
+    starts; bit-exact against the oracle's sequential worker loop."""
+    sizes = [4097, 1, 33, 100_003, 6, 64, 250_000, 5000]
+    k = [41, 1, 33, 1000, 0, 64, 2500, 5000]
+    L = _layout(gc, sizes, k=k)
+    rng = np.random.default_rng(100 + W)
+    pays = [_random_payload(L, rng, kind) for _ in range(W)]
+    base = _grad(L.numel, 7).numpy()
+    out = torch.from_numpy(base).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    _receiver_run(gc, L, kind, pays, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(_receiver_ref(L, kind, pays, base)))
+
+
+@pytest.mark.parametrize("kind", ["f32", "sign"])
+def test_sparse_receiver_clustered_indices(gc, kind):
+    """Every worker sends the same first k_t indices: a few windows hold all
+    entries, and every element gets W contributions, which must still be
+    added in worker order."""
+    sizes = [300_000, 20_000]
+    L = _layout(gc, sizes, k=[3000, 200])
+    rng = np.random.default_rng(5)
+    pays = [_random_payload(L, rng, kind, clustered=True) for _ in range(8)]
+    base = _grad(L.numel, 9).numpy()
+    out = torch.from_numpy(base).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    _receiver_run(gc, L, kind, pays, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(_receiver_ref(L, kind, pays, base)))
+
+
+def test_sparse_receiver_subnormal_sums_are_ieee(gc):
+    """The window pass adds with L2 atomics, whose hardware add flushes
+    subnormals; sums with subnormal operands or results must still equal the
+    IEEE sums of the oracle (base values, addends and cancelling pairs in the
+    subnormal range)."""
+    n = 4096
+    L = _layout(gc, [n], k=[n])
+    rng = np.random.default_rng(12)
+    tiny = np.float32(2.0 ** -140)
+    base = (rng.integers(-1000, 1000, n) * tiny).astype(F32)          # subnormal or zero
+    base[::5] = (rng.standard_normal(base[::5].size) * 1e-38).astype(F32)
+    idx = torch.arange(n, dtype=torch.int32, device="cuda")
+    v0 = (rng.integers(-1000, 1000, n) * tiny).astype(F32)            # subnormal addends
+    v1 = (-base.astype(np.float64) - v0.astype(np.float64) + rng.integers(-3, 4, n) * 2.0 ** -149).astype(F32)
+    v2 = (rng.standard_normal(n) * 1e-3).astype(F32)                  # normal
+    vals = [torch.from_numpy(v).cuda() for v in (v0, v1, v2)]
+    out = torch.from_numpy(base.copy()).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    gc.sparse_decompress_accumulate(L, [idx, idx, idx], vals, None, None, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    ref = base.copy()
+    oracle.sparse_accumulate(L.off, L.koff, [np.arange(n, dtype=np.int32)] * 3, [v0, v1, v2], None, None, ref)
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))
+
+
+def test_sparse_receiver_flags_unsorted_indices(gc):
+    """Indices out of ascending order are reported; entries inside their
+    tensor's window are still added (here the tensor is one window)."""
+    L = _layout(gc, [4096], k=[4])
+    idx = torch.tensor([7, 3, 900, 5], dtype=torch.int32, device="cuda")     # one window, not ascending
+    val = torch.tensor([1.0, 2.0, 4.0, 8.0], device="cuda")
+    out = torch.zeros(4096, device="cuda")
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    gc.sparse_decompress_accumulate(L, [idx, idx], [val, val], None, None, out, ws)
+    d = gc.get_device_status(ws, raise_on_error=False)
+    assert d.error_bits & gc.GC_DIAG_INDEX_ORDER and not d.error_bits & gc.GC_DIAG_INDEX_RANGE
+    o = out.cpu().numpy()
+    assert o[7] == 2.0 and o[3] == 4.0 and o[900] == 8.0 and o[5] == 16.0 and o.sum() == 30.0
+
+
 def test_sparse_decompress_flags_bad_index(gc):
     L = _layout(gc, [10, 20], k=[1, 1])
     out = torch.zeros(30, device="cuda")
