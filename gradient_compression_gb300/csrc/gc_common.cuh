@@ -100,6 +100,27 @@ __host__ __device__ inline void sample_plan(int64_t n, int64_t k, int64_t* runs,
   *m = r * RUN;
 }
 
+// CTAs that sample a tensor: one for a small sample; for a sample of at
+// least SFILTER_RUNS runs, `split` of them but no fewer than
+// SAMPLE_RUNS_PER_CTA runs each (each filters its share of the runs; the
+// last to finish finds the threshold).  `split` spreads the arena's large
+// samples over about two CTAs per SM: arenas with many large tensors keep
+// one CTA per tensor.
+constexpr int64_t SAMPLE_RUNS_PER_CTA = 128;
+__host__ __device__ inline bool sample_splittable(int64_t n, int64_t k) {
+  if (k <= 0 || k >= n) return false;
+  int64_t runs, stride, m;
+  sample_plan(n, k, &runs, &stride, &m);
+  return runs >= SFILTER_RUNS;
+}
+__host__ __device__ inline int64_t sample_ctas(int64_t n, int64_t k, int split) {
+  if (!sample_splittable(n, k)) return 1;
+  int64_t runs, stride, m;
+  sample_plan(n, k, &runs, &stride, &m);
+  const int64_t most = runs / SAMPLE_RUNS_PER_CTA;
+  return split < most ? (split > 1 ? split : 1) : (most > 1 ? most : 1);
+}
+
 // Element offset of sample run r inside its stride window: a hashed jitter
 // (multiple of 4, run stays inside the window) so that runs of a tensor do
 // not sit at a power-of-two spacing, which would map them all onto the same

@@ -91,7 +91,10 @@ struct TopkArgs {
   int32_t* cidx;
   float* cval;
   uint32_t* skey;
-  int64_t U, UB, C, S, N, K;
+  int64_t* sblk;       // [T+1] first sampling CTA of each tensor
+  uint32_t* scnt;      // [2T] per tensor: keys in its sample list, sampling CTAs finished (zeroed per call)
+  int64_t U, UB, C, S, N, K, SB;
+  int ssplit;          // sampling CTAs per large sample (sample_ctas)
 };
 
 // ============================================================================ plan
@@ -127,11 +130,11 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0, carry_w = 0;
+  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0, carry_w = 0, carry_sb = 0;
   const bool sampled = A.sampled != 0;
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
-    int64_t nu = 0, nb = 0, nc = 0, ns = 0, nw = 0;
+    int64_t nu = 0, nb = 0, nc = 0, ns = 0, nw = 0, nsb = 0;
     if (t < A.T) {
       const int64_t n = A.off[t + 1] - A.off[t];
       const int64_t k = A.kk[t];
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       nb = ublocks_of(n);
       nc = cand_capacity(n, k);
       nw = k > 0 ? (k + 31) >> 5 : 0;
+      nsb = sampled ? sample_ctas(n, k, A.ssplit) : 0;
       TensorState st;
       memset(&st, 0, sizeof st);
       if (sampled && k > 0) {
@@ -205,6 +209,9 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     int64_t ew = block_excl_scan_i64(nw, s_warp, &tot);
     if (t < A.T) A.kwoff[t] = carry_w + ew;
     carry_w += tot;
+    int64_t esb = block_excl_scan_i64(nsb, s_warp, &tot);
+    if (t < A.T) A.sblk[t] = carry_sb + esb;
+    carry_sb += tot;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -213,7 +220,8 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     A.cand_off[A.T] = carry_c;
     A.soff[A.T] = carry_s;
     A.kwoff[A.T] = carry_w;
-    if (s_bad || carry_u != A.U || carry_b != A.UB || carry_c != A.C || carry_s != A.S ||
+    A.sblk[A.T] = carry_sb;
+    if (s_bad || carry_u != A.U || carry_b != A.UB || carry_c != A.C || carry_s != A.S || carry_sb != A.SB ||
         A.off[0] != 0 || A.off[A.T] != A.N || A.koff[0] != 0 || A.koff[A.T] != A.K) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
@@ -465,9 +473,10 @@ __device__ uint32_t find_bucket(const uint32_t* row, uint32_t rank, uint32_t* ab
   return b;
 }
 
-// Threshold estimate t_est from a strided sample of acc, one CTA of 512
-// threads per tensor (two CTAs per SM, so that every tensor's CTA starts in
-// the first wave; each warp keeps SRUNS runs in flight).  The sample is runs
+// Threshold estimate t_est from a strided sample of acc, by CTAs of 512
+// threads (two per SM; each warp keeps SR runs in flight): one per tensor,
+// or for a sample of at least SFILTER_RUNS runs one per SAMPLE_RUNS_PER_CTA
+// runs, which filter their shares and leave the search to the last of them.  The sample is runs
 // of RUN = 128 consecutive elements (one warp, 16 bytes per lane per input)
 // spaced `stride` apart; small tensors are sampled completely.
 //
@@ -568,15 +577,105 @@ __device__ __forceinline__ void sample_keys(const TopkArgs& A, int t, int64_t ba
   }
 }
 
+// The pilot of the filtered search: SPILOT runs spread evenly over the
+// sample, their keys in sl; returns the floor F (the level-2 edge of the
+// pilot key of rank rp).  Leaves sh zero.
+template <int MODE>
+__device__ uint32_t sample_pilot_floor(const TopkArgs& A, int t, int64_t base, int64_t n, int64_t stride, int runs,
+                                       uint32_t rp, bool vec, float gmul, uint32_t* sh, uint32_t* sl,
+                                       uint32_t* s_warp, uint32_t* s_res) {
+  constexpr int SR = sample_runs_in_flight<MODE>();
+  const unsigned lane = lane_id();
+  const int nwarp = blockDim.x >> 5, w = threadIdx.x >> 5;
+  uint32_t key[SR][4];
+  unsigned okm[SR];
+  const int ps = runs / SPILOT;
+  for (int i0 = w; i0 < SPILOT; i0 += SR * nwarp) {
+    sample_keys<MODE, SR>(A, t, base, n, stride, i0, nwarp, SPILOT, ps, vec, gmul, lane, key, okm);
+#pragma unroll
+    for (int h = 0; h < SR; ++h) {
+      const int i = i0 + h * nwarp;
+      if (i < SPILOT) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sl[i * RUN + 4 * lane + c] = key[h][c];
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < SLIST; i += blockDim.x) atomicAdd(sh + (sl[i] >> 21), 1u);
+  __syncthreads();
+  uint32_t pabove;
+  const uint32_t p1 = find_bucket(sh, rp, &pabove, s_warp, s_res);
+  for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  __syncthreads();
+  uint32_t F = 0u;
+  if (p1 != 0xFFFFFFFFu) {
+    for (int i = threadIdx.x; i < SLIST; i += blockDim.x) {
+      const uint32_t kk = sl[i];
+      if ((kk >> 21) == p1) atomicAdd(sh + ((kk >> 10) & 0x7FFu), 1u);
+    }
+    __syncthreads();
+    uint32_t pabove2;
+    const uint32_t p2 = find_bucket(sh, rp - pabove, &pabove2, s_warp, s_res);
+    F = (p1 << 21) | (p2 == 0xFFFFFFFFu ? 0u : (p2 << 10));
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
+  }
+  __syncthreads();
+  return F;
+}
+
+// The filtered pass over sample runs [r_lo, r_hi): the keys >= F go to the
+// level-1 histogram sh and to a list, at positions reserved with atomics on
+// *cnt (a shared counter for a list in shared memory, or a global one for
+// the tensor's list in the sample key buffer); positions at or above cap are
+// counted but not stored.
+template <int MODE>
+__device__ void sample_filter_pass(const TopkArgs& A, int t, int64_t base, int64_t n, int64_t stride, int r_lo,
+                                   int r_hi, bool vec, float gmul, uint32_t F, uint32_t* sh, uint32_t* list,
+                                   uint32_t cap, uint32_t* cnt) {
+  constexpr int SR = sample_runs_in_flight<MODE>();
+  const unsigned lane = lane_id();
+  const int nwarp = blockDim.x >> 5, w = threadIdx.x >> 5;
+  uint32_t key[SR][4];
+  unsigned okm[SR];
+  for (int r0 = r_lo + w; r0 < r_hi; r0 += SR * nwarp) {
+    sample_keys<MODE, SR>(A, t, base, n, stride, r0, nwarp, r_hi, 1, vec, gmul, lane, key, okm);
+#pragma unroll
+    for (int h = 0; h < SR; ++h) {
+      unsigned msk = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) msk |= (((okm[h] >> c) & 1u) && key[h][c] >= F ? 1u : 0u) << c;
+      if (__any_sync(FULL, msk != 0u)) {
+        unsigned pre, tot;
+        warp_count_scan(__popc(msk), lane, &pre, &tot);
+        uint32_t at = 0u;
+        if (lane == 0) at = atomicAdd(cnt, tot);
+        at = __shfl_sync(FULL, at, 0) + pre;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if ((msk >> c) & 1u) {
+            atomicAdd(sh + (key[h][c] >> 21), 1u);
+            if (at < cap) list[at] = key[h][c];
+            ++at;
+          }
+        }
+      }
+    }
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t s_cnt;
+  __shared__ uint32_t s_last;
   __shared__ uint32_t sh[NBINS];
   __shared__ uint32_t sl[SLIST];
-  const int t = blockIdx.x;
   if (aborted(A)) return;
+  const int t = find_segment(A.sblk, A.T, (int64_t)blockIdx.x);
+  const int cta = (int)((int64_t)blockIdx.x - A.sblk[t]);
+  const int nctas = (int)(A.sblk[t + 1] - A.sblk[t]);
   TensorState* st = A.ts + t;
   if (st->flags & TS_NOEMIT) return;
   const int64_t base = A.off[t], n = A.off[t + 1] - base;
@@ -590,7 +689,7 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   const int64_t m = min((int64_t)runs * RUN, n);
   const float gmul = st->gmul;
   if (j > m) {
-    if (threadIdx.x == 0) st->t_est = floor_key;
+    if (threadIdx.x == 0 && cta == 0) st->t_est = floor_key;
     return;
   }
   const unsigned lane = lane_id();
@@ -601,74 +700,56 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   unsigned okm[SR];
   uint32_t b1 = 0xFFFFFFFFu, above = 0u, lvl2_n = 0u;
   const uint32_t* lvl2 = nullptr;  // keys for level 2 (shared list or sample buffer)
-  bool filtered = false;
+  bool have_b1 = false, lvl2_shared = false;
+  uint32_t* sk = A.skey + A.soff[t];
 
   for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-  if (runs >= SFILTER_RUNS) {
-    // pilot: runs i * ps, i < SPILOT, keys kept in sl
-    const int ps = runs / SPILOT;
-    for (int i0 = w; i0 < SPILOT; i0 += SR * nwarp) {
-      sample_keys<MODE, SR>(A, t, base, n, stride, i0, nwarp, SPILOT, ps, vec, gmul, lane, key, okm);
-#pragma unroll
-      for (int h = 0; h < SR; ++h) {
-        const int i = i0 + h * nwarp;
-        if (i < SPILOT) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sl[i * RUN + 4 * lane + c] = key[h][c];
-        }
-      }
+  if (threadIdx.x == 0) s_cnt = 0u;
+  __syncthreads();
+  if (nctas > 1) {
+    // Several CTAs: each filters its share of the runs into the tensor's list
+    // in the sample key buffer (room for the whole sample) and the tensor's
+    // global histogram row; the last CTA to finish finds the threshold and
+    // clears the row (the streaming pass reuses it).
+    const uint32_t F = sample_pilot_floor<MODE>(A, t, base, n, stride, runs, plan.w, vec, gmul, sh, sl, s_warp,
+                                                s_res);
+    const int r_lo = (int)((int64_t)runs * cta / nctas), r_hi = (int)((int64_t)runs * (cta + 1) / nctas);
+    sample_filter_pass<MODE>(A, t, base, n, stride, r_lo, r_hi, vec, gmul, F, sh, sk, (uint32_t)m,
+                             A.scnt + 2 * t);
+    __syncthreads();
+    uint32_t* row = A.hist + (size_t)t * NBINS;
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x)
+      if (sh[i]) atomicAdd(row + i, sh[i]);
+    __threadfence();  // every thread's list entries and histogram counts before the CTA's count
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(A.scnt + 2 * t + 1, 1u) == (uint32_t)(nctas - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const uint32_t c = __ldcg(A.scnt + 2 * t);
+    for (int i = threadIdx.x; i < NBINS; i += blockDim.x) {
+      sh[i] = __ldcg(row + i);
+      row[i] = 0u;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < SLIST; i += blockDim.x) atomicAdd(sh + (sl[i] >> 21), 1u);
-    __syncthreads();
-    const uint32_t rp = plan.w;
-    uint32_t pabove;
-    const uint32_t p1 = find_bucket(sh, rp, &pabove, s_warp, s_res);
+    if (c >= (uint32_t)j) {
+      have_b1 = true;
+      lvl2 = sk;
+      lvl2_n = c;
+      b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
+    }
     for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
-    uint32_t F = 0u;
-    if (p1 != 0xFFFFFFFFu) {
-      for (int i = threadIdx.x; i < SLIST; i += blockDim.x) {
-        const uint32_t kk = sl[i];
-        if ((kk >> 21) == p1) atomicAdd(sh + ((kk >> 10) & 0x7FFu), 1u);
-      }
-      __syncthreads();
-      uint32_t pabove2;
-      const uint32_t p2 = find_bucket(sh, rp - pabove, &pabove2, s_warp, s_res);
-      F = (p1 << 21) | (p2 == 0xFFFFFFFFu ? 0u : (p2 << 10));
-      for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
-    }
-    if (threadIdx.x == 0) s_cnt = 0u;
-    __syncthreads();
-    // filtered pass: histogram of the keys >= F, list of them in sl
-    for (int r0 = w; r0 < runs; r0 += SR * nwarp) {
-      sample_keys<MODE, SR>(A, t, base, n, stride, r0, nwarp, runs, 1, vec, gmul, lane, key, okm);
-#pragma unroll
-      for (int h = 0; h < SR; ++h) {
-        unsigned msk = 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) msk |= (((okm[h] >> c) & 1u) && key[h][c] >= F ? 1u : 0u) << c;
-        if (__any_sync(FULL, msk != 0u)) {
-          unsigned pre, tot;
-          warp_count_scan(__popc(msk), lane, &pre, &tot);
-          uint32_t at = 0u;
-          if (lane == 0) at = atomicAdd(&s_cnt, tot);
-          at = __shfl_sync(FULL, at, 0) + pre;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if ((msk >> c) & 1u) {
-              atomicAdd(sh + (key[h][c] >> 21), 1u);
-              if (at < (uint32_t)SLIST) sl[at] = key[h][c];
-              ++at;
-            }
-          }
-        }
-      }
-    }
+  } else if (runs >= SFILTER_RUNS) {
+    // One CTA, filtered search with the list in shared memory.
+    const uint32_t F = sample_pilot_floor<MODE>(A, t, base, n, stride, runs, plan.w, vec, gmul, sh, sl, s_warp,
+                                                s_res);
+    sample_filter_pass<MODE>(A, t, base, n, stride, 0, runs, vec, gmul, F, sh, sl, (uint32_t)SLIST, &s_cnt);
     __syncthreads();
     const uint32_t c = s_cnt;
     if (c >= (uint32_t)j && c <= (uint32_t)SLIST) {
-      filtered = true;
+      have_b1 = true;
+      lvl2_shared = true;
       lvl2 = sl;
       lvl2_n = c;
       b1 = find_bucket(sh, (uint32_t)j, &above, s_warp, s_res);
@@ -676,9 +757,8 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
     for (int i = threadIdx.x; i < NBINS; i += blockDim.x) sh[i] = 0u;
     __syncthreads();
   }
-  if (!filtered) {
+  if (!have_b1) {
     // direct path: level 1 over every sample key, keys kept in the sample buffer
-    uint32_t* sk = A.skey + A.soff[t];
     for (int r0 = w; r0 < runs; r0 += SR * nwarp) {
       sample_keys<MODE, SR>(A, t, base, n, stride, r0, nwarp, runs, 1, vec, gmul, lane, key, okm);
 #pragma unroll
@@ -714,7 +794,7 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
 #pragma unroll
     for (int u = 0; u < U8; ++u) {
       const uint32_t i = i0 + u * blockDim.x + threadIdx.x;
-      kk[u] = i < lvl2_n ? (filtered ? lvl2[i] : __ldcg(lvl2 + i)) : 0u;
+      kk[u] = i < lvl2_n ? (lvl2_shared ? lvl2[i] : __ldcg(lvl2 + i)) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < U8; ++u) {
@@ -1639,11 +1719,31 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
 // ============================================================================ host side
 
 struct TopkLayoutTotals {
-  int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0;
+  int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0, SB = 0;
+  int split = 1;
 };
 
-static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
+// Sampling CTAs per large sample: enough to give about two CTAs per SM of
+// the current device when the arena has few large tensors.
+static int sampling_split(const gc_layout* h) {
+  int large = 0;
+  for (int t = 0; t < h->num_tensors; ++t)
+    if (sample_splittable(h->off[t + 1] - h->off[t], h->k[t])) ++large;
+  if (large == 0) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();  // leave no error state behind
+    sms = 152;
+  }
+  const int f = (2 * sms) / large;
+  return f < 1 ? 1 : (f > 64 ? 64 : f);
+}
+
+// split_for_launch: also choose the sampling split for the current device
+// (the workspace size does not depend on it).
+static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled, bool split_for_launch = false) {
   TopkLayoutTotals r;
+  if (sampled && split_for_launch) r.split = sampling_split(h);
   for (int t = 0; t < h->num_tensors; ++t) {
     const int64_t n = h->off[t + 1] - h->off[t];
     const int64_t k = h->k[t];
@@ -1655,6 +1755,7 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
       sample_plan(n, k, &runs, &stride, &m);
       r.S += m;
     }
+    if (sampled) r.SB += sample_ctas(n, k, r.split);
     r.K += k;
   }
   r.N = h->off[h->num_tensors];
@@ -1663,8 +1764,8 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled) {
 
 struct TopkCarve {
   size_t zero_bytes = 0, total = 0;
-  size_t o_ts, o_hist, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
-      o_cidx, o_cval, o_skey, o_upart, o_kwoff;
+  size_t o_ts, o_hist, o_scnt, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
+      o_cidx, o_cval, o_skey, o_upart, o_kwoff, o_sblk;
 };
 
 static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
@@ -1677,6 +1778,7 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   };
   c.o_ts = take(sizeof(TensorState) * (size_t)T);
   c.o_hist = take((size_t)T * NBINS * 4);
+  c.o_scnt = take(8 * (size_t)T);
   c.zero_bytes = p;
   c.o_units = take(8 * (size_t)(T + 1));
   c.o_ublk = take(8 * (size_t)(T + 1));
@@ -1693,6 +1795,7 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   c.o_skey = take(4 * (size_t)z.S);
   c.o_upart = take(8 * (size_t)z.U);
   c.o_kwoff = take(8 * (size_t)(T + 1));
+  c.o_sblk = take(8 * (size_t)(T + 1));
   c.total = p;
   return c;
 }
@@ -1753,7 +1856,7 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
   }
   pe.done(A.sampled ? 0 : 1, s);
   if (A.sampled) {
-    k_sample<MODE><<<T, 512, 0, s>>>(A);
+    k_sample<MODE><<<(unsigned)A.SB, 512, 0, s>>>(A);
     pe.done(1, s);
   }
   if (MODE == MODE_MOM) {
@@ -1840,7 +1943,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   if (!aligned16(g) || (e && !aligned16(e)) || (u && !aligned16(u)) || (v && !aligned16(v)))
     return GC_ERR_ALIGNMENT;
   const bool sampled = mode != MODE_RANDK;
-  const TopkLayoutTotals z = totals_of(host, sampled);
+  const TopkLayoutTotals z = totals_of(host, sampled, true);
   const TopkCarve c = carve_topk(host->num_tensors, z);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < c.total) return GC_ERR_WORKSPACE;
   if (z.K == 0 && z.N == 0) return GC_OK;
@@ -1898,12 +2001,16 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.slev = kq.slev;
   A.bits = kq.bits;
   A.kwoff = reinterpret_cast<int64_t*>(w + c.o_kwoff);
+  A.sblk = reinterpret_cast<int64_t*>(w + c.o_sblk);
+  A.scnt = reinterpret_cast<uint32_t*>(w + c.o_scnt);
   A.U = z.U;
   A.UB = z.UB;
   A.C = z.C;
   A.S = z.S;
   A.N = z.N;
   A.K = z.K;
+  A.SB = z.SB;
+  A.ssplit = z.split;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   pe.start(s);
