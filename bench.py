@@ -769,6 +769,8 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
     for w in range(warmup):
         step(w)
     torch.cuda.synchronize()
+    if op in ("topk", "randk") and lname in ("flat", "resnet50"):
+        extra["graph_replay"] = graph_replay(gc, L, grads, a, idx, val, flags, ws, warmup, steps, flush)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for s_ in range(steps):
         if flush is not None:
@@ -804,6 +806,43 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
                       "peak_from": "%d SMs x 64 per clock x 2070 MHz" % sm_count}
     row.update(extra)
     return row
+
+
+def graph_replay(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush):
+    """The same call captured once per resident gradient into a CUDA graph
+    (gc_ef_topk_compress_dev_iter: the iteration counter lives on the device
+    and advances per replay) and replayed alternately: the per-call time
+    without the host's per-launch work.  Runs on copies of the state."""
+    dev = grads[0].device
+    e = e.clone()
+    it_dev = torch.zeros(1, dtype=torch.int64, device=dev)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for g in grads[:2]:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                gc.ef_topk_compress_dev_iter(L, g, e, idx, val, None, None, 5, it_dev, flags, ws)
+        graphs.append(graph)
+    torch.cuda.synchronize()
+    for w in range(warmup):
+        graphs[w % 2].replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s_ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        evs[s_][0].record()
+        graphs[s_ % 2].replay()
+        evs[s_][1].record()
+    torch.cuda.synchronize()
+    times = [a_.elapsed_time(b_) for a_, b_ in evs]
+    del graphs
+    return {"ms_per_call": statistics.mean(times), "ms_min": min(times),
+            "how": "one CUDA-graph capture of gc_ef_topk_compress_dev_iter per resident gradient, replayed "
+                   "alternately (two of the gradients)"}
 
 
 def measure_rows(gc, dev, args):

@@ -1,14 +1,17 @@
 """Randomized parity: seeded random layouts (1 to 40 tensors, sizes from 1
 to ~400K elements, k from 0 to n), mixed value distributions and every
 selection flag, GPU against the oracle, EF state carried over two
-iterations.  Complements the fixed cases of test_gpu_parity.py."""
+iterations; the quantizers of the kept values and the sparse receiver over
+the same kind of layouts.  Complements the fixed cases of
+test_gpu_parity.py."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
-from test_gpu_parity import F32, _bits, _topk_check
+from test_gpu_parity import (F32, _bits, _kept_quant_check, _random_payload, _receiver_ref, _receiver_run,
+                             _topk_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +121,32 @@ def test_momentum_random_layouts(gc, seed):
                 assert np.array_equal(q.cpu().numpy()[ka:kb], rq), f"it {it} tensor {t}: codes"
         assert np.array_equal(_bits(u.cpu().numpy()), _bits(u_h)), f"it {it}: u"
         assert np.array_equal(_bits(v.cpu().numpy()), _bits(v_h)), f"it {it}: v"
+
+
+@pytest.mark.parametrize("seed", list(range(6)))
+def test_kept_quantizers_random_layouts(gc, seed):
+    sizes, k, grad = _random_case(seed + 120)
+    L = gc.Layout(workloads.prefix(sizes), k, device="cuda")
+    kind = ["qsgd", "sign"][seed % 2]
+    flags = [gc.GC_EF, 0, gc.GC_EF | gc.GC_FORCE_EXACT][seed % 3]
+    e = np.zeros(L.numel, F32) if flags & gc.GC_EF else None
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    for it in range(2):
+        e = _kept_quant_check(gc, L, grad(it), e, kind, flags, seed=seed, it=it, ws=ws,
+                              s_levels=[16, 1, 127, 7][seed % 4])
+
+
+@pytest.mark.parametrize("seed", list(range(4)))
+def test_receiver_random_layouts(gc, seed):
+    sizes, k, _ = _random_case(seed + 160)
+    L = gc.Layout(workloads.prefix(sizes), k, device="cuda")
+    rng = np.random.default_rng(seed + 170)
+    kind = ["f32", "int8", "qsgd", "sign"][seed]
+    W = int(rng.integers(1, 11))
+    pays = [_random_payload(L, rng, kind) for _ in range(W)]
+    base = (rng.standard_normal(L.numel) * 1e-3).astype(F32)
+    out = torch.from_numpy(base).cuda()
+    ws = gc.alloc_workspace(L, gc.GC_OP_DECOMPRESS)
+    _receiver_run(gc, L, kind, pays, out, ws)
+    assert gc.get_device_status(ws).error_bits == 0
+    assert np.array_equal(_bits(out.cpu().numpy()), _bits(_receiver_ref(L, kind, pays, base)))
