@@ -627,6 +627,8 @@ ROWS = {
     "bert_large_clip_ef_topk_0.1pct": ("bert_large", "clip", 0.001, 10,
                                        "DGC local clipping (max norm = half of ||g_t||) + EF Top-k 0.1%"),
     "bert_large_powersgd_r4": ("bert_large", "powersgd", None, 10, "PowerSGD rank 4 with EF on every weight matrix"),
+    "bert_large_powersgd_r4_lazy": ("bert_large", "powersgd_lazy", None, 10,
+                                    "PowerSGD rank 4 with EF, residual kept pending (two passes over M per call)"),
 }
 # --op name -> row (the short names of the single-row mode)
 OPS = {"flat": "flat_2p20_ef_topk_0.1pct", "resnet_topk": "resnet50_ef_topk_1pct", "randk": "resnet50_randk_1pct",
@@ -635,7 +637,7 @@ OPS = {"flat": "flat_2p20_ef_topk_0.1pct", "resnet_topk": "resnet50_ef_topk_1pct
        "sign_lazy": "gpt2_medium_sign_ef_one_pass", "qsgd": "gpt2_medium_qsgd16", "int8": "gpt2_medium_int8_sr_ef",
        "momentum": "gpt2_medium_momentum_topk_0.5pct", "decompress": "llama3_8b_decompress_w8",
        "threshold": "bert_large_threshold", "clip": "bert_large_clip_ef_topk_0.1pct",
-       "powersgd": "bert_large_powersgd_r4"}
+       "powersgd": "bert_large_powersgd_r4", "powersgd_lazy": "bert_large_powersgd_r4_lazy"}
 
 
 def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
@@ -710,7 +712,7 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
         def step(it):
             gc.ef_topk_compress_quantized(L, grads[it % 2], e, idx, None, q, bits, sc, kind, 16, 5, it, gc.GC_EF, ws)
         algo = 12 * N + (5 * K if op == "topk_qsgd" else 4 * K + 4 * L.kept_words) + 4 * T
-    elif op == "powersgd":
+    elif op in ("powersgd", "powersgd_lazy"):
         mats = workloads.matrices_of(layout)
         ml = gc.MatrixLayout([int(layout.off[t]) for t, _, _ in mats], [m for _, m, _ in mats],
                              [n for _, _, n in mats], device=dev)
@@ -719,13 +721,19 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
         qv = torch.randn(int(ml.qoff[-1]) * R, device=dev)
         pv = torch.empty(int(ml.poff[-1]) * R, device=dev)
         ws = gc.powersgd_workspace(ml, R)
+        pvs = [pv, torch.empty_like(pv)]
 
         def step(it):
-            gc.powersgd_compress(ml, R, grads[it % 2], e, qv, pv, None, ws)
+            if op == "powersgd":
+                gc.powersgd_compress(ml, R, grads[it % 2], e, qv, pv, None, ws)
+            else:
+                gc.powersgd_compress_lazy(ml, R, grads[it % 2], e, qv, pvs[it % 2], None if it == 0 else pvs[(it - 1) % 2],
+                                          None, ws)
         melems = sum(m * n for _, m, n in mats)
         algo = 12 * melems + 4 * R * (int(ml.poff[-1]) + int(ml.qoff[-1]))
         extra = {"matrices": len(mats), "matrix_elements": melems, "rank": R,
-                 "passes": "M = G + E and P = MQ (12 B/elt), Q = M^T P (4), E = M - PQ^T (8)"}
+                 "passes": ("M = G + E and P = MQ (12 B/elt), Q = M^T P (4), E = M - PQ^T (8)" if op == "powersgd"
+                            else "E = M_prev - P_prev Q_prev^T, M = G + E and P = MQ (12 B/elt), Q = M^T P (4)")}
     elif op in ("sign", "sign_lazy", "qsgd", "int8"):
         ws = gc.alloc_workspace(L, gc.GC_OP_QUANTIZE if op in ("qsgd", "int8") else gc.GC_OP_SIGN)
         sc = torch.empty(T, device=dev)

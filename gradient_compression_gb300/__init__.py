@@ -71,6 +71,8 @@ def lib() -> C.CDLL:
         L.gc_powersgd_workspace_size.argtypes = [MLP, I32, C.POINTER(SZ)]
         L.gc_powersgd_compress.argtypes = [MLP, MLP, I32, P, P, P, P, P, P, SZ, P]
         L.gc_powersgd_decompress_accumulate.argtypes = [MLP, MLP, I32, P, P, P, P, SZ, P]
+        L.gc_powersgd_compress_lazy.argtypes = [MLP, MLP, I32, P, P, P, P, P, P, P, SZ, P]
+        L.gc_powersgd_residual_materialize.argtypes = [MLP, MLP, I32, P, P, P, P, SZ, P]
         L.gc_ef_topk_compress_clipped.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_ef_threshold_compress.argtypes = [LP, LP, P, P, P, P, P, P, P, P, U64, U64, U32, P, SZ, P]
         L.gc_warmup_density.argtypes = [I64, I64, C.c_double, C.c_double, I32, I32]
@@ -97,7 +99,8 @@ def lib() -> C.CDLL:
                      "gc_ef_topk_compress_lazy", "gc_ef_residual_materialize",
                      "gc_sign_compress_lazy", "gc_sign_residual_materialize", "gc_ef_threshold_compress",
                      "gc_ef_topk_compress_clipped", "gc_powersgd_workspace_size", "gc_powersgd_compress",
-                     "gc_powersgd_decompress_accumulate",
+                     "gc_powersgd_decompress_accumulate", "gc_powersgd_compress_lazy",
+                     "gc_powersgd_residual_materialize",
                      "gc_ef_topk_compress_momentum", "gc_ef_topk_compress_quantized",
                      "gc_ef_topk_compress_momentum_quantized",
                      "gc_sign_compress", "gc_quantize_stochastic", "gc_sparse_decompress_accumulate",
@@ -225,6 +228,20 @@ def powersgd_compress(ml, rank, g, e, q, p, p_raw, workspace, stream=None):
     _check(lib().gc_powersgd_compress(ml.dev(), ml.host(), int(rank), _ptr(g), _ptr(e), _ptr(q), _ptr(p),
                                       _ptr(p_raw), _ptr(workspace), workspace.numel(), _stream(stream)),
            "gc_powersgd_compress")
+
+
+def powersgd_compress_lazy(ml, rank, g, e, q, p, p_prev, p_raw, workspace, stream=None):
+    """powersgd_compress with the residual kept pending (e holds M; p_prev is
+    the previous call's p, or None when e is a plain residual)."""
+    _check(lib().gc_powersgd_compress_lazy(ml.dev(), ml.host(), int(rank), _ptr(g), _ptr(e), _ptr(q), _ptr(p),
+                                           _ptr(p_prev), _ptr(p_raw), _ptr(workspace), workspace.numel(),
+                                           _stream(stream)), "gc_powersgd_compress_lazy")
+
+
+def powersgd_residual_materialize(ml, rank, e, p, q, workspace, stream=None):
+    _check(lib().gc_powersgd_residual_materialize(ml.dev(), ml.host(), int(rank), _ptr(e), _ptr(p), _ptr(q),
+                                                  _ptr(workspace), workspace.numel(), _stream(stream)),
+           "gc_powersgd_residual_materialize")
 
 
 def powersgd_decompress_accumulate(ml, rank, p, q, out, workspace, stream=None):

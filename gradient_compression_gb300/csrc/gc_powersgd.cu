@@ -19,6 +19,8 @@
 //   k_pmtp  256 x 1024 tiles of M: partial column sums of M^T P
 //   k_pqred fixed-order sum of the partials -> Q
 //   k_pres  the same tiles, Q^T staged in shared memory: E = M - P Q^T
+//           (the pending-residual entry point skips it: the next call's
+//           k_pmq makes the residual from E = M, P and Q on the fly)
 // Reductions: fused multiply-add partial sums in fp32 over a few terms,
 // added into a compensated fp32 accumulator per thread, then combined across
 // lanes, warps and tiles by compensated fp32 additions in a fixed order
@@ -57,6 +59,7 @@ struct PsArgs {
   float* q;
   float* p;
   float* p_raw;
+  const float* p_prev;  // pending residual: the previous call's P (E holds its M), else null
   float* out;
   uint32_t* diag;
   int64_t* rowoff;   // [T+1] prefix of m
@@ -216,6 +219,16 @@ __device__ __forceinline__ void load_row(const float* base, float v[R]) {
   }
 }
 
+// s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, as the method
+// states, then E = M - s (residual) or out += s (receiver).
+template <int R, bool DECODE>
+__device__ __forceinline__ float pres_one(float x, const float pv[R], const float qv[R]) {
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[k]));
+  return DECODE ? __fadd_rn(x, s) : __fsub_rn(x, s);
+}
+
 // M = G + E (stored into E) and partial sums of P_raw = M Q over the tiles
 // of M^T P (PS_RC rows x PS_CC columns).  The tile's Q columns are staged
 // transposed in shared memory; a warp takes a row and a lane 4 consecutive
@@ -224,7 +237,11 @@ __device__ __forceinline__ void load_row(const float* base, float v[R]) {
 // over PS_FLUSH columns into compensated accumulators, reduced across lanes
 // by a fixed-order reduce-scatter, and one lane per k stores the row's
 // partial for this column tile.  Matrices with misaligned rows go one column per lane.
-template <int R>
+// PEND: E holds the previous call's M, whose residual M - P_prev Q_prev^T is
+// made here first, element by element with the arithmetic of k_pres (Q_prev
+// is this call's warm start, the Q staged in shared memory), so the result
+// is bit-identical to the eager residual.
+template <int R, bool PEND>
 __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
   constexpr int PG = 4;  // 128-column groups per step: PG * 4 = PS_FLUSH columns per lane
   static_assert(PG * 4 == PS_FLUSH, "one compensated addition per step");
@@ -256,6 +273,8 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
       float part[R];
 #pragma unroll
       for (int k = 0; k < R; ++k) part[k] = 0.0f;
+      float pv[R];
+      if (PEND) load_row<R>(A.p_prev + (A.rowoff[t] + i) * R, pv);
       if (vec) {
         const float4* g4 = reinterpret_cast<const float4*>(A.g + rb);
         float4* e4 = reinterpret_cast<float4*>(A.e + rb);
@@ -272,6 +291,24 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
             if (vi < nv) {
               mv[u] = ld_stream(g4 + vi);
               ev[u] = ld_stream(e4 + vi);
+            }
+          }
+          if (PEND) {
+#pragma unroll
+            for (int u = 0; u < PG; ++u) {
+              const int vi = v0 + 32 * u;
+              if (vi < nv) {
+                float qv[4][R];
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                  const float4 qk = *reinterpret_cast<const float4*>(&sq[k][4 * vi]);
+                  qv[0][k] = qk.x; qv[1][k] = qk.y; qv[2][k] = qk.z; qv[3][k] = qk.w;
+                }
+                ev[u].x = pres_one<R, false>(ev[u].x, pv, qv[0]);
+                ev[u].y = pres_one<R, false>(ev[u].y, pv, qv[1]);
+                ev[u].z = pres_one<R, false>(ev[u].z, pv, qv[2]);
+                ev[u].w = pres_one<R, false>(ev[u].w, pv, qv[3]);
+              }
             }
           }
 #pragma unroll
@@ -306,7 +343,14 @@ __global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
       } else {
         int fl = 0;
         for (int j = (int)lane; j < cw; j += 32) {
-          const float mvj = __fadd_rn(__ldcs(A.g + rb + j), __ldcs(A.e + rb + j));
+          float evj = __ldcs(A.e + rb + j);
+          if (PEND) {
+            float qv[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) qv[k] = sq[k][j];
+            evj = pres_one<R, false>(evj, pv, qv);
+          }
+          const float mvj = __fadd_rn(__ldcs(A.g + rb + j), evj);
           __stcs(A.e + rb + j, mvj);
 #pragma unroll
           for (int k = 0; k < R; ++k) part[k] = __fmaf_rn(mvj, sq[k][j], part[k]);
@@ -675,16 +719,6 @@ __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
   }
 }
 
-// s_ij = sum_k P_ik Q_jk accumulated in k order in fp32, as the method
-// states, then E = M - s (residual) or out += s (receiver).
-template <int R, bool DECODE>
-__device__ __forceinline__ float pres_one(float x, const float pv[R], const float qv[R]) {
-  float s = 0.0f;
-#pragma unroll
-  for (int k = 0; k < R; ++k) s = __fadd_rn(s, __fmul_rn(pv[k], qv[k]));
-  return DECODE ? __fadd_rn(x, s) : __fsub_rn(x, s);
-}
-
 // E = M - P Q^T (or out += P Q^T) over the same PS_RC x PS_CC tiles as
 // M^T P.  The tile's Q columns are staged transposed in shared memory
 // (Q^T[k][c]), so a lane reads the R values of its 4 consecutive columns
@@ -822,9 +856,12 @@ static unsigned ps_tile_grid(K kernel, size_t smem, int64_t tiles) {
 }
 
 template <int R>
-static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
+static void ps_launch_compress(const PsArgs& A, cudaStream_t s, bool lazy) {
   k_psplan<<<1, 1024, 0, s>>>(A);
-  k_pmq<R><<<ps_tile_grid(k_pmq<R>, 0, A.Tiles), 256, 0, s>>>(A);
+  if (A.p_prev)
+    k_pmq<R, true><<<ps_tile_grid(k_pmq<R, true>, 0, A.Tiles), 256, 0, s>>>(A);
+  else
+    k_pmq<R, false><<<ps_tile_grid(k_pmq<R, false>, 0, A.Tiles), 256, 0, s>>>(A);
   k_ppred<R><<<(unsigned)std::min<int64_t>((A.Mrows + 255) / 256, 65535), 256, 0, s>>>(A);
   k_porth<R><<<A.T, 1024, 0, s>>>(A, 0);
   if (A.Big > 0) {
@@ -847,7 +884,7 @@ static void ps_launch_compress(const PsArgs& A, cudaStream_t s) {
   }
   k_pmtp<R><<<ps_tile_grid(k_pmtp<R>, 0, A.Tiles), 256, 0, s>>>(A);
   k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
-  k_pres<R, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  if (!lazy) k_pres<R, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
 }
 
 static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* host, int32_t rank,
@@ -915,11 +952,63 @@ extern "C" gc_status gc_powersgd_compress(const gc_matrix_layout* dev, const gc_
   A.p = p;
   A.p_raw = p_raw;
   if (rank == 1)
-    ps_launch_compress<1>(A, s);
+    ps_launch_compress<1>(A, s, false);
   else if (rank == 2)
-    ps_launch_compress<2>(A, s);
+    ps_launch_compress<2>(A, s, false);
   else
-    ps_launch_compress<4>(A, s);
+    ps_launch_compress<4>(A, s, false);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_powersgd_compress_lazy(const gc_matrix_layout* dev, const gc_matrix_layout* host,
+                                               int32_t rank, const float* g, float* e, float* q, float* p,
+                                               const float* p_prev, float* p_raw, void* workspace,
+                                               size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_powersgd_compress_lazy");
+  if (!g || !e || !q || !p) return GC_ERR_INVALID_ARG;
+  if (p_prev == p) return GC_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(e) || !aligned16(q) || !aligned16(p) || (p_prev && !aligned16(p_prev)))
+    return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PsArgs A;
+  const gc_status st = ps_setup(dev, host, rank, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.g = g;
+  A.e = e;
+  A.q = q;
+  A.p = p;
+  A.p_raw = p_raw;
+  A.p_prev = p_prev;
+  if (rank == 1)
+    ps_launch_compress<1>(A, s, true);
+  else if (rank == 2)
+    ps_launch_compress<2>(A, s, true);
+  else
+    ps_launch_compress<4>(A, s, true);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+extern "C" gc_status gc_powersgd_residual_materialize(const gc_matrix_layout* dev,
+                                                      const gc_matrix_layout* host, int32_t rank,
+                                                      float* e, const float* p, const float* q,
+                                                      void* workspace, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("gc_powersgd_residual_materialize");
+  if (!e || !p || !q) return GC_ERR_INVALID_ARG;
+  if (!aligned16(e) || !aligned16(q) || !aligned16(p)) return GC_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PsArgs A;
+  const gc_status st = ps_setup(dev, host, rank, workspace, ws_bytes, s, &A);
+  if (st != GC_OK) return st;
+  A.e = e;
+  A.p = const_cast<float*>(p);
+  A.q = const_cast<float*>(q);
+  k_psplan<<<1, 1024, 0, s>>>(A);
+  if (rank == 1)
+    k_pres<1, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  else if (rank == 2)
+    k_pres<2, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  else
+    k_pres<4, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 

@@ -306,6 +306,28 @@ gc_status gc_powersgd_compress(const gc_matrix_layout* dev, const gc_matrix_layo
                                int32_t rank, const float* g, float* e, float* q, float* p,
                                float* p_raw, void* workspace, size_t ws_bytes, void* stream);
 
+/* gc_powersgd_compress with the residual kept pending: the step's last pass,
+ * E = M - P Q^T, is not run; e keeps M, and the next call makes the residual
+ * element by element (same fp32 operations, so results are bit-identical to
+ * gc_powersgd_compress) before it adds g.  One pass over the matrices fewer
+ * per call.
+ *   e:      in: a plain residual (p_prev == NULL) or the previous call's M;
+ *           out: this call's M.
+ *   q:      in: the previous call's Q (warm start, and the Q of the pending
+ *           residual); out: this call's Q.
+ *   p_prev: the previous call's (orthonormal) p, or NULL; must not be p (keep
+ *           two p buffers and alternate them).
+ * gc_powersgd_residual_materialize(e, p, q) turns the pending form into the
+ * plain residual (E = M - P Q^T with this call's p and q). */
+gc_status gc_powersgd_compress_lazy(const gc_matrix_layout* dev, const gc_matrix_layout* host,
+                                    int32_t rank, const float* g, float* e, float* q, float* p,
+                                    const float* p_prev, float* p_raw, void* workspace,
+                                    size_t ws_bytes, void* stream);
+gc_status gc_powersgd_residual_materialize(const gc_matrix_layout* dev,
+                                           const gc_matrix_layout* host, int32_t rank, float* e,
+                                           const float* p, const float* q, void* workspace,
+                                           size_t ws_bytes, void* stream);
+
 /* Receiver of one PowerSGD payload: out += P Q^T per matrix, with the same
  * fp32 accumulation as the residual (call once per worker, in order). */
 gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* dev,

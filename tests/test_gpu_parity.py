@@ -990,6 +990,44 @@ def test_powersgd_steps(gc, rank):
     _powersgd_check(gc, rank, PS_SHAPES, 40 + rank, iters=3)
 
 
+@pytest.mark.parametrize("rank", [1, 2, 4])
+def test_powersgd_lazy_matches_eager(gc, rank):
+    """The pending-residual entry point against gc_powersgd_compress on the
+    same inputs, four chained calls: P and Q bit-identical every call, and
+    the materialized residual (on a copy) bit-identical to the eager one.
+    The eager path is checked against the oracle by the tests above."""
+    shapes = [(1, 1), (17, 33), (300, 1024), (2000, 257), (9000, 16)]
+    rng = np.random.default_rng(70 + rank)
+    starts, pos = [], 0
+    for i, (m, n) in enumerate(shapes):
+        pos += 3 * (i % 2)
+        starts.append(pos)
+        pos += m * n
+    N = pos
+    ml = gc.MatrixLayout(starts, [a for a, _ in shapes], [b for _, b in shapes], device="cuda")
+    Msum, Nsum = int(ml.poff[-1]), int(ml.qoff[-1])
+    e0 = torch.from_numpy((0.1 * rng.standard_normal(N)).astype(F32)).cuda()
+    q0 = torch.from_numpy(rng.standard_normal(Nsum * rank).astype(F32)).cuda()
+    e_eager, q_eager = e0.clone(), q0.clone()
+    e_lazy, q_lazy = e0.clone(), q0.clone()
+    p_eager = torch.empty(Msum * rank, device="cuda")
+    p_lazy = [torch.empty(Msum * rank, device="cuda") for _ in range(2)]
+    ws = gc.powersgd_workspace(ml, rank)
+    for it in range(4):
+        g = torch.from_numpy(rng.standard_normal(N).astype(F32)).cuda()
+        gc.powersgd_compress(ml, rank, g, e_eager, q_eager, p_eager, None, ws)
+        cur, prev = p_lazy[it % 2], (p_lazy[(it - 1) % 2] if it else None)
+        gc.powersgd_compress_lazy(ml, rank, g, e_lazy, q_lazy, cur, prev, None, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        assert torch.equal(cur.view(torch.int32), p_eager.view(torch.int32)), f"call {it}: P"
+        assert torch.equal(q_lazy.view(torch.int32), q_eager.view(torch.int32)), f"call {it}: Q"
+        e_mat = e_lazy.clone()
+        gc.powersgd_residual_materialize(ml, rank, e_mat, cur, q_lazy, ws)
+        assert torch.equal(e_mat.view(torch.int32), e_eager.view(torch.int32)), f"call {it}: residual"
+    with pytest.raises(gc.GCError):
+        gc.powersgd_compress_lazy(ml, rank, g, e_lazy, q_lazy, cur, cur, None, ws)
+
+
 @pytest.mark.parametrize("rank", [1, 4])
 def test_powersgd_tall_matrices(gc, rank):
     """Matrices taller than 8192 rows (Gram-Schmidt on a cluster of CTAs),
