@@ -113,7 +113,14 @@ __host__ __device__ inline bool sample_splittable(int64_t n, int64_t k) {
   sample_plan(n, k, &runs, &stride, &m);
   return runs >= SFILTER_RUNS;
 }
+// Tensors of at most NOSAMPLE_N elements are not sampled: every element is a
+// candidate, which costs less than a sampling CTA; the bound is a warp's
+// candidate staging of one unit (WCAP), so the streaming pass can stage them
+// all.  A tensor with nothing to select (k = 0 or k = n) is not sampled
+// either.
+constexpr int64_t NOSAMPLE_N = WCAP;
 __host__ __device__ inline int64_t sample_ctas(int64_t n, int64_t k, int split) {
+  if (k <= 0 || k >= n || n <= NOSAMPLE_N) return 0;
   if (!sample_splittable(n, k)) return 1;
   int64_t runs, stride, m;
   sample_plan(n, k, &runs, &stride, &m);

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
         const double tau = floor(want * 4294967296.0 / (double)n);
         st.t_est = (tau >= 4294967296.0) ? 0u : ~((uint32_t)tau - 1u);
       }
-      if (k >= n) st.t_est = 0u;
+      if (k >= n || (sampled && n <= NOSAMPLE_N)) st.t_est = 0u;  // every element a candidate
       if (A.tau && k > 0) {
         const float tau = A.tau[t];
         if (tau >= 0.0f) {
@@ -1856,7 +1856,7 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
   }
   pe.done(A.sampled ? 0 : 1, s);
   if (A.sampled) {
-    k_sample<MODE><<<(unsigned)A.SB, 512, 0, s>>>(A);
+    if (A.SB > 0) k_sample<MODE><<<(unsigned)A.SB, 512, 0, s>>>(A);
     pe.done(1, s);
   }
   if (MODE == MODE_MOM) {
