@@ -1,8 +1,9 @@
 """Parity at the benchmark sizes and iteration counts, through the C ABI, in
 the launch configuration bench.py times.
 
-- BERT-large (335,141,888 elements): EF Top-k 0.1% + int8, ten iterations
-  with the residual carried, every tensor against the oracle every iteration.
+- BERT-large (335,141,888 elements): EF Top-k 0.1% + int8, and + QSGD or
+  sign of the kept values, ten iterations with the residual carried, every
+  tensor against the oracle every iteration.
 - GPT-2-medium (354,823,168 elements): sign + EF, QSGD s = 16 and momentum
   correction Top-k 0.5%, ten iterations each with their state carried, every
   tensor against the oracle every iteration.
@@ -256,3 +257,51 @@ def test_llama3_8b_topk_int8_and_decompress_full(gc):
                                  [p[0][ka:kb].cpu().numpy() for p in pays], [p[1][ka:kb].cpu().numpy() for p in pays],
                                  None, None, ref)
         assert np.array_equal(_bits(out[a:b].cpu().numpy()), _bits(ref)), f"decompress tensor {t}"
+
+
+@pytest.mark.parametrize("kind", ["qsgd", "sign"])
+def test_bert_large_topk_kept_quantizers_full(gc, kind):
+    """EF Top-k 0.1% + QSGD s = 16 or sign of the kept values on the BERT-large
+    arena, ten iterations with the residual carried: indices, codes or bits,
+    decoded values and residual bit-exact against the oracle given the GPU's
+    per-tensor scale, which must be within 1e-6 of the oracle's."""
+    lay = workloads.bert_large_layout()
+    k = workloads.k_per_tensor(lay.sizes, 0.001)
+    L = gc.Layout(lay.off, k, device="cuda")
+    T, N, K = lay.num_tensors, lay.numel, L.total_k
+    kq = {"qsgd": gc.GC_KEPT_QSGD, "sign": gc.GC_KEPT_SIGN}[kind]
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    val = torch.empty(K, device="cuda")
+    q = torch.empty(K, dtype=torch.int8, device="cuda") if kind == "qsgd" else None
+    bits = torch.empty(L.kept_words, dtype=torch.int32, device="cuda") if kind == "sign" else None
+    sc = torch.empty(T, device="cuda")
+    e = torch.zeros(N, device="cuda")
+    e_ref = np.zeros(N, F32)
+    kw = workloads.prefix((L.k + 31) // 32)
+    for it in range(10):
+        g = workloads.make_grad(3, lay, it, device="cuda")
+        gc.ef_topk_compress_quantized(L, g, e, idx, val, q, bits, sc, kq, 16, 7, it, gc.GC_EF, ws)
+        assert gc.get_device_status(ws).error_bits == 0
+        g_h, gi, gv, gsc, ge = g.cpu().numpy(), idx.cpu().numpy(), val.cpu().numpy(), sc.cpu().numpy(), e.cpu().numpy()
+        gq = q.cpu().numpy() if q is not None else None
+        gb = bits.cpu().numpy().view(np.uint32) if bits is not None else None
+
+        def one(t):
+            a, b = int(L.off[t]), int(L.off[t + 1])
+            ka, kb = int(L.koff[t]), int(L.koff[t + 1])
+            _, _, _, _, s_ref = oracle.ef_topk_quantized_tensor(g_h[a:b], e_ref[a:b].copy(), int(L.k[t]), kind, 16,
+                                                                base=a, seed=7, it=it)
+            assert abs(float(gsc[t]) - s_ref) <= 1e-6 * abs(s_ref), f"it {it} tensor {t}: scale"
+            et = e_ref[a:b].copy()
+            ri, rv, rq, rb, _ = oracle.ef_topk_quantized_tensor(g_h[a:b], et, int(L.k[t]), kind, 16, base=a, seed=7,
+                                                                it=it, scale_given=float(gsc[t]))
+            assert np.array_equal(gi[ka:kb], ri), f"it {it} tensor {t}: indices"
+            assert np.array_equal(_bits(gv[ka:kb]), _bits(rv)), f"it {it} tensor {t}: decoded values"
+            if kind == "qsgd":
+                assert np.array_equal(gq[ka:kb], rq), f"it {it} tensor {t}: codes"
+            else:
+                assert np.array_equal(gb[kw[t]:kw[t + 1]], rb), f"it {it} tensor {t}: bits"
+            assert np.array_equal(_bits(ge[a:b]), _bits(et)), f"it {it} tensor {t}: residual"
+            e_ref[a:b] = et
+        _pool_map(one, range(T))
