@@ -242,7 +242,7 @@ __device__ __forceinline__ float pres_one(float x, const float pv[R], const floa
 // is this call's warm start, the Q staged in shared memory), so the result
 // is bit-identical to the eager residual.
 template <int R, bool PEND>
-__global__ void __launch_bounds__(256) k_pmq(PsArgs A) {
+__global__ void __launch_bounds__(256, PEND ? 3 : 1) k_pmq(PsArgs A) {
   constexpr int PG = 4;  // 128-column groups per step: PG * 4 = PS_FLUSH columns per lane
   static_assert(PG * 4 == PS_FLUSH, "one compensated addition per step");
   __shared__ __align__(16) float sq[R][PS_CC];
