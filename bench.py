@@ -196,7 +196,10 @@ class ClockSampler:
                 continue
         if not rows:
             return None
-        load = [r for r in rows if r["util"] >= 50] or rows
+        load = [r for r in rows if r["util"] >= 50]
+        if not load:
+            return {"sm_mhz": None, "sm_max_mhz": max(r["max"] for r in rows), "reasons": [], "samples": 0,
+                    "note": "no sample under load: the timed region is shorter than the 100 ms sampling period"}
         reasons = set()
         for r in load:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
