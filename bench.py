@@ -802,6 +802,7 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
     if op == "decompress":
         row.update(value=K * extra["workers"] / (ms * 1e-3) / 1e9, unit="G entries/s")
         row["sector_bound_frac"] = extra["sector_bound_bytes"] / (ms * 1e-3) / 1e9 / peak
+        extra["random_access_reference"] = random_access_reference(L, k, idxs, vals, out, ms)
     else:
         row.update(value=4.0 * N / (ms * 1e-3) / 1e9, unit=UNIT, elems_per_s=N / (ms * 1e-3))
     if op in ("qsgd", "randk"):
@@ -817,6 +818,39 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
                       "peak_from": "%d SMs x 64 per clock x 2070 MHz" % sm_count}
     row.update(extra)
     return row
+
+
+def random_access_reference(L, k, idxs, vals, out, ms, reps=5):
+    """What the memory system gives for the receiver's access pattern with
+    PyTorch's own kernels, on the same arena and the same W payloads'
+    positions (arena-global, worker after worker): a plain gather (random
+    reads only) and index_add_ (random read-modify-writes).  A yardstick for
+    the receiver, not part of any path."""
+    dev = out.device
+    base = torch.repeat_interleave(torch.as_tensor(np.asarray(L.off[:-1], np.int64), device=dev),
+                                   torch.as_tensor(np.asarray(k, np.int64), device=dev))
+    gidx = torch.cat([ix.long() + base for ix in idxs])
+    v = torch.cat(vals)
+    buf = torch.empty_like(v)
+    res = {}
+    for name, fn in (("gather_ms", lambda: torch.index_select(out, 0, gidx, out=buf)),
+                     ("index_add_ms", lambda: out.index_add_(0, gidx, v))):
+        fn()
+        fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a_, b_ in evs:
+            a_.record()
+            fn()
+            b_.record()
+        torch.cuda.synchronize()
+        res[name] = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+    del gidx, v, buf
+    torch.cuda.empty_cache()
+    res["receiver_ms"] = ms
+    res["how"] = ("torch.index_select (random reads) and Tensor.index_add_ (random read-modify-writes) of the "
+                  "same payload positions in the same arena, mean of %d calls" % reps)
+    return res
 
 
 def graph_replay(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush):
