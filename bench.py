@@ -782,6 +782,10 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
     torch.cuda.synchronize()
     if op in ("topk", "randk") and lname in ("flat", "resnet50"):
         extra["graph_replay"] = graph_replay(gc, L, grads, a, idx, val, flags, ws, warmup, steps, flush)
+    if op == "topk":
+        extra["one_launch"] = int(gc.get_device_status(ws).one_launch)
+        if extra["one_launch"]:
+            extra["multi_kernel"] = multi_kernel_time(gc, L, grads, a, idx, val, flags, ws, warmup, steps, flush)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for s_ in range(steps):
         if flush is not None:
@@ -851,6 +855,27 @@ def random_access_reference(L, k, idxs, vals, out, ms, reps=5):
     res["how"] = ("torch.index_select (random reads) and Tensor.index_add_ (random read-modify-writes) of the "
                   "same payload positions in the same arena, mean of %d calls" % reps)
     return res
+
+
+def multi_kernel_time(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush):
+    """The same calls through the multi-kernel pipeline (GC_MULTI_KERNEL), for
+    comparison with the one-launch path.  Runs on a copy of the state."""
+    e = e.clone()
+    fl = flags | gc.GC_MULTI_KERNEL
+    for w in range(warmup):
+        gc.ef_topk_compress(L, grads[w % len(grads)], e, idx, val, None, None, 5, w, fl, ws)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s_ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        evs[s_][0].record()
+        gc.ef_topk_compress(L, grads[(warmup + s_) % len(grads)], e, idx, val, None, None, 5, warmup + s_, fl, ws)
+        evs[s_][1].record()
+    torch.cuda.synchronize()
+    times = [a_.elapsed_time(b_) for a_, b_ in evs]
+    return {"ms_per_call": statistics.mean(times), "ms_min": min(times),
+            "how": "the same calls with GC_MULTI_KERNEL (a memset and 13 kernels)"}
 
 
 def graph_replay(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush):

@@ -18,12 +18,13 @@ LIB_PATH = os.path.join(_HERE, "libgc.so")
 
 GC_OK, GC_ERR_INVALID_ARG, GC_ERR_LAYOUT, GC_ERR_WORKSPACE, GC_ERR_ALIGNMENT, GC_ERR_CUDA, GC_ERR_DEVICE = range(7)
 GC_EF, GC_INT8, GC_RANDK, GC_UNBIASED, GC_NO_MASK, GC_FORCE_EXACT = 0x1, 0x2, 0x4, 0x8, 0x10, 0x100
+GC_MULTI_KERNEL = 0x200
 GC_OP_TOPK, GC_OP_MOMENTUM, GC_OP_SIGN, GC_OP_QUANTIZE, GC_OP_DECOMPRESS = range(5)
 GC_Q_INT8, GC_Q_QSGD = 0, 1
 GC_DENSE_SIGN, GC_DENSE_INT8, GC_DENSE_QSGD = 0, 1, 2
 GC_KEPT_INT8, GC_KEPT_QSGD, GC_KEPT_SIGN = 1, 2, 3
 GC_DIAG_LAYOUT_MISMATCH, GC_DIAG_SELECT, GC_DIAG_INDEX_RANGE, GC_DIAG_BAD_THRESHOLD = 0x1, 0x2, 0x4, 0x8
-GC_DIAG_INDEX_ORDER = 0x10
+GC_DIAG_INDEX_ORDER, GC_DIAG_TIMEOUT = 0x10, 0x20
 GC_NOALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 
 
@@ -37,7 +38,7 @@ class gc_matrix_layout(C.Structure):
 
 class gc_diag(C.Structure):
     _fields_ = [("error_bits", C.c_uint32), ("exact_tensors", C.c_uint32),
-                ("overflow_tensors", C.c_uint32), ("reserved", C.c_uint32)]
+                ("overflow_tensors", C.c_uint32), ("one_launch", C.c_uint32)]
 
 
 class GCError(RuntimeError):

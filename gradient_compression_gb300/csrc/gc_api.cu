@@ -49,7 +49,7 @@ extern "C" gc_status gc_get_device_status(const void* workspace, size_t ws_bytes
                                           gc_diag* out) {
   NvtxRange nvtx_range("gc_get_device_status");
   if (!workspace || ws_bytes < DIAG_BYTES || !out) return GC_ERR_INVALID_ARG;
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  uint32_t w[5] = {0u, 0u, 0u, 0u, 0u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(w, workspace, sizeof w, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return GC_ERR_CUDA;
@@ -57,7 +57,7 @@ extern "C" gc_status gc_get_device_status(const void* workspace, size_t ws_bytes
   out->error_bits = w[DIAG_ERR];
   out->exact_tensors = w[DIAG_EXACT];
   out->overflow_tensors = w[DIAG_OVF];
-  out->reserved = 0u;
+  out->one_launch = w[DIAG_PATH];
   return w[DIAG_ERR] ? GC_ERR_DEVICE : GC_OK;
 }
 

@@ -40,7 +40,7 @@ constexpr uint32_t TS_DENSE = 2u;     // select with full passes over the tensor
 constexpr uint32_t TS_OVERFLOW = 4u;  // candidate staging overflowed
 
 // Diagnostic words at the head of every workspace.
-constexpr int DIAG_ERR = 0, DIAG_EXACT = 1, DIAG_OVF = 2, DIAG_ABORT = 3;
+constexpr int DIAG_ERR = 0, DIAG_EXACT = 1, DIAG_OVF = 2, DIAG_ABORT = 3, DIAG_PATH = 4;
 constexpr size_t DIAG_BYTES = 256;
 
 struct alignas(16) TensorState {

@@ -27,6 +27,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "gc_common.cuh"
 #include "gc_host.h"
@@ -1716,6 +1717,493 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
   }
 }
 
+// ============================================================================ one-launch path
+
+// Small arenas (at most FNMAX elements in at most FTMAX tensors) spend most
+// of the multi-kernel pipeline's time in launch gaps and short phases.  Here
+// one cooperative launch, every CTA resident at once, runs the whole call,
+// with grid-wide barriers between its phases:
+//   1  acc = g + e, e <- acc; level-1 histogram (key >> 21) and largest key
+//      per tensor
+//   2  each CTA finds the level-1 bucket of its tensors' k-th key; level-2
+//      histogram ((key >> 10) & 2047) of that bucket, re-reading acc (L1- or
+//      L2-resident at these sizes)
+//   3  level-2 bucket; level-3 histogram (key & 1023) of the 22-bit prefix
+//   4  the k-th key and how many of its ties are kept; per-unit counts of
+//      keys above and equal to it
+//   5  index-ordered compaction into the payload, int8 codes, residual
+// A CTA owns the same contiguous range of 2048-element units in every phase
+// (a unit never straddles two tensors) and repeats the bucket searches of
+// its own tensors from the global histograms, so the four barriers are the
+// only waits between CTAs.  The keys, their total order (ties to the lower
+// index) and the payload writer (emit_kept) are the pipeline's, so the
+// results are identical to it.
+constexpr int FTHREADS = 512;
+constexpr int FUNIT_SHIFT = 11;
+constexpr int FUNIT = 1 << FUNIT_SHIFT;  // one float4 per thread
+constexpr int FTMAX = 1024;
+constexpr int64_t FNMAX = int64_t(1) << 22;  // above ~7M elements the pipeline is faster (measured)
+constexpr int FTCACHE = 64;                 // tensors one CTA's units may span
+constexpr int FBATCH = 2;                   // units whose loads are in flight together (phase 1)
+constexpr int FB = 2;                       // the same for the later phases (acc only)
+constexpr uint32_t FSPIN_LIMIT = 1u << 20;  // polls of a barrier (about a second)
+static_assert(FTHREADS * 4 == FUNIT, "one float4 per thread per unit");
+
+struct FusedArgs {
+  TopkArgs A;        // inputs, outputs and the fields emit_kept reads
+  uint32_t* bar;     // arrivals at the grid barriers (zeroed per call)
+  uint32_t* maxkey;  // [T] largest key per tensor (zeroed per call)
+  uint32_t* h1;      // [T][NBINS] level-1 histograms (zeroed per call)
+  uint32_t* h2;      // [T][NBINS] level 2, then [T][NBINS] level 3 (cleared in phase 1)
+  uint32_t* ugt;     // [U] keys above the k-th key, per unit
+  uint32_t* ueq;     // [U] keys equal to it, per unit
+  int64_t U;
+  uint32_t spin_limit;
+};
+
+// One tensor's k-th key search as seen by one CTA.
+struct FSel {
+  uint32_t b1, b2, r2, r3, thr, r_eq;
+  float s;  // int8 scale
+  int live;  // k_t > 0 and every level found its bucket
+};
+
+struct FUnitRef {
+  int t;
+  int64_t base;  // arena index of the tensor's element 0
+  int64_t n;
+  int64_t li0;   // local index of the unit's element 0
+  int len;       // elements in the unit (1 .. FUNIT)
+};
+
+// Unit u, walking the tensor index t forward (units are visited in order).
+__device__ __forceinline__ FUnitRef funit(const int64_t* s_off, const int32_t* s_uoff, int* t, int64_t u) {
+  while ((int64_t)s_uoff[*t + 1] <= u) ++*t;
+  FUnitRef r;
+  r.t = *t;
+  r.base = s_off[r.t];
+  r.n = s_off[r.t + 1] - r.base;
+  r.li0 = (u - (int64_t)s_uoff[r.t]) << FUNIT_SHIFT;
+  r.len = (int)min((int64_t)FUNIT, r.n - r.li0);
+  return r;
+}
+
+// This thread's elements li0 + 4 tid .. + 3 of the unit; returns how many
+// exist.  One 16-byte load when the tensor starts on a 16-byte boundary.
+template <bool STREAM>
+__device__ __forceinline__ int fload4(const float* src, const FUnitRef& r, float x[4]) {
+  const int o = 4 * (int)threadIdx.x;
+  const int c = max(0, min(4, r.len - o));
+  const int64_t gi = r.base + r.li0 + o;
+  if (c == 4 && (gi & 3) == 0) {
+    const float4* p = reinterpret_cast<const float4*>(src + gi);
+    const float4 v = STREAM ? __ldcs(p) : *p;
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = j < c ? src[gi + j] : 0.0f;
+  }
+  return c;
+}
+
+// The elements of up to NB consecutive units (fewer at u1), loads issued together.
+template <int NB>
+__device__ __forceinline__ void fload_batch(const float* src, const int64_t* s_off, const int32_t* s_uoff, int* t,
+                                            int64_t ub, int64_t u1, float x[NB][4], int c[NB]) {
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    c[j] = 0;
+    if (ub + j < u1) {
+      const FUnitRef r = funit(s_off, s_uoff, t, ub + j);
+      c[j] = fload4<false>(src, r, x[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ void fstore4(float* dst, const FUnitRef& r, const float x[4], int c) {
+  const int64_t gi = r.base + r.li0 + 4 * (int)threadIdx.x;
+  if (c == 4 && (gi & 3) == 0) {
+    *reinterpret_cast<float4*>(dst + gi) = make_float4(x[0], x[1], x[2], x[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < c) dst[gi + j] = x[j];
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the cooperative launch: false when the call is
+// aborted.  Every wait is bounded: after spin_limit polls the CTA sets
+// GC_DIAG_TIMEOUT and the abort word, which ends the other CTAs' waits too.
+__device__ bool fused_barrier(const FusedArgs& F, uint32_t* target, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *target += gridDim.x;
+    __threadfence();
+    atomicAdd(F.bar, 1u);
+    int ok = 1;
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(F.bar) < *target) {
+      if (*reinterpret_cast<volatile uint32_t*>(F.A.diag + DIAG_ABORT) != 0u) {
+        ok = 0;
+        break;
+      }
+      if (++spins > F.spin_limit) {
+        atomicOr(F.A.diag + DIAG_ERR, GC_DIAG_TIMEOUT);
+        atomicExch(F.A.diag + DIAG_ABORT, 1u);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// Adds the shared histogram to a global row and clears it (block-wide).
+__device__ __forceinline__ void fflush_hist(uint32_t* s_hist, uint32_t* row) {
+  __syncthreads();
+  for (int b = threadIdx.x; b < NBINS; b += blockDim.x) {
+    const uint32_t v = s_hist[b];
+    if (v) {
+      atomicAdd(row + b, v);
+      s_hist[b] = 0u;
+    }
+  }
+  __syncthreads();
+}
+
+// find_bucket on a global row written by other CTAs: copied through L2 into
+// shared memory first.
+__device__ __forceinline__ uint32_t ffind(const uint32_t* row, uint32_t rank, uint32_t* above, uint32_t* s_row,
+                                          uint32_t* s_warp, uint32_t* s_res) {
+  for (int b = threadIdx.x; b < NBINS; b += blockDim.x) s_row[b] = __ldcg(row + b);
+  __syncthreads();
+  return find_bucket(s_row, rank, above, s_warp, s_res);
+}
+
+template <bool EF>
+__global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
+  __shared__ int64_t s_off[FTMAX + 1];
+  __shared__ int32_t s_uoff[FTMAX + 1];
+  __shared__ uint32_t s_hist[NBINS];
+  __shared__ uint32_t s_row[NBINS];
+  __shared__ uint32_t s_warp[33];
+  __shared__ uint32_t s_res[3];
+  __shared__ FSel s_sel[FTCACHE];
+  __shared__ int s_ok;
+  const TopkArgs& A = F.A;
+  const int T = A.T;
+  const int tid = threadIdx.x;
+  const float* src = EF ? A.e : A.g;  // acc after phase 1
+
+  // ---- layout: every CTA reads and checks all of it, so all agree
+  if (tid == 0) s_ok = 1;
+  for (int i = tid; i <= T; i += blockDim.x) s_off[i] = A.off[i];
+  for (int i = tid; i < NBINS; i += blockDim.x) s_hist[i] = 0u;
+  __syncthreads();
+  uint32_t carry = 0u;
+  for (int b0 = 0; b0 < T; b0 += blockDim.x) {
+    const int t = b0 + tid;
+    uint32_t nu = 0u;
+    if (t < T) {
+      const int64_t n = s_off[t + 1] - s_off[t];
+      const int64_t k = A.kk[t];
+      if (n < 1 || n > FNMAX || k < 0 || k > n || A.koff[t + 1] - A.koff[t] != k)
+        s_ok = 0;
+      else
+        nu = (uint32_t)((n + FUNIT - 1) >> FUNIT_SHIFT);
+    }
+    uint32_t ex, tot;
+    block_scan_u32(nu, s_warp, &ex, &tot);
+    if (t < T) s_uoff[t] = (int32_t)(carry + ex);
+    carry += tot;
+  }
+  if (tid == 0) {
+    s_uoff[T] = (int32_t)carry;
+    if (s_off[0] != 0 || s_off[T] != A.N || A.koff[0] != 0 || A.koff[T] != A.K || (int64_t)carry != F.U) s_ok = 0;
+  }
+  __syncthreads();
+  if (!s_ok) {
+    if (blockIdx.x == 0 && tid == 0) {
+      atomicOr(A.diag + DIAG_ERR, GC_DIAG_LAYOUT_MISMATCH);
+      atomicExch(A.diag + DIAG_ABORT, 1u);
+    }
+    return;  // every CTA returns here: no barrier is waited on
+  }
+  if (blockIdx.x == 0 && tid == 0) A.diag[DIAG_PATH] = 1u;
+
+  // ---- this CTA's units and tensors
+  const int64_t G = gridDim.x;
+  const int64_t u0 = F.U * (int64_t)blockIdx.x / G, u1 = F.U * ((int64_t)blockIdx.x + 1) / G;
+  int tA = 0;
+  {
+    int lo = 0, hi = T;  // last t with s_uoff[t] <= u0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)s_uoff[mid] <= u0) lo = mid; else hi = mid;
+    }
+    tA = lo;
+  }
+  bool work = u1 > u0;
+  if (work) {
+    int tB = tA;
+    while ((int64_t)s_uoff[tB + 1] <= u1 - 1) ++tB;
+    if (tB - tA + 1 > FTCACHE) {  // the host sizes the grid so that this cannot happen
+      if (tid == 0) atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+      work = false;
+    }
+  }
+  uint32_t target = 0u;  // barrier arrivals awaited (thread 0)
+
+  // ---- phase 1: acc, e <- acc, level-1 histograms, largest keys
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < 2 * (int64_t)T * NBINS; i += G * blockDim.x)
+    __stcg(F.h2 + i, 0u);
+  if (work) {
+    int t = tA;
+    uint32_t mx = 0u;
+    for (int64_t ub = u0; ub < u1; ub += FBATCH) {
+      FUnitRef r[FBATCH];
+      float gx[FBATCH][4], ex[FBATCH][4];
+      int c[FBATCH];
+#pragma unroll
+      for (int j = 0; j < FBATCH; ++j) {
+        c[j] = 0;
+        if (ub + j < u1) {
+          r[j] = funit(s_off, s_uoff, &t, ub + j);
+          c[j] = fload4<!EF>(A.g, r[j], gx[j]);
+          if (EF) fload4<false>(A.e, r[j], ex[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < FBATCH; ++j) {
+        if (ub + j >= u1) break;
+        float a[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) a[q] = EF ? __fadd_rn(gx[j][q], ex[j][q]) : gx[j][q];
+        if (EF) fstore4(A.e, r[j], a, c[j]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = mag_key(a[q]);
+          smem_hist_add(s_hist, key >> 21, q < c[j]);
+          if (q < c[j]) mx = max(mx, key);
+        }
+        if (ub + j + 1 == u1 || (int64_t)s_uoff[r[j].t + 1] == ub + j + 1) {  // the tensor's last unit here
+          fflush_hist(s_hist, F.h1 + (size_t)r[j].t * NBINS);
+          if (A.int8) {
+            const uint32_t wm = warp_max_u32(mx);
+            if ((tid & 31) == 0) s_warp[tid >> 5] = wm;
+            __syncthreads();
+            if (tid == 0) {
+              uint32_t m = 0u;
+              for (int w = 0; w < FTHREADS / 32; ++w) m = max(m, s_warp[w]);
+              atomicMax(F.maxkey + r[j].t, m);
+            }
+            __syncthreads();
+          }
+          mx = 0u;
+        }
+      }
+    }
+  }
+  if (!fused_barrier(F, &target, &s_ok)) return;
+
+  // Phases 2-5 re-read acc; FB units' loads are issued together.
+  // ---- phase 2: level-1 bucket; level-2 histograms
+  if (work) {
+    int tl = tA, t = tA;
+    for (int64_t ub = u0; ub < u1; ub += FB) {
+      float x[FB][4];
+      int c[FB];
+      fload_batch<FB>(src, s_off, s_uoff, &tl, ub, u1, x, c);
+#pragma unroll
+      for (int j = 0; j < FB; ++j) {
+        const int64_t u = ub + j;
+        if (u >= u1) break;
+        const FUnitRef r = funit(s_off, s_uoff, &t, u);
+        FSel* sl = s_sel + (r.t - tA);
+        if (u == u0 || (int64_t)s_uoff[r.t] == u) {
+          const int64_t k = A.kk[r.t];
+          uint32_t above = 0u, b = 0xFFFFFFFFu;
+          if (k > 0) b = ffind(F.h1 + (size_t)r.t * NBINS, (uint32_t)k, &above, s_row, s_warp, s_res);
+          if (tid == 0) {
+            sl->live = (k > 0 && b != 0xFFFFFFFFu) ? 1 : 0;
+            if (k > 0 && b == 0xFFFFFFFFu) atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+            sl->b1 = b;
+            sl->r2 = (uint32_t)k - above;
+          }
+          __syncthreads();
+        }
+        if (!sl->live) continue;
+        const uint32_t b1 = sl->b1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = mag_key(x[j][q]);
+          smem_hist_add(s_hist, (key >> 10) & 0x7FFu, q < c[j] && (key >> 21) == b1);
+        }
+        if (u + 1 == u1 || (int64_t)s_uoff[r.t + 1] == u + 1) fflush_hist(s_hist, F.h2 + (size_t)r.t * NBINS);
+      }
+    }
+  }
+  if (!fused_barrier(F, &target, &s_ok)) return;
+
+  // ---- phase 3: level-2 bucket; level-3 histograms
+  uint32_t* const h3 = F.h2 + (size_t)T * NBINS;
+  if (work) {
+    int tl = tA, t = tA;
+    for (int64_t ub = u0; ub < u1; ub += FB) {
+      float x[FB][4];
+      int c[FB];
+      fload_batch<FB>(src, s_off, s_uoff, &tl, ub, u1, x, c);
+#pragma unroll
+      for (int j = 0; j < FB; ++j) {
+        const int64_t u = ub + j;
+        if (u >= u1) break;
+        const FUnitRef r = funit(s_off, s_uoff, &t, u);
+        FSel* sl = s_sel + (r.t - tA);
+        if (!sl->live) continue;
+        if (u == u0 || (int64_t)s_uoff[r.t] == u) {
+          uint32_t above = 0u;
+          const uint32_t b = ffind(F.h2 + (size_t)r.t * NBINS, sl->r2, &above, s_row, s_warp, s_res);
+          if (tid == 0) {
+            if (b == 0xFFFFFFFFu) {
+              atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+              sl->live = 0;
+            }
+            sl->b2 = b;
+            sl->r3 = sl->r2 - above;
+          }
+          __syncthreads();
+          if (!sl->live) continue;
+        }
+        const uint32_t pfx = (sl->b1 << 11) | sl->b2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = mag_key(x[j][q]);
+          smem_hist_add(s_hist, key & 0x3FFu, q < c[j] && (key >> 10) == pfx);
+        }
+        if (u + 1 == u1 || (int64_t)s_uoff[r.t + 1] == u + 1) fflush_hist(s_hist, h3 + (size_t)r.t * NBINS);
+      }
+    }
+  }
+  if (!fused_barrier(F, &target, &s_ok)) return;
+
+  // ---- phase 4: the k-th key, kept ties, scale; per-unit counts
+  if (work) {
+    int tl = tA, t = tA;
+    for (int64_t ub = u0; ub < u1; ub += FB) {
+      float x[FB][4];
+      int c[FB];
+      fload_batch<FB>(src, s_off, s_uoff, &tl, ub, u1, x, c);
+#pragma unroll
+      for (int j = 0; j < FB; ++j) {
+        const int64_t u = ub + j;
+        if (u >= u1) break;
+        const FUnitRef r = funit(s_off, s_uoff, &t, u);
+        FSel* sl = s_sel + (r.t - tA);
+        const bool owner = (int64_t)s_uoff[r.t] == u;  // this CTA holds the tensor's first unit
+        if (u == u0 || owner) {
+          if (sl->live) {
+            uint32_t above = 0u;
+            const uint32_t b = ffind(h3 + (size_t)r.t * NBINS, sl->r3, &above, s_row, s_warp, s_res);
+            if (tid == 0) {
+              if (b == 0xFFFFFFFFu) {
+                atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+                sl->live = 0;
+              }
+              sl->thr = (((sl->b1 << 11) | sl->b2) << 10) | b;
+              sl->r_eq = sl->r3 - above;
+              sl->s = A.int8 ? __fdiv_rn(key_magnitude(__ldcg(F.maxkey + r.t)), 127.0f) : 0.0f;
+            }
+          }
+          __syncthreads();
+          if (owner && tid == 0 && A.int8) A.scale[r.t] = sl->live ? sl->s : 0.0f;
+        }
+        uint32_t v = 0u;
+        if (sl->live) {
+          const uint32_t thr = sl->thr;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t key = mag_key(x[j][q]);
+            if (q < c[j]) v += (key > thr ? 1u : 0u) | (key == thr ? 0x10000u : 0u);
+          }
+        }
+        uint32_t ex, tot;
+        block_scan_u32(v, s_warp, &ex, &tot);  // unit counts < 2^16 each
+        if (tid == 0) {
+          F.ugt[u] = tot & 0xFFFFu;
+          F.ueq[u] = tot >> 16;
+        }
+      }
+    }
+  }
+  if (!fused_barrier(F, &target, &s_ok)) return;
+
+  // ---- phase 5: payload and residual, in index order
+  if (work) {
+    int tl = tA, t = tA;
+    uint32_t bgt = 0u, beq = 0u;  // this tensor's keys above / equal to the k-th key before the unit
+    for (int64_t ub = u0; ub < u1; ub += FB) {
+      float x[FB][4];
+      int c[FB];
+      fload_batch<FB>(src, s_off, s_uoff, &tl, ub, u1, x, c);
+#pragma unroll
+      for (int j = 0; j < FB; ++j) {
+        const int64_t u = ub + j;
+        if (u >= u1) break;
+        const FUnitRef r = funit(s_off, s_uoff, &t, u);
+        const FSel S = s_sel[r.t - tA];
+        if (!S.live) continue;
+        if (u == u0 || (int64_t)s_uoff[r.t] == u) {
+          uint32_t pg = 0u, pe = 0u;
+          for (int64_t w = (int64_t)s_uoff[r.t] + tid; w < u; w += blockDim.x) {
+            pg += __ldcg(F.ugt + w);
+            pe += __ldcg(F.ueq + w);
+          }
+          uint32_t ex;
+          block_scan_u32(pg, s_warp, &ex, &bgt);
+          block_scan_u32(pe, s_warp, &ex, &beq);
+        }
+        unsigned gtm = 0u, eqm = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t key = mag_key(x[j][q]);
+          gtm |= (q < c[j] && key > S.thr ? 1u : 0u) << q;
+          eqm |= (q < c[j] && key == S.thr ? 1u : 0u) << q;
+        }
+        uint32_t epre, etot;
+        block_scan_u32((uint32_t)__popc(eqm), s_warp, &epre, &etot);
+        unsigned selm = gtm;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (((eqm >> q) & 1u) && beq + epre + (uint32_t)__popc(eqm & ((1u << q) - 1u)) < S.r_eq) selm |= 1u << q;
+        uint32_t spre, stot;
+        block_scan_u32((uint32_t)__popc(selm), s_warp, &spre, &stot);
+        const int64_t pos0 = A.koff[r.t] + (int64_t)bgt + (int64_t)min(beq, S.r_eq) + spre;
+        for (unsigned m = selm; m != 0u; m &= m - 1u) {
+          const int q = __ffs(m) - 1;
+          const float xv = q == 0 ? x[j][0] : (q == 1 ? x[j][1] : (q == 2 ? x[j][2] : x[j][3]));
+          emit_kept<MODE_TOPK, KQ_NONE>(A, r.t, r.base, r.n, r.li0 + 4 * tid + q, xv,
+                                        pos0 + __popc(selm & ((1u << q) - 1u)), S.s, false);
+        }
+        bgt += __ldcg(F.ugt + u);
+        beq += etot;
+      }
+    }
+  }
+}
+
 // ============================================================================ host side
 
 struct TopkLayoutTotals {
@@ -1800,8 +2288,43 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   return c;
 }
 
+// ---------------------------------------------------------------- one-launch path (host)
+
+struct FusedCarve {
+  int64_t U = 0;
+  size_t zero_bytes = 0, total = 0;
+  size_t o_bar = 0, o_max = 0, o_h1 = 0, o_h2 = 0, o_ugt = 0, o_ueq = 0;
+};
+
+static bool fused_layout_fits(const gc_layout* h) {
+  return h->num_tensors <= FTMAX && h->off[h->num_tensors] <= FNMAX;
+}
+
+static FusedCarve carve_fused(const gc_layout* h) {
+  FusedCarve c;
+  const int T = h->num_tensors;
+  for (int t = 0; t < T; ++t) c.U += (h->off[t + 1] - h->off[t] + FUNIT - 1) >> FUNIT_SHIFT;
+  size_t p = DIAG_BYTES;
+  auto take = [&p](size_t bytes) {
+    const size_t at = p;
+    p = align_up(p + bytes, 256);
+    return at;
+  };
+  c.o_bar = take(4);
+  c.o_max = take(4 * (size_t)T);
+  c.o_h1 = take((size_t)T * NBINS * 4);
+  c.zero_bytes = p;
+  c.o_h2 = take(2 * (size_t)T * NBINS * 4);
+  c.o_ugt = take(4 * (size_t)c.U);
+  c.o_ueq = take(4 * (size_t)c.U);
+  c.total = p;
+  return c;
+}
+
 size_t topk_workspace_bytes(const gc_layout* h, bool sampled) {
-  return carve_topk(h->num_tensors, totals_of(h, sampled)).total;
+  size_t b = carve_topk(h->num_tensors, totals_of(h, sampled)).total;
+  if (sampled && fused_layout_fits(h)) b = std::max(b, carve_fused(h).total);
+  return b;
 }
 
 template <class K>
@@ -1845,6 +2368,72 @@ struct PhaseEvents {
       record(phase, s);
   }
 };
+
+// Grid of the cooperative launch: every CTA resident (at most the SMs times
+// the CTAs that fit on one), at most one per unit, and no CTA's contiguous
+// unit range spanning more than FTCACHE tensors.  0 if the path cannot run.
+static int fused_grid(const gc_layout* h, int64_t U, bool ef) {
+  int dev = 0, sms = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ef ? k_fused<true> : k_fused<false>, FTHREADS, 0) !=
+          cudaSuccess) {
+    cudaGetLastError();  // leave no error state behind
+    return 0;
+  }
+  if (!coop || per_sm < 1 || U < 1) return 0;
+  int64_t G = (int64_t)sms * per_sm;
+  if (G > U) G = U;
+  const int T = h->num_tensors;
+  std::vector<int64_t> uoff(T + 1, 0);
+  for (int t = 0; t < T; ++t) uoff[t + 1] = uoff[t] + ((h->off[t + 1] - h->off[t] + FUNIT - 1) >> FUNIT_SHIFT);
+  int ta = 0;
+  for (int64_t b = 0; b < G; ++b) {
+    const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
+    if (u1 <= u0) continue;
+    while (uoff[ta + 1] <= u0) ++ta;
+    int tb = ta;
+    while (uoff[tb + 1] <= u1 - 1) ++tb;
+    if (tb - ta + 1 > FTCACHE) return 0;
+  }
+  return (int)G;
+}
+
+static gc_status launch_fused(const TopkArgs& A0, const gc_layout* host, const FusedCarve& fc, int G, void* ws,
+                              cudaStream_t s, const PhaseEvents& pe) {
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  FusedArgs F;
+  memset(&F, 0, sizeof F);
+  F.A = A0;
+  F.bar = reinterpret_cast<uint32_t*>(w + fc.o_bar);
+  F.maxkey = reinterpret_cast<uint32_t*>(w + fc.o_max);
+  F.h1 = reinterpret_cast<uint32_t*>(w + fc.o_h1);
+  F.h2 = reinterpret_cast<uint32_t*>(w + fc.o_h2);
+  F.ugt = reinterpret_cast<uint32_t*>(w + fc.o_ugt);
+  F.ueq = reinterpret_cast<uint32_t*>(w + fc.o_ueq);
+  F.U = fc.U;
+  F.spin_limit = FSPIN_LIMIT;
+  pe.start(s);
+  if (cudaMemsetAsync(ws, 0, fc.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
+  pe.done(0, s);
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(FTHREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  memset(&attr, 0, sizeof attr);
+  attr.id = cudaLaunchAttributeCooperative;
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = F.A.ef ? cudaLaunchKernelEx(&cfg, k_fused<true>, F) : cudaLaunchKernelEx(&cfg, k_fused<false>, F);
+  if (err != cudaSuccess) return GC_ERR_CUDA;
+  for (int ph = 1; ph <= 4; ++ph) pe.done(ph, s);  // one launch: the inner phases take no time of their own
+  (void)host;
+  return GC_OK;
+}
 
 template <int MODE>
 static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
@@ -2013,6 +2602,17 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.ssplit = z.split;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mode == MODE_TOPK && !rd && !tau && !clip && kq.kind == KQ_NONE &&
+      !(flags & (GC_FORCE_EXACT | GC_MULTI_KERNEL)) && fused_layout_fits(host)) {
+    const FusedCarve fc = carve_fused(host);
+    const int G = ws_bytes >= fc.total ? fused_grid(host, fc.U, A.ef != 0) : 0;
+    if (G > 0) {
+      const gc_status fst = launch_fused(A, host, fc, G, ws, s, pe);
+      if (fst != GC_OK) return fst;
+      if (iter_dev) k_iter_advance<<<1, 1, 0, s>>>(iter_dev);
+      return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    }
+  }
   pe.start(s);
   if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
   pe.done(0, s);
@@ -2040,7 +2640,7 @@ static gc_status topk_entry(const gc_layout* dev, const gc_layout* host, const f
                             int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                             uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
                             void* stream, const PhaseEvents& pe, uint64_t* iter_dev = nullptr) {
-  const uint32_t known = GC_EF | GC_INT8 | GC_RANDK | GC_UNBIASED | GC_FORCE_EXACT;
+  const uint32_t known = GC_EF | GC_INT8 | GC_RANDK | GC_UNBIASED | GC_FORCE_EXACT | GC_MULTI_KERNEL;
   if (flags & ~known) return GC_ERR_INVALID_ARG;
   const bool randk = (flags & GC_RANDK) != 0u;
   if (randk && (flags & GC_INT8)) return GC_ERR_INVALID_ARG;

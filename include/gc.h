@@ -91,6 +91,8 @@ typedef enum gc_status {
 #define GC_LAZY 0x20u       /* set by gc_ef_topk_compress_lazy; not accepted elsewhere */
 #define GC_FORCE_EXACT 0x100u /* select with full passes over the tensor instead of the
                                  sampled candidate threshold (same results; for testing) */
+#define GC_MULTI_KERNEL 0x200u /* Top-k: run the multi-kernel pipeline even where the one-launch
+                                  path would (same results; for testing and comparison) */
 
 /* Operations, for gc_workspace_size. */
 typedef enum gc_op {
@@ -122,7 +124,7 @@ typedef struct gc_diag {
   uint32_t error_bits;       /* GC_DIAG_* bits */
   uint32_t exact_tensors;    /* tensors selected by full passes (fallback or GC_FORCE_EXACT) */
   uint32_t overflow_tensors; /* tensors whose candidate list overflowed (then selected exactly) */
-  uint32_t reserved;
+  uint32_t one_launch;       /* 1 if the call ran as one cooperative launch (see GC_MULTI_KERNEL) */
 } gc_diag;
 
 #define GC_DIAG_LAYOUT_MISMATCH 0x1u /* dev and host layouts disagree; the call did nothing */
@@ -131,6 +133,8 @@ typedef struct gc_diag {
 #define GC_DIAG_BAD_THRESHOLD 0x8u   /* a threshold or clipping norm was negative or NaN */
 #define GC_DIAG_INDEX_ORDER 0x10u    /* decompress met a worker's indices not ascending within a
                                         tensor; see gc_sparse_decompress_accumulate */
+#define GC_DIAG_TIMEOUT 0x20u        /* a grid-wide wait of the one-launch path ran out (about a
+                                        second); that call's outputs are incomplete */
 
 /* CUDA-graph capture.  gc_ef_topk_compress_dev_iter and
  * gc_quantize_stochastic_dev_iter are gc_ef_topk_compress and
@@ -162,7 +166,13 @@ gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32_t flags, s
  * int32[sum k].  val: device fp32[sum k] (required without GC_INT8,
  * optional with it).  q: device int8[sum k] and scale: device fp32[T],
  * both required iff GC_INT8.  seed, iter: Philox key and counter words.
- * GC_INT8 cannot be combined with GC_RANDK. */
+ * GC_INT8 cannot be combined with GC_RANDK.
+ * Launches.  Top-k on an arena of at most 2^22 elements in at most 1024
+ * tensors runs as one cooperative launch (all CTAs resident) whose phases
+ * meet at four grid-wide barriers; every wait there is bounded and sets
+ * GC_DIAG_TIMEOUT if it runs out.  gc_diag.one_launch reports it.  Other
+ * arenas, random-k, GC_FORCE_EXACT and GC_MULTI_KERNEL use the multi-kernel
+ * pipeline (a memset and 13 kernels).  Both give identical results. */
 gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
                               int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                               uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,

@@ -70,6 +70,8 @@ def test_topk_random_layouts(gc, seed):
     L = gc.Layout(workloads.prefix(sizes), k, device="cuda")
     flags = [gc.GC_EF, gc.GC_EF | gc.GC_INT8, 0, gc.GC_EF | gc.GC_FORCE_EXACT,
              gc.GC_EF | gc.GC_INT8 | gc.GC_FORCE_EXACT][seed % 5]
+    if seed % 2:
+        flags |= gc.GC_MULTI_KERNEL  # odd seeds: the pipeline; even seeds mostly the one-launch path
     e = np.zeros(L.numel, F32) if flags & gc.GC_EF else None
     ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
     for it in range(2):

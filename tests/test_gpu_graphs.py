@@ -29,9 +29,11 @@ def _grads(n):
     return [torch.randn(n, generator=torch.Generator().manual_seed(900 + i)).cuda() * 1e-3 for i in range(STEPS)]
 
 
-@pytest.mark.parametrize("flags_name", ["randk_ef", "topk_int8"])
+@pytest.mark.parametrize("flags_name", ["randk_ef", "topk_int8", "topk_int8_pipeline"])
 def test_topk_graph_replay_matches_direct_calls(gc, flags_name):
-    flags = {"randk_ef": gc.GC_EF | gc.GC_RANDK, "topk_int8": gc.GC_EF | gc.GC_INT8}[flags_name]
+    # topk_int8 captures the one-launch path (a cooperative kernel node)
+    flags = {"randk_ef": gc.GC_EF | gc.GC_RANDK, "topk_int8": gc.GC_EF | gc.GC_INT8,
+             "topk_int8_pipeline": gc.GC_EF | gc.GC_INT8 | gc.GC_MULTI_KERNEL}[flags_name]
     int8 = bool(flags & gc.GC_INT8)
     sizes = np.asarray(SIZES)
     L = gc.Layout(workloads.prefix(sizes), workloads.k_per_tensor(sizes, 0.01), device="cuda")

@@ -61,10 +61,12 @@ def _layout(gc, sizes, rho):
 SIZES = [4097, 1, 33, 100_003, 6, 70_000, 300_001]
 
 
-@pytest.mark.parametrize("flags_name", ["ef_int8", "ef", "randk", "ef_exact"])
+@pytest.mark.parametrize("flags_name", ["ef_int8", "ef", "noef", "randk", "ef_exact", "ef_int8_pipeline", "ef_pipeline"])
 def test_topk_writes_stay_in_bounds(gc, flags_name):
-    flags = {"ef_int8": gc.GC_EF | gc.GC_INT8, "ef": gc.GC_EF, "randk": gc.GC_EF | gc.GC_RANDK,
-             "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT}[flags_name]
+    # this layout runs as one cooperative launch unless a flag asks for the pipeline
+    flags = {"ef_int8": gc.GC_EF | gc.GC_INT8, "ef": gc.GC_EF, "noef": 0, "randk": gc.GC_EF | gc.GC_RANDK,
+             "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT, "ef_int8_pipeline": gc.GC_EF | gc.GC_INT8 | gc.GC_MULTI_KERNEL,
+             "ef_pipeline": gc.GC_EF | gc.GC_MULTI_KERNEL}[flags_name]
     L = _layout(gc, SIZES, 0.01)
     N, K, T = L.numel, L.total_k, L.T
     int8 = bool(flags & gc.GC_INT8)

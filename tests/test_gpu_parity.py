@@ -53,8 +53,17 @@ def _grad(n, seed, kind="t3"):
     return x.float()
 
 
+def _one_launch_expected(gc, L, flags):
+    """Whether gc_ef_topk_compress runs as one cooperative launch: Top-k on
+    at most 2^22 elements in at most 1024 tensors, unless a flag asks for
+    the multi-kernel pipeline (random-k and GC_FORCE_EXACT use it too)."""
+    return (not flags & (gc.GC_RANDK | gc.GC_FORCE_EXACT | gc.GC_MULTI_KERNEL) and L.T <= 1024
+            and L.numel <= (1 << 22))
+
+
 def _topk_check(gc, L, g_h, e_h, flags, seed, it, ws=None, expect_exact=None):
-    """Runs one GPU call and the oracle; asserts bit-exact payload and residual."""
+    """Runs one GPU call and the oracle; asserts bit-exact payload and residual,
+    and that the call took the launch path the layout and flags call for."""
     dev = L.device
     K = L.total_k
     int8 = bool(flags & gc.GC_INT8)
@@ -69,6 +78,7 @@ def _topk_check(gc, L, g_h, e_h, flags, seed, it, ws=None, expect_exact=None):
     gc.ef_topk_compress(L, g, e, idx, val, q, sc, seed, it, flags, ws)
     diag = gc.get_device_status(ws)
     assert diag.error_bits == 0
+    assert diag.one_launch == int(_one_launch_expected(gc, L, flags)), (diag.one_launch, flags)
     if expect_exact is not None:
         assert diag.exact_tensors == expect_exact, (diag.exact_tensors, expect_exact)
     gi, gv = idx.cpu().numpy()[:K], val.cpu().numpy()[:K]
@@ -108,13 +118,23 @@ LAYOUTS = {
 }
 
 
+# "one_launch": the default path of these small layouts; "pipeline": the
+# multi-kernel pipeline forced with GC_MULTI_KERNEL (GC_FORCE_EXACT implies it)
+PATHS = ["one_launch", "pipeline"]
+
+
 @pytest.mark.parametrize("name", sorted(LAYOUTS))
 @pytest.mark.parametrize("flags_name", ["ef", "ef_int8", "noef", "ef_exact", "ef_int8_exact"])
-def test_topk_layouts(gc, name, flags_name):
+@pytest.mark.parametrize("path", PATHS)
+def test_topk_layouts(gc, name, flags_name, path):
     sizes = LAYOUTS[name]
     flags = {"ef": gc.GC_EF, "ef_int8": gc.GC_EF | gc.GC_INT8, "noef": 0,
              "ef_exact": gc.GC_EF | gc.GC_FORCE_EXACT,
              "ef_int8_exact": gc.GC_EF | gc.GC_INT8 | gc.GC_FORCE_EXACT}[flags_name]
+    if flags & gc.GC_FORCE_EXACT and path == "one_launch":
+        pytest.skip("GC_FORCE_EXACT always runs the pipeline")
+    if path == "pipeline":
+        flags |= gc.GC_MULTI_KERNEL
     rng = np.random.default_rng(len(sizes))
     k = [int(min(n, max(0, int(rng.integers(0, 3)) if n < 8 else int(np.ceil(0.01 * n))))) for n in sizes]
     if len(sizes) > 2:
@@ -275,18 +295,20 @@ def test_kept_quantizer_arguments(gc):
 
 
 @pytest.mark.parametrize("kind", ["ties", "zeros"])
-@pytest.mark.parametrize("exact", [False, True])
-def test_topk_ties(gc, kind, exact):
+@pytest.mark.parametrize("path", ["one_launch", "pipeline", "pipeline_exact"])
+def test_topk_ties(gc, kind, path):
     sizes = [10_000, 4096, 333, 70_000]
     L = _layout(gc, sizes, k=[37, 4096, 1, 700])
     n = L.numel
-    flags = gc.GC_EF | (gc.GC_FORCE_EXACT if exact else 0)
+    exact = path == "pipeline_exact"
+    flags = gc.GC_EF | {"one_launch": 0, "pipeline": gc.GC_MULTI_KERNEL,
+                        "pipeline_exact": gc.GC_FORCE_EXACT}[path]
     e = np.zeros(n, F32)
     if kind == "zeros":
         e[::5] = -0.0
     g = _grad(n, 1, kind).numpy()
     _, d = _topk_check(gc, L, g, e, flags, seed=1, it=0)
-    if kind == "ties" and not exact:
+    if kind == "ties" and path == "pipeline":
         # 20% of the 70,000-element tensor ties at the largest magnitude: more
         # candidates than its capacity, so the overflow fallback must have run
         assert d.overflow_tensors >= 1 and d.exact_tensors >= 1
@@ -294,12 +316,13 @@ def test_topk_ties(gc, kind, exact):
 
 @pytest.mark.parametrize("rho", [0.001, 0.01])
 @pytest.mark.parametrize("flags_name", ["ef", "ef_int8"])
-def test_topk_boundary_ties(gc, rho, flags_name):
+@pytest.mark.parametrize("path", PATHS)
+def test_topk_boundary_ties(gc, rho, flags_name, path):
     """A group of equal magnitudes straddles the k-th rank (ties kept by lowest
     index); 0.1% gives short candidate chunks per unit, 1% long ones, so both
     candidate walks of the payload write meet a partial tie group."""
     n = 300_000
-    flags = gc.GC_EF | (gc.GC_INT8 if flags_name == "ef_int8" else 0)
+    flags = gc.GC_EF | (gc.GC_INT8 if flags_name == "ef_int8" else 0) | (gc.GC_MULTI_KERNEL if path == "pipeline" else 0)
     L = _layout(gc, [n, 4099], rho=rho)
     g = _grad(L.numel, 21).numpy()
     k0 = int(L.k[0])
@@ -313,27 +336,44 @@ def test_topk_boundary_ties(gc, rho, flags_name):
     assert d.overflow_tensors == 0
 
 
-def test_topk_flat_2p20_ten_iterations(gc):
+@pytest.mark.parametrize("path", PATHS)
+def test_topk_flat_2p20_ten_iterations(gc, path):
     """One flat fp32 gradient of 2^20 elements at 0.1% (k = 1049), EF, 10 fresh gradients."""
     lay = workloads.flat_layout(1 << 20)
     L = _layout(gc, lay.sizes, rho=0.001)
     assert L.total_k == 1049
+    flags = gc.GC_EF | (gc.GC_MULTI_KERNEL if path == "pipeline" else 0)
     e = np.zeros(L.numel, F32)
-    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
     for it in range(10):
         g = workloads.make_grad(1, lay, it).numpy()
-        e, d = _topk_check(gc, L, g, e, gc.GC_EF, seed=0, it=it, ws=ws, expect_exact=0)
+        e, d = _topk_check(gc, L, g, e, flags, seed=0, it=it, ws=ws, expect_exact=0)
+
+
+@pytest.mark.parametrize("n", [1 << 22, (1 << 22) + 1])
+def test_one_launch_size_boundary(gc, n):
+    """2^22 elements is the largest arena the one-launch path takes; one more
+    element and the call runs the pipeline (the check inside _topk_check)."""
+    sizes = [n - 3000, 1000, 2000]
+    L = _layout(gc, sizes, rho=0.001)
+    e = np.zeros(L.numel, F32)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF | gc.GC_INT8)
+    for it in range(2):
+        g = _grad(L.numel, 50 + it).numpy()
+        e, _ = _topk_check(gc, L, g, e, gc.GC_EF | gc.GC_INT8, seed=4, it=it, ws=ws)
 
 
 def test_topk_resnet50_and_randk(gc):
+    """ResNet-50 (25.6M elements, above the one-launch path's 2^22): the pipeline."""
     lay = workloads.resnet50_layout()
     L = _layout(gc, lay.sizes, rho=0.01)
     assert L.total_k == 255_658
+    flags = gc.GC_EF
     e = np.zeros(L.numel, F32)
-    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
     for it in range(3):
         g = workloads.make_grad(2, lay, it).numpy()
-        e, d = _topk_check(gc, L, g, e, gc.GC_EF, seed=2, it=it, ws=ws)
+        e, d = _topk_check(gc, L, g, e, flags, seed=2, it=it, ws=ws)
         assert d.exact_tensors <= 3      # only degenerate tensors may need full passes
     e = np.zeros(L.numel, F32)
     for it in range(2):
@@ -776,7 +816,9 @@ def test_dense_decompress(gc, kind):
     assert np.array_equal(_bits(out.cpu().numpy()), _bits(ref))
 
 
-def test_layout_mismatch_is_reported_not_run(gc):
+@pytest.mark.parametrize("path", PATHS)
+def test_layout_mismatch_is_reported_not_run(gc, path):
+    flags = gc.GC_EF | (gc.GC_MULTI_KERNEL if path == "pipeline" else 0)
     sizes = [1000, 2000]
     L = _layout(gc, sizes, k=[10, 20])
     bad = _layout(gc, [1000, 3000], k=[10, 20])          # device copy disagrees with the host mirror
@@ -785,11 +827,11 @@ def test_layout_mismatch_is_reported_not_run(gc):
     e = torch.zeros(3000, device="cuda")
     idx = torch.full((30,), -7, dtype=torch.int32, device="cuda")
     val = torch.zeros(30, device="cuda")
-    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, gc.GC_EF)
-    gc.ef_topk_compress(L, g, e, idx, val, None, None, 0, 0, gc.GC_EF, ws)
+    ws = gc.alloc_workspace(L, gc.GC_OP_TOPK, flags)
+    gc.ef_topk_compress(L, g, e, idx, val, None, None, 0, 0, flags, ws)
     d = gc.get_device_status(ws, raise_on_error=False)
     assert d.error_bits & gc.GC_DIAG_LAYOUT_MISMATCH
-    assert (idx.cpu() == -7).all()
+    assert (idx.cpu() == -7).all() and not bool(e.any())
 
 
 # ----------------------------------------------------------------------------- lazy residual
