@@ -518,6 +518,27 @@ def test_quantize_layouts(gc, mode, s, ef):
         e = _quant_check(gc, L, g, e, mode, s, seed=11, it=it)
 
 
+@pytest.mark.parametrize("mode,s,ef", [("int8", 0, True), ("qsgd", 16, False), ("qsgd", 16, True)])
+def test_quantize_large_and_ragged_tensors(gc, mode, s, ef):
+    """A tensor of 2^23 + 3 elements among one-element, misaligned and
+    ragged ones (unit tails of 1023 and 1 elements)."""
+    sizes = [1, (1 << 23) + 3, 4097, 33, 1024, 1023, 100_003, 6, 2_000_001]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n = L.numel
+    e = (np.random.default_rng(2).standard_normal(n) * 1e-5).astype(F32) if ef else None
+    for it in range(2):
+        e = _quant_check(gc, L, _grad(n, 90 + it).numpy(), e, mode, s, seed=12, it=it)
+
+
+def test_sign_large_and_ragged_tensors(gc):
+    sizes = [1, (1 << 23) + 3, 4097, 33, 1024, 1023, 100_003, 6, 2_000_001]
+    L = _layout(gc, sizes, k=[0] * len(sizes))
+    n = L.numel
+    e = np.zeros(n, F32)
+    for it in range(2):
+        e = _sign_check(gc, L, _grad(n, 95 + it).numpy(), e)
+
+
 def test_quantize_zero_tensor(gc):
     L = _layout(gc, [100, 37], k=[0, 0])
     for mode, s in (("int8", 0), ("qsgd", 16)):
