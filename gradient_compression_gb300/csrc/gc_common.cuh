@@ -210,6 +210,47 @@ __device__ __forceinline__ uint32_t philox_word(const PhiloxKey& K, uint64_t ite
   return uint4_word(philox_block(K, iter, i >> 2, purpose), (int)(i & 3));
 }
 
+// Philox4x32-10 blocks of one (key, iteration, purpose) whose block index b
+// is below 2^32 (arenas of fewer than 2^34 elements): the counter is
+// (b, 0, iter, purpose), so in the first round the product of the iteration
+// word and in the second round the product of the first round's (constant)
+// first word are the same for every block.  They are taken once here; the
+// rounds are otherwise those of philox_block, which gives the same words.
+struct PhiloxLo {
+  uint32_t cp, c2, c3, c5;
+  __device__ __forceinline__ PhiloxLo(const PhiloxKey& key, uint64_t iter, uint32_t purpose) {
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint32_t)iter;  // round 0: product of the iteration word
+    const uint32_t x1 = (uint32_t)(p1 >> 32) ^ key.k[0];           // round 0 output x (counter y = 0)
+    const uint32_t y1 = (uint32_t)p1;                              // round 0 output y
+    const uint64_t q0 = (uint64_t)0xD2511F53u * x1;                // round 1: product of x
+    cp = purpose ^ key.k[1];
+    c2 = y1 ^ key.k[2];
+    c3 = (uint32_t)(q0 >> 32) ^ key.k[3];
+    c5 = (uint32_t)q0 ^ key.k[5];
+  }
+  // the same key as the constructor's
+  __device__ __forceinline__ uint4 block(const PhiloxKey& K, uint32_t b) const {
+    // round 0: x = b, y = 0, z = iter, w = purpose
+    const uint64_t a0 = (uint64_t)0xD2511F53u * b;
+    const uint32_t z1 = (uint32_t)(a0 >> 32) ^ cp, w1 = (uint32_t)a0;
+    // round 1: its x-product is constant (c3 and, through w2, c5 carry it)
+    const uint64_t a1 = (uint64_t)0xCD9E8D57u * z1;
+    uint4 c = make_uint4((uint32_t)(a1 >> 32) ^ c2, (uint32_t)a1, w1 ^ c3, 0u);
+    // round 2: w is round 1's constant low product, folded into c5
+    {
+      const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p1 = (uint64_t)0xCD9E8D57u * c.z;
+      c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k[4], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c5, (uint32_t)p0);
+    }
+#pragma unroll
+    for (int r = 3; r < 10; ++r) {
+      const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p1 = (uint64_t)0xCD9E8D57u * c.z;
+      c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k[2 * r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ K.k[2 * r + 1],
+                     (uint32_t)p0);
+    }
+    return c;
+  }
+};
+
 constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
 // Advances a device-resident iteration counter by one (the last kernel of a

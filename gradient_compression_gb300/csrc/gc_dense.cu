@@ -480,7 +480,9 @@ __device__ __forceinline__ void quant_slot(const DenseArgs& A, const Divisor& dv
   }
 }
 
-template <int OP, bool EF>
+// LO: the arena has fewer than 2^34 elements, so every Philox block index
+// fits in 32 bits and the full steps take the shortened rounds of PhiloxLo.
+template <int OP, bool EF, bool LO>
 __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
   if (aborted(A)) return;
   const unsigned lane = lane_id();
@@ -489,6 +491,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
   const float* src = EF ? A.e : A.g;
   const uint32_t purpose = (OP == DOP_INT8) ? PURPOSE_INT8 : PURPOSE_QSGD;
   const uint64_t iter = A.iter_dev ? *A.iter_dev : A.iter;
+  const PhiloxLo plo(A.pk, iter, purpose);
   for (int64_t u = (int64_t)blockIdx.x * DWARPS + warp; u < A.U; u += nwarps) {
     const UnitRef r = unit_ref(A, u);
     const int64_t g0 = r.base + r.lstart;
@@ -511,7 +514,10 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
           for (int j = 0; j < 4; ++j) x[j] = ld_stream(s4 + v0 + 32 * j + (int)lane);
           uint4 rw[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) rw[j] = philox_block(A.pk, iter, b0 + (uint64_t)(v0 + 32 * j + (int)lane), purpose);
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t b = b0 + (uint64_t)(v0 + 32 * j + (int)lane);
+            rw[j] = LO ? plo.block(A.pk, (uint32_t)b) : philox_block(A.pk, iter, b, purpose);
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int vi = v0 + 32 * j + (int)lane;
@@ -671,8 +677,10 @@ static void launch_quant(const DenseArgs& A, cudaStream_t s) {
   k_dreduce<<<A.T, 256, 0, s>>>(A);
   if (OP == DOP_SIGN)
     k_sign2<EF><<<dense_grid(k_sign2<EF>, A.U), DTHREADS, 0, s>>>(A);
+  else if (A.N < (int64_t(1) << 34))
+    k_quant2<OP, EF, true><<<dense_grid(k_quant2<OP, EF, true>, A.U), DTHREADS, 0, s>>>(A);
   else
-    k_quant2<OP, EF><<<dense_grid(k_quant2<OP, EF>, A.U), DTHREADS, 0, s>>>(A);
+    k_quant2<OP, EF, false><<<dense_grid(k_quant2<OP, EF, false>, A.U), DTHREADS, 0, s>>>(A);
 }
 
 }  // namespace gc
