@@ -782,6 +782,9 @@ def measure_row(gc, dev, name, warmup, steps=None, layout_name=None):
     torch.cuda.synchronize()
     if op in ("topk", "randk") and lname in ("flat", "resnet50"):
         extra["graph_replay"] = graph_replay(gc, L, grads, a, idx, val, flags, ws, warmup, steps, flush)
+    if op in ("topk", "topk_int8", "randk", "momentum", "clip", "threshold", "topk_qsgd", "topk_sign"):
+        d = gc.get_device_status(ws)
+        extra["last_warmup_call"] = {"exact_tensors": int(d.exact_tensors), "overflow_tensors": int(d.overflow_tensors)}
     if op == "topk":
         extra["one_launch"] = int(gc.get_device_status(ws).one_launch)
         if extra["one_launch"]:

@@ -23,7 +23,7 @@ constexpr int NBINS = 2048;
 constexpr int WCAP = 512;
 // Tensors at most this long are sampled completely when the candidate
 // threshold is estimated.
-constexpr int64_t SMALL_N = 65536;
+constexpr int64_t SMALL_N = 16384;
 // Expected number of Top-k members in a tensor's sample.
 constexpr int64_t SAMPLE_HITS = 128;
 constexpr int RUN = 128;  // sampled elements per contiguous run (one warp, one float4 per lane)

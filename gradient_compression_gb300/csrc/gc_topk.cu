@@ -1432,6 +1432,8 @@ __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
 // per unit block.  For QSGD / sign of the kept values, also each unit
 // block's fp64 sum of x^2 or |x| over its elements above the k-th key (the
 // kept ties, all of magnitude |k-th key|, are added per tensor by k_scan).
+constexpr uint32_t CNT_WARP_MIN = 64;  // chunks longer than this are counted by the whole warp
+
 template <int MODE, bool KSUM>
 __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
@@ -1471,26 +1473,60 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
           s_eq[ui] = eq;
         }
       }
-    } else if (tid < ub.nu) {
+    } else {
       // a thread per unit (the concatenated walk of k_write measured slower
-      // here: counting costs less per entry than finding its unit)
-      const uint2 ch = A.chunk[ub.u0 + tid];
-      const uint32_t* ck = A.ckey + A.cand_off[ub.t] + ch.x;
+      // here: counting costs less per entry than finding its unit), except
+      // for long chunks (a unit of an unsampled tensor of up to 512
+      // elements holds all of them): the warp counts those together, 128
+      // entries per step
+      const unsigned lane = lane_id();
+      const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
+      const uint32_t* ckb = A.ckey + A.cand_off[ub.t];
       uint32_t gt = 0u, eq = 0u;
-      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
+      for (unsigned longm = __ballot_sync(FULL, ch.y > CNT_WARP_MIN); longm != 0u; longm &= longm - 1u) {
+        const int o = __ffs(longm) - 1;
+        const uint32_t ox = __shfl_sync(FULL, ch.x, o), oy = __shfl_sync(FULL, ch.y, o);
+        uint32_t g2 = 0u, e2 = 0u;
+        for (uint32_t j0 = 0; j0 < oy; j0 += 128u) {
+          uint32_t kk[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t j = j0 + 32u * u + lane;
+            kk[u] = j < oy ? __ldcs(ckb + ox + j) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool v = j0 + 32u * u + lane < oy;
+            g2 += v && kk[u] > st.thr;
+            e2 += v && kk[u] == st.thr;
+            if (kq && v && kk[u] > st.thr) ksum += kept_term(A.qkind, kk[u]);
+          }
+        }
+        g2 = __reduce_add_sync(FULL, g2);
+        e2 = __reduce_add_sync(FULL, e2);
+        if ((int)lane == o) {
+          gt = g2;
+          eq = e2;
+        }
+      }
+      const uint32_t* ck = ckb + ch.x;
+      const uint32_t ny = ch.y > CNT_WARP_MIN ? 0u : ch.y;
+      for (uint32_t j0 = 0; j0 < ny; j0 += 8) {
         uint32_t kk[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ch.y ? __ldcs(ck + j0 + u) : 0u;
+        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ny ? __ldcs(ck + j0 + u) : 0u;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const bool v = j0 + u < ch.y;
+          const bool v = j0 + u < ny;
           gt += v && kk[u] > st.thr;
           eq += v && kk[u] == st.thr;
           if (kq && v && kk[u] > st.thr) ksum += kept_term(A.qkind, kk[u]);
         }
       }
-      s_gt[tid] = gt;
-      s_eq[tid] = eq;
+      if (tid < ub.nu) {
+        s_gt[tid] = gt;
+        s_eq[tid] = eq;
+      }
     }
   }
   __syncthreads();
