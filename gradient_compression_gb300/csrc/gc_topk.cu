@@ -1432,8 +1432,6 @@ __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
 // per unit block.  For QSGD / sign of the kept values, also each unit
 // block's fp64 sum of x^2 or |x| over its elements above the k-th key (the
 // kept ties, all of magnitude |k-th key|, are added per tensor by k_scan).
-constexpr uint32_t CNT_WARP_MIN = 64;  // chunks longer than this are counted by the whole warp
-
 template <int MODE, bool KSUM>
 __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
@@ -1474,58 +1472,53 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
         }
       }
     } else {
-      // a thread per unit (the concatenated walk of k_write measured slower
-      // here: counting costs less per entry than finding its unit), except
-      // for long chunks (a unit of an unsampled tensor of up to 512
-      // elements holds all of them): the warp counts those together, 128
-      // entries per step
+      // The warp's 32 chunks walked as one sequence, 32 entries per step
+      // (see chunk_owner and k_write): loads contiguous across the lanes,
+      // CP steps' loads in flight; a unit's counts are the differences of
+      // the running counts at its chunk's start and at the next chunk's.  A
+      // thread per unit issued a separate sector request per lane for every
+      // load (25 us on ResNet-50 at 1%, the largest unit blocks the long pole).
       const unsigned lane = lane_id();
       const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
       const uint32_t* ckb = A.ckey + A.cand_off[ub.t];
-      uint32_t gt = 0u, eq = 0u;
-      for (unsigned longm = __ballot_sync(FULL, ch.y > CNT_WARP_MIN); longm != 0u; longm &= longm - 1u) {
-        const int o = __ffs(longm) - 1;
-        const uint32_t ox = __shfl_sync(FULL, ch.x, o), oy = __shfl_sync(FULL, ch.y, o);
-        uint32_t g2 = 0u, e2 = 0u;
-        for (uint32_t j0 = 0; j0 < oy; j0 += 128u) {
-          uint32_t kk[4];
+      unsigned L;
+      const uint32_t off = warp_excl_scan(ch.y, lane, &L);
+      uint32_t Gc = 0u, Ec = 0u, gs = 0u, es = 0u;
+      constexpr int CP = 4;
+      for (uint32_t wg = 0; wg < L; wg += 32u * CP) {
+        uint32_t pk[CP];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t j = j0 + 32u * u + lane;
-            kk[u] = j < oy ? __ldcs(ckb + ox + j) : 0u;
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const bool v = j0 + 32u * u + lane < oy;
-            g2 += v && kk[u] > st.thr;
-            e2 += v && kk[u] == st.thr;
-            if (kq && v && kk[u] > st.thr) ksum += kept_term(A.qkind, kk[u]);
-          }
+        for (int p = 0; p < CP; ++p) {
+          const uint32_t e = wg + 32u * p + lane;
+          const int o = chunk_owner(off, e);
+          const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
+          pk[p] = e < L ? __ldcs(ckb + chx_o + (e - off_o)) : 0u;
         }
-        g2 = __reduce_add_sync(FULL, g2);
-        e2 = __reduce_add_sync(FULL, e2);
-        if ((int)lane == o) {
-          gt = g2;
-          eq = e2;
+#pragma unroll
+        for (int p = 0; p < CP; ++p) {
+          const uint32_t ws = wg + 32u * p;
+          if (ws >= L) break;
+          const bool act = ws + lane < L;
+          const bool isgt = act && pk[p] > st.thr, iseq = act && pk[p] == st.thr;
+          const unsigned gm = __ballot_sync(FULL, isgt), em = __ballot_sync(FULL, iseq);
+          if (kq && isgt) ksum += kept_term(A.qkind, pk[p]);
+          if (off - ws < 32u) {
+            const unsigned below = (1u << (off - ws)) - 1u;
+            gs = Gc + __popc(gm & below);
+            es = Ec + __popc(em & below);
+          }
+          Gc += __popc(gm);
+          Ec += __popc(em);
         }
       }
-      const uint32_t* ck = ckb + ch.x;
-      const uint32_t ny = ch.y > CNT_WARP_MIN ? 0u : ch.y;
-      for (uint32_t j0 = 0; j0 < ny; j0 += 8) {
-        uint32_t kk[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) kk[u] = j0 + u < ny ? __ldcs(ck + j0 + u) : 0u;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool v = j0 + u < ny;
-          gt += v && kk[u] > st.thr;
-          eq += v && kk[u] == st.thr;
-          if (kq && v && kk[u] > st.thr) ksum += kept_term(A.qkind, kk[u]);
-        }
+      if (off >= L) {  // empty chunks after the last entry
+        gs = Gc;
+        es = Ec;
       }
+      const uint32_t gn = __shfl_down_sync(FULL, gs, 1), en = __shfl_down_sync(FULL, es, 1);
       if (tid < ub.nu) {
-        s_gt[tid] = gt;
-        s_eq[tid] = eq;
+        s_gt[tid] = (lane == 31 ? Gc : gn) - gs;
+        s_eq[tid] = (lane == 31 ? Ec : en) - es;
       }
     }
   }
@@ -1668,13 +1661,14 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
           });
     }
   } else {
-    // Candidate path.  Long chunks (the warp's units average 40 or more
-    // candidates): a thread walks its unit's chunk.  Short chunks: the warp's
-    // 32 chunks are walked as one sequence (see chunk_owner), and kept and
-    // tie counts inside a unit are differences of running counts over the
-    // sequence, taken at the unit's first entry; this keeps every lane busy
-    // when a few long chunks would otherwise hold the warp (measured faster
-    // at 0.1-0.5% density, slower at 1%: random-k on ResNet-50).
+    // Candidate path: the warp's 32 chunks are walked as one sequence (see
+    // chunk_owner), 32 entries per step with loads and stores contiguous
+    // across the lanes, and kept and tie counts inside a unit are
+    // differences of running counts over the sequence, taken at the unit's
+    // first entry.  A thread walking its own unit's chunk (the earlier path
+    // for chunks of 40 or more candidates) issues a separate 32-byte sector
+    // request per lane for every load and store; at 1% density on ResNet-50
+    // that held the largest unit blocks at 35-43 us against 28 us here.
     const unsigned lane = lane_id();
     const unsigned lt = (1u << lane) - 1u;
     const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
@@ -1683,53 +1677,44 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
     unsigned L;
     const uint32_t off = warp_excl_scan(ch.y, lane, &L);
     const int64_t cb = A.cand_off[ub.t];
-    if (L >= 32u * 40u) {
-      const int64_t cu = cb + ch.x;
-      int64_t selpos = sel0;
-      uint32_t eqrun = 0u;
-      for (uint32_t j0 = 0; j0 < ch.y; j0 += 8) {
-        uint32_t kk[8];
-        int32_t ci[8];
-        float cv[8];
+    uint32_t Kc = 0u, Ec = 0u, ks = 0u, es = 0u;
+    // WP steps' loads are issued before any of them is used (the entries'
+    // owners and addresses depend only on the chunk table, not on data)
+    constexpr int WP = 4;
+    for (uint32_t wg = 0; wg < L; wg += 32u * WP) {
+      uint32_t pkey[WP];
+      int32_t pli[WP];
+      float px[WP];
+      int pown[WP];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool v = j0 + u < ch.y;
-          kk[u] = v ? __ldcs(A.ckey + cu + j0 + u) : 0u;
-          ci[u] = v ? __ldcs(A.cidx + cu + j0 + u) : 0;
-          cv[u] = v ? __ldcs(A.cval + cu + j0 + u) : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (j0 + u >= ch.y) break;
-          const bool iseq = kk[u] == thr;
-          const bool sel = kk[u] > thr || (iseq && eqb + eqrun < r_eq);
-          const bool last = iseq && eqb + eqrun + 1u == r_eq;
-          eqrun += iseq;
-          if (sel) {
-            emit_kept<MODE, KQ>(A, ub.t, ub.base, ub.n, ci[u], cv[u], kbase + selpos, s, last);
-            ++selpos;
-          }
+      for (int p = 0; p < WP; ++p) {
+        const uint32_t e = wg + 32u * p + lane;
+        const int o = chunk_owner(off, e);
+        const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
+        pown[p] = o;
+        pkey[p] = 0u;
+        pli[p] = 0;
+        px[p] = 0.0f;
+        if (e < L) {
+          const int64_t c = cb + chx_o + (e - off_o);
+          pkey[p] = __ldcs(A.ckey + c);
+          pli[p] = __ldcs(A.cidx + c);
+          px[p] = __ldcs(A.cval + c);
         }
       }
-      return;
-    }
-    uint32_t Kc = 0u, Ec = 0u, ks = 0u, es = 0u;
-    for (uint32_t ws = 0; ws < L; ws += 32u) {
+#pragma unroll
+    for (int p = 0; p < WP; ++p) {
+      const uint32_t ws = wg + 32u * p;
+      if (ws >= L) break;
       const uint32_t e = ws + lane;
-      const int o = chunk_owner(off, e);
-      const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
+      const int o = pown[p];
+      const uint32_t off_o = __shfl_sync(FULL, off, o);
       const uint32_t eqb_o = __shfl_sync(FULL, eqb, o), sel0_o = __shfl_sync(FULL, sel0, o);
       const uint32_t es_o = __shfl_sync(FULL, es, o), ks_o = __shfl_sync(FULL, ks, o);
       const bool act = e < L;
-      uint32_t key = 0u;
-      int32_t li = 0;
-      float x = 0.0f;
-      if (act) {
-        const int64_t c = cb + chx_o + (e - off_o);
-        key = __ldcs(A.ckey + c);
-        li = __ldcs(A.cidx + c);
-        x = __ldcs(A.cval + c);
-      }
+      const uint32_t key = pkey[p];
+      const int32_t li = pli[p];
+      const float x = px[p];
       const bool iseq = act && key == thr;
       const unsigned eqm = __ballot_sync(FULL, iseq);
       // the owner's first entry is in this step (off_o - ws <= 31 for every lane)
@@ -1749,6 +1734,7 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
       }
       Kc += __popc(selm);
       Ec += __popc(eqm);
+    }
     }
   }
 }
