@@ -92,7 +92,9 @@ struct TopkArgs {
   int32_t* cidx;
   float* cval;
   uint32_t* skey;
-  int64_t* sblk;       // [T+1] first sampling CTA of each tensor
+  int64_t* sblk;       // [T+1] first sampling CTA of each tensor (tensor order)
+  int64_t* sord;       // [T]   where the tensor's CTAs start in the dispatch order (planner scratch)
+  int2* smap;          // [SB]  sampling CTA (dispatch order) -> (tensor, its CTA index)
   uint32_t* scnt;      // [2T] per tensor: keys in its sample list, sampling CTAs finished (zeroed per call)
   int64_t U, UB, C, S, N, K, SB;
   int ssplit;          // sampling CTAs per large sample (sample_ctas)
@@ -131,11 +133,11 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
-  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0, carry_w = 0, carry_sb = 0;
+  int64_t carry_u = 0, carry_b = 0, carry_c = 0, carry_s = 0, carry_w = 0, carry_sb = 0, carry_lb = 0, carry_xb = 0;
   const bool sampled = A.sampled != 0;
   for (int base = 0; base < A.T; base += blockDim.x) {
     const int t = base + threadIdx.x;
-    int64_t nu = 0, nb = 0, nc = 0, ns = 0, nw = 0, nsb = 0;
+    int64_t nu = 0, nb = 0, nc = 0, ns = 0, nw = 0, nsb = 0, nlb = 0, nxb = 0;
     if (t < A.T) {
       const int64_t n = A.off[t + 1] - A.off[t];
       const int64_t k = A.kk[t];
@@ -145,6 +147,11 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       nc = cand_capacity(n, k);
       nw = k > 0 ? (k + 31) >> 5 : 0;
       nsb = sampled ? sample_ctas(n, k, A.ssplit) : 0;
+      // long samples (the filtered search) are dispatched before short ones
+      if (sample_splittable(n, k))
+        nlb = nsb;
+      else
+        nxb = nsb;
       TensorState st;
       memset(&st, 0, sizeof st);
       if (sampled && k > 0) {
@@ -213,8 +220,24 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     int64_t esb = block_excl_scan_i64(nsb, s_warp, &tot);
     if (t < A.T) A.sblk[t] = carry_sb + esb;
     carry_sb += tot;
+    // dispatch order of the sampling CTAs: the long samples' CTAs first (a
+    // short sample's CTA takes a fraction of a long one's time, so the short
+    // ones fill the slots that free up instead of holding long ones back to
+    // a second wave); short starts are offset by the long total below
+    int64_t elb = block_excl_scan_i64(nlb, s_warp, &tot);
+    const int64_t tl = tot;
+    int64_t exb = block_excl_scan_i64(nxb, s_warp, &tot);
+    if (t < A.T) A.sord[t] = nlb > 0 ? carry_lb + elb : -1 - (carry_xb + exb);
+    carry_lb += tl;
+    carry_xb += tot;
   }
   __syncthreads();
+  for (int t = threadIdx.x; t < A.T; t += blockDim.x) {
+    const int64_t o = A.sord[t];
+    const int64_t start = o >= 0 ? o : carry_lb + (-1 - o);
+    const int64_t cnt = (t + 1 < A.T ? A.sblk[t + 1] : carry_sb) - A.sblk[t];
+    for (int64_t c = 0; c < cnt && start + c < A.SB; ++c) A.smap[start + c] = make_int2(t, (int)c);
+  }
   if (threadIdx.x == 0) {
     A.units_off[A.T] = carry_u;
     A.ublk_off[A.T] = carry_b;
@@ -674,8 +697,9 @@ __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
   __shared__ uint32_t sh[NBINS];
   __shared__ uint32_t sl[SLIST];
   if (aborted(A)) return;
-  const int t = find_segment(A.sblk, A.T, (int64_t)blockIdx.x);
-  const int cta = (int)((int64_t)blockIdx.x - A.sblk[t]);
+  const int2 me = A.smap[blockIdx.x];
+  const int t = me.x;
+  const int cta = me.y;
   const int nctas = (int)(A.sblk[t + 1] - A.sblk[t]);
   TensorState* st = A.ts + t;
   if (st->flags & TS_NOEMIT) return;
@@ -2229,7 +2253,7 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
 // ============================================================================ host side
 
 struct TopkLayoutTotals {
-  int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0, SB = 0;
+  int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0, SB = 0, SBmax = 0;
   int split = 1;
 };
 
@@ -2265,7 +2289,10 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled, bool split_f
       sample_plan(n, k, &runs, &stride, &m);
       r.S += m;
     }
-    if (sampled) r.SB += sample_ctas(n, k, r.split);
+    if (sampled) {
+      r.SB += sample_ctas(n, k, r.split);
+      r.SBmax += sample_ctas(n, k, 64);  // the dispatch table fits any device's split (at most 64)
+    }
     r.K += k;
   }
   r.N = h->off[h->num_tensors];
@@ -2275,7 +2302,7 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled, bool split_f
 struct TopkCarve {
   size_t zero_bytes = 0, total = 0;
   size_t o_ts, o_hist, o_scnt, o_units, o_ublk, o_cand, o_soff, o_chunk, o_ugt, o_ueq, o_bgt, o_beq, o_ckey,
-      o_cidx, o_cval, o_skey, o_upart, o_kwoff, o_sblk;
+      o_cidx, o_cval, o_skey, o_upart, o_kwoff, o_sblk, o_sord, o_smap;
 };
 
 static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
@@ -2306,6 +2333,8 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
   c.o_upart = take(8 * (size_t)z.U);
   c.o_kwoff = take(8 * (size_t)(T + 1));
   c.o_sblk = take(8 * (size_t)(T + 1));
+  c.o_sord = take(8 * (size_t)T);
+  c.o_smap = take(8 * (size_t)(z.SBmax > 0 ? z.SBmax : 1));
   c.total = p;
   return c;
 }
@@ -2613,6 +2642,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.bits = kq.bits;
   A.kwoff = reinterpret_cast<int64_t*>(w + c.o_kwoff);
   A.sblk = reinterpret_cast<int64_t*>(w + c.o_sblk);
+  A.sord = reinterpret_cast<int64_t*>(w + c.o_sord);
+  A.smap = reinterpret_cast<int2*>(w + c.o_smap);
   A.scnt = reinterpret_cast<uint32_t*>(w + c.o_scnt);
   A.U = z.U;
   A.UB = z.UB;
