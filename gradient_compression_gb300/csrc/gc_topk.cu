@@ -1498,7 +1498,8 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
     } else {
       // The warp's 32 chunks walked as one sequence, 32 entries per step
       // (see chunk_owner and k_write): loads contiguous across the lanes,
-      // CP steps' loads in flight; a unit's counts are the differences of
+      // CP steps' loads in flight and the next CP steps' issued before these
+      // are counted; a unit's counts are the differences of
       // the running counts at its chunk's start and at the next chunk's.  A
       // thread per unit issued a separate sector request per lane for every
       // load (25 us on ResNet-50 at 1%, the largest unit blocks the long pole).
@@ -1509,15 +1510,21 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
       const uint32_t off = warp_excl_scan(ch.y, lane, &L);
       uint32_t Gc = 0u, Ec = 0u, gs = 0u, es = 0u;
       constexpr int CP = 4;
-      for (uint32_t wg = 0; wg < L; wg += 32u * CP) {
-        uint32_t pk[CP];
+      uint32_t pk[CP], nk[CP];
+      auto load_group = [&](uint32_t wg, uint32_t* gk) {
 #pragma unroll
         for (int p = 0; p < CP; ++p) {
           const uint32_t e = wg + 32u * p + lane;
           const int o = chunk_owner(off, e);
           const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
-          pk[p] = e < L ? __ldcs(ckb + chx_o + (e - off_o)) : 0u;
+          gk[p] = e < L ? __ldcs(ckb + chx_o + (e - off_o)) : 0u;
         }
+      };
+      if (L > 0u) load_group(0u, nk);
+      for (uint32_t wg = 0; wg < L; wg += 32u * CP) {
+#pragma unroll
+        for (int p = 0; p < CP; ++p) pk[p] = nk[p];
+        if (wg + 32u * CP < L) load_group(wg + 32u * CP, nk);  // the next group's loads first
 #pragma unroll
         for (int p = 0; p < CP; ++p) {
           const uint32_t ws = wg + 32u * p;
@@ -1625,7 +1632,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
 }
 
 template <int MODE, int KQ>
-__global__ void __launch_bounds__(256) k_write(TopkArgs A) {
+__global__ void __launch_bounds__(256, 3) k_write(TopkArgs A) {
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
@@ -1703,29 +1710,41 @@ __global__ void __launch_bounds__(256) k_write(TopkArgs A) {
     const int64_t cb = A.cand_off[ub.t];
     uint32_t Kc = 0u, Ec = 0u, ks = 0u, es = 0u;
     // WP steps' loads are issued before any of them is used (the entries'
-    // owners and addresses depend only on the chunk table, not on data)
+    // owners and addresses depend only on the chunk table, not on data), and
+    // the next WP steps' loads before this group is processed
     constexpr int WP = 4;
-    for (uint32_t wg = 0; wg < L; wg += 32u * WP) {
-      uint32_t pkey[WP];
-      int32_t pli[WP];
-      float px[WP];
-      int pown[WP];
+    uint32_t pkey[WP], nkey[WP];
+    int32_t pli[WP], nli[WP];
+    float px[WP], nx[WP];
+    int pown[WP], nown[WP];
+    auto load_group = [&](uint32_t wg, uint32_t* gk, int32_t* gl, float* gx, int* go) {
 #pragma unroll
       for (int p = 0; p < WP; ++p) {
         const uint32_t e = wg + 32u * p + lane;
         const int o = chunk_owner(off, e);
         const uint32_t off_o = __shfl_sync(FULL, off, o), chx_o = __shfl_sync(FULL, ch.x, o);
-        pown[p] = o;
-        pkey[p] = 0u;
-        pli[p] = 0;
-        px[p] = 0.0f;
+        go[p] = o;
+        gk[p] = 0u;
+        gl[p] = 0;
+        gx[p] = 0.0f;
         if (e < L) {
           const int64_t c = cb + chx_o + (e - off_o);
-          pkey[p] = __ldcs(A.ckey + c);
-          pli[p] = __ldcs(A.cidx + c);
-          px[p] = __ldcs(A.cval + c);
+          gk[p] = __ldcs(A.ckey + c);
+          gl[p] = __ldcs(A.cidx + c);
+          gx[p] = __ldcs(A.cval + c);
         }
       }
+    };
+    if (L > 0u) load_group(0u, nkey, nli, nx, nown);
+    for (uint32_t wg = 0; wg < L; wg += 32u * WP) {
+#pragma unroll
+      for (int p = 0; p < WP; ++p) {
+        pkey[p] = nkey[p];
+        pli[p] = nli[p];
+        px[p] = nx[p];
+        pown[p] = nown[p];
+      }
+      if (wg + 32u * WP < L) load_group(wg + 32u * WP, nkey, nli, nx, nown);
 #pragma unroll
     for (int p = 0; p < WP; ++p) {
       const uint32_t ws = wg + 32u * p;
