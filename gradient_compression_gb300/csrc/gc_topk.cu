@@ -102,34 +102,50 @@ struct TopkArgs {
 
 // ============================================================================ plan
 
-__device__ int64_t block_excl_scan_i64(int64_t v, int64_t* s_warp, int64_t* total) {
+// Exclusive block scans of NV values per thread at once (one pass of warp
+// shuffles and three barriers for all of them); tot receives the totals.
+template <int NV>
+__device__ void block_excl_scan_multi(int64_t (&v)[NV], int64_t (*s_w)[32], int64_t (&tot)[NV]) {
   const unsigned lane = lane_id(), w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int64_t x = v;
+  int64_t x[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) x[i] = v[i];
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int64_t y = __shfl_up_sync(FULL, x, d);
-    if (lane >= (unsigned)d) x += y;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int64_t y = __shfl_up_sync(FULL, x[i], d);
+      if (lane >= (unsigned)d) x[i] += y;
+    }
   }
-  if (lane == 31) s_warp[w] = x;
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) s_w[i][w] = x[i];
+  }
   __syncthreads();
   if (w == 0) {
-    int64_t z = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int64_t y = __shfl_up_sync(FULL, z, d);
-      if (lane >= (unsigned)d) z += y;
+    for (int i = 0; i < NV; ++i) {
+      int64_t z = lane < nw ? s_w[i][lane] : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(FULL, z, d);
+        if (lane >= (unsigned)d) z += y;
+      }
+      if (lane < nw) s_w[i][lane] = z;  // inclusive warp prefix
     }
-    if (lane < nw) s_warp[lane] = z;  // inclusive warp prefix
   }
   __syncthreads();
-  const int64_t before = (w == 0 ? 0 : s_warp[w - 1]);
-  *total = s_warp[nw - 1];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    tot[i] = s_w[i][nw - 1];
+    v[i] = (w == 0 ? 0 : s_w[i][w - 1]) + x[i] - v[i];
+  }
   __syncthreads();
-  return before + x - v;
 }
 
 __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
-  __shared__ int64_t s_warp[32];
+  __shared__ int64_t s_scan[8][32];
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
@@ -201,35 +217,30 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       if (A.count_out && (st.flags & TS_NOEMIT)) A.count_out[t] = 0;
       if ((A.int8 || A.qkind != KQ_NONE) && k <= 0) A.scale[t] = 0.0f;
     }
-    int64_t tot;
-    int64_t eu = block_excl_scan_i64(nu, s_warp, &tot);
-    if (t < A.T) A.units_off[t] = carry_u + eu;
-    carry_u += tot;
-    int64_t eb = block_excl_scan_i64(nb, s_warp, &tot);
-    if (t < A.T) A.ublk_off[t] = carry_b + eb;
-    carry_b += tot;
-    int64_t ec = block_excl_scan_i64(nc, s_warp, &tot);
-    if (t < A.T) A.cand_off[t] = carry_c + ec;
-    carry_c += tot;
-    int64_t es = block_excl_scan_i64(ns, s_warp, &tot);
-    if (t < A.T) A.soff[t] = carry_s + es;
-    carry_s += tot;
-    int64_t ew = block_excl_scan_i64(nw, s_warp, &tot);
-    if (t < A.T) A.kwoff[t] = carry_w + ew;
-    carry_w += tot;
-    int64_t esb = block_excl_scan_i64(nsb, s_warp, &tot);
-    if (t < A.T) A.sblk[t] = carry_sb + esb;
-    carry_sb += tot;
-    // dispatch order of the sampling CTAs: the long samples' CTAs first (a
-    // short sample's CTA takes a fraction of a long one's time, so the short
-    // ones fill the slots that free up instead of holding long ones back to
-    // a second wave); short starts are offset by the long total below
-    int64_t elb = block_excl_scan_i64(nlb, s_warp, &tot);
-    const int64_t tl = tot;
-    int64_t exb = block_excl_scan_i64(nxb, s_warp, &tot);
-    if (t < A.T) A.sord[t] = nlb > 0 ? carry_lb + elb : -1 - (carry_xb + exb);
-    carry_lb += tl;
-    carry_xb += tot;
+    // all eight prefix tables in one block scan
+    int64_t v[8] = {nu, nb, nc, ns, nw, nsb, nlb, nxb}, tot[8];
+    block_excl_scan_multi<8>(v, s_scan, tot);
+    if (t < A.T) {
+      A.units_off[t] = carry_u + v[0];
+      A.ublk_off[t] = carry_b + v[1];
+      A.cand_off[t] = carry_c + v[2];
+      A.soff[t] = carry_s + v[3];
+      A.kwoff[t] = carry_w + v[4];
+      A.sblk[t] = carry_sb + v[5];
+      // dispatch order of the sampling CTAs: the long samples' CTAs first (a
+      // short sample's CTA takes a fraction of a long one's time, so the
+      // short ones fill the slots that free up instead of holding long ones
+      // back to a second wave); short starts are offset by the long total below
+      A.sord[t] = nlb > 0 ? carry_lb + v[6] : -1 - (carry_xb + v[7]);
+    }
+    carry_u += tot[0];
+    carry_b += tot[1];
+    carry_c += tot[2];
+    carry_s += tot[3];
+    carry_w += tot[4];
+    carry_sb += tot[5];
+    carry_lb += tot[6];
+    carry_xb += tot[7];
   }
   __syncthreads();
   for (int t = threadIdx.x; t < A.T; t += blockDim.x) {
