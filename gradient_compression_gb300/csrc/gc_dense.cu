@@ -259,9 +259,11 @@ __device__ __forceinline__ int dense_code(float x, const Divisor& dv, int s_leve
   if (OP == DOP_INT8) {
     int c = 0;
     if (NZ || sc != 0.0f) {
-      // |x| <= max|acc| keeps |x| / s near 127; the clamp (which cannot
-      // change min(127, .)) only guards the float -> int conversion
-      c = stochastic_round(fminf(dv.div(fabsf(x)), 128.0f), r);
+      // the scale is this call's max|acc| / 127, so |x| / s stays within an
+      // ulp or two of 127 and inside stochastic_round's domain; no clamp is
+      // needed before it (a non-finite x gives a NaN quotient, whose floor
+      // comes out far above 127 and is cut to 127 here, as a clamp would)
+      c = stochastic_round(dv.div(fabsf(x)), r);
       c = c > 127 ? 127 : c;
       c = signbit(x) ? -c : c;
     }
@@ -270,8 +272,10 @@ __device__ __forceinline__ int dense_code(float x, const Divisor& dv, int s_leve
   }
   int level = 0;
   if (NZ || sc != 0.0f) {
-    float y = dv.div(__fmul_rn(fabsf(x), (float)s_levels));
-    y = fminf(y, (float)s_levels + 1.0f);
+    // the scale is this call's norm, within 1e-6 of ||acc|| >= |x|, so y
+    // stays within a hair of s_levels (no clamp before stochastic_round; a
+    // non-finite x gives a NaN y, whose floor is cut to s_levels by the min)
+    const float y = dv.div(__fmul_rn(fabsf(x), (float)s_levels));
     level = min(s_levels, stochastic_round(y, r));
   }
   const bool neg = signbit(x);
