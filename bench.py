@@ -51,11 +51,11 @@ WORKLOADS = {
     "flat_2p20": (1, 0.001, False, [0]),
 }
 CFG, RHO, INT8 = 5, 0.001, True
-# kernels libgc launches per gc_ef_topk_compress call (Top-k mode): plan,
-# the sampled threshold estimate, the streaming pass, the level-1 select,
-# three histogram passes (full-pass level 1, candidate levels 2 and 3) with
-# their selects, count, scan, write
-LAUNCHES_PER_STEP = 13
+# kernels libgc launches per gc_ef_topk_compress call (Top-k mode): the
+# workspace zeroing, plan, the sampled threshold estimate, the streaming
+# pass, the level-1 select, three histogram passes (full-pass level 1,
+# candidate levels 2 and 3) with their selects, count, scan, write
+LAUNCHES_PER_STEP = 14
 # bytes the streaming pass must move per element: read g, read e, write e
 STREAM_BYTES_PER_ELEM = 12
 # integer multiplies of one Philox4x32-10 word (random-k keys, QSGD rounding)
@@ -878,7 +878,7 @@ def multi_kernel_time(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush
     torch.cuda.synchronize()
     times = [a_.elapsed_time(b_) for a_, b_ in evs]
     return {"ms_per_call": statistics.mean(times), "ms_min": min(times),
-            "how": "the same calls with GC_MULTI_KERNEL (a memset and 13 kernels)"}
+            "how": "the same calls with GC_MULTI_KERNEL (14 chained kernels)"}
 
 
 def graph_replay(gc, L, grads, e, idx, val, flags, ws, warmup, steps, flush):

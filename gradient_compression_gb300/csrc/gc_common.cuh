@@ -11,6 +11,61 @@ namespace gc {
 
 constexpr unsigned FULL = 0xffffffffu;
 
+// ---------------------------------------------------------------- chained launches
+// The kernels of one call run back to back in one stream.  Each is issued as
+// a programmatic dependent launch (launch_chained) and starts with
+// chain_wait(): the wait returns once the kernels before it in the stream
+// have completed and their writes are visible (at once for a plain launch),
+// and the trigger after it lets the next kernel's CTAs be scheduled while
+// this grid's last CTAs run, so the launch gap between two phases is hidden
+// without any change to what either reads or writes.
+__device__ __forceinline__ void chain_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// kern<<<grid, block, smem, s>>>(args...) as a programmatic dependent launch;
+// a launch the runtime refuses with that attribute is issued plainly (a
+// configuration error then stays for the caller's cudaGetLastError).
+template <typename... P, typename... Arg>
+static void launch_chained(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           const Arg&... args) {
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) {
+    (void)cudaGetLastError();
+    kern<<<grid, block, smem, s>>>(args...);
+  }
+}
+
+// Zeroes a call's workspace head (16-byte aligned, n16 16-byte words, then
+// ntail bytes) as the first kernel of the call's chain.
+static __global__ void __launch_bounds__(256) k_zero(uint4* p, size_t n16, unsigned char* tail, int ntail) {
+  chain_wait();
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n16; i += (size_t)gridDim.x * 256)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (blockIdx.x == 0 && (int)threadIdx.x < ntail) tail[threadIdx.x] = 0;
+}
+
+// cudaMemsetAsync(p, 0, bytes, s) for a 16-byte aligned p, as a chained
+// launch; false if the launch failed.
+static bool zero_chained(void* p, size_t bytes, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  const size_t blocks = (n16 + 255) / 256;
+  const unsigned grid = blocks < 1 ? 1u : (blocks > 2048 ? 2048u : (unsigned)blocks);
+  launch_chained(k_zero, grid, 256, 0, s, static_cast<uint4*>(p), n16, static_cast<unsigned char*>(p) + n16 * 16,
+                 (int)(bytes % 16));
+  return cudaGetLastError() == cudaSuccess;
+}
+
 // Work unit: one warp streams UNIT consecutive elements of one tensor.
 constexpr int UNIT_SHIFT = 12;
 constexpr int64_t UNIT = int64_t(1) << UNIT_SHIFT;
@@ -255,7 +310,10 @@ constexpr uint32_t PURPOSE_INT8 = 1, PURPOSE_QSGD = 2, PURPOSE_RANDK = 3;
 
 // Advances a device-resident iteration counter by one (the last kernel of a
 // *_dev_iter call).
-static __global__ void k_iter_advance(uint64_t* iter) { *iter += 1u; }
+static __global__ void k_iter_advance(uint64_t* iter) {
+  chain_wait();
+  *iter += 1u;
+}
 
 // ---------------------------------------------------------------- rounding
 // Stochastic rounding of 0 <= x < 2^23: floor(x) + 1 iff r * 2^-32 < frac(x),

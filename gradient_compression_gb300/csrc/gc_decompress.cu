@@ -70,6 +70,7 @@ struct DecompArgs {
 // Window tables from the device layout (one CTA); a disagreement with the
 // host's window count means the device and host layouts differ.
 __global__ void __launch_bounds__(1024) k_dplan(DecompArgs A) {
+  chain_wait();
   __shared__ int64_t s_w[32], s_b[32];
   int64_t carry = 0, carry_b = 0;
   for (int base = 0; base < A.T; base += blockDim.x) {
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(1024) k_dplan(DecompArgs A) {
 // that every entry, even one with a negative index, lands in some window);
 // starts[w][NW] = K.
 __global__ void __launch_bounds__(256) k_dstarts(DecompArgs A) {
+  chain_wait();
   if (A.diag[DIAG_ABORT]) return;
   const int64_t stride = A.NW + 1;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -204,6 +206,7 @@ __device__ __forceinline__ void add_exact(float* o, float v) {
 // distinct, so the atomics of one phase never meet on an element.
 template <int DK>
 __global__ void __launch_bounds__(DW_THREADS) k_dphase(DecompArgs A) {
+  chain_wait();
   __shared__ int64_t s_s[DW_GROUP], s_e[DW_GROUP];
   if (A.diag[DIAG_ABORT]) return;
   const int64_t gw = blockIdx.x;
@@ -281,7 +284,7 @@ static gc_status run_decompress(int dk, const gc_layout* dev, const gc_layout* h
   const size_t need = carve_decomp(T, NW, &o_wo, &o_wsh, &o_kw, &o_st);
   if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < need) return GC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
+  if (!zero_chained(workspace, DIAG_BYTES, s)) return GC_ERR_CUDA;
   const int64_t K = host->koff[T];
   if (K == 0 || W == 0) return GC_OK;
   unsigned char* wsp = static_cast<unsigned char*>(workspace);
@@ -299,7 +302,7 @@ static gc_status run_decompress(int dk, const gc_layout* dev, const gc_layout* h
   A.starts = reinterpret_cast<int64_t*>(wsp + o_st);
   A.NW = NW;
   A.K = K;
-  k_dplan<<<1, 1024, 0, s>>>(A);
+  launch_chained(k_dplan, 1, 1024, 0, s, A);
   for (int w0 = 0; w0 < W; w0 += DW_GROUP) {
     A.W = W - w0 < DW_GROUP ? W - w0 : DW_GROUP;
     for (int j = 0; j < DW_GROUP; ++j) {
@@ -311,13 +314,13 @@ static gc_status run_decompress(int dk, const gc_layout* dev, const gc_layout* h
       A.scale[j] = in && scale ? scale[w0 + j] : nullptr;
     }
     const int64_t nthr = (NW + 1) * A.W;
-    k_dstarts<<<(unsigned)((nthr + 255) / 256), 256, 0, s>>>(A);
+    launch_chained(k_dstarts, (unsigned)((nthr + 255) / 256), 256, 0, s, A);
     if (NW > 0) {
       switch (dk) {
-        case DK_F32: k_dphase<DK_F32><<<(unsigned)NW, DW_THREADS, 0, s>>>(A); break;
-        case DK_INT8: k_dphase<DK_INT8><<<(unsigned)NW, DW_THREADS, 0, s>>>(A); break;
-        case DK_QSGD: k_dphase<DK_QSGD><<<(unsigned)NW, DW_THREADS, 0, s>>>(A); break;
-        default: k_dphase<DK_SIGN><<<(unsigned)NW, DW_THREADS, 0, s>>>(A); break;
+        case DK_F32: launch_chained(k_dphase<DK_F32>, (unsigned)NW, DW_THREADS, 0, s, A); break;
+        case DK_INT8: launch_chained(k_dphase<DK_INT8>, (unsigned)NW, DW_THREADS, 0, s, A); break;
+        case DK_QSGD: launch_chained(k_dphase<DK_QSGD>, (unsigned)NW, DW_THREADS, 0, s, A); break;
+        default: launch_chained(k_dphase<DK_SIGN>, (unsigned)NW, DW_THREADS, 0, s, A); break;
       }
     }
   }

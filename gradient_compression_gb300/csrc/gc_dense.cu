@@ -51,6 +51,7 @@ struct DenseArgs {
 __device__ __forceinline__ bool aborted(const DenseArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
 
 __global__ void __launch_bounds__(1024) k_dplan(DenseArgs A) {
+  chain_wait();
   __shared__ int64_t s_warp[32];
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -139,6 +140,7 @@ __device__ __forceinline__ UnitRef unit_ref(const DenseArgs& A, int64_t u) {
 // Pass 1: acc (+ EF write-back) and the per-unit reduction input.
 template <int OP, bool EF>
 __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int warp = threadIdx.x >> 5;
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(DTHREADS) k_dense1(DenseArgs A) {
 
 // Per-tensor scale from the unit partials (fixed order, so deterministic).
 __global__ void __launch_bounds__(256) k_dreduce(DenseArgs A) {
+  chain_wait();
   __shared__ double s_part[256];
   if (aborted(A)) return;
   const int t = blockIdx.x;
@@ -289,6 +292,7 @@ __device__ __forceinline__ int dense_code(float x, const Divisor& dv, int s_leve
 // Pass 2 of the sign compressor: bits and residual.
 template <bool EF>
 __global__ void __launch_bounds__(DTHREADS) k_sign2(DenseArgs A) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int warp = threadIdx.x >> 5;
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(DTHREADS) k_sign2(DenseArgs A) {
 // With PREV, e holds the previous call's acc.
 template <bool PREV>
 __global__ void __launch_bounds__(DTHREADS) k_sign_lazy(DenseArgs A, const float* prev_mu) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int warp = threadIdx.x >> 5;
@@ -488,6 +493,7 @@ __device__ __forceinline__ void quant_slot(const DenseArgs& A, const Divisor& dv
 // fits in 32 bits and the full steps take the shortened rounds of PhiloxLo.
 template <int OP, bool EF, bool LO>
 __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int warp = threadIdx.x >> 5;
@@ -565,6 +571,7 @@ __global__ void __launch_bounds__(DTHREADS) k_quant2(DenseArgs A) {
 template <int KIND>
 __global__ void __launch_bounds__(DTHREADS) k_ddecode(DenseArgs A, const void* data, const float* scl,
                                                       float* out) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int warp = threadIdx.x >> 5;
@@ -670,21 +677,21 @@ static gc_status dense_setup(const gc_layout* dev, const gc_layout* host, void* 
   A->U = z.U;
   A->W = z.W;
   A->N = z.N;
-  if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
-  k_dplan<<<1, 1024, 0, s>>>(*A);
+  if (!zero_chained(ws, c.zero_bytes, s)) return GC_ERR_CUDA;
+  launch_chained(k_dplan, 1, 1024, 0, s, *A);
   return GC_OK;
 }
 
 template <int OP, bool EF>
 static void launch_quant(const DenseArgs& A, cudaStream_t s) {
-  k_dense1<OP, EF><<<dense_grid(k_dense1<OP, EF>, A.U), DTHREADS, 0, s>>>(A);
-  k_dreduce<<<A.T, 256, 0, s>>>(A);
+  launch_chained(k_dense1<OP, EF>, dense_grid(k_dense1<OP, EF>, A.U), DTHREADS, 0, s, A);
+  launch_chained(k_dreduce, A.T, 256, 0, s, A);
   if (OP == DOP_SIGN)
-    k_sign2<EF><<<dense_grid(k_sign2<EF>, A.U), DTHREADS, 0, s>>>(A);
+    launch_chained(k_sign2<EF>, dense_grid(k_sign2<EF>, A.U), DTHREADS, 0, s, A);
   else if (A.N < (int64_t(1) << 34))
-    k_quant2<OP, EF, true><<<dense_grid(k_quant2<OP, EF, true>, A.U), DTHREADS, 0, s>>>(A);
+    launch_chained(k_quant2<OP, EF, true>, dense_grid(k_quant2<OP, EF, true>, A.U), DTHREADS, 0, s, A);
   else
-    k_quant2<OP, EF, false><<<dense_grid(k_quant2<OP, EF, false>, A.U), DTHREADS, 0, s>>>(A);
+    launch_chained(k_quant2<OP, EF, false>, dense_grid(k_quant2<OP, EF, false>, A.U), DTHREADS, 0, s, A);
 }
 
 }  // namespace gc
@@ -744,7 +751,7 @@ static gc_status quantize_entry(const gc_layout* dev, const gc_layout* host, con
     if (e) launch_quant<DOP_QSGD, true>(A, s);
     else launch_quant<DOP_QSGD, false>(A, s);
   }
-  if (iter_dev) k_iter_advance<<<1, 1, 0, s>>>(iter_dev);
+  if (iter_dev) launch_chained(k_iter_advance, 1, 1, 0, s, iter_dev);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
@@ -789,11 +796,14 @@ extern "C" gc_status gc_dense_decompress_accumulate(const gc_layout* dev, const 
   A.s_levels = s_levels;
   for (int w = 0; w < W; ++w) {
     if (kind == GC_DENSE_SIGN)
-      k_ddecode<GC_DENSE_SIGN><<<dense_grid(k_ddecode<GC_DENSE_SIGN>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+      launch_chained(k_ddecode<GC_DENSE_SIGN>, dense_grid(k_ddecode<GC_DENSE_SIGN>, A.U), DTHREADS, 0, s, A, data[w],
+                     scale[w], out);
     else if (kind == GC_DENSE_INT8)
-      k_ddecode<GC_DENSE_INT8><<<dense_grid(k_ddecode<GC_DENSE_INT8>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+      launch_chained(k_ddecode<GC_DENSE_INT8>, dense_grid(k_ddecode<GC_DENSE_INT8>, A.U), DTHREADS, 0, s, A, data[w],
+                     scale[w], out);
     else
-      k_ddecode<GC_DENSE_QSGD><<<dense_grid(k_ddecode<GC_DENSE_QSGD>, A.U), DTHREADS, 0, s>>>(A, data[w], scale[w], out);
+      launch_chained(k_ddecode<GC_DENSE_QSGD>, dense_grid(k_ddecode<GC_DENSE_QSGD>, A.U), DTHREADS, 0, s, A, data[w],
+                     scale[w], out);
   }
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
@@ -816,10 +826,11 @@ extern "C" gc_status gc_sign_compress_lazy(const gc_layout* dev, const gc_layout
   A.bits = bits;
   A.scale = mean_abs;
   if (prev_mean_abs)
-    k_sign_lazy<true><<<dense_grid(k_sign_lazy<true>, A.U), DTHREADS, 0, s>>>(A, prev_mean_abs);
+    launch_chained(k_sign_lazy<true>, dense_grid(k_sign_lazy<true>, A.U), DTHREADS, 0, s, A, prev_mean_abs);
   else
-    k_sign_lazy<false><<<dense_grid(k_sign_lazy<false>, A.U), DTHREADS, 0, s>>>(A, nullptr);
-  k_dreduce<<<A.T, 256, 0, s>>>(A);
+    launch_chained(k_sign_lazy<false>, dense_grid(k_sign_lazy<false>, A.U), DTHREADS, 0, s, A,
+                   (const float*)nullptr);
+  launch_chained(k_dreduce, A.T, 256, 0, s, A);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 

@@ -76,6 +76,7 @@ struct PsArgs {
 __device__ __forceinline__ bool ps_aborted(const PsArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
 
 __global__ void __launch_bounds__(1024) k_psplan(PsArgs A) {
+  chain_wait();
   __shared__ int64_t s_warp[32];
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -243,6 +244,7 @@ __device__ __forceinline__ float pres_one(float x, const float pv[R], const floa
 // is bit-identical to the eager residual.
 template <int R, bool PEND>
 __global__ void __launch_bounds__(256, PEND ? 3 : 1) k_pmq(PsArgs A) {
+  chain_wait();
   constexpr int PG = 4;  // 128-column groups per step: PG * 4 = PS_FLUSH columns per lane
   static_assert(PG * 4 == PS_FLUSH, "one compensated addition per step");
   __shared__ __align__(16) float sq[R][PS_CC];
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(256, PEND ? 3 : 1) k_pmq(PsArgs A) {
 // (compensated fp32); thread per row.
 template <int R>
 __global__ void __launch_bounds__(256) k_ppred(PsArgs A) {
+  chain_wait();
   if (ps_aborted(A)) return;
   for (int64_t gr = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gr < A.Mrows;
        gr += (int64_t)gridDim.x * blockDim.x) {
@@ -541,6 +544,7 @@ __device__ __forceinline__ void porth_matrix(const PsArgs& A, int t, int rank) {
 // larger ones (big = 1, used only if the cluster launch is refused).
 template <int R>
 __global__ void __launch_bounds__(1024) k_porth(PsArgs A, int big) {
+  chain_wait();
   if (ps_aborted(A)) return;
   const int t = blockIdx.x;
   if ((A.rows[t] > PORTH_BIG) != (big != 0)) return;
@@ -552,6 +556,7 @@ __global__ void __launch_bounds__(1024) k_porth(PsArgs A, int big) {
 // launch, reads the same in all of them), so all reach every barrier.
 template <int R>
 __global__ void __launch_bounds__(1024) k_porthc(PsArgs A) {
+  chain_wait();
   if (ps_aborted(A)) return;
   const int64_t ci = blockIdx.x / PORTH_CL;
   const int t = find_segment(A.bigoff, A.T, ci);
@@ -598,6 +603,7 @@ __device__ __forceinline__ void pmtp_flush(Nm acc[4][R], float part[4][R]) {
 
 template <int R>
 __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
+  chain_wait();
   __shared__ __align__(16) float4 sbuf[PT_NS * PT_RS * 256];
   __shared__ __align__(16) float sp[PS_RC * R];  // the tile's rows of P
   if (ps_aborted(A)) return;
@@ -690,6 +696,7 @@ __global__ void __launch_bounds__(256, 3) k_pmtp(PsArgs A) {
 // Q_jk = sum over row tiles of the partials, in tile order (compensated fp32).
 template <int R>
 __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
+  chain_wait();
   if (ps_aborted(A)) return;
   for (int64_t gc = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gc < A.Ncols;
        gc += (int64_t)gridDim.x * blockDim.x) {
@@ -727,6 +734,7 @@ __global__ void __launch_bounds__(256) k_pqred(PsArgs A) {
 // misaligned rows go one column per lane.
 template <int R, bool DECODE>
 __global__ void __launch_bounds__(256) k_pres(PsArgs A) {
+  chain_wait();
   constexpr int PG = 4;  // 128-column groups per step
   __shared__ __align__(16) float sq[R][PS_CC];
   if (ps_aborted(A)) return;
@@ -857,13 +865,13 @@ static unsigned ps_tile_grid(K kernel, size_t smem, int64_t tiles) {
 
 template <int R>
 static void ps_launch_compress(const PsArgs& A, cudaStream_t s, bool lazy) {
-  k_psplan<<<1, 1024, 0, s>>>(A);
+  launch_chained(k_psplan, 1, 1024, 0, s, A);
   if (A.p_prev)
-    k_pmq<R, true><<<ps_tile_grid(k_pmq<R, true>, 0, A.Tiles), 256, 0, s>>>(A);
+    launch_chained(k_pmq<R, true>, ps_tile_grid(k_pmq<R, true>, 0, A.Tiles), 256, 0, s, A);
   else
-    k_pmq<R, false><<<ps_tile_grid(k_pmq<R, false>, 0, A.Tiles), 256, 0, s>>>(A);
-  k_ppred<R><<<(unsigned)std::min<int64_t>((A.Mrows + 255) / 256, 65535), 256, 0, s>>>(A);
-  k_porth<R><<<A.T, 1024, 0, s>>>(A, 0);
+    launch_chained(k_pmq<R, false>, ps_tile_grid(k_pmq<R, false>, 0, A.Tiles), 256, 0, s, A);
+  launch_chained(k_ppred<R>, (unsigned)std::min<int64_t>((A.Mrows + 255) / 256, 65535), 256, 0, s, A);
+  launch_chained(k_porth<R>, A.T, 1024, 0, s, A, 0);
   if (A.Big > 0) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -882,9 +890,9 @@ static void ps_launch_compress(const PsArgs& A, cudaStream_t s, bool lazy) {
       k_porth<R><<<A.T, 1024, 0, s>>>(A, 1);
     }
   }
-  k_pmtp<R><<<ps_tile_grid(k_pmtp<R>, 0, A.Tiles), 256, 0, s>>>(A);
-  k_pqred<R><<<(unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s>>>(A);
-  if (!lazy) k_pres<R, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+  launch_chained(k_pmtp<R>, ps_tile_grid(k_pmtp<R>, 0, A.Tiles), 256, 0, s, A);
+  launch_chained(k_pqred<R>, (unsigned)std::min<int64_t>((A.Ncols + 255) / 256, 65535), 256, 0, s, A);
+  if (!lazy) launch_chained(k_pres<R, false>, (unsigned)A.Tiles, 256, 0, s, A);
 }
 
 static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* host, int32_t rank,
@@ -917,7 +925,7 @@ static gc_status ps_setup(const gc_matrix_layout* dev, const gc_matrix_layout* h
   A->Parts = z.Parts;
   A->PParts = z.PParts;
   A->Big = z.Big;
-  if (cudaMemsetAsync(ws, 0, DIAG_BYTES, s) != cudaSuccess) return GC_ERR_CUDA;
+  if (!zero_chained(ws, DIAG_BYTES, s)) return GC_ERR_CUDA;
   return GC_OK;
 }
 
@@ -1002,13 +1010,13 @@ extern "C" gc_status gc_powersgd_residual_materialize(const gc_matrix_layout* de
   A.e = e;
   A.p = const_cast<float*>(p);
   A.q = const_cast<float*>(q);
-  k_psplan<<<1, 1024, 0, s>>>(A);
+  launch_chained(k_psplan, 1, 1024, 0, s, A);
   if (rank == 1)
-    k_pres<1, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<1, false>, (unsigned)A.Tiles, 256, 0, s, A);
   else if (rank == 2)
-    k_pres<2, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<2, false>, (unsigned)A.Tiles, 256, 0, s, A);
   else
-    k_pres<4, false><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<4, false>, (unsigned)A.Tiles, 256, 0, s, A);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
@@ -1027,12 +1035,12 @@ extern "C" gc_status gc_powersgd_decompress_accumulate(const gc_matrix_layout* d
   A.p = const_cast<float*>(p);
   A.q = const_cast<float*>(q);
   A.out = out;
-  k_psplan<<<1, 1024, 0, s>>>(A);
+  launch_chained(k_psplan, 1, 1024, 0, s, A);
   if (rank == 1)
-    k_pres<1, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<1, true>, (unsigned)A.Tiles, 256, 0, s, A);
   else if (rank == 2)
-    k_pres<2, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<2, true>, (unsigned)A.Tiles, 256, 0, s, A);
   else
-    k_pres<4, true><<<(unsigned)A.Tiles, 256, 0, s>>>(A);
+    launch_chained(k_pres<4, true>, (unsigned)A.Tiles, 256, 0, s, A);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

@@ -145,6 +145,7 @@ __device__ void block_excl_scan_multi(int64_t (&v)[NV], int64_t (*s_w)[32], int6
 }
 
 __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
+  chain_wait();
   __shared__ int64_t s_scan[8][32];
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -377,6 +378,7 @@ __device__ __forceinline__ void acc4_from_inputs(const TopkArgs& A, int t, int64
 
 // Per-unit partial sums of g^2 (scaled compensated fp32 per lane, fp64 across lanes).
 __global__ void __launch_bounds__(256) k_gnorm(TopkArgs A) {
+  chain_wait();
   if (aborted(A)) return;
   const unsigned lane = lane_id();
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -425,6 +427,7 @@ __global__ void __launch_bounds__(256) k_gnorm(TopkArgs A) {
 // Per tensor: N = ||g_t||_2 (fixed-order fp64 sum of the unit partials) and
 // the clipping multiplier c = C / N when N > C, else 1.
 __global__ void __launch_bounds__(256) k_gscale(TopkArgs A) {
+  chain_wait();
   __shared__ double s_part[256];
   if (aborted(A)) return;
   const int t = blockIdx.x;
@@ -701,6 +704,7 @@ __device__ void sample_filter_pass(const TopkArgs& A, int t, int64_t base, int64
 
 template <int MODE>
 __global__ void __launch_bounds__(512, 2) k_sample(TopkArgs A) {
+  chain_wait();
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t s_cnt;
@@ -974,6 +978,7 @@ __device__ void select_level(const TopkArgs& A, int t, int phase, const uint32_t
 
 // One radix level of the k-th key search for every tensor (one CTA each).
 __global__ void __launch_bounds__(256) k_select(TopkArgs A, int phase) {
+  chain_wait();
   __shared__ uint32_t s_warp[33];
   __shared__ uint32_t s_res[3];
   if (aborted(A)) return;
@@ -1047,6 +1052,7 @@ constexpr size_t STREAM_SMEM = (size_t)STREAM_WARPS * WCAP * (4 + 4 + 2);
 
 template <int MODE, bool EF, bool LOADG, bool LAZY>
 __global__ void __launch_bounds__(STREAM_THREADS, MODE == MODE_TOPK ? (LAZY ? 3 : GC_STREAM_MINB) : 2) k_stream(TopkArgs A) {
+  chain_wait();
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const unsigned lane = lane_id();
@@ -1306,6 +1312,7 @@ __device__ __forceinline__ void dense_unit_walk(const TopkArgs& A, const float* 
 // candidate level-1 histogram comes from the streaming pass).
 template <int MODE>
 __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
+  chain_wait();
   __shared__ uint32_t sh[NBINS];
   __shared__ uint32_t s_max, s_tau;
   if (aborted(A)) return;
@@ -1428,6 +1435,7 @@ __device__ double block_sum_f64(double v, double* s_d) {
 // unit blocks' sums in a fixed order plus the kept ties, then
 // N = (float)sqrt(sum x^2) or mu = (float)(sum |x| / k).
 __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
+  chain_wait();
   __shared__ uint32_t s_warp[33];
   __shared__ double s_d[32];
   if (aborted(A)) return;
@@ -1469,6 +1477,7 @@ __global__ void __launch_bounds__(256) k_scan(TopkArgs A) {
 // kept ties, all of magnitude |k-th key|, are added per tensor by k_scan).
 template <int MODE, bool KSUM>
 __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
+  chain_wait();
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
   __shared__ double s_d[32];
@@ -1644,6 +1653,7 @@ __device__ __forceinline__ void emit_kept(const TopkArgs& A, int t, int64_t base
 
 template <int MODE, int KQ>
 __global__ void __launch_bounds__(256, 3) k_write(TopkArgs A) {
+  chain_wait();
   __shared__ uint32_t s_gt[UB_UNITS], s_eq[UB_UNITS];
   __shared__ uint32_t s_warp[33];
   if (aborted(A)) return;
@@ -2425,7 +2435,7 @@ static int stream_grid(K kernel, int64_t units) {
 template <int MODE, bool EF, bool LOADG, bool LAZY = false>
 static void launch_stream(const TopkArgs& A, cudaStream_t s) {
   auto kern = k_stream<MODE, EF, LOADG, LAZY>;
-  k_stream<MODE, EF, LOADG, LAZY><<<stream_grid(kern, A.U), STREAM_THREADS, STREAM_SMEM, s>>>(A);
+  launch_chained(kern, stream_grid(kern, A.U), STREAM_THREADS, STREAM_SMEM, s, A);
 }
 
 // Optional CUDA events recorded on the call's stream.  With n <= 5 they
@@ -2519,14 +2529,14 @@ static gc_status launch_fused(const TopkArgs& A0, const gc_layout* host, const F
 template <int MODE>
 static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents& pe) {
   const int T = A.T;
-  k_plan<<<1, 1024, 0, s>>>(A);
+  launch_chained(k_plan, 1, 1024, 0, s, A);
   if (A.clip) {
-    k_gnorm<<<stream_grid(k_gnorm, A.U), 256, 0, s>>>(A);
-    k_gscale<<<T, 256, 0, s>>>(A);
+    launch_chained(k_gnorm, stream_grid(k_gnorm, A.U), 256, 0, s, A);
+    launch_chained(k_gscale, T, 256, 0, s, A);
   }
   pe.done(A.sampled ? 0 : 1, s);
   if (A.sampled) {
-    if (A.SB > 0) k_sample<MODE><<<(unsigned)A.SB, 512, 0, s>>>(A);
+    if (A.SB > 0) launch_chained(k_sample<MODE>, (unsigned)A.SB, 512, 0, s, A);
     pe.done(1, s);
   }
   if (MODE == MODE_MOM) {
@@ -2552,33 +2562,33 @@ static void launch_pipeline(const TopkArgs& A, cudaStream_t s, const PhaseEvents
   // a histogram pass and a select per level (running each tensor's select in
   // the last CTA of its histogram pass measured slower on the Llama arena:
   // 0.186 against 0.155 ms)
-  k_select<<<T, 256, 0, s>>>(A, PH_C1);
+  launch_chained(k_select, T, 256, 0, s, A, (int)PH_C1);
   pe.done(0, s);
-  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 1);
+  launch_chained(k_hist<MODE>, UBg, 256, 0, s, A, 1);
   pe.done(0, s);
-  k_select<<<T, 256, 0, s>>>(A, PH_C1D);
+  launch_chained(k_select, T, 256, 0, s, A, (int)PH_C1D);
   pe.done(0, s);
-  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 2);
+  launch_chained(k_hist<MODE>, UBg, 256, 0, s, A, 2);
   pe.done(0, s);
-  k_select<<<T, 256, 0, s>>>(A, PH_C2);
+  launch_chained(k_select, T, 256, 0, s, A, (int)PH_C2);
   pe.done(0, s);
-  k_hist<MODE><<<UBg, 256, 0, s>>>(A, 3);
+  launch_chained(k_hist<MODE>, UBg, 256, 0, s, A, 3);
   pe.done(0, s);
-  k_select<<<T, 256, 0, s>>>(A, PH_C3);
+  launch_chained(k_select, T, 256, 0, s, A, (int)PH_C3);
   pe.done(3, s);
   if (MODE != MODE_RANDK && A.qkind != KQ_NONE)
-    k_count<MODE, MODE != MODE_RANDK><<<UBg, 256, 0, s>>>(A);
+    launch_chained(k_count<MODE, MODE != MODE_RANDK>, UBg, 256, 0, s, A);
   else
-    k_count<MODE, false><<<UBg, 256, 0, s>>>(A);
+    launch_chained(k_count<MODE, false>, UBg, 256, 0, s, A);
   pe.done(0, s);
-  k_scan<<<T, 256, 0, s>>>(A);
+  launch_chained(k_scan, T, 256, 0, s, A);
   pe.done(0, s);
   if (MODE != MODE_RANDK && A.qkind == KQ_QSGD)
-    k_write<MODE, MODE != MODE_RANDK ? KQ_QSGD : KQ_NONE><<<UBg, 256, 0, s>>>(A);
+    launch_chained(k_write<MODE, MODE != MODE_RANDK ? KQ_QSGD : KQ_NONE>, UBg, 256, 0, s, A);
   else if (MODE != MODE_RANDK && A.qkind == KQ_SIGN)
-    k_write<MODE, MODE != MODE_RANDK ? KQ_SIGN : KQ_NONE><<<UBg, 256, 0, s>>>(A);
+    launch_chained(k_write<MODE, MODE != MODE_RANDK ? KQ_SIGN : KQ_NONE>, UBg, 256, 0, s, A);
   else
-    k_write<MODE, KQ_NONE><<<UBg, 256, 0, s>>>(A);
+    launch_chained(k_write<MODE, KQ_NONE>, UBg, 256, 0, s, A);
   pe.done(4, s);
 }
 
@@ -2697,7 +2707,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
     }
   }
   pe.start(s);
-  if (cudaMemsetAsync(ws, 0, c.zero_bytes, s) != cudaSuccess) return GC_ERR_CUDA;
+  if (!zero_chained(ws, c.zero_bytes, s)) return GC_ERR_CUDA;
   pe.done(0, s);
   if (kq.kind == KQ_SIGN) {
     // the payload write sets the bits of the positive kept values
@@ -2711,7 +2721,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
     launch_pipeline<MODE_RANDK>(A, s, pe);
   else
     launch_pipeline<MODE_MOM>(A, s, pe);
-  if (iter_dev) k_iter_advance<<<1, 1, 0, s>>>(iter_dev);
+  if (iter_dev) launch_chained(k_iter_advance, 1, 1, 0, s, iter_dev);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 

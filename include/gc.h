@@ -172,7 +172,9 @@ gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32_t flags, s
  * meet at four grid-wide barriers; every wait there is bounded and sets
  * GC_DIAG_TIMEOUT if it runs out.  gc_diag.one_launch reports it.  Other
  * arenas, random-k, GC_FORCE_EXACT and GC_MULTI_KERNEL use the multi-kernel
- * pipeline (a memset and 13 kernels).  Both give identical results. */
+ * pipeline (14 kernels chained as programmatic dependent launches: each
+ * waits for the previous one's completion before touching memory).  Both
+ * give identical results. */
 gc_status gc_ef_topk_compress(const gc_layout* dev, const gc_layout* host, const float* g, float* e,
                               int32_t* idx, float* val, int8_t* q, float* scale, uint64_t seed,
                               uint64_t iter, uint32_t flags, void* workspace, size_t ws_bytes,
