@@ -144,16 +144,17 @@ class Layout:
     """A flat-arena layout: host arrays (validation, sizing) + device copies.
 
     off[t]..off[t+1] are tensor t's elements; k (optional) kept entries per
-    tensor; koff their prefix sum.
+    tensor; koff their running sum from koff0 (0 for a whole arena; a
+    bucket, made by Layout.bucket, keeps its arena's offsets).
     """
 
-    def __init__(self, off, k=None, device="cuda"):
+    def __init__(self, off, k=None, device="cuda", koff0=0):
         self.off = np.ascontiguousarray(off, dtype=np.int64)
         self.T = int(self.off.size - 1)
         if k is not None:
             self.k = np.ascontiguousarray(k, dtype=np.int64)
-            self.koff = np.zeros(self.T + 1, np.int64)
-            self.koff[1:] = np.cumsum(self.k)
+            self.koff = np.full(self.T + 1, int(koff0), np.int64)
+            self.koff[1:] += np.cumsum(self.k)
         else:
             self.k = self.koff = None
         self.device = torch.device(device)
@@ -168,13 +169,36 @@ class Layout:
                 self._dev_koff = torch.from_numpy(self.koff).to(self.device)
             self._dev = gc_layout(self.T, _ptr(self._dev_off), _ptr(self._dev_k), _ptr(self._dev_koff))
 
+    def bucket(self, t0: int, t1: int) -> "Layout":
+        """Tensors t0 .. t1-1 as a layout of their own with this arena's
+        element and entry offsets: calls on it read and write the whole
+        arena's element and payload arrays at those offsets, and the
+        per-tensor arrays and sign-bit words passed offset to tensor t0
+        (word_offset / kept_word_offset)."""
+        if not 0 <= t0 < t1 <= self.T:
+            raise ValueError(f"bucket [{t0}, {t1}) outside 0..{self.T}")
+        k = None if self.k is None else self.k[t0:t1]
+        return Layout(self.off[t0:t1 + 1], k, device=self.device,
+                      koff0=0 if self.koff is None else int(self.koff[t0]))
+
     @property
     def numel(self) -> int:
+        """Elements the arena's arrays must hold (the end of the last tensor)."""
         return int(self.off[-1])
 
     @property
     def total_k(self) -> int:
+        """Entries the payload arrays must hold (the end of the last tensor's)."""
         return int(self.koff[-1]) if self.koff is not None else 0
+
+    def word_offset(self, t: int) -> int:
+        """First sign-bit word of tensor t (dense sign compressor)."""
+        n = np.diff(self.off[:t + 1])
+        return int(((n + 31) // 32).sum())
+
+    def kept_word_offset(self, t: int) -> int:
+        """First word of tensor t's kept-value sign bits."""
+        return int(((self.k[:t] + 31) // 32).sum())
 
     @property
     def kept_words(self) -> int:

@@ -64,7 +64,8 @@ struct DecompArgs {
   int32_t* wsh;     // [T]   log2 of the tensor's window size
   int64_t* kwoff;   // [T+1] first sign-bit word of each tensor (DK_SIGN)
   int64_t* starts;  // [DW_GROUP][NW+1] first entry of each window, per worker
-  int64_t NW, K;
+  int64_t NW, K;        // windows; K = koff[T], the end of the entries
+  int64_t off0, koff0;  // off[0] and koff[0] of the host layout (nonzero for a bucket)
 };
 
 // Window tables from the device layout (one CTA); a disagreement with the
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(1024) k_dplan(DecompArgs A) {
   if (threadIdx.x == 0) {
     A.wo[A.T] = carry;
     A.kwoff[A.T] = carry_b;
-    if (carry != A.NW || A.off[0] != 0 || A.koff[0] != 0 || A.koff[A.T] != A.K) {
+    if (carry != A.NW || A.off[0] != A.off0 || A.koff[0] != A.koff0 || A.koff[A.T] != A.K) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -286,7 +287,7 @@ static gc_status run_decompress(int dk, const gc_layout* dev, const gc_layout* h
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!zero_chained(workspace, DIAG_BYTES, s)) return GC_ERR_CUDA;
   const int64_t K = host->koff[T];
-  if (K == 0 || W == 0) return GC_OK;
+  if (K == host->koff[0] || W == 0) return GC_OK;
   unsigned char* wsp = static_cast<unsigned char*>(workspace);
   DecompArgs A;
   memset(&A, 0, sizeof A);
@@ -302,6 +303,8 @@ static gc_status run_decompress(int dk, const gc_layout* dev, const gc_layout* h
   A.starts = reinterpret_cast<int64_t*>(wsp + o_st);
   A.NW = NW;
   A.K = K;
+  A.off0 = host->off[0];
+  A.koff0 = host->koff[0];
   launch_chained(k_dplan, 1, 1024, 0, s, A);
   for (int w0 = 0; w0 < W; w0 += DW_GROUP) {
     A.W = W - w0 < DW_GROUP ? W - w0 : DW_GROUP;

@@ -46,6 +46,7 @@ struct DenseArgs {
   int64_t* woff;      // [T+1]
   double* upart;      // [U]
   int64_t U, W, N;
+  int64_t off0;  // off[0] of the host layout (nonzero for a bucket)
 };
 
 __device__ __forceinline__ bool aborted(const DenseArgs& A) { return A.diag[DIAG_ABORT] != 0u; }
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(1024) k_dplan(DenseArgs A) {
   if (threadIdx.x == 0) {
     A.units_off[A.T] = carry_u;
     A.woff[A.T] = carry_w;
-    if (s_bad || carry_u != A.U || carry_w != A.W || A.off[0] != 0 || A.off[A.T] != A.N) {
+    if (s_bad || carry_u != A.U || carry_w != A.W || A.off[0] != A.off0 || A.off[A.T] - A.off0 != A.N) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -614,7 +615,7 @@ static DenseTotals dense_totals(const gc_layout* h) {
     z.U += units_of(n);
     z.W += (n + 31) >> 5;
   }
-  z.N = h->off[h->num_tensors];
+  z.N = h->off[h->num_tensors] - h->off[0];
   return z;
 }
 
@@ -677,6 +678,7 @@ static gc_status dense_setup(const gc_layout* dev, const gc_layout* host, void* 
   A->U = z.U;
   A->W = z.W;
   A->N = z.N;
+  A->off0 = host->off[0];
   if (!zero_chained(ws, c.zero_bytes, s)) return GC_ERR_CUDA;
   launch_chained(k_dplan, 1, 1024, 0, s, *A);
   return GC_OK;
@@ -688,7 +690,7 @@ static void launch_quant(const DenseArgs& A, cudaStream_t s) {
   launch_chained(k_dreduce, A.T, 256, 0, s, A);
   if (OP == DOP_SIGN)
     launch_chained(k_sign2<EF>, dense_grid(k_sign2<EF>, A.U), DTHREADS, 0, s, A);
-  else if (A.N < (int64_t(1) << 34))
+  else if (A.off0 + A.N < (int64_t(1) << 34))
     launch_chained(k_quant2<OP, EF, true>, dense_grid(k_quant2<OP, EF, true>, A.U), DTHREADS, 0, s, A);
   else
     launch_chained(k_quant2<OP, EF, false>, dense_grid(k_quant2<OP, EF, false>, A.U), DTHREADS, 0, s, A);

@@ -97,6 +97,7 @@ struct TopkArgs {
   int2* smap;          // [SB]  sampling CTA (dispatch order) -> (tensor, its CTA index)
   uint32_t* scnt;      // [2T] per tensor: keys in its sample list, sampling CTAs finished (zeroed per call)
   int64_t U, UB, C, S, N, K, SB;
+  int64_t off0, koff0;  // off[0] and koff[0] of the host layout (nonzero for a bucket)
   int ssplit;          // sampling CTAs per large sample (sample_ctas)
 };
 
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
     A.kwoff[A.T] = carry_w;
     A.sblk[A.T] = carry_sb;
     if (s_bad || carry_u != A.U || carry_b != A.UB || carry_c != A.C || carry_s != A.S || carry_sb != A.SB ||
-        A.off[0] != 0 || A.off[A.T] != A.N || A.koff[0] != 0 || A.koff[A.T] != A.K) {
+        A.off[0] != A.off0 || A.off[A.T] - A.off0 != A.N || A.koff[0] != A.koff0 || A.koff[A.T] - A.koff0 != A.K) {
       A.diag[DIAG_ERR] |= GC_DIAG_LAYOUT_MISMATCH;
       A.diag[DIAG_ABORT] = 1u;
     }
@@ -2018,7 +2019,9 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
   }
   if (tid == 0) {
     s_uoff[T] = (int32_t)carry;
-    if (s_off[0] != 0 || s_off[T] != A.N || A.koff[0] != 0 || A.koff[T] != A.K || (int64_t)carry != F.U) s_ok = 0;
+    if (s_off[0] != A.off0 || s_off[T] - A.off0 != A.N || A.koff[0] != A.koff0 || A.koff[T] - A.koff0 != A.K ||
+        (int64_t)carry != F.U)
+      s_ok = 0;
   }
   __syncthreads();
   if (!s_ok) {
@@ -2335,7 +2338,7 @@ static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled, bool split_f
     }
     r.K += k;
   }
-  r.N = h->off[h->num_tensors];
+  r.N = h->off[h->num_tensors] - h->off[0];
   return r;
 }
 
@@ -2388,7 +2391,7 @@ struct FusedCarve {
 };
 
 static bool fused_layout_fits(const gc_layout* h) {
-  return h->num_tensors <= FTMAX && h->off[h->num_tensors] <= FNMAX;
+  return h->num_tensors <= FTMAX && h->off[h->num_tensors] - h->off[0] <= FNMAX;
 }
 
 static FusedCarve carve_fused(const gc_layout* h) {
@@ -2691,6 +2694,8 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.S = z.S;
   A.N = z.N;
   A.K = z.K;
+  A.off0 = host->off[0];
+  A.koff0 = host->koff[0];
   A.SB = z.SB;
   A.ssplit = z.split;
 

@@ -60,6 +60,20 @@
  *  - g, e, u, v, out must be 16-byte aligned.
  *  - Argument errors are returned before anything is enqueued.  No C++
  *    exception crosses this interface.
+ *
+ * Buckets.  A layout may describe tensors t0 .. t1-1 of a larger arena: off
+ * and koff are then that arena's own offsets of those tensors (off[0] and
+ * koff[0] need not be 0).  Per-element arrays (g, e, u, v, out, dense int8 /
+ * QSGD codes) and per-entry arrays (idx, val, q) are passed as the WHOLE
+ * arena's arrays and are read and written at those offsets only; per-tensor
+ * arrays (k, scale, mean_abs, thresholds, norms, counts, residual
+ * descriptors) and sign-bit words are passed offset to the bucket's first
+ * tensor (its word offset is the sum of ceil(n / 32), or of ceil(k / 32) for
+ * the kept-value bits, over the arena's earlier tensors).  Random numbers
+ * are drawn at arena indices, so compressing an arena bucket by bucket, in
+ * any order or concurrently on several streams (each call with its own
+ * workspace), gives exactly the whole-arena call's outputs: a training loop
+ * can compress each bucket as soon as backward has produced its gradients.
  */
 #ifndef GC_H_
 #define GC_H_
@@ -74,8 +88,8 @@ extern "C" {
 typedef enum gc_status {
   GC_OK = 0,
   GC_ERR_INVALID_ARG = 1, /* null pointer where one is required, bad flag or mode */
-  GC_ERR_LAYOUT = 2,      /* off not starting at 0 / not increasing, n_t >= 2^31, k_t > n_t,
-                             koff not the prefix sum of k */
+  GC_ERR_LAYOUT = 2,      /* off[0] or koff[0] negative, off not increasing, n_t >= 2^31,
+                             k_t > n_t, koff[t+1] - koff[t] != k_t */
   GC_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than gc_workspace_size */
   GC_ERR_ALIGNMENT = 4,   /* a data pointer is not 16-byte aligned */
   GC_ERR_CUDA = 5,        /* a CUDA launch or copy failed (cudaGetLastError) */
@@ -114,9 +128,12 @@ typedef enum gc_op {
 
 typedef struct gc_layout {
   int32_t num_tensors;  /* T >= 1 */
-  const int64_t* off;   /* [T+1] element offsets, off[0] = 0, strictly increasing */
+  const int64_t* off;   /* [T+1] element offsets, strictly increasing; off[0] = 0 for a whole
+                           arena, > 0 for a bucket (see Buckets above) */
   const int64_t* k;     /* [T] kept entries per tensor, 0 <= k_t <= n_t; may be NULL for dense ops */
-  const int64_t* koff;  /* [T+1] prefix sum of k; may be NULL for dense ops */
+  const int64_t* koff;  /* [T+1] koff[t+1] = koff[t] + k_t; koff[0] = 0 for a whole arena, the
+                           arena's own koff of the first tensor for a bucket; may be NULL for
+                           dense ops */
 } gc_layout;
 
 /* Diagnostics of the last call that used a workspace. */

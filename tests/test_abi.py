@@ -69,6 +69,28 @@ def test_layout_validation(gc):
     assert gc.lib().gc_workspace_size(lay.host(), 99, 0, C.byref(out)) == gc.GC_ERR_INVALID_ARG
 
 
+def test_bucket_layouts_are_accepted_and_sized_like_their_tensors(gc):
+    """A bucket (tensors t0..t1-1 of a larger arena, with that arena's
+    offsets) validates, and needs the workspace of the same tensors laid
+    out from zero; negative offsets are layout errors."""
+    sizes, k = [100, 4097, 33, 70_001, 6], [1, 5, 2, 70, 6]
+    whole = gc.Layout(np.concatenate([[0], np.cumsum(sizes)]), np.asarray(k, np.int64), device="cpu")
+    b = whole.bucket(1, 4)
+    assert list(b.off) == [100, 4197, 4230, 74231] and list(b.koff) == [1, 6, 8, 78]
+    alone = gc.Layout(np.concatenate([[0], np.cumsum(sizes[1:4])]), np.asarray(k[1:4], np.int64), device="cpu")
+    for op, flags in [(gc.GC_OP_TOPK, gc.GC_EF), (gc.GC_OP_TOPK, gc.GC_RANDK), (gc.GC_OP_MOMENTUM, 0),
+                      (gc.GC_OP_SIGN, 0), (gc.GC_OP_QUANTIZE, 0), (gc.GC_OP_DECOMPRESS, 0)]:
+        assert gc.workspace_size(b, op, flags) == gc.workspace_size(alone, op, flags) > 0
+    out = C.c_size_t()
+    neg = gc.Layout([-4, 10], np.asarray([1], np.int64), device="cpu")
+    assert gc.lib().gc_workspace_size(neg.host(), gc.GC_OP_TOPK, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    assert gc.lib().gc_workspace_size(neg.host(), gc.GC_OP_SIGN, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    negk = gc.Layout([0, 10], np.asarray([1], np.int64), device="cpu", koff0=-1)
+    assert gc.lib().gc_workspace_size(negk.host(), gc.GC_OP_TOPK, 0, C.byref(out)) == gc.GC_ERR_LAYOUT
+    with pytest.raises(ValueError):
+        whole.bucket(3, 3)
+
+
 def test_argument_errors_return_before_any_launch(gc):
     lay = _host_layout(gc, [100], [5])
     L = gc.lib()
