@@ -69,9 +69,13 @@ static bool zero_chained(void* p, size_t bytes, cudaStream_t s) {
 // Work unit: one warp streams UNIT consecutive elements of one tensor.
 constexpr int UNIT_SHIFT = 12;
 constexpr int64_t UNIT = int64_t(1) << UNIT_SHIFT;
-// Unit block: UB_UNITS consecutive units of one tensor, one CTA of the
-// selection kernels (thread per unit on the candidate path).
+// Unit block: consecutive units of one tensor, one CTA of 8 warps in the
+// selection kernels; on the candidate path a warp walks the candidate
+// chunks of 1/8 of them.  UB_UNITS units per block (32 per warp), or
+// UB_UNITS_DENSE (8 per warp) in arenas with many candidates per unit, where
+// the longest walks set the kernels' time.
 constexpr int UB_UNITS = 256;
+constexpr int UB_UNITS_DENSE = 64;
 // Radix digits of the 32-bit selection key: 11 + 11 + 10 bits.
 constexpr int NBINS = 2048;
 // Per-warp candidate staging capacity in shared memory (entries per unit).
@@ -131,8 +135,8 @@ __host__ __device__ inline int64_t cand_capacity(int64_t n, int64_t k) {
 }
 
 __host__ __device__ inline int64_t units_of(int64_t n) { return (n + UNIT - 1) >> UNIT_SHIFT; }
-__host__ __device__ inline int64_t ublocks_of(int64_t n) {
-  return (units_of(n) + UB_UNITS - 1) / UB_UNITS;
+__host__ __device__ inline int64_t ublocks_of(int64_t n, int ubu) {
+  return (units_of(n) + ubu - 1) / ubu;
 }
 
 // Sample plan of a tensor: `runs` runs of RUN consecutive elements spaced

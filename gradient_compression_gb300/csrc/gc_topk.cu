@@ -98,6 +98,7 @@ struct TopkArgs {
   uint32_t* scnt;      // [2T] per tensor: keys in its sample list, sampling CTAs finished (zeroed per call)
   int64_t U, UB, C, S, N, K, SB;
   int64_t off0, koff0;  // off[0] and koff[0] of the host layout (nonzero for a bucket)
+  int ubu;              // units per unit block (UB_UNITS or UB_UNITS_DENSE)
   int ssplit;          // sampling CTAs per large sample (sample_ctas)
 };
 
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
       const int64_t k = A.kk[t];
       if (n < 1 || n > INT64_C(2147483647) || k < 0 || k > n || A.koff[t + 1] - A.koff[t] != k) s_bad = 1;
       nu = units_of(n);
-      nb = ublocks_of(n);
+      nb = ublocks_of(n, A.ubu);
       nc = cand_capacity(n, k);
       nw = k > 0 ? (k + 31) >> 5 : 0;
       nsb = sampled ? sample_ctas(n, k, A.ssplit) : 0;
@@ -1254,8 +1255,8 @@ struct UnitBlock {
 __device__ __forceinline__ UnitBlock unit_block(const TopkArgs& A) {
   UnitBlock r;
   r.t = find_segment(A.ublk_off, A.T, (int64_t)blockIdx.x);
-  r.u0 = A.units_off[r.t] + ((int64_t)blockIdx.x - A.ublk_off[r.t]) * UB_UNITS;
-  const int64_t u1 = min(r.u0 + UB_UNITS, A.units_off[r.t + 1]);
+  r.u0 = A.units_off[r.t] + ((int64_t)blockIdx.x - A.ublk_off[r.t]) * A.ubu;
+  const int64_t u1 = min(r.u0 + A.ubu, A.units_off[r.t + 1]);
   r.nu = (int)(u1 - r.u0);
   r.base = A.off[r.t];
   r.n = A.off[r.t + 1] - r.base;
@@ -1392,7 +1393,7 @@ __global__ void __launch_bounds__(256) k_hist(TopkArgs A, int level) {
   }
 }
 
-// The candidate chunks of a warp's 32 units are walked as one concatenated
+// The candidate chunks of a warp's units are walked as one concatenated
 // sequence, 32 entries per step with one entry per lane, so that loads are
 // contiguous and no lane idles on a short chunk.  `off` is this lane's
 // exclusive prefix of the chunk lengths; returns the lane whose chunk holds
@@ -1517,7 +1518,7 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
         }
       }
     } else {
-      // The warp's 32 chunks walked as one sequence, 32 entries per step
+      // The warp's chunks (32 or 8 units) walked as one sequence, 32 entries per step
       // (see chunk_owner and k_write): loads contiguous across the lanes,
       // CP steps' loads in flight and the next CP steps' issued before these
       // are counted; a unit's counts are the differences of
@@ -1525,7 +1526,10 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
       // thread per unit issued a separate sector request per lane for every
       // load (25 us on ResNet-50 at 1%, the largest unit blocks the long pole).
       const unsigned lane = lane_id();
-      const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
+      const int wu = A.ubu >> 3;  // units per warp; lanes >= wu own empty chunks
+      const int ui = (tid >> 5) * wu + (int)lane;
+      const bool own = (int)lane < wu && ui < ub.nu;
+      const uint2 ch = own ? A.chunk[ub.u0 + ui] : make_uint2(0u, 0u);
       const uint32_t* ckb = A.ckey + A.cand_off[ub.t];
       unsigned L;
       const uint32_t off = warp_excl_scan(ch.y, lane, &L);
@@ -1568,9 +1572,9 @@ __global__ void __launch_bounds__(256) k_count(TopkArgs A) {
         es = Ec;
       }
       const uint32_t gn = __shfl_down_sync(FULL, gs, 1), en = __shfl_down_sync(FULL, es, 1);
-      if (tid < ub.nu) {
-        s_gt[tid] = (lane == 31 ? Gc : gn) - gs;
-        s_eq[tid] = (lane == 31 ? Ec : en) - es;
+      if (own) {
+        s_gt[ui] = (lane == 31 ? Gc : gn) - gs;
+        s_eq[ui] = (lane == 31 ? Ec : en) - es;
       }
     }
   }
@@ -1714,7 +1718,7 @@ __global__ void __launch_bounds__(256, 3) k_write(TopkArgs A) {
           });
     }
   } else {
-    // Candidate path: the warp's 32 chunks are walked as one sequence (see
+    // Candidate path: the warp's chunks (32 or 8 units) are walked as one sequence (see
     // chunk_owner), 32 entries per step with loads and stores contiguous
     // across the lanes, and kept and tie counts inside a unit are
     // differences of running counts over the sequence, taken at the unit's
@@ -1724,9 +1728,12 @@ __global__ void __launch_bounds__(256, 3) k_write(TopkArgs A) {
     // that held the largest unit blocks at 35-43 us against 28 us here.
     const unsigned lane = lane_id();
     const unsigned lt = (1u << lane) - 1u;
-    const uint2 ch = tid < ub.nu ? A.chunk[ub.u0 + tid] : make_uint2(0u, 0u);
-    const uint32_t eqb = s_eq[tid];                   // ties before this unit
-    const uint32_t sel0 = s_gt[tid] + min(eqb, r_eq);  // kept before this unit
+    const int wu = A.ubu >> 3;  // units per warp; lanes >= wu own empty chunks
+    const int ui = (tid >> 5) * wu + (int)lane;
+    const bool own = (int)lane < wu && ui < ub.nu;
+    const uint2 ch = own ? A.chunk[ub.u0 + ui] : make_uint2(0u, 0u);
+    const uint32_t eqb = own ? s_eq[ui] : 0u;                 // ties before this unit
+    const uint32_t sel0 = own ? s_gt[ui] + min(eqb, r_eq) : 0u;  // kept before this unit
     unsigned L;
     const uint32_t off = warp_excl_scan(ch.y, lane, &L);
     const int64_t cb = A.cand_off[ub.t];
@@ -2298,7 +2305,22 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
 struct TopkLayoutTotals {
   int64_t U = 0, UB = 0, C = 0, S = 0, N = 0, K = 0, SB = 0, SBmax = 0;
   int split = 1;
+  int ubu = UB_UNITS;
 };
+
+// Units per unit block: UB_UNITS_DENSE when the arena keeps at least 16
+// elements per 4096-element unit on average (1% density and up), where a
+// warp walking 32 units' candidates sets the count and write kernels' time;
+// UB_UNITS otherwise, where small blocks would only add CTAs.  A function of
+// the layout alone, so the workspace query and the call agree.
+static int unit_block_units(const gc_layout* h) {
+  int64_t K = 0, U = 0;
+  for (int t = 0; t < h->num_tensors; ++t) {
+    K += h->k[t];
+    U += units_of(h->off[t + 1] - h->off[t]);
+  }
+  return K >= 16 * U ? UB_UNITS_DENSE : UB_UNITS;
+}
 
 // Sampling CTAs per large sample: enough to give about two CTAs per SM of
 // the current device when the arena has few large tensors.
@@ -2321,11 +2343,12 @@ static int sampling_split(const gc_layout* h) {
 static TopkLayoutTotals totals_of(const gc_layout* h, bool sampled, bool split_for_launch = false) {
   TopkLayoutTotals r;
   if (sampled && split_for_launch) r.split = sampling_split(h);
+  r.ubu = unit_block_units(h);
   for (int t = 0; t < h->num_tensors; ++t) {
     const int64_t n = h->off[t + 1] - h->off[t];
     const int64_t k = h->k[t];
     r.U += units_of(n);
-    r.UB += ublocks_of(n);
+    r.UB += ublocks_of(n, r.ubu);
     r.C += cand_capacity(n, k);
     if (sampled && k > 0) {
       int64_t runs, stride, m;
@@ -2696,6 +2719,7 @@ static gc_status run_topk(int mode, const gc_layout* dev, const gc_layout* host,
   A.K = z.K;
   A.off0 = host->off[0];
   A.koff0 = host->koff[0];
+  A.ubu = z.ubu;
   A.SB = z.SB;
   A.ssplit = z.split;
 
