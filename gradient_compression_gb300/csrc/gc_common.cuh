@@ -83,8 +83,10 @@ constexpr int WCAP = 512;
 // Tensors at most this long are sampled completely when the candidate
 // threshold is estimated.
 constexpr int64_t SMALL_N = 16384;
-// Expected number of Top-k members in a tensor's sample.
-constexpr int64_t SAMPLE_HITS = 128;
+// Expected number of Top-k members in a tensor's sample: 128, or 64 for a
+// tensor that keeps less than 0.2% of its elements, whose sample of 128 / rho
+// elements would otherwise be an eighth of a 1M-element tensor.
+__host__ __device__ inline int64_t sample_hits(int64_t n, int64_t k) { return 500 * k < n ? 64 : 128; }
 constexpr int RUN = 128;  // sampled elements per contiguous run (one warp, one float4 per lane)
 // Threshold estimate from the sample: pilot runs, shared-memory key list
 // (the pilot's keys, then the keys above the pilot's floor), and the
@@ -149,7 +151,8 @@ __host__ __device__ inline void sample_plan(int64_t n, int64_t k, int64_t* runs,
     *m = n;
     return;
   }
-  int64_t want = (SAMPLE_HITS * n + k - 1) / k;  // ceil(SAMPLE_HITS / rho)
+  const int64_t hits = sample_hits(n, k);
+  int64_t want = (hits * n + k - 1) / k;  // ceil(hits / rho)
   int64_t r = (want + RUN - 1) / RUN;
   int64_t rmax = n / RUN;
   if (r > rmax) r = rmax;

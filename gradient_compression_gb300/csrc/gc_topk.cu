@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(1024) k_plan(TopkArgs A) {
         // the sample key of rank j bounds t_est: j = k for a complete sample,
         // else the expected count lam of Top-k members in the sample plus five
         // standard deviations (and 6).  Fewer than k candidates then needs a
-        // Poisson(lam) count of at least j (about 1e-7 at lam = 128); with four
+        // Poisson(lam) count of at least j (about 1e-7 at lam = 64 or 128); with four
         // (and 4) about one tensor-step in 10^4 fell short under error
         // feedback and took the full-pass path.  Each standard deviation of
         // margin costs about 7% more candidates.
