@@ -1841,6 +1841,7 @@ constexpr int FTCACHE = 64;                 // tensors one CTA's units may span
 constexpr int FBATCH = 2;                   // units whose loads are in flight together (phase 1)
 constexpr int FB = 2;                       // the same for the later phases (acc only)
 constexpr uint32_t FSPIN_LIMIT = 1u << 20;  // polls of a barrier (about a second)
+constexpr uint32_t FLMAX = 4096;  // level-1 bucket keys per tensor up to which level 3 reads the list
 static_assert(FTHREADS * 4 == FUNIT, "one float4 per thread per unit");
 
 struct FusedArgs {
@@ -1851,6 +1852,9 @@ struct FusedArgs {
   uint32_t* h2;      // [T][NBINS] level 2, then [T][NBINS] level 3 (cleared in phase 1)
   uint32_t* ugt;     // [U] keys above the k-th key, per unit
   uint32_t* ueq;     // [U] keys equal to it, per unit
+  uint32_t* lcnt;    // [T] keys of the k-th key's level-1 bucket per tensor, then a flag word
+                     // set when one exceeds FLMAX (zeroed per call)
+  uint32_t* lkey;    // [N] those keys, tensor t's from off[t] - off[0]
   int64_t U;
   uint32_t spin_limit;
 };
@@ -2143,10 +2147,25 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
         }
         if (!sl->live) continue;
         const uint32_t b1 = sl->b1;
+        uint32_t* const lt = F.lkey + (s_off[r.t] - A.off0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t key = mag_key(x[j][q]);
-          smem_hist_add(s_hist, (key >> 10) & 0x7FFu, q < c[j] && (key >> 21) == b1);
+          const bool in = q < c[j] && (key >> 21) == b1;
+          smem_hist_add(s_hist, (key >> 10) & 0x7FFu, in);
+          // the bucket's keys also go to the tensor's list (one atomic per
+          // warp), so that level 3 can read them instead of re-reading acc
+          const unsigned m = __ballot_sync(FULL, in);
+          if (m) {
+            const unsigned lane = tid & 31, lead = __ffs(m) - 1;
+            uint32_t base = 0u;
+            if (lane == lead) {
+              base = atomicAdd(F.lcnt + r.t, (unsigned)__popc(m));
+              if (base + (uint32_t)__popc(m) > FLMAX) atomicOr(F.lcnt + T, 1u);
+            }
+            base = __shfl_sync(FULL, base, lead);
+            if (in) lt[base + __popc(m & ((1u << lane) - 1u))] = key;
+          }
         }
         if (u + 1 == u1 || (int64_t)s_uoff[r.t + 1] == u + 1) fflush_hist(s_hist, F.h2 + (size_t)r.t * NBINS);
       }
@@ -2154,9 +2173,14 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
   }
   if (!fused_barrier(F, &target, &s_ok)) return;
 
+  // Every tensor's level-1 bucket list within FLMAX keys: level 3 is searched
+  // in those lists at the start of phase 4, and phase 3 with its barrier is
+  // skipped.  The flag was final at the barrier, so every CTA decides alike.
+  const bool lists = __ldcg(F.lcnt + T) == 0u;
+
   // ---- phase 3: level-2 bucket; level-3 histograms
   uint32_t* const h3 = F.h2 + (size_t)T * NBINS;
-  if (work) {
+  if (work && !lists) {
     int tl = tA, t = tA;
     for (int64_t ub = u0; ub < u1; ub += FB) {
       float x[FB][4];
@@ -2193,7 +2217,7 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
       }
     }
   }
-  if (!fused_barrier(F, &target, &s_ok)) return;
+  if (!lists && !fused_barrier(F, &target, &s_ok)) return;
 
   // ---- phase 4: the k-th key, kept ties, scale; per-unit counts
   if (work) {
@@ -2210,7 +2234,49 @@ __global__ void __launch_bounds__(FTHREADS, 2) k_fused(FusedArgs F) {
         FSel* sl = s_sel + (r.t - tA);
         const bool owner = (int64_t)s_uoff[r.t] == u;  // this CTA holds the tensor's first unit
         if (u == u0 || owner) {
-          if (sl->live) {
+          if (sl->live && lists) {
+            // level 2 as phase 3 would find it, then level 3 over the list
+            uint32_t above = 0u;
+            const uint32_t b = ffind(F.h2 + (size_t)r.t * NBINS, sl->r2, &above, s_row, s_warp, s_res);
+            if (tid == 0) {
+              if (b == 0xFFFFFFFFu) {
+                atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+                sl->live = 0;
+              }
+              sl->b2 = b;
+              sl->r3 = sl->r2 - above;
+            }
+            __syncthreads();
+            if (sl->live) {
+              const uint32_t pfx = (sl->b1 << 11) | sl->b2;
+              const uint32_t nl = __ldcg(F.lcnt + r.t);
+              const uint32_t* lt = F.lkey + (s_off[r.t] - A.off0);
+              for (uint32_t i0 = 0; i0 < nl; i0 += 4 * blockDim.x) {  // at most two rounds of loads
+                uint32_t kk[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const uint32_t i = i0 + v * blockDim.x + tid;
+                  kk[v] = i < nl ? __ldcg(lt + i) : 0u;
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  if (i0 + v * blockDim.x + tid < nl && (kk[v] >> 10) == pfx) atomicAdd(s_hist + (kk[v] & 0x3FFu), 1u);
+              }
+              __syncthreads();
+              uint32_t above3 = 0u;
+              const uint32_t b3 = find_bucket(s_hist, sl->r3, &above3, s_warp, s_res);
+              for (int i = tid; i < 1024; i += blockDim.x) s_hist[i] = 0u;
+              if (tid == 0) {
+                if (b3 == 0xFFFFFFFFu) {
+                  atomicOr(A.diag + DIAG_ERR, GC_DIAG_SELECT);
+                  sl->live = 0;
+                }
+                sl->thr = (pfx << 10) | b3;
+                sl->r_eq = sl->r3 - above3;
+                sl->s = A.int8 ? __fdiv_rn(key_magnitude(__ldcg(F.maxkey + r.t)), 127.0f) : 0.0f;
+              }
+            }
+          } else if (sl->live) {
             uint32_t above = 0u;
             const uint32_t b = ffind(h3 + (size_t)r.t * NBINS, sl->r3, &above, s_row, s_warp, s_res);
             if (tid == 0) {
@@ -2410,7 +2476,7 @@ static TopkCarve carve_topk(int T, const TopkLayoutTotals& z) {
 struct FusedCarve {
   int64_t U = 0;
   size_t zero_bytes = 0, total = 0;
-  size_t o_bar = 0, o_max = 0, o_h1 = 0, o_h2 = 0, o_ugt = 0, o_ueq = 0;
+  size_t o_bar = 0, o_max = 0, o_h1 = 0, o_lcnt = 0, o_h2 = 0, o_ugt = 0, o_ueq = 0, o_lkey = 0;
 };
 
 static bool fused_layout_fits(const gc_layout* h) {
@@ -2430,10 +2496,12 @@ static FusedCarve carve_fused(const gc_layout* h) {
   c.o_bar = take(4);
   c.o_max = take(4 * (size_t)T);
   c.o_h1 = take((size_t)T * NBINS * 4);
+  c.o_lcnt = take(4 * ((size_t)T + 1));
   c.zero_bytes = p;
   c.o_h2 = take(2 * (size_t)T * NBINS * 4);
   c.o_ugt = take(4 * (size_t)c.U);
   c.o_ueq = take(4 * (size_t)c.U);
+  c.o_lkey = take(4 * (size_t)(h->off[T] - h->off[0]));
   c.total = p;
   return c;
 }
@@ -2528,6 +2596,8 @@ static gc_status launch_fused(const TopkArgs& A0, const gc_layout* host, const F
   F.h2 = reinterpret_cast<uint32_t*>(w + fc.o_h2);
   F.ugt = reinterpret_cast<uint32_t*>(w + fc.o_ugt);
   F.ueq = reinterpret_cast<uint32_t*>(w + fc.o_ueq);
+  F.lcnt = reinterpret_cast<uint32_t*>(w + fc.o_lcnt);
+  F.lkey = reinterpret_cast<uint32_t*>(w + fc.o_lkey);
   F.U = fc.U;
   F.spin_limit = FSPIN_LIMIT;
   pe.start(s);
