@@ -27,6 +27,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -108,10 +109,15 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the streaming pass's source files with comments and blank
+    lines removed: a change to the code voids the recorded traffic, an edit
+    of a comment does not."""
     h = hashlib.sha256()
     for f in ("gc_topk.cu", "gc_common.cuh"):
-        with open(os.path.join(ROOT, "gradient_compression_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "gradient_compression_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -1823,13 +1823,16 @@ __global__ void __launch_bounds__(256, 3) k_write(TopkArgs A) {
 //      histogram ((key >> 10) & 2047) of that bucket, re-reading acc (L1- or
 //      L2-resident at these sizes)
 //   3  level-2 bucket; level-3 histogram (key & 1023) of the 22-bit prefix
+//      (skipped, with its barrier, when every tensor's level-1 bucket holds
+//      at most FLMAX keys: phase 2 also lists those keys per tensor and
+//      phase 4 finds both remaining buckets from the histogram and the list)
 //   4  the k-th key and how many of its ties are kept; per-unit counts of
 //      keys above and equal to it
 //   5  index-ordered compaction into the payload, int8 codes, residual
 // A CTA owns the same contiguous range of 2048-element units in every phase
 // (a unit never straddles two tensors) and repeats the bucket searches of
-// its own tensors from the global histograms, so the four barriers are the
-// only waits between CTAs.  The keys, their total order (ties to the lower
+// its own tensors from the global histograms, so the barriers (three or
+// four) are the only waits between CTAs.  The keys, their total order (ties to the lower
 // index) and the payload writer (emit_kept) are the pipeline's, so the
 // results are identical to it.
 constexpr int FTHREADS = 512;

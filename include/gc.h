@@ -186,7 +186,7 @@ gc_status gc_workspace_size(const gc_layout* host, int32_t op, uint32_t flags, s
  * GC_INT8 cannot be combined with GC_RANDK.
  * Launches.  Top-k on an arena of at most 2^22 elements in at most 1024
  * tensors runs as one cooperative launch (all CTAs resident) whose phases
- * meet at four grid-wide barriers; every wait there is bounded and sets
+ * meet at three or four grid-wide barriers; every wait there is bounded and sets
  * GC_DIAG_TIMEOUT if it runs out.  gc_diag.one_launch reports it.  Other
  * arenas, random-k, GC_FORCE_EXACT and GC_MULTI_KERNEL use the multi-kernel
  * pipeline (14 kernels chained as programmatic dependent launches: each
