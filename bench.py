@@ -108,16 +108,20 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def code_text(src):
+    """C/C++/CUDA source without comments, trailing blanks and empty lines."""
+    text = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash():
-    """Hash of the streaming pass's source files with comments and blank
-    lines removed: a change to the code voids the recorded traffic, an edit
-    of a comment does not."""
+    """Hash of the streaming pass's source files as code_text: a change to
+    the code voids the recorded traffic, an edit of a comment does not."""
     h = hashlib.sha256()
     for f in ("gc_topk.cu", "gc_common.cuh"):
         with open(os.path.join(ROOT, "gradient_compression_gb300", "csrc", f)) as fh:
-            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
-        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.split("\n"))
-        h.update("\n".join(ln for ln in lines if ln).encode())
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -91,6 +91,28 @@ def test_bucket_layouts_are_accepted_and_sized_like_their_tensors(gc):
         whole.bucket(3, 3)
 
 
+def test_bucket_offsets_match_brute_force(gc):
+    """Layout.bucket keeps the arena's element and entry offsets; the word
+    offsets a caller passes with a bucket are sums over the earlier tensors."""
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        T = int(rng.integers(1, 12))
+        sizes = rng.integers(1, 5000, T)
+        k = np.minimum(sizes, rng.integers(0, 300, T))
+        L = gc.Layout(np.concatenate([[0], np.cumsum(sizes)]), k.astype(np.int64), device="cpu")
+        t0 = int(rng.integers(0, T))
+        t1 = int(rng.integers(t0 + 1, T + 1))
+        B = L.bucket(t0, t1)
+        assert B.T == t1 - t0
+        assert list(B.off) == [int(sum(sizes[:t])) for t in range(t0, t1 + 1)]
+        assert list(B.koff) == [int(sum(k[:t])) for t in range(t0, t1 + 1)]
+        assert list(B.k) == list(k[t0:t1])
+        assert L.word_offset(t0) == sum((int(n) + 31) // 32 for n in sizes[:t0])
+        assert L.kept_word_offset(t0) == sum((int(x) + 31) // 32 for x in k[:t0])
+        assert B.words == sum((int(n) + 31) // 32 for n in sizes[t0:t1])
+        assert B.kept_words == sum((int(x) + 31) // 32 for x in k[t0:t1])
+
+
 def test_argument_errors_return_before_any_launch(gc):
     lay = _host_layout(gc, [100], [5])
     L = gc.lib()
