@@ -63,7 +63,8 @@
  *
  * Buckets.  A layout may describe tensors t0 .. t1-1 of a larger arena: off
  * and koff are then that arena's own offsets of those tensors (off[0] and
- * koff[0] need not be 0).  Per-element arrays (g, e, u, v, out, dense int8 /
+ * koff[0] need not be 0), so the arena's own layout arrays serve:
+ * {t1 - t0, off + t0, k + t0, koff + t0}, on the host and on the device.  Per-element arrays (g, e, u, v, out, dense int8 /
  * QSGD codes) and per-entry arrays (idx, val, q) are passed as the WHOLE
  * arena's arrays and are read and written at those offsets only; per-tensor
  * arrays (k, scale, mean_abs, thresholds, norms, counts, residual
